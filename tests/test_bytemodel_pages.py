@@ -1,0 +1,78 @@
+"""The byte model of a batched decode step against the numbers the pages print
+(tests/golden/byte_model_pages.json, each value cited to its page)."""
+import json
+import os
+
+import pytest
+
+from oracle import bytemodel as bm
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "byte_model_pages.json")))
+
+
+def test_kv_bytes_per_token_exact_and_q8_ratio():
+    g = GOLD["kv_bytes_per_token_exact"]
+    f16 = bm.kv_bytes_per_token(g["n_layers"], g["n_kv_heads"], g["head_dim"], "f16")
+    q8 = bm.kv_bytes_per_token(g["n_layers"], g["n_kv_heads"], g["head_dim"], "q8_0")
+    assert f16 == g["f16"] == 147456
+    assert q8 == g["q8_0"] == 78336
+    assert q8 / f16 == 34 / 64          # Q8_0 "halves" KV up to its fp16 scale per 32
+    assert abs(f16 - GOLD["kv_bytes_per_token_f16"]["value"]) / f16 < 0.01
+
+
+def test_crossover_b8_page2():
+    W, k = GOLD["weights_bytes"]["value"], GOLD["kv_bytes_per_token_f16"]["value"]
+    g = GOLD["crossover_b8_f16"]
+    assert abs(bm.crossover(W, 8, k) - g["value"]) <= g["tolerance"]
+    # at the crossover the private KV read equals the shared weight read
+    L = bm.crossover(W, 8, k)
+    assert abs(8 * L * k - W) / W < 1e-12
+
+
+def test_speedup_table_page2():
+    W, k = GOLD["weights_bytes"]["value"], GOLD["kv_bytes_per_token_f16"]["value"]
+    for L, printed in GOLD["speedup_b8_table"]["rows"]:
+        s = bm.speedup(W, 8, L, k)
+        assert abs(s - printed) <= GOLD["speedup_b8_table"]["tolerance"], (L, s, printed)
+    assert bm.speedup(W, 8, 0, k) == 8.0
+
+
+def test_crossover_page3_fp16_and_q8():
+    g = GOLD["crossover_b8_f16_p3"]
+    W = g["weights_mb"] * 1e6
+    k = g["kv_mb_per_token"] * 1e6
+    assert abs(bm.crossover(W, 8, k) - g["value"]) <= g["tolerance"]
+    q8 = GOLD["crossover_b8_q8_p3"]
+    assert abs(bm.crossover(W, 8, k / 2) - q8["value"]) / q8["value"] <= q8["relative_tolerance"]
+
+
+def test_fig1_time_model_page1():
+    g = GOLD["fig1_step_ms"]
+    for B, t, agg, per in zip(g["batch"], g["step_ms"], g["aggregate_tok_s"],
+                              g["per_sequence_tok_s"]):
+        model_t = bm.time_model_ms(B, 0, per_seq_ms=1.1, k_ms_per_token=0.0)
+        assert abs(model_t - t) < 1e-9
+        assert abs(1000.0 * B / model_t - agg) < 0.6
+        assert abs(1000.0 / model_t - per) < 0.06
+
+
+def test_ceiling_table_page3():
+    rows = GOLD["ceiling_b8_table"]["rows_ctx_f16_q8"]
+    # fit the per-token KV time k from the first printed point, check the rest
+    ctx0, f16_0, _ = rows[0]
+    t0 = 8000.0 / f16_0
+    k = ((t0 - 16.9) / 8 - 1.1) / ctx0
+    for ctx, f16, q8 in rows:
+        if f16 is not None:
+            assert abs(8000.0 / bm.time_model_ms(8, ctx, k_ms_per_token=k) - f16) < 1.5
+        assert abs(8000.0 / bm.time_model_ms(8, ctx, k_ms_per_token=k / 2) - q8) < 1.5
+
+
+def test_weight_bytes_of_synthetic_model():
+    W = bm.weight_bytes()
+    assert W == 4_767_858_688
+    assert bm.weight_bytes(with_norms=False) == 4_766_662_656
+    # step bytes are linear in B and L, and the weight term is independent of B
+    k = 147456
+    assert bm.step_bytes(W, 8, 2048, k) - bm.step_bytes(W, 4, 2048, k) == 4 * 2048 * k
+    assert bm.step_bytes(W, 1, 0, k) == W
