@@ -1,0 +1,218 @@
+/*
+ * zdec.h -- C ABI of a batched, Q4_K-quantized decode step for one GB300.
+ *
+ * The operation: one decode step of a grouped-query-attention decoder for B
+ * sequences at once.  The Q4_K weight stream is read once per step and shared
+ * by all B sequences; each sequence reads its own KV cache (fp16 or Q8_0).
+ * Source: the blog pages "Eight concurrent agents pull 5.6x more tokens from
+ * one RX 9070 XT" (sections "The weight read is the only term that does not
+ * scale", "RDNA4 pads the batch dimension to 16"), "Batched swarm: the KV read
+ * does not amortize" ("The two halves of a decode-step memory bill") and "Q8
+ * KV cache pushes an RDNA4 swarm crossover from 5k to 10k tokens" ("Why Q8 is
+ * close to free and where the sharp edges are": quantized KV is dequantized
+ * inside the fused attention kernel).
+ *
+ * Conventions for every call:
+ *   - No exception crosses this ABI.  Every call returns a zdec_status; on
+ *     failure zdec_last_error(ctx) holds a message (per context; calls that
+ *     take no context report through zdec_last_global_error()).
+ *   - A failed call changes no state unless its comment says otherwise.
+ *   - All GPU work is enqueued on the CUDA stream given to zdec_create (or,
+ *     for the stateless op entry points, on the stream argument; NULL means
+ *     the legacy default stream).  Calls are asynchronous unless noted.
+ *   - "dev" pointers are CUDA device pointers; "host" pointers are ordinary
+ *     (pageable or pinned) host memory.  The library never frees caller
+ *     memory and never keeps caller pointers past the call, except the
+ *     output pointers of zdec_decode_step, which it writes asynchronously.
+ *   - fp16 means IEEE binary16 bit patterns (uint16_t).
+ */
+#ifndef ZDEC_H
+#define ZDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZDEC_OK = 0,
+    ZDEC_ERR_ARG = -1,          /* bad argument: null pointer, out-of-range index, bad shape  */
+    ZDEC_ERR_OOM = -2,          /* device or host allocation failed; nothing was created        */
+    ZDEC_ERR_CAPACITY = -3,     /* the sequence would exceed max_L tokens                      */
+    ZDEC_ERR_POSITION = -4,     /* positions[b] != number of tokens cached for sequence b      */
+    ZDEC_ERR_UNSUPPORTED = -5,  /* shape outside what the kernels implement (see zdec_create)  */
+    ZDEC_ERR_CUDA = -6,         /* a CUDA runtime call failed; message has cudaGetErrorString  */
+    ZDEC_ERR_TIMEOUT = -7,      /* a bounded device wait gave up (reported by zdec_sync)       */
+    ZDEC_ERR_DEVICE = -8        /* a device-side check flagged an error (reported by zdec_sync) */
+} zdec_status;
+
+typedef enum { ZDEC_KV_F16 = 0, ZDEC_KV_Q8_0 = 1 } zdec_kv_dtype;
+
+/* Model shape.  Supported: hidden and ffn multiples of 512, n_q_heads*head_dim
+ * a multiple of 512, head_dim == 128, n_q_heads/n_kv_heads == 4 (the grouped
+ * attention kernel handles groups of four query heads), vocab >= 1. */
+typedef struct {
+    int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    float rope_theta;   /* RoPE base; rotate-half pairs (i, i+head_dim/2)  */
+    float rms_eps;      /* RMSNorm epsilon                                 */
+} zdec_model_desc;
+
+/* Weights as HOST pointers to canonical Q4_K rows.  A canonical Q4_K block
+ * holds 256 consecutive weights of one row in 144 bytes:
+ *   [0:2] d (fp16) [2:4] dmin (fp16) [4:16] sixteen 6-bit fields, field i at
+ *   bits 6i..6i+5 of the little-endian 96-bit word: fields 0-7 sub-block
+ *   scales sc_j, 8-15 sub-block mins m_j; [16:144] codes, byte t = element 2t
+ *   (low nibble) | element 2t+1 (high nibble).  Weight i (sub-block j = i/32)
+ *   is (d*sc_j)*q_i - dmin*m_j.
+ * A rows x cols matrix is row-major: row r is cols/256 consecutive blocks.
+ * Shapes: embed [vocab x hidden] (also the tied LM head), wq [n_q*hd x hidden],
+ * wk, wv [n_kv*hd x hidden], wo [hidden x n_q*hd], w_gate, w_up [ffn x hidden],
+ * w_down [hidden x ffn]; norms are fp32 [hidden].  Per-layer arrays have
+ * n_layers entries.  The library copies and repacks everything at create;
+ * the caller may free these afterwards. */
+typedef struct {
+    const void *embed;
+    const float *final_norm;
+    const float *const *attn_norm;
+    const float *const *ffn_norm;
+    const void *const *wq, *const *wk, *const *wv, *const *wo;
+    const void *const *w_gate, *const *w_up, *const *w_down;
+} zdec_weights;
+
+typedef struct zdec_ctx zdec_ctx;
+
+/* Create a decoder: validate the shape, allocate on the current CUDA device
+ * (repacked weights ~0.5625 B/weight, the KV arena of max_B x max_L tokens,
+ * the per-step workspace), repack the weights on the GPU and wait for it.
+ * kv_dtype fixes the cache format: F16 (2 B/element) or Q8_0 (32-element
+ * blocks: 32 int8 codes + one fp16 scale).  max_B <= 32.  cuda_stream is a
+ * cudaStream_t (NULL: a new non-blocking stream owned by the context).
+ * Returns ZDEC_ERR_OOM (nothing allocated is kept) if the arena does not fit. */
+zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights,
+                        zdec_kv_dtype kv_dtype, int max_B, int max_L, void *cuda_stream,
+                        zdec_ctx **out);
+void zdec_destroy(zdec_ctx *ctx);
+
+/* Append n_tokens already-rotated K/V rows to sequence `seq`, starting at its
+ * current length.  k_f16 / v_f16: [n_layers][n_tokens][n_kv_heads][head_dim]
+ * fp16, host memory (on_device = 0; the call waits for the copy) or device
+ * memory (on_device = 1; asynchronous).  A Q8_0 cache quantizes every
+ * 32-element block on write: amax = max|x|, d = amax/127 (fp32 division),
+ * scale = fp16(d), code = clamp(rint(x/d), -127, 127) (ties to even), all-zero
+ * blocks store scale 0.  ZDEC_ERR_CAPACITY if len + n_tokens > max_L. */
+zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f16,
+                           const void *v_f16, int on_device);
+
+/* Flags of zdec_decode_step. */
+#define ZDEC_STEP_HOST_IO  1   /* tokens/positions are host, logits/ids host; the call
+                                  copies in, runs, copies out and waits */
+#define ZDEC_STEP_EAGER    2   /* launch kernel by kernel instead of replaying a CUDA graph */
+
+/* One decode step for sequences (slots) 0..B-1, B <= max_B.
+ *   tokens [B] int32 token ids, positions [B] int32: position b must equal the
+ *   number of tokens cached for slot b.  With host I/O the check happens
+ *   before anything is enqueued (ZDEC_ERR_POSITION); with device inputs the
+ *   first kernel checks it and zdec_sync reports ZDEC_ERR_DEVICE.
+ *   logits [B][vocab] fp32 (may be NULL), ids [B] int32 greedy argmax (lowest
+ *   index on ties).
+ * The step embeds each token, runs every layer (RMSNorm, QKV, RoPE, KV append,
+ * split-K attention, O projection + residual, RMSNorm, SwiGLU FFN + residual),
+ * the final RMSNorm and the tied LM head, appends each sequence's new K/V at
+ * its position and advances its length by one.  ZDEC_ERR_CAPACITY (nothing
+ * enqueued) if a sequence is full.  Without ZDEC_STEP_HOST_IO the call is
+ * asynchronous; outputs are valid after zdec_sync or a stream sync. */
+zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tokens,
+                             const int32_t *positions, float *logits, int32_t *ids, int flags);
+
+/* Wait for the context's stream and report any device-side status
+ * (ZDEC_ERR_DEVICE / ZDEC_ERR_TIMEOUT), clearing it. */
+zdec_status zdec_sync(zdec_ctx *ctx);
+
+zdec_status zdec_reset_seq(zdec_ctx *ctx, int seq);            /* length := 0 */
+zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len);
+const char *zdec_last_error(const zdec_ctx *ctx);
+const char *zdec_last_global_error(void);
+
+/* Which dense kernel runs the Q4_K projections: 0 = by measured switch point
+ * (B <= switch uses the dequant-matvec, else the mma.sync GEMM), 1 = always
+ * the matvec (B <= 4 only), 2 = always the mma.sync GEMM.  Takes effect at the
+ * next step (cached CUDA graphs are rebuilt). */
+zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl);
+
+typedef struct {
+    size_t weight_bytes;      /* repacked weights on the device              */
+    size_t arena_bytes;       /* KV arena                                    */
+    size_t workspace_bytes;   /* per-step activations, partials, logits     */
+    size_t kv_bytes_per_token;/* per sequence, K+V over all layers           */
+    int kernels_per_step;     /* kernel launches of one step (last B used)   */
+    int attn_splits;          /* split-K factor of the attention (last B)    */
+    int matvec_max_B;         /* switch point in use                         */
+} zdec_info;
+zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info);
+
+/* Per-kernel timing: runs one eager step (like ZDEC_STEP_EAGER, device inputs)
+ * with a CUDA event pair around every launch on the context stream, waits, and
+ * writes up to `cap` records: kind[i] (see ZDEC_KERNEL_*), ms[i].  *n receives
+ * the number of launches.  The step is a real step (lengths advance). */
+enum { ZDEC_KERNEL_EMBED = 0, ZDEC_KERNEL_PREP = 1, ZDEC_KERNEL_GEMM_QKV = 2,
+       ZDEC_KERNEL_ATTENTION = 3, ZDEC_KERNEL_GEMM_O = 4, ZDEC_KERNEL_GEMM_GATEUP = 5,
+       ZDEC_KERNEL_GEMM_DOWN = 6, ZDEC_KERNEL_GEMM_LMHEAD = 7, ZDEC_KERNEL_ARGMAX = 8 };
+zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *tokens_dev,
+                              const int32_t *positions_dev, float *logits_dev, int32_t *ids_dev,
+                              int *kind, float *ms, int cap, int *n);
+
+/* ------------------------------------------------------------ debug ---
+ * Read-backs used by the parity tests.  All synchronous; host outputs. */
+enum { ZDEC_T_EMBED = 0, ZDEC_T_WQ = 1, ZDEC_T_WK = 2, ZDEC_T_WV = 3, ZDEC_T_WO = 4,
+       ZDEC_T_GATE = 5, ZDEC_T_UP = 6, ZDEC_T_DOWN = 7 };
+/* Rows [row0, row0+nrows) of tensor `which` (layer ignored for EMBED),
+ * unpacked from the device's repacked layout back to canonical 144-byte
+ * blocks (out: nrows * cols/256 * 144 bytes). */
+zdec_status zdec_debug_export_q4k(zdec_ctx *ctx, int which, int layer, int row0, int nrows,
+                                  void *out_host);
+/* The same rows dequantized on the device, fp32 (out: nrows * cols floats). */
+zdec_status zdec_debug_dequant(zdec_ctx *ctx, int which, int layer, int row0, int nrows,
+                               float *out_host);
+/* Stored KV of sequence `seq`, layer `layer`, tokens [t0, t0+n) in canonical
+ * token-major layout [n][n_kv_heads][head_dim]: F16 -> k,v fp16 (ks, vs
+ * unused, may be NULL); Q8_0 -> k,v int8 codes and ks,vs fp16 scales
+ * [n][n_kv_heads][head_dim/32]. */
+zdec_status zdec_debug_read_kv(zdec_ctx *ctx, int seq, int layer, int t0, int n, void *k,
+                               void *v, void *ks, void *vs);
+/* Arm a capture of the fp32 residual stream for the next zdec_decode_step,
+ * which then runs eagerly, waits, and fills out [B][n_layers+1][hidden]
+ * (after the embedding and after each layer) before it returns.  out must
+ * hold B*(n_layers+1)*hidden floats for the B of that step; host memory. */
+zdec_status zdec_debug_capture_hidden(zdec_ctx *ctx, float *out_host);
+/* Attention alone on the cached tokens 0..positions[b] of layer `layer`
+ * (nothing appended): q [B][n_q_heads][head_dim] fp32 already rotated,
+ * o [B][n_q_heads][head_dim] fp32.  Host memory. */
+zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, const float *q_host,
+                                 const int32_t *positions_host, float *o_host);
+
+/* ------------------------------------------------------- stateless ops ---
+ * The dense Q4_K projection on its own (used for kernel-level parity and the
+ * GEMM roofline).  N multiple of 16, K multiple of 512, 1 <= B <= 32. */
+
+/* Bytes of the repacked layout of an N x K matrix (== canonical bytes). */
+size_t zdec_q4k_repacked_bytes(int N, int K);
+/* canonical_dev (N*K/256 blocks, row-major) -> repacked_dev.  Device memory. */
+zdec_status zdec_q4k_repack(const void *canonical_dev, int N, int K, void *repacked_dev,
+                            void *stream);
+/* Scratch bytes zdec_q4k_gemm needs for B rows of length K. */
+size_t zdec_q4k_gemm_workspace_bytes(int K, int B);
+/* y[b][n] = sum_k W[n][k] x[b][k] for b < B.  x_dev fp32 [B][K], y_dev fp32
+ * [B][N], workspace_dev >= zdec_q4k_gemm_workspace_bytes(K, B) bytes, 16-byte
+ * aligned, owned by the caller.  impl: 1 = dequant-matvec (B <= 4),
+ * 2 = mma.sync GEMM.  Activations are rounded to fp16 on the way in; weights
+ * are exact; accumulation is fp32. */
+zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B,
+                          float *y_dev, int impl, void *workspace_dev, size_t workspace_bytes,
+                          void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZDEC_H */

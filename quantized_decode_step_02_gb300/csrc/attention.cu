@@ -1,0 +1,560 @@
+// attention.cu -- per-sequence KV read: split-K flash-decode over an fp16 or
+// Q8_0 cache, dequantized inside the kernel, plus the KV append paths.
+//
+// Each sequence reads its own cache every step; nothing here is shared across
+// the batch ("Batched swarm: the KV read does not amortize", "The two halves
+// of a decode-step memory bill").  A quantized cache only saves bytes if the
+// attention kernel reads the compressed format and dequantizes on chip ("Q8
+// KV cache pushes an RDNA4 swarm crossover...", "Why Q8 is close to free and
+// where the sharp edges are"), which is what the Q8_0 instantiation does.
+//
+// Grid: (split s, kv head g, sequence b); 128 threads.  The 4 query heads of
+// a kv head share one read of its K/V tiles.  A split covers Ts tokens
+// (a multiple of 64, Ts = ceil(ceil((pos+1)/S) / 64) * 64), streamed through
+// two shared-memory stages of 64 tokens with cp.async.  Both products run on
+// mma.sync.m16n8k16 with fp32 accumulation:
+//   scores: A = q (rows 0-3 the fp16 high parts of the 4 heads, rows 8-11 the
+//           low parts, so q keeps ~22 bits), B = K^T (8 tokens per MMA);
+//   output: A = p (same hi/lo split), B = V (8 head dims per MMA) read from a
+//           V^T tile, whose layout makes each thread's four tokens adjacent.
+// Q8_0: codes become exact fp16 integers in registers; K scales multiply the
+// per-32-dim partial scores, V scales are folded into p per 32-dim block.
+// The last CTA of each (b, g) (atomic ticket, no waiting) merges the splits'
+// (max, sum, unnormalised output) partials.
+#include "zdec_kernels.cuh"
+
+namespace zdec {
+
+constexpr uint32_t AFULL = 0xFFFFFFFFu;
+
+template <int KVT> struct AttnLayout;
+template <> struct AttnLayout<0> {          // fp16
+    static constexpr int K_STRIDE = 288;    // bytes per token row (256 + pad)
+    static constexpr int V_STRIDE = 160;    // bytes per head-dim row of V^T (128 + pad)
+    static constexpr int K_BYTES = ATT_CHUNK * K_STRIDE;
+    static constexpr int V_BYTES = HD * V_STRIDE;
+    static constexpr int KS_BYTES = 0, VS_BYTES = 0;
+    static constexpr int STAGE = K_BYTES + V_BYTES;
+};
+template <> struct AttnLayout<1> {          // Q8_0
+    static constexpr int K_STRIDE = 144;    // 128 codes + pad
+    static constexpr int V_STRIDE = 80;     // 64 codes + pad
+    static constexpr int K_BYTES = ATT_CHUNK * K_STRIDE;
+    static constexpr int V_BYTES = HD * V_STRIDE;
+    static constexpr int KS_BYTES = ATT_CHUNK * 4 * 2;   // [token][4] fp16
+    static constexpr int VS_BYTES = 4 * ATT_CHUNK * 2;   // [blk][token] fp16
+    static constexpr int STAGE = K_BYTES + V_BYTES + KS_BYTES + VS_BYTES;
+};
+
+size_t attention_smem_bytes(int kv_dtype) {
+    size_t stages = kv_dtype ? 2 * AttnLayout<1>::STAGE : 2 * AttnLayout<0>::STAGE;
+    size_t merge = (4 * 4 * 2 + 4 * 4 * HD) * sizeof(float);
+    return stages > merge ? stages : merge;
+}
+
+// Base of the (slot, layer, kv head) plane for a tensor of `per_token` bytes
+// per token (K planes) or `per_dim` rows (V^T planes).
+__device__ __forceinline__ size_t plane_index(const KvArena &a, int slot, int layer, int g) {
+    return ((size_t)slot * a.n_layers + layer) * a.n_kv + g;
+}
+
+// -------------------------------------------------------- chunk staging ---
+// Copy history tokens [c0, min(c0+64, H)) of the plane into a stage.  Partial
+// 16-byte segments of V^T may pull in tokens >= H; those columns are zeroed
+// by the fix-up before use.
+template <int KVT>
+__device__ __forceinline__ void issue_chunk(const AttnParams &p, uint8_t *stage, int b, int g, int c0,
+                                            int H) {
+    using Lay = AttnLayout<KVT>;
+    int nt = min(ATT_CHUNK, H - c0);
+    if (nt <= 0) return;
+    size_t pi = plane_index(p.kv, b, p.layer, g);
+    const int Lp = p.kv.Lp;
+    uint8_t *sK = stage, *sV = stage + Lay::K_BYTES;
+    if (KVT == 0) {
+        const uint8_t *gK = p.kv.k + (pi * Lp + c0) * (HD * 2);
+        const uint8_t *gV = p.kv.v + pi * HD * (size_t)Lp * 2 + (size_t)c0 * 2;
+        for (int i = threadIdx.x; i < nt * 16; i += blockDim.x) {
+            int t = i >> 4, sg = i & 15;
+            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + (size_t)t * 256 + sg * 16);
+        }
+        int vseg = (nt + 7) >> 3;   // 8 tokens per 16 bytes
+        for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
+            int d = i / vseg, sg = i % vseg;
+            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + (size_t)d * Lp * 2 + sg * 16);
+        }
+    } else {
+        uint8_t *sKs = stage + Lay::K_BYTES + Lay::V_BYTES, *sVs = sKs + Lay::KS_BYTES;
+        const uint8_t *gK = p.kv.k + (pi * Lp + c0) * HD;
+        const uint8_t *gKs = p.kv.ks + (pi * Lp + c0) * 8;
+        const uint8_t *gV = p.kv.v + pi * HD * (size_t)Lp + c0;
+        const uint8_t *gVs = p.kv.vs + pi * 4 * (size_t)Lp * 2 + (size_t)c0 * 2;
+        for (int i = threadIdx.x; i < nt * 8; i += blockDim.x) {
+            int t = i >> 3, sg = i & 7;
+            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + (size_t)t * HD + sg * 16);
+        }
+        for (int i = threadIdx.x; i < (nt + 1) / 2; i += blockDim.x)   // 2 tokens of scales per 16 B
+            cp_async16(sKs + i * 16, gKs + (size_t)i * 16);
+        int vseg = (nt + 15) >> 4;   // 16 tokens per 16 bytes
+        for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
+            int d = i / vseg, sg = i % vseg;
+            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + (size_t)d * Lp + sg * 16);
+        }
+        int sseg = (nt + 7) >> 3;    // 8 tokens of one scale row per 16 B
+        for (int i = threadIdx.x; i < 4 * sseg; i += blockDim.x) {
+            int bl = i / sseg, sg = i % sseg;
+            cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + (size_t)bl * Lp * 2 + sg * 16);
+        }
+    }
+}
+
+__device__ __forceinline__ void codes4_to_h2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    // bytes b0..b3 (int8) -> (b0, b1), (b2, b3) as exact fp16 integers:
+    // flip the sign bit, place each byte under exponent 0x64 (value 1024 + byte),
+    // subtract 1024 + 128
+    uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __float2half2_rn(1152.0f);
+    lo = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4140)), bias));
+    hi = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4342)), bias));
+}
+
+// Q8_0 of 32 fp16 values held one per lane: returns this lane's code, and the
+// fp16 scale bits.  amax/127 by IEEE division, codes by IEEE division by the
+// fp32 scale, round half to even, clamp to +-127; all-zero blocks -> 0, 0.
+__device__ __forceinline__ int8_t q8_0_lane(__half xh, uint16_t &scale_bits) {
+    float x = __half2float(xh);
+    float amax = fabsf(x);
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(AFULL, amax, o));
+    if (amax == 0.0f) { scale_bits = 0; return 0; }
+    float d = __fdiv_rn(amax, 127.0f);
+    scale_bits = __half_as_ushort(__float2half_rn(d));
+    int q = __float2int_rn(__fdiv_rn(x, d));
+    q = max(-127, min(127, q));
+    return (int8_t)q;
+}
+
+// --------------------------------------------------------------- kernel ---
+template <int KVT>
+__global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
+    using Lay = AttnLayout<KVT>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ __align__(16) uint8_t s_newk[HD * 2], s_newv[HD * 2];   // new token (fp16 or codes)
+    __shared__ uint16_t s_newks[4], s_newvs[4];
+    __shared__ int s_last;
+
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int pos = p.positions[b];       // staged before the step: not a predecessor output
+    if (pos < 0 || pos >= p.max_L) return;   // bad device input: flagged by the embedding kernel
+    const int ntok = pos + 1;
+    const int Ts = (((ntok + p.S - 1) / p.S) + ATT_CHUNK - 1) / ATT_CHUNK * ATT_CHUNK;
+    const int T0 = s * Ts;
+    if (T0 >= ntok) return;               // empty split; the combiner does not wait for it
+    const int T1 = min(T0 + Ts, ntok);
+    const int H = p.append ? min(T1, pos) : T1;   // tokens read from the arena
+    const int nchunks = (T1 - T0 + ATT_CHUNK - 1) / ATT_CHUNK;
+    const int n_used = (ntok + Ts - 1) / Ts;
+    const bool has_new = p.append && T1 == ntok;
+
+    uint8_t *stage0 = smem, *stage1 = smem + Lay::STAGE;
+    issue_chunk<KVT>(p, stage0, b, g, T0, H);
+    cp_async_commit();
+    if (nchunks > 1) issue_chunk<KVT>(p, stage1, b, g, T0 + ATT_CHUNK, H);
+    cp_async_commit();
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // ---- query fragments: head 4g+gid (gid < 4), dims 16s' + 4tig + {0..3}
+    uint32_t qa[8][4];
+    {
+        const float qscale = 0.08838834764831845f;   // 1/sqrt(128)
+        const int hq = GROUP * g + gid;
+        const float *qrow = p.qkv + (size_t)b * p.qkv_ld + (size_t)hq * HD;
+        const float2 *cs = p.rope + (size_t)pos * (HD / 2);
+#pragma unroll
+        for (int st = 0; st < 8; st++) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                int d = 16 * st + 4 * tig + e;
+                float x = 0.0f;
+                if (gid < GROUP) {
+                    x = qrow[d];
+                    if (p.append) {
+                        int i = d & 63;
+                        float2 c = cs[i];
+                        x = d < 64 ? x * c.x - qrow[d + 64] * c.y : x * c.x + qrow[d - 64] * c.y;
+                    }
+                }
+                v[e] = x * qscale;
+            }
+            __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
+            float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            qa[st][0] = h2_as_u32(h01);
+            qa[st][1] = h2_as_u32(__floats2half2_rn(v[0] - f01.x, v[1] - f01.y));
+            qa[st][2] = h2_as_u32(h23);
+            qa[st][3] = h2_as_u32(__floats2half2_rn(v[2] - f23.x, v[3] - f23.y));
+        }
+    }
+
+    // ---- the new token: rotate k, round to fp16, quantize (Q8_0), append
+    if (has_new && warp == 0) {
+        const float *krow = p.qkv + (size_t)b * p.qkv_ld + (size_t)(p.nq + g) * HD;
+        const float *vrow = p.qkv + (size_t)b * p.qkv_ld + (size_t)(p.nq + p.kv.n_kv + g) * HD;
+        const float2 *cs = p.rope + (size_t)pos * (HD / 2);
+        size_t pi = plane_index(p.kv, b, p.layer, g);
+        const int Lp = p.kv.Lp;
+        float kx[4], vx[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) { kx[i] = krow[lane + 32 * i]; vx[i] = vrow[lane + 32 * i]; }
+        float kr[4];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {   // pairs (d, d+64): d = lane + 32 i
+            float2 c = cs[lane + 32 * i];
+            kr[i] = kx[i] * c.x - kx[i + 2] * c.y;
+            kr[i + 2] = kx[i + 2] * c.x + kx[i] * c.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            int d = lane + 32 * i;
+            __half kh = __float2half_rn(kr[i]), vh = __float2half_rn(vx[i]);
+            if (KVT == 0) {
+                reinterpret_cast<__half *>(p.kv.k)[(pi * Lp + pos) * HD + d] = kh;
+                reinterpret_cast<__half *>(p.kv.v)[(pi * HD + d) * (size_t)Lp + pos] = vh;
+                reinterpret_cast<__half *>(s_newk)[d] = kh;
+                reinterpret_cast<__half *>(s_newv)[d] = vh;
+            } else {
+                uint16_t ksb, vsb;
+                int8_t kc = q8_0_lane(kh, ksb), vc = q8_0_lane(vh, vsb);
+                reinterpret_cast<int8_t *>(p.kv.k)[(pi * Lp + pos) * HD + d] = kc;
+                reinterpret_cast<int8_t *>(p.kv.v)[(pi * HD + d) * (size_t)Lp + pos] = vc;
+                reinterpret_cast<int8_t *>(s_newk)[d] = kc;
+                reinterpret_cast<int8_t *>(s_newv)[d] = vc;
+                if (lane == 0) {
+                    reinterpret_cast<uint16_t *>(p.kv.ks)[(pi * Lp + pos) * 4 + i] = ksb;
+                    reinterpret_cast<uint16_t *>(p.kv.vs)[(pi * 4 + i) * (size_t)Lp + pos] = vsb;
+                    s_newks[i] = ksb;
+                    s_newvs[i] = vsb;
+                }
+            }
+        }
+    }
+
+    // ---- online softmax state (meaningful on lanes gid < 4: head 4g+gid)
+    float m_run = -INFINITY, l_run = 0.0f;
+    float oacc[16][4];
+#pragma unroll
+    for (int dn = 0; dn < 16; dn++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) oacc[dn][i] = 0.0f;
+    const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+    for (int ci = 0; ci < nchunks; ci++) {
+        uint8_t *st = (ci & 1) ? stage1 : stage0;
+        const int c0 = T0 + ci * ATT_CHUNK;
+        cp_async_wait<1>();
+        __syncthreads();
+        // fix-up: zero V columns past the loaded history, insert the new token
+        {
+            const int zfrom = max(H, c0) - c0, cend = min(ATT_CHUNK, T1 - c0 + 0);
+            uint8_t *sV = st + Lay::K_BYTES;
+            if (zfrom < ATT_CHUNK) {
+                for (int i = threadIdx.x; i < HD * (ATT_CHUNK - zfrom); i += blockDim.x) {
+                    int d = i / (ATT_CHUNK - zfrom), t = zfrom + i % (ATT_CHUNK - zfrom);
+                    if (KVT == 0) reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE)[t] = __ushort_as_half(0);
+                    else sV[d * Lay::V_STRIDE + t] = 0;
+                }
+                if (KVT == 1) {
+                    uint16_t *sVs = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES);
+                    for (int i = threadIdx.x; i < 4 * (ATT_CHUNK - zfrom); i += blockDim.x)
+                        sVs[(i / (ATT_CHUNK - zfrom)) * ATT_CHUNK + zfrom + i % (ATT_CHUNK - zfrom)] = 0;
+                }
+            }
+            __syncthreads();
+            if (has_new && pos >= c0 && pos < c0 + ATT_CHUNK) {
+                int t = pos - c0;
+                uint8_t *sK = st;
+                int d = threadIdx.x;   // 128 threads, one head dim each
+                if (KVT == 0) {
+                    reinterpret_cast<__half *>(sK + t * Lay::K_STRIDE)[d] = reinterpret_cast<__half *>(s_newk)[d];
+                    reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE)[t] = reinterpret_cast<__half *>(s_newv)[d];
+                } else {
+                    sK[t * Lay::K_STRIDE + d] = s_newk[d];
+                    sV[d * Lay::V_STRIDE + t] = s_newv[d];
+                    if (d < 4) {
+                        uint16_t *sKs = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES);
+                        uint16_t *sVs = sKs + ATT_CHUNK * 4;
+                        sKs[t * 4 + d] = s_newks[d];
+                        sVs[d * ATT_CHUNK + t] = s_newvs[d];
+                    }
+                }
+            }
+            __syncthreads();
+            (void)cend;
+        }
+
+        const int tb = c0 + 16 * warp;   // this warp's 16 tokens
+        if (tb < T1) {
+            const uint8_t *sK = st;
+            const uint8_t *sV = st + Lay::K_BYTES;
+            // ---- scores S[head][token], tokens of n-tile nt, slot c: 4(c>>1) + 2nt + (c&1)
+            float S[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++) {
+                const int tr = 16 * warp + 4 * (gid >> 1) + 2 * nt + (gid & 1);
+#pragma unroll
+                for (int i = 0; i < 4; i++) S[nt][i] = 0.0f;
+                if (KVT == 0) {
+#pragma unroll
+                    for (int st8 = 0; st8 < 8; st8++) {
+                        uint2 kb = *reinterpret_cast<const uint2 *>(sK + tr * Lay::K_STRIDE + (16 * st8 + 4 * tig) * 2);
+                        mma16816(S[nt], qa[st8], kb.x, kb.y, S[nt]);
+                    }
+                } else {
+                    const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES);
+                    const int ta = 16 * warp + 4 * tig + 2 * nt;   // tokens of columns 2tig, 2tig+1
+#pragma unroll
+                    for (int bl = 0; bl < 4; bl++) {
+                        float tmp[4];
+#pragma unroll
+                        for (int hs = 0; hs < 2; hs++) {
+                            const int st8 = 2 * bl + hs;
+                            uint32_t w = *reinterpret_cast<const uint32_t *>(sK + tr * Lay::K_STRIDE + 16 * st8 + 4 * tig);
+                            uint32_t b0, b1;
+                            codes4_to_h2(w, b0, b1);
+                            if (hs) mma16816(tmp, qa[st8], b0, b1, tmp);
+                            else mma16816(tmp, qa[st8], b0, b1, zero4);
+                        }
+                        float ka = __half2float(__ushort_as_half(sKs[ta * 4 + bl]));
+                        float kb = __half2float(__ushort_as_half(sKs[(ta + 1) * 4 + bl]));
+                        S[nt][0] += ka * tmp[0];
+                        S[nt][1] += kb * tmp[1];
+                        S[nt][2] += ka * tmp[2];
+                        S[nt][3] += kb * tmp[3];
+                    }
+                }
+            }
+            // ---- online softmax on this tile (head gid, tokens 4tig + {0,1,2,3})
+            float sc[4];
+            sc[0] = S[0][0] + S[0][2];
+            sc[1] = S[0][1] + S[0][3];
+            sc[2] = S[1][0] + S[1][2];
+            sc[3] = S[1][1] + S[1][3];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                int t = tb + 4 * tig + e;
+                if (t >= T1 || gid >= GROUP) sc[e] = -INFINITY;
+            }
+            float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 2));
+            const float m_new = fmaxf(m_run, mt);
+            float alpha = 1.0f, pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (m_new != -INFINITY) {
+                alpha = expf(m_run - m_new);   // m_run = -inf -> 0
+#pragma unroll
+                for (int e = 0; e < 4; e++) pr[e] = expf(sc[e] - m_new);
+            }
+            m_run = m_new;
+            l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+#pragma unroll
+            for (int dn = 0; dn < 16; dn++)
+#pragma unroll
+                for (int i = 0; i < 4; i++) oacc[dn][i] *= alpha;
+            // ---- output += P V
+            if (KVT == 0) {
+                uint32_t pa[4];
+                __half2 h01 = __floats2half2_rn(pr[0], pr[1]), h23 = __floats2half2_rn(pr[2], pr[3]);
+                float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                pa[0] = h2_as_u32(h01);
+                pa[1] = h2_as_u32(__floats2half2_rn(pr[0] - f01.x, pr[1] - f01.y));
+                pa[2] = h2_as_u32(h23);
+                pa[3] = h2_as_u32(__floats2half2_rn(pr[2] - f23.x, pr[3] - f23.y));
+#pragma unroll
+                for (int dn = 0; dn < 16; dn++) {
+                    const int d = 8 * dn + gid;
+                    uint2 vb = *reinterpret_cast<const uint2 *>(sV + d * Lay::V_STRIDE + (16 * warp + 4 * tig) * 2);
+                    mma16816(oacc[dn], pa, vb.x, vb.y, oacc[dn]);
+                }
+            } else {
+                const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES);
+                const int tl = 16 * warp + 4 * tig;
+#pragma unroll
+                for (int bl = 0; bl < 4; bl++) {
+                    float q4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) q4[e] = pr[e] * __half2float(__ushort_as_half(sVs[bl * ATT_CHUNK + tl + e]));
+                    uint32_t pa[4];
+                    __half2 h01 = __floats2half2_rn(q4[0], q4[1]), h23 = __floats2half2_rn(q4[2], q4[3]);
+                    float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    pa[0] = h2_as_u32(h01);
+                    pa[1] = h2_as_u32(__floats2half2_rn(q4[0] - f01.x, q4[1] - f01.y));
+                    pa[2] = h2_as_u32(h23);
+                    pa[3] = h2_as_u32(__floats2half2_rn(q4[2] - f23.x, q4[3] - f23.y));
+#pragma unroll
+                    for (int dq = 0; dq < 4; dq++) {
+                        const int dn = 4 * bl + dq, d = 8 * dn + gid;
+                        uint32_t w = *reinterpret_cast<const uint32_t *>(sV + d * Lay::V_STRIDE + tl);
+                        uint32_t b0, b1;
+                        codes4_to_h2(w, b0, b1);
+                        mma16816(oacc[dn], pa, b0, b1, oacc[dn]);
+                    }
+                }
+            }
+        }
+        __syncthreads();   // everyone is done with this stage
+        if (ci + 2 < nchunks) issue_chunk<KVT>(p, st, b, g, T0 + (ci + 2) * ATT_CHUNK, H);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // ---- merge the 4 warps of this CTA (smem reused after the stages)
+    float *wm = reinterpret_cast<float *>(smem);          // [4 warps][4 heads]
+    float *wl = wm + 16;
+    float *wo = wl + 16;                                   // [4][4][128]
+    float l_tot = l_run;
+    l_tot += __shfl_xor_sync(AFULL, l_tot, 1);
+    l_tot += __shfl_xor_sync(AFULL, l_tot, 2);
+    __syncthreads();
+    if (gid < GROUP) {
+        if (tig == 0) { wm[warp * 4 + gid] = m_run; wl[warp * 4 + gid] = l_tot; }
+#pragma unroll
+        for (int dn = 0; dn < 16; dn++)
+#pragma unroll
+            for (int e = 0; e < 2; e++)
+                wo[(warp * 4 + gid) * HD + 8 * dn + 2 * tig + e] = oacc[dn][e] + oacc[dn][2 + e];
+    }
+    __syncthreads();
+    const int head = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
+    {
+        float M = -INFINITY;
+        for (int w = 0; w < 4; w++) M = fmaxf(M, wm[w * 4 + head]);
+        float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int w = 0; w < 4; w++) {
+            float mw = wm[w * 4 + head];
+            float f = mw == -INFINITY ? 0.0f : expf(mw - M);
+            L += f * wl[w * 4 + head];
+            for (int e = 0; e < 4; e++) O[e] += f * wo[(w * 4 + head) * HD + d0 + e];
+        }
+        float *pp = p.part + ((((size_t)b * p.kv.n_kv + g) * p.S + s) * 4 + head) * (HD + 2);
+        if ((threadIdx.x & 31) == 0) { pp[0] = M; pp[1] = L; }
+        for (int e = 0; e < 4; e++) pp[2 + d0 + e] = O[e];
+    }
+    // ---- last CTA of (b, g) merges the splits
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = atomicAdd(&p.tickets[b * p.kv.n_kv + g], 1);
+        s_last = (t == n_used - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    {
+        const float *base = p.part + (((size_t)b * p.kv.n_kv + g) * p.S) * 4 * (HD + 2);
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < n_used; s2++) M = fmaxf(M, __ldcg(base + ((size_t)s2 * 4 + head) * (HD + 2)));
+        float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int s2 = 0; s2 < n_used; s2++) {
+            const float *ps = base + ((size_t)s2 * 4 + head) * (HD + 2);
+            float ms = __ldcg(ps);
+            float f = ms == -INFINITY ? 0.0f : expf(ms - M);
+            L += f * __ldcg(ps + 1);
+            for (int e = 0; e < 4; e++) O[e] += f * __ldcg(ps + 2 + d0 + e);
+        }
+        float inv = 1.0f / L;
+        float *o = p.o + (size_t)b * p.nq * HD + (size_t)(GROUP * g + head) * HD + d0;
+        for (int e = 0; e < 4; e++) o[e] = O[e] * inv;
+        if (threadIdx.x == 0) p.tickets[b * p.kv.n_kv + g] = 0;
+    }
+}
+
+cudaError_t attention_setup(int kv_dtype) {
+    int smem = (int)attention_smem_bytes(kv_dtype);
+    if (kv_dtype == 0)
+        return cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return cudaFuncSetAttribute(attention_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream) {
+    dim3 grid(p.S, p.kv.n_kv, p.B), block(128);
+    size_t smem = attention_smem_bytes(p.kv.kv_dtype);
+    if (p.kv.kv_dtype == 0) return launch_k(attention_kernel<0>, grid, block, smem, pdl, stream, p);
+    return launch_k(attention_kernel<1>, grid, block, smem, pdl, stream, p);
+}
+
+// ------------------------------------------------------------ bulk append ---
+// One warp per (layer, token, kv head); lane holds dims lane + 32 i, i.e.
+// element `lane` of Q8_0 block i.
+__global__ void kv_append_kernel(const KvArena a, int slot, int t0, int n,
+                                 const uint16_t *__restrict__ k16, const uint16_t *__restrict__ v16) {
+    long w = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    int lane = threadIdx.x & 31;
+    if (w >= (long)a.n_layers * n * a.n_kv) return;
+    int g = (int)(w % a.n_kv);
+    int t = (int)((w / a.n_kv) % n);
+    int l = (int)(w / ((long)a.n_kv * n));
+    const uint16_t *ks = k16 + (((size_t)l * n + t) * a.n_kv + g) * HD;
+    const uint16_t *vs = v16 + (((size_t)l * n + t) * a.n_kv + g) * HD;
+    size_t pi = plane_index(a, slot, l, g);
+    int pos = t0 + t;
+    for (int i = 0; i < 4; i++) {
+        int d = lane + 32 * i;
+        uint16_t kb = ks[d], vb = vs[d];
+        if (a.kv_dtype == 0) {
+            reinterpret_cast<uint16_t *>(a.k)[(pi * a.Lp + pos) * HD + d] = kb;
+            reinterpret_cast<uint16_t *>(a.v)[(pi * HD + d) * (size_t)a.Lp + pos] = vb;
+        } else {
+            uint16_t ksb, vsb;
+            int8_t kc = q8_0_lane(__ushort_as_half(kb), ksb);
+            int8_t vc = q8_0_lane(__ushort_as_half(vb), vsb);
+            reinterpret_cast<int8_t *>(a.k)[(pi * a.Lp + pos) * HD + d] = kc;
+            reinterpret_cast<int8_t *>(a.v)[(pi * HD + d) * (size_t)a.Lp + pos] = vc;
+            if (lane == 0) {
+                reinterpret_cast<uint16_t *>(a.ks)[(pi * a.Lp + pos) * 4 + i] = ksb;
+                reinterpret_cast<uint16_t *>(a.vs)[(pi * 4 + i) * (size_t)a.Lp + pos] = vsb;
+            }
+        }
+    }
+}
+
+cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const uint16_t *k16,
+                             const uint16_t *v16, cudaStream_t stream) {
+    long warps = (long)a.n_layers * n * a.n_kv;
+    if (warps == 0) return cudaSuccess;
+    kv_append_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(a, slot, t0, n, k16, v16);
+    return cudaGetLastError();
+}
+
+// One thread per (token, kv head, dim) of one layer.
+__global__ void kv_read_kernel(const KvArena a, int slot, int layer, int t0, int n, uint8_t *k,
+                               uint8_t *v, uint16_t *ks, uint16_t *vs) {
+    long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)n * a.n_kv * HD) return;
+    int d = (int)(i % HD), g = (int)((i / HD) % a.n_kv), t = (int)(i / ((long)HD * a.n_kv));
+    size_t pi = plane_index(a, slot, layer, g);
+    int pos = t0 + t;
+    if (a.kv_dtype == 0) {
+        reinterpret_cast<uint16_t *>(k)[i] = reinterpret_cast<const uint16_t *>(a.k)[(pi * a.Lp + pos) * HD + d];
+        reinterpret_cast<uint16_t *>(v)[i] = reinterpret_cast<const uint16_t *>(a.v)[(pi * HD + d) * (size_t)a.Lp + pos];
+    } else {
+        k[i] = a.k[(pi * a.Lp + pos) * HD + d];
+        v[i] = a.v[(pi * HD + d) * (size_t)a.Lp + pos];
+        if ((d & 31) == 0) {
+            size_t o = ((size_t)t * a.n_kv + g) * 4 + (d >> 5);
+            ks[o] = reinterpret_cast<const uint16_t *>(a.ks)[(pi * a.Lp + pos) * 4 + (d >> 5)];
+            vs[o] = reinterpret_cast<const uint16_t *>(a.vs)[(pi * 4 + (d >> 5)) * (size_t)a.Lp + pos];
+        }
+    }
+}
+
+cudaError_t launch_kv_read(const KvArena &a, int slot, int layer, int t0, int n, uint8_t *k,
+                           uint8_t *v, uint16_t *ks, uint16_t *vs, cudaStream_t stream) {
+    long total = (long)n * a.n_kv * HD;
+    if (total == 0) return cudaSuccess;
+    kv_read_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(a, slot, layer, t0, n, k, v, ks, vs);
+    return cudaGetLastError();
+}
+
+}  // namespace zdec

@@ -1,0 +1,842 @@
+// zdec.cu -- host runtime behind include/zdec.h: weight upload + repack, the
+// KV arena, the per-step workspace, the launch sequence of one decode step
+// (replayed as a CUDA graph whose kernel edges are programmatic, so each
+// kernel's weight prefetch overlaps its predecessor's tail), and the
+// read-backs the parity tests use.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/zdec.h"
+#include "zdec_kernels.cuh"
+
+using namespace zdec;
+
+namespace {
+
+thread_local std::string g_global_error;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+size_t tile_bytes(int rows16, int nsb) { return (size_t)rows16 * nsb * TILE_BYTES; }
+
+struct LayerW {
+    uint8_t *qkv, *o, *gu, *down;
+    float *attn_norm, *ffn_norm;
+};
+
+struct Launch {      // one entry of a profiled step
+    int kind;
+    cudaEvent_t t0, t1;
+};
+
+}  // namespace
+
+struct zdec_ctx {
+    zdec_model_desc d{};
+    int kv_dtype = 0, max_B = 0, max_L = 0, Lp = 0, Bp_max = 0;
+    int qd = 0, kvd = 0, qkv_ld = 0, nsb_h = 0, nsb_f = 0, nsb_q = 0, nrt_vocab = 0;
+    int num_sms = 0;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    // device memory
+    uint8_t *wbuf = nullptr;
+    size_t wbytes = 0;
+    uint8_t *embed = nullptr;
+    float *final_norm = nullptr;
+    std::vector<LayerW> L;
+    KvArena arena{};
+    size_t arena_bytes = 0;
+    std::vector<void *> arena_allocs;
+    float2 *rope = nullptr;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    float *x = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *logits = nullptr;
+    float *part = nullptr, *amax_v = nullptr;
+    int *amax_i = nullptr, *tickets = nullptr;
+    __half *x16 = nullptr;
+    uint2 *sx = nullptr;
+    int32_t *tok_dev = nullptr, *pos_dev = nullptr, *ids_dev = nullptr, *len_dev = nullptr;
+    uint32_t *status = nullptr;
+    int32_t *pinned_io = nullptr;      // [2*max_B] staging of host tokens/positions
+    // host state
+    std::vector<int> len_host;
+    int gemm_impl = 0, matvec_max_B = 0;
+    std::map<std::tuple<int, const void *, int>, cudaGraphExec_t> graphs;
+    std::string err;
+    int last_kernels = 0, last_splits = 0;
+    // instrumentation of the next/current eager step
+    std::vector<Launch> *prof = nullptr;
+    float *capture_dev_host = nullptr;   // pinned [L+1][B][H] while a capture is armed
+    float *capture_user = nullptr;       // [B][L+1][H]
+};
+
+static zdec_status fail(zdec_ctx *c, zdec_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c) c->err = buf;
+    else g_global_error = buf;
+    return s;
+}
+
+#define CK(call)                                                                              \
+    do {                                                                                      \
+        cudaError_t e_ = (call);                                                              \
+        if (e_ != cudaSuccess)                                                                \
+            return fail(ctx, ZDEC_ERR_CUDA, "%s failed: %s (%s:%d)", #call,                   \
+                        cudaGetErrorString(e_), __FILE__, __LINE__);                          \
+    } while (0)
+
+// ---------------------------------------------------------------- create ---
+static zdec_status validate_desc(const zdec_model_desc *d) {
+    zdec_ctx *ctx = nullptr;
+    if (d->n_layers < 1 || d->hidden < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->vocab < 1 ||
+        d->ffn < 1)
+        return fail(ctx, ZDEC_ERR_ARG, "model dimensions must be positive");
+    if (d->head_dim != HD)
+        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "head_dim %d unsupported (kernels implement %d)", d->head_dim, HD);
+    if (d->n_q_heads != GROUP * d->n_kv_heads)
+        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "n_q_heads must be %d * n_kv_heads", GROUP);
+    if (d->hidden % 512 || d->ffn % 512 || (d->n_q_heads * d->head_dim) % 512)
+        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "hidden, ffn and n_q_heads*head_dim must be multiples of 512");
+    if (!(d->rms_eps >= 0.0f) || !(d->rope_theta > 0.0f))
+        return fail(ctx, ZDEC_ERR_ARG, "rms_eps must be >= 0 and rope_theta > 0");
+    return ZDEC_OK;
+}
+
+static void free_ctx(zdec_ctx *ctx) {
+    if (!ctx) return;
+    for (auto &kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
+    cudaFree(ctx->wbuf);
+    for (void *p : ctx->arena_allocs) cudaFree(p);
+    cudaFree(ctx->rope);
+    cudaFree(ctx->ws);
+    cudaFreeHost(ctx->pinned_io);
+    cudaFreeHost(ctx->capture_dev_host);
+    if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
+    delete ctx;
+}
+
+static zdec_status upload_weights(zdec_ctx *ctx, const zdec_weights *w) {
+    const zdec_model_desc &d = ctx->d;
+    const int H = d.hidden, F = d.ffn;
+    const size_t canon_row_h = (size_t)ctx->nsb_h * CANON_BLOCK;
+    const size_t canon_row_f = (size_t)ctx->nsb_f * CANON_BLOCK;
+    const size_t canon_row_q = (size_t)ctx->nsb_q * CANON_BLOCK;
+    size_t stage_bytes = std::max({(size_t)d.vocab * canon_row_h, (size_t)(ctx->qd + 2 * ctx->kvd) * canon_row_h,
+                                   (size_t)2 * F * canon_row_h, (size_t)H * canon_row_f,
+                                   (size_t)H * canon_row_q});
+    uint8_t *stage = nullptr;
+    if (cudaMalloc(&stage, stage_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ctx, ZDEC_ERR_OOM, "cannot allocate %zu bytes of upload staging", stage_bytes);
+    }
+    auto done = [&](zdec_status s) { cudaFree(stage); return s; };
+    auto up = [&](const void *src, size_t off, size_t bytes) -> cudaError_t {
+        return cudaMemcpyAsync(stage + off, src, bytes, cudaMemcpyHostToDevice, ctx->stream);
+    };
+    cudaError_t e;
+    // tied embedding / LM head
+    if ((e = up(w->embed, 0, (size_t)d.vocab * canon_row_h)) != cudaSuccess ||
+        (e = launch_repack(stage, nullptr, 0, d.vocab, ctx->nrt_vocab, ctx->nsb_h, ctx->embed, ctx->stream)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(ctx->stream)) != cudaSuccess)
+        return done(fail(ctx, ZDEC_ERR_CUDA, "embedding upload: %s", cudaGetErrorString(e)));
+    if ((e = cudaMemcpy(ctx->final_norm, w->final_norm, H * sizeof(float), cudaMemcpyHostToDevice)) != cudaSuccess)
+        return done(fail(ctx, ZDEC_ERR_CUDA, "final norm upload: %s", cudaGetErrorString(e)));
+    for (int l = 0; l < d.n_layers; l++) {
+        LayerW &lw = ctx->L[l];
+        size_t qb = (size_t)ctx->qd * canon_row_h, kb = (size_t)ctx->kvd * canon_row_h;
+        bool ok = (e = up(w->wq[l], 0, qb)) == cudaSuccess && (e = up(w->wk[l], qb, kb)) == cudaSuccess &&
+                  (e = up(w->wv[l], qb + kb, kb)) == cudaSuccess &&
+                  (e = launch_repack(stage, nullptr, 0, ctx->qd + 2 * ctx->kvd, (ctx->qd + 2 * ctx->kvd) / 16,
+                                     ctx->nsb_h, lw.qkv, ctx->stream)) == cudaSuccess &&
+                  (e = cudaStreamSynchronize(ctx->stream)) == cudaSuccess;
+        ok = ok && (e = up(w->wo[l], 0, (size_t)H * canon_row_q)) == cudaSuccess &&
+             (e = launch_repack(stage, nullptr, 0, H, H / 16, ctx->nsb_q, lw.o, ctx->stream)) == cudaSuccess &&
+             (e = cudaStreamSynchronize(ctx->stream)) == cudaSuccess;
+        size_t gb = (size_t)F * canon_row_h;
+        ok = ok && (e = up(w->w_gate[l], 0, gb)) == cudaSuccess && (e = up(w->w_up[l], gb, gb)) == cudaSuccess &&
+             (e = launch_repack(stage, stage + gb, 1, F, F / 8, ctx->nsb_h, lw.gu, ctx->stream)) == cudaSuccess &&
+             (e = cudaStreamSynchronize(ctx->stream)) == cudaSuccess;
+        ok = ok && (e = up(w->w_down[l], 0, (size_t)H * canon_row_f)) == cudaSuccess &&
+             (e = launch_repack(stage, nullptr, 0, H, H / 16, ctx->nsb_f, lw.down, ctx->stream)) == cudaSuccess &&
+             (e = cudaStreamSynchronize(ctx->stream)) == cudaSuccess;
+        ok = ok && (e = cudaMemcpy(lw.attn_norm, w->attn_norm[l], H * sizeof(float), cudaMemcpyHostToDevice)) == cudaSuccess &&
+             (e = cudaMemcpy(lw.ffn_norm, w->ffn_norm[l], H * sizeof(float), cudaMemcpyHostToDevice)) == cudaSuccess;
+        if (!ok) return done(fail(ctx, ZDEC_ERR_CUDA, "layer %d upload: %s", l, cudaGetErrorString(e)));
+    }
+    return done(ZDEC_OK);
+}
+
+extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights,
+                                   zdec_kv_dtype kv_dtype, int max_B, int max_L, void *cuda_stream,
+                                   zdec_ctx **out) {
+    zdec_ctx *ctx = nullptr;
+    if (!desc || !weights || !out) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    *out = nullptr;
+    zdec_status vs = validate_desc(desc);
+    if (vs != ZDEC_OK) return vs;
+    if (kv_dtype != ZDEC_KV_F16 && kv_dtype != ZDEC_KV_Q8_0) return fail(ctx, ZDEC_ERR_ARG, "bad kv_dtype");
+    if (max_B < 1 || max_B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "max_B must be in [1, %d]", MAX_B);
+    if (max_L < 1) return fail(ctx, ZDEC_ERR_ARG, "max_L must be >= 1");
+    if (!weights->embed || !weights->final_norm || !weights->attn_norm || !weights->ffn_norm ||
+        !weights->wq || !weights->wk || !weights->wv || !weights->wo || !weights->w_gate ||
+        !weights->w_up || !weights->w_down)
+        return fail(ctx, ZDEC_ERR_ARG, "null weight pointer");
+
+    ctx = new zdec_ctx();
+    ctx->d = *desc;
+    const zdec_model_desc &d = ctx->d;
+    ctx->kv_dtype = kv_dtype;
+    ctx->max_B = max_B;
+    ctx->max_L = max_L;
+    ctx->Lp = (int)align_up((size_t)max_L, ATT_CHUNK);
+    ctx->Bp_max = (int)align_up((size_t)max_B, 8);
+    ctx->qd = d.n_q_heads * d.head_dim;
+    ctx->kvd = d.n_kv_heads * d.head_dim;
+    ctx->qkv_ld = ctx->qd + 2 * ctx->kvd;
+    ctx->nsb_h = d.hidden / QK;
+    ctx->nsb_f = d.ffn / QK;
+    ctx->nsb_q = ctx->qd / QK;
+    ctx->nrt_vocab = (d.vocab + 15) / 16;
+    ctx->L.resize(d.n_layers);
+    ctx->len_host.assign(max_B, 0);
+    if (const char *e = getenv("ZDEC_MATVEC_MAX_B")) ctx->matvec_max_B = std::max(0, std::min(4, atoi(e)));
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev);
+
+    auto bail = [&](zdec_status s) { free_ctx(ctx); return s; };
+    if (cuda_stream) ctx->stream = (cudaStream_t)cuda_stream;
+    else {
+        if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess)
+            return bail(fail(nullptr, ZDEC_ERR_CUDA, "cudaStreamCreate failed"));
+        ctx->own_stream = true;
+    }
+    // ---- weights: one allocation, 256-byte aligned sub-buffers
+    const int H = d.hidden, F = d.ffn, NL = d.n_layers;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    size_t o_embed = take(tile_bytes(ctx->nrt_vocab, ctx->nsb_h));
+    size_t o_fn = take(H * sizeof(float));
+    std::vector<size_t> oq(NL), oo(NL), og(NL), od(NL), on1(NL), on2(NL);
+    for (int l = 0; l < NL; l++) {
+        oq[l] = take(tile_bytes((ctx->qd + 2 * ctx->kvd) / 16, ctx->nsb_h));
+        oo[l] = take(tile_bytes(H / 16, ctx->nsb_q));
+        og[l] = take(tile_bytes(F / 8, ctx->nsb_h));
+        od[l] = take(tile_bytes(H / 16, ctx->nsb_f));
+        on1[l] = take(H * sizeof(float));
+        on2[l] = take(H * sizeof(float));
+    }
+    ctx->wbytes = off;
+    if (cudaMalloc(&ctx->wbuf, ctx->wbytes) != cudaSuccess) {
+        cudaGetLastError();
+        return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate %zu bytes of weights", ctx->wbytes));
+    }
+    ctx->embed = ctx->wbuf + o_embed;
+    ctx->final_norm = reinterpret_cast<float *>(ctx->wbuf + o_fn);
+    for (int l = 0; l < NL; l++)
+        ctx->L[l] = {ctx->wbuf + oq[l], ctx->wbuf + oo[l], ctx->wbuf + og[l], ctx->wbuf + od[l],
+                     reinterpret_cast<float *>(ctx->wbuf + on1[l]), reinterpret_cast<float *>(ctx->wbuf + on2[l])};
+
+    // ---- KV arena
+    KvArena &a = ctx->arena;
+    a.kv_dtype = kv_dtype;
+    a.n_layers = NL;
+    a.n_kv = d.n_kv_heads;
+    a.Lp = ctx->Lp;
+    size_t planes = (size_t)max_B * NL * d.n_kv_heads;
+    size_t kb = planes * ctx->Lp * HD * (kv_dtype ? 1 : 2);
+    std::vector<std::pair<uint8_t **, size_t>> want = {{&a.k, kb}, {&a.v, kb}};
+    if (kv_dtype) {
+        want.push_back({&a.ks, planes * ctx->Lp * 4 * 2});
+        want.push_back({&a.vs, planes * ctx->Lp * 4 * 2});
+    }
+    for (auto &w : want) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, w.second) != cudaSuccess) {
+            cudaGetLastError();
+            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate the KV arena (%zu bytes for max_B=%d, max_L=%d)",
+                             w.second, max_B, max_L));
+        }
+        ctx->arena_allocs.push_back(p);
+        *w.first = (uint8_t *)p;
+        ctx->arena_bytes += w.second;
+        if (cudaMemsetAsync(p, 0, w.second, ctx->stream) != cudaSuccess)
+            return bail(fail(nullptr, ZDEC_ERR_CUDA, "arena memset failed"));
+    }
+
+    // ---- RoPE table [max_L][64] (cos, sin), angles in double
+    {
+        std::vector<float2> tab((size_t)max_L * (HD / 2));
+        std::vector<double> inv(HD / 2);
+        for (int i = 0; i < HD / 2; i++) inv[i] = std::pow((double)d.rope_theta, -2.0 * i / HD);
+        for (int t = 0; t < max_L; t++)
+            for (int i = 0; i < HD / 2; i++) {
+                double ang = (double)t * inv[i];
+                tab[(size_t)t * (HD / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+        if (cudaMalloc(&ctx->rope, tab.size() * sizeof(float2)) != cudaSuccess ||
+            cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate the RoPE table"));
+        }
+    }
+
+    // ---- workspace
+    {
+        const int Bm = max_B, Bp = ctx->Bp_max;
+        const int Kmax = std::max({H, F, ctx->qd});
+        int lm_grid = (ctx->nrt_vocab + 7) / 8;
+        size_t w = 0;
+        auto t = [&](size_t bytes) { size_t o = w; w = align_up(w + bytes, 256); return o; };
+        size_t ox = t((size_t)Bm * H * 4), oqkv = t((size_t)Bm * ctx->qkv_ld * 4), oo2 = t((size_t)Bm * ctx->qd * 4);
+        size_t oact = t((size_t)Bm * F * 4), olog = t((size_t)Bm * d.vocab * 4);
+        size_t opart = t((size_t)Bm * d.n_kv_heads * 64 * 4 * (HD + 2) * 4);
+        size_t oav = t((size_t)lm_grid * MAX_B * 4), oai = t((size_t)lm_grid * MAX_B * 4);
+        size_t otk = t((size_t)Bm * d.n_kv_heads * 4);
+        size_t ox16 = t((size_t)Bp * Kmax * 2), osx = t((size_t)Bp * (Kmax / QK) * 4 * 8);
+        size_t otok = t(Bm * 4), opos = t(Bm * 4), oids = t(Bm * 4), olen = t(Bm * 4), ost = t(4);
+        ctx->ws_bytes = w;
+        if (cudaMalloc(&ctx->ws, w) != cudaSuccess) {
+            cudaGetLastError();
+            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate %zu bytes of workspace", w));
+        }
+        uint8_t *b = (uint8_t *)ctx->ws;
+        ctx->x = (float *)(b + ox); ctx->qkv = (float *)(b + oqkv); ctx->o = (float *)(b + oo2);
+        ctx->act = (float *)(b + oact); ctx->logits = (float *)(b + olog); ctx->part = (float *)(b + opart);
+        ctx->amax_v = (float *)(b + oav); ctx->amax_i = (int *)(b + oai); ctx->tickets = (int *)(b + otk);
+        ctx->x16 = (__half *)(b + ox16); ctx->sx = (uint2 *)(b + osx);
+        ctx->tok_dev = (int32_t *)(b + otok); ctx->pos_dev = (int32_t *)(b + opos);
+        ctx->ids_dev = (int32_t *)(b + oids); ctx->len_dev = (int32_t *)(b + olen);
+        ctx->status = (uint32_t *)(b + ost);
+        if (cudaMemsetAsync(ctx->ws, 0, w, ctx->stream) != cudaSuccess)
+            return bail(fail(nullptr, ZDEC_ERR_CUDA, "workspace memset failed"));
+        if (cudaMallocHost(&ctx->pinned_io, 2 * Bm * sizeof(int32_t)) != cudaSuccess)
+            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate pinned staging"));
+    }
+    if (attention_setup(kv_dtype) != cudaSuccess)
+        return bail(fail(nullptr, ZDEC_ERR_CUDA, "attention smem attribute failed"));
+
+    zdec_status us = upload_weights(ctx, weights);
+    if (us != ZDEC_OK) {
+        g_global_error = ctx->err;
+        return bail(us);
+    }
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess)
+        return bail(fail(nullptr, ZDEC_ERR_CUDA, "create: %s", cudaGetErrorString(cudaGetLastError())));
+    *out = ctx;
+    return ZDEC_OK;
+}
+
+extern "C" void zdec_destroy(zdec_ctx *ctx) {
+    if (!ctx) return;
+    cudaStreamSynchronize(ctx->stream);
+    free_ctx(ctx);
+}
+
+extern "C" const char *zdec_last_error(const zdec_ctx *ctx) { return ctx ? ctx->err.c_str() : g_global_error.c_str(); }
+extern "C" const char *zdec_last_global_error(void) { return g_global_error.c_str(); }
+
+// ------------------------------------------------------------- append ---
+extern "C" zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f16,
+                                      const void *v_f16, int on_device) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (seq < 0 || seq >= ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "seq %d out of range", seq);
+    if (n_tokens < 0 || (n_tokens > 0 && (!k_f16 || !v_f16))) return fail(ctx, ZDEC_ERR_ARG, "bad tokens/pointers");
+    if ((long)ctx->len_host[seq] + n_tokens > ctx->max_L)
+        return fail(ctx, ZDEC_ERR_CAPACITY, "sequence %d: %d + %d tokens exceed max_L %d", seq,
+                    ctx->len_host[seq], n_tokens, ctx->max_L);
+    if (n_tokens == 0) return ZDEC_OK;
+    const zdec_model_desc &d = ctx->d;
+    size_t bytes = (size_t)d.n_layers * n_tokens * d.n_kv_heads * HD * 2;
+    const uint16_t *kd = (const uint16_t *)k_f16, *vd = (const uint16_t *)v_f16;
+    void *tmp = nullptr;
+    if (!on_device) {
+        if (cudaMalloc(&tmp, 2 * bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, ZDEC_ERR_OOM, "cannot stage %zu bytes of KV", 2 * bytes);
+        }
+        CK(cudaMemcpyAsync(tmp, k_f16, bytes, cudaMemcpyHostToDevice, ctx->stream));
+        CK(cudaMemcpyAsync((uint8_t *)tmp + bytes, v_f16, bytes, cudaMemcpyHostToDevice, ctx->stream));
+        kd = (const uint16_t *)tmp;
+        vd = (const uint16_t *)((uint8_t *)tmp + bytes);
+    }
+    int t0 = ctx->len_host[seq];
+    cudaError_t e = launch_kv_append(ctx->arena, seq, t0, n_tokens, kd, vd, ctx->stream);
+    int32_t newlen = t0 + n_tokens;
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ctx->len_dev + seq, &newlen, 4, cudaMemcpyHostToDevice, ctx->stream);
+    if (!on_device) {
+        cudaError_t e2 = cudaStreamSynchronize(ctx->stream);
+        cudaFree(tmp);
+        if (e == cudaSuccess) e = e2;
+    } else if (e == cudaSuccess) {
+        e = cudaStreamSynchronize(ctx->stream);   // the host length source is read asynchronously
+    }
+    if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "append_kv: %s", cudaGetErrorString(e));
+    ctx->len_host[seq] = newlen;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_reset_seq(zdec_ctx *ctx, int seq) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (seq < 0 || seq >= ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "seq %d out of range", seq);
+    int32_t zero = 0;
+    CK(cudaMemcpyAsync(ctx->len_dev + seq, &zero, 4, cudaMemcpyHostToDevice, ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+    ctx->len_host[seq] = 0;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
+    if (!ctx || !len) return fail(nullptr, ZDEC_ERR_ARG, "null argument");
+    if (seq < 0 || seq >= ctx->max_B) return ZDEC_ERR_ARG;
+    *len = ctx->len_host[seq];
+    return ZDEC_OK;
+}
+
+// --------------------------------------------------------------- step ---
+static int attn_splits(const zdec_ctx *ctx, int B) {
+    int per = B * ctx->d.n_kv_heads;
+    int s = (4 * ctx->num_sms + per - 1) / per;
+    return std::max(1, std::min(64, s));
+}
+
+static int pick_impl(const zdec_ctx *ctx, int B) {
+    if (B > 4) return 2;
+    if (ctx->gemm_impl == 1) return 1;
+    if (ctx->gemm_impl == 2) return 2;
+    return B <= ctx->matvec_max_B ? 1 : 2;
+}
+
+// Enqueue the whole step for rows 0..B-1.  logits_out may be null.
+static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pdl) {
+    const zdec_model_desc &d = ctx->d;
+    const int H = d.hidden, F = d.ffn, Bp = (int)align_up((size_t)B, 8);
+    const int impl = pick_impl(ctx, B);
+    cudaStream_t s = ctx->stream;
+    int nk = 0;
+    cudaError_t e;
+    auto mark = [&](int kind, bool begin) {
+        if (!ctx->prof) return;
+        if (begin) {
+            Launch L{kind, nullptr, nullptr};
+            cudaEventCreate(&L.t0);
+            cudaEventCreate(&L.t1);
+            cudaEventRecord(L.t0, s);
+            ctx->prof->push_back(L);
+        } else {
+            cudaEventRecord(ctx->prof->back().t1, s);
+        }
+    };
+    auto capture_x = [&](int slot) -> cudaError_t {
+        if (!ctx->capture_dev_host) return cudaSuccess;
+        return cudaMemcpyAsync(ctx->capture_dev_host + (size_t)slot * B * H, ctx->x, (size_t)B * H * 4,
+                               cudaMemcpyDeviceToHost, s);
+    };
+#define STEP(kind, call)                 \
+    do {                                 \
+        mark(kind, true);                \
+        if ((e = (call)) != cudaSuccess) \
+            return e;                    \
+        mark(kind, false);               \
+        nk++;                            \
+    } while (0)
+
+    STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev,
+                                         ctx->len_dev, ctx->status, B, ctx->x, H, pdl, s));
+    if ((e = capture_x(0)) != cudaSuccess) return e;
+    GemmParams gp{};
+    gp.x16 = ctx->x16;
+    gp.sx = ctx->sx;
+    gp.B = B;
+    AttnParams ap{};
+    ap.kv = ctx->arena;
+    ap.nq = d.n_q_heads;
+    ap.positions = ctx->pos_dev;
+    ap.qkv = ctx->qkv;
+    ap.qkv_ld = ctx->qkv_ld;
+    ap.rope = ctx->rope;
+    ap.append = 1;
+    ap.S = attn_splits(ctx, B);
+    ap.part = ctx->part;
+    ap.tickets = ctx->tickets;
+    ap.o = ctx->o;
+    ap.B = B;
+    ap.max_L = ctx->max_L;
+    for (int l = 0; l < d.n_layers; l++) {
+        const LayerW &lw = ctx->L[l];
+        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->x, H, H, lw.attn_norm, d.rms_eps, B, Bp, ctx->x16, ctx->sx, pdl, s));
+        gp.W = lw.qkv; gp.N = ctx->qkv_ld; gp.nrt = ctx->qkv_ld / 16; gp.nsb = ctx->nsb_h;
+        gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld; gp.rt_per_cta = 2; gp.ksplit = 4;
+        STEP(ZDEC_KERNEL_GEMM_QKV, launch_gemm(gp, EPI_STORE, impl, pdl, s));
+        ap.layer = l;
+        STEP(ZDEC_KERNEL_ATTENTION, launch_attention(ap, pdl, s));
+        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->o, ctx->qd, ctx->qd, nullptr, 0.0f, B, Bp, ctx->x16, ctx->sx, pdl, s));
+        gp.W = lw.o; gp.N = H; gp.nrt = H / 16; gp.nsb = ctx->nsb_q;
+        gp.out = ctx->x; gp.ldo = H; gp.rt_per_cta = 1; gp.ksplit = 8;
+        STEP(ZDEC_KERNEL_GEMM_O, launch_gemm(gp, EPI_RESID, impl, pdl, s));
+        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->x, H, H, lw.ffn_norm, d.rms_eps, B, Bp, ctx->x16, ctx->sx, pdl, s));
+        gp.W = lw.gu; gp.N = F; gp.nrt = F / 8; gp.nsb = ctx->nsb_h;
+        gp.out = ctx->act; gp.ldo = F; gp.rt_per_cta = 4; gp.ksplit = 2;
+        STEP(ZDEC_KERNEL_GEMM_GATEUP, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s));
+        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->act, F, F, nullptr, 0.0f, B, Bp, ctx->x16, ctx->sx, pdl, s));
+        gp.W = lw.down; gp.N = H; gp.nrt = H / 16; gp.nsb = ctx->nsb_f;
+        gp.out = ctx->x; gp.ldo = H; gp.rt_per_cta = 1; gp.ksplit = 8;
+        STEP(ZDEC_KERNEL_GEMM_DOWN, launch_gemm(gp, EPI_RESID, impl, pdl, s));
+        if ((e = capture_x(l + 1)) != cudaSuccess) return e;
+    }
+    STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->x, H, H, ctx->final_norm, d.rms_eps, B, Bp, ctx->x16, ctx->sx, pdl, s));
+    gp.W = ctx->embed; gp.N = d.vocab; gp.nrt = ctx->nrt_vocab; gp.nsb = ctx->nsb_h;
+    gp.out = logits_out; gp.ldo = d.vocab; gp.rt_per_cta = 8; gp.ksplit = 1;
+    gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
+    STEP(ZDEC_KERNEL_GEMM_LMHEAD, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s));
+    STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, gemm_grid(gp), B, ctx->ids_dev,
+                                                 ctx->pos_dev, ctx->len_dev, pdl, s));
+#undef STEP
+    ctx->last_kernels = nk;
+    ctx->last_splits = ap.S;
+    return cudaSuccess;
+}
+
+static zdec_status check_step_args(zdec_ctx *ctx, int B, const int32_t *tokens, const int32_t *positions,
+                                   int32_t *ids) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (B < 1 || B > ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "B=%d outside [1, %d]", B, ctx->max_B);
+    if (!tokens || !positions || !ids) return fail(ctx, ZDEC_ERR_ARG, "null tokens/positions/ids");
+    for (int b = 0; b < B; b++)
+        if (ctx->len_host[b] + 1 > ctx->max_L)
+            return fail(ctx, ZDEC_ERR_CAPACITY, "sequence %d is full (%d tokens)", b, ctx->max_L);
+    return ZDEC_OK;
+}
+
+// Stage inputs: host pointers are validated and copied through pinned memory.
+static zdec_status stage_inputs(zdec_ctx *ctx, int B, const int32_t *tokens, const int32_t *positions, bool host) {
+    if (host) {
+        for (int b = 0; b < B; b++) {
+            if (positions[b] != ctx->len_host[b])
+                return fail(ctx, ZDEC_ERR_POSITION, "positions[%d] = %d but sequence %d holds %d tokens", b,
+                            positions[b], b, ctx->len_host[b]);
+            if (tokens[b] < 0 || tokens[b] >= ctx->d.vocab)
+                return fail(ctx, ZDEC_ERR_ARG, "tokens[%d] = %d outside the vocabulary", b, tokens[b]);
+        }
+        CK(cudaStreamSynchronize(ctx->stream));   // the pinned staging may still be in flight
+        memcpy(ctx->pinned_io, tokens, B * 4);
+        memcpy(ctx->pinned_io + ctx->max_B, positions, B * 4);
+        CK(cudaMemcpyAsync(ctx->tok_dev, ctx->pinned_io, B * 4, cudaMemcpyHostToDevice, ctx->stream));
+        CK(cudaMemcpyAsync(ctx->pos_dev, ctx->pinned_io + ctx->max_B, B * 4, cudaMemcpyHostToDevice, ctx->stream));
+    } else {
+        CK(cudaMemcpyAsync(ctx->tok_dev, tokens, B * 4, cudaMemcpyDeviceToDevice, ctx->stream));
+        CK(cudaMemcpyAsync(ctx->pos_dev, positions, B * 4, cudaMemcpyDeviceToDevice, ctx->stream));
+    }
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tokens,
+                                        const int32_t *positions, float *logits, int32_t *ids, int flags) {
+    zdec_status st = check_step_args(ctx, B, tokens, positions, ids);
+    if (st != ZDEC_OK) return st;
+    const bool host = flags & ZDEC_STEP_HOST_IO;
+    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host;
+    st = stage_inputs(ctx, B, tokens, positions, host);
+    if (st != ZDEC_OK) return st;
+    float *lg = host ? (logits ? ctx->logits : nullptr) : logits;
+    const int impl = pick_impl(ctx, B);
+    if (eager) {
+        CK(enqueue_step(ctx, B, lg, true));
+    } else {
+        auto key = std::make_tuple(B, (const void *)lg, impl);
+        auto it = ctx->graphs.find(key);
+        if (it == ctx->graphs.end()) {
+            cudaGraph_t graph;
+            CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+            cudaError_t e = enqueue_step(ctx, B, lg, true);
+            cudaError_t e2 = cudaStreamEndCapture(ctx->stream, &graph);
+            if (e != cudaSuccess || e2 != cudaSuccess) {
+                if (e2 == cudaSuccess) cudaGraphDestroy(graph);
+                return fail(ctx, ZDEC_ERR_CUDA, "step capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
+            }
+            cudaGraphExec_t exec;
+            cudaError_t e3 = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (e3 != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e3));
+            it = ctx->graphs.emplace(key, exec).first;
+        }
+        CK(cudaGraphLaunch(it->second, ctx->stream));
+    }
+    if (host) {
+        if (logits)
+            CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)B * ctx->d.vocab * 4, cudaMemcpyDeviceToHost, ctx->stream));
+        CK(cudaMemcpyAsync(ids, ctx->ids_dev, B * 4, cudaMemcpyDeviceToHost, ctx->stream));
+    } else {
+        CK(cudaMemcpyAsync(ids, ctx->ids_dev, B * 4, cudaMemcpyDeviceToDevice, ctx->stream));
+    }
+    for (int b = 0; b < B; b++) ctx->len_host[b]++;
+    if (ctx->capture_dev_host) {   // armed hidden-state capture: wait and reorder
+        cudaError_t e = cudaStreamSynchronize(ctx->stream);
+        const int H = ctx->d.hidden, NL1 = ctx->d.n_layers + 1;
+        if (e == cudaSuccess)
+            for (int b = 0; b < B; b++)
+                for (int l = 0; l < NL1; l++)
+                    memcpy(ctx->capture_user + ((size_t)b * NL1 + l) * H,
+                           ctx->capture_dev_host + ((size_t)l * B + b) * H, (size_t)H * sizeof(float));
+        cudaFreeHost(ctx->capture_dev_host);
+        ctx->capture_dev_host = nullptr;
+        ctx->capture_user = nullptr;
+        if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "captured step: %s", cudaGetErrorString(e));
+    }
+    if (host) return zdec_sync(ctx);
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_sync(zdec_ctx *ctx) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    CK(cudaStreamSynchronize(ctx->stream));
+    uint32_t st = 0;
+    CK(cudaMemcpy(&st, ctx->status, 4, cudaMemcpyDeviceToHost));
+    if (st) {
+        uint32_t zero = 0;
+        CK(cudaMemcpy(ctx->status, &zero, 4, cudaMemcpyHostToDevice));
+        if (st & STATUS_TIMEOUT) return fail(ctx, ZDEC_ERR_TIMEOUT, "a bounded device wait gave up");
+        return fail(ctx, ZDEC_ERR_DEVICE, "device check failed (status 0x%x:%s%s)", st,
+                    (st & STATUS_POSITION) ? " position != cached length" : "",
+                    (st & STATUS_TOKEN) ? " token outside the vocabulary" : "");
+    }
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (impl < 0 || impl > 2) return fail(ctx, ZDEC_ERR_ARG, "impl must be 0, 1 or 2");
+    ctx->gemm_impl = impl;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info) {
+    if (!ctx || !info) return fail(nullptr, ZDEC_ERR_ARG, "null argument");
+    info->weight_bytes = ctx->wbytes;
+    info->arena_bytes = ctx->arena_bytes;
+    info->workspace_bytes = ctx->ws_bytes;
+    info->kv_bytes_per_token = (size_t)ctx->d.n_layers * ctx->d.n_kv_heads * HD * 2 * (ctx->kv_dtype ? 1 : 2) +
+                               (ctx->kv_dtype ? (size_t)ctx->d.n_layers * ctx->d.n_kv_heads * 4 * 2 * 2 : 0);
+    info->kernels_per_step = ctx->last_kernels;
+    info->attn_splits = ctx->last_splits;
+    info->matvec_max_B = ctx->matvec_max_B;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *tokens_dev,
+                                         const int32_t *positions_dev, float *logits_dev, int32_t *ids_dev,
+                                         int *kind, float *ms, int cap, int *n) {
+    zdec_status st = check_step_args(ctx, B, tokens_dev, positions_dev, ids_dev);
+    if (st != ZDEC_OK) return st;
+    if (!n || (cap > 0 && (!kind || !ms))) return fail(ctx, ZDEC_ERR_ARG, "null output");
+    st = stage_inputs(ctx, B, tokens_dev, positions_dev, false);
+    if (st != ZDEC_OK) return st;
+    std::vector<Launch> launches;
+    ctx->prof = &launches;
+    cudaError_t e = enqueue_step(ctx, B, logits_dev, false);
+    ctx->prof = nullptr;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ids_dev, ctx->ids_dev, B * 4, cudaMemcpyDeviceToDevice, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    for (size_t i = 0; i < launches.size(); i++) {
+        float t = 0.0f;
+        if (e == cudaSuccess) cudaEventElapsedTime(&t, launches[i].t0, launches[i].t1);
+        if ((int)i < cap) { kind[i] = launches[i].kind; ms[i] = t; }
+        cudaEventDestroy(launches[i].t0);
+        cudaEventDestroy(launches[i].t1);
+    }
+    *n = (int)launches.size();
+    if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "profile step: %s", cudaGetErrorString(e));
+    for (int b = 0; b < B; b++) ctx->len_host[b]++;
+    return zdec_sync(ctx);
+}
+
+// -------------------------------------------------------------- debug ---
+static zdec_status tensor_info(zdec_ctx *ctx, int which, int layer, const uint8_t *&tiles, int &row_map,
+                               int &row_off, int &rows, int &nsb) {
+    const zdec_model_desc &d = ctx->d;
+    if (which != ZDEC_T_EMBED && (layer < 0 || layer >= d.n_layers)) return fail(ctx, ZDEC_ERR_ARG, "bad layer");
+    row_map = 0;
+    row_off = 0;
+    switch (which) {
+        case ZDEC_T_EMBED: tiles = ctx->embed; rows = d.vocab; nsb = ctx->nsb_h; break;
+        case ZDEC_T_WQ: tiles = ctx->L[layer].qkv; rows = ctx->qd; nsb = ctx->nsb_h; break;
+        case ZDEC_T_WK: tiles = ctx->L[layer].qkv; row_off = ctx->qd; rows = ctx->kvd; nsb = ctx->nsb_h; break;
+        case ZDEC_T_WV: tiles = ctx->L[layer].qkv; row_off = ctx->qd + ctx->kvd; rows = ctx->kvd; nsb = ctx->nsb_h; break;
+        case ZDEC_T_WO: tiles = ctx->L[layer].o; rows = d.hidden; nsb = ctx->nsb_q; break;
+        case ZDEC_T_GATE: tiles = ctx->L[layer].gu; row_map = 1; rows = d.ffn; nsb = ctx->nsb_h; break;
+        case ZDEC_T_UP: tiles = ctx->L[layer].gu; row_map = 2; rows = d.ffn; nsb = ctx->nsb_h; break;
+        case ZDEC_T_DOWN: tiles = ctx->L[layer].down; rows = d.hidden; nsb = ctx->nsb_f; break;
+        default: return fail(ctx, ZDEC_ERR_ARG, "bad tensor id %d", which);
+    }
+    return ZDEC_OK;
+}
+
+template <typename P, typename F>
+static zdec_status debug_rows(zdec_ctx *ctx, int which, int layer, int row0, int nrows, void *out, P per_row,
+                              F launch) {
+    if (!ctx || !out) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    const uint8_t *tiles;
+    int row_map, row_off, rows, nsb;
+    zdec_status st = tensor_info(ctx, which, layer, tiles, row_map, row_off, rows, nsb);
+    if (st != ZDEC_OK) return st;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > rows) return fail(ctx, ZDEC_ERR_ARG, "rows out of range");
+    if (nrows == 0) return ZDEC_OK;
+    void *dbuf = nullptr;
+    size_t bytes = (size_t)nrows * per_row(nsb);
+    if (cudaMalloc(&dbuf, bytes) != cudaSuccess) { cudaGetLastError(); return fail(ctx, ZDEC_ERR_OOM, "debug buffer"); }
+    cudaError_t e = launch(tiles, row_map, nsb, row_off + row0, nrows, dbuf);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out, dbuf, bytes, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    cudaFree(dbuf);
+    if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "debug read: %s", cudaGetErrorString(e));
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_debug_export_q4k(zdec_ctx *ctx, int which, int layer, int row0, int nrows, void *out_host) {
+    return debug_rows(ctx, which, layer, row0, nrows, out_host,
+                      [](int nsb) { return (size_t)nsb * CANON_BLOCK; },
+                      [&](const uint8_t *t, int rm, int nsb, int r0, int nr, void *dst) {
+                          return launch_export_canonical(t, rm, nsb, r0, nr, (uint8_t *)dst, ctx->stream);
+                      });
+}
+
+extern "C" zdec_status zdec_debug_dequant(zdec_ctx *ctx, int which, int layer, int row0, int nrows, float *out_host) {
+    return debug_rows(ctx, which, layer, row0, nrows, out_host,
+                      [](int nsb) { return (size_t)nsb * QK * sizeof(float); },
+                      [&](const uint8_t *t, int rm, int nsb, int r0, int nr, void *dst) {
+                          return launch_dequant_rows(t, rm, nsb, r0, nr, (float *)dst, ctx->stream);
+                      });
+}
+
+extern "C" zdec_status zdec_debug_read_kv(zdec_ctx *ctx, int seq, int layer, int t0, int n, void *k, void *v,
+                                          void *ks, void *vs) {
+    if (!ctx || !k || !v) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    if (ctx->kv_dtype && (!ks || !vs)) return fail(ctx, ZDEC_ERR_ARG, "Q8_0 read needs scale buffers");
+    if (seq < 0 || seq >= ctx->max_B || layer < 0 || layer >= ctx->d.n_layers || t0 < 0 || n < 0 ||
+        t0 + n > ctx->max_L)
+        return fail(ctx, ZDEC_ERR_ARG, "range out of bounds");
+    if (n == 0) return ZDEC_OK;
+    const int nkv = ctx->d.n_kv_heads;
+    size_t es = ctx->kv_dtype ? 1 : 2;
+    size_t kb = (size_t)n * nkv * HD * es, sb = ctx->kv_dtype ? (size_t)n * nkv * 4 * 2 : 0;
+    uint8_t *buf = nullptr;
+    if (cudaMalloc(&buf, 2 * kb + 2 * sb + 16) != cudaSuccess) { cudaGetLastError(); return fail(ctx, ZDEC_ERR_OOM, "debug buffer"); }
+    uint16_t *dks = sb ? (uint16_t *)(buf + 2 * kb) : nullptr, *dvs = sb ? (uint16_t *)(buf + 2 * kb + sb) : nullptr;
+    cudaError_t e = launch_kv_read(ctx->arena, seq, layer, t0, n, buf, buf + kb, dks, dvs, ctx->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(k, buf, kb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(v, buf + kb, kb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess && sb) e = cudaMemcpyAsync(ks, dks, sb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess && sb) e = cudaMemcpyAsync(vs, dvs, sb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    cudaFree(buf);
+    if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "kv read: %s", cudaGetErrorString(e));
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_debug_capture_hidden(zdec_ctx *ctx, float *out_host) {
+    if (!ctx || !out_host) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    if (!ctx->capture_dev_host) {
+        size_t bytes = (size_t)(ctx->d.n_layers + 1) * ctx->max_B * ctx->d.hidden * sizeof(float);
+        if (cudaMallocHost(&ctx->capture_dev_host, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, ZDEC_ERR_OOM, "cannot allocate %zu pinned bytes for the capture", bytes);
+        }
+    }
+    ctx->capture_user = out_host;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, const float *q_host,
+                                            const int32_t *positions_host, float *o_host) {
+    if (!ctx || !q_host || !positions_host || !o_host) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    if (B < 1 || B > ctx->max_B || layer < 0 || layer >= ctx->d.n_layers) return fail(ctx, ZDEC_ERR_ARG, "bad B/layer");
+    for (int b = 0; b < B; b++)
+        if (positions_host[b] < 0 || positions_host[b] >= ctx->len_host[b])
+            return fail(ctx, ZDEC_ERR_ARG, "position %d of row %d is not a cached token", positions_host[b], b);
+    const int qd = ctx->qd;
+    CK(cudaMemcpy2DAsync(ctx->qkv, ctx->qkv_ld * 4, q_host, qd * 4, qd * 4, B, cudaMemcpyHostToDevice, ctx->stream));
+    CK(cudaMemcpyAsync(ctx->pos_dev, positions_host, B * 4, cudaMemcpyHostToDevice, ctx->stream));
+    AttnParams ap{};
+    ap.kv = ctx->arena;
+    ap.layer = layer;
+    ap.nq = ctx->d.n_q_heads;
+    ap.positions = ctx->pos_dev;
+    ap.qkv = ctx->qkv;
+    ap.qkv_ld = ctx->qkv_ld;
+    ap.rope = ctx->rope;
+    ap.append = 0;
+    ap.S = attn_splits(ctx, B);
+    ap.part = ctx->part;
+    ap.tickets = ctx->tickets;
+    ap.o = ctx->o;
+    ap.B = B;
+    ap.max_L = ctx->max_L;
+    CK(launch_attention(ap, false, ctx->stream));
+    CK(cudaMemcpyAsync(o_host, ctx->o, (size_t)B * qd * 4, cudaMemcpyDeviceToHost, ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+    return ZDEC_OK;
+}
+
+// ---------------------------------------------------------- stateless ---
+extern "C" size_t zdec_q4k_repacked_bytes(int N, int K) {
+    if (N <= 0 || K <= 0 || N % 16 || K % QK) return 0;
+    return (size_t)N * (K / QK) * CANON_BLOCK;
+}
+
+extern "C" zdec_status zdec_q4k_repack(const void *canonical_dev, int N, int K, void *repacked_dev, void *stream) {
+    zdec_ctx *ctx = nullptr;
+    if (!canonical_dev || !repacked_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
+    if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
+    CK(launch_repack((const uint8_t *)canonical_dev, nullptr, 0, N, N / 16, K / QK, (uint8_t *)repacked_dev,
+                     (cudaStream_t)stream));
+    return ZDEC_OK;
+}
+
+extern "C" size_t zdec_q4k_gemm_workspace_bytes(int K, int B) {
+    if (K <= 0 || K % QK || B < 1 || B > MAX_B) return 0;
+    size_t Bp = align_up((size_t)B, 8);
+    return align_up(Bp * K * 2, 256) + Bp * (K / QK) * 4 * 8;
+}
+
+extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B, float *y_dev,
+                                     int impl, void *workspace_dev, size_t workspace_bytes, void *stream) {
+    zdec_ctx *ctx = nullptr;
+    if (!repacked_dev || !x_dev || !y_dev || !workspace_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
+    if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
+    if (B < 1 || B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "B must be in [1, %d]", MAX_B);
+    if (impl != 1 && impl != 2) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1 or 2");
+    if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
+    if (workspace_bytes < zdec_q4k_gemm_workspace_bytes(K, B)) return fail(ctx, ZDEC_ERR_ARG, "workspace too small");
+    if ((uintptr_t)workspace_dev % 16 || (uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "pointers must be 16-byte aligned");
+    size_t Bp = align_up((size_t)B, 8);
+    __half *x16 = (__half *)workspace_dev;
+    uint2 *sx = (uint2 *)((uint8_t *)workspace_dev + align_up(Bp * K * 2, 256));
+    cudaStream_t s = (cudaStream_t)stream;
+    CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, (int)Bp, x16, sx, false, s));
+    GemmParams gp{};
+    gp.W = (const uint8_t *)repacked_dev;
+    gp.N = N;
+    gp.nrt = N / 16;
+    gp.nsb = K / QK;
+    gp.x16 = x16;
+    gp.sx = sx;
+    gp.B = B;
+    gp.out = y_dev;
+    gp.ldo = N;
+    gp.rt_per_cta = 2;
+    gp.ksplit = 4;
+    CK(launch_gemm(gp, EPI_STORE, impl, false, s));
+    return ZDEC_OK;
+}

@@ -1,0 +1,110 @@
+// zdec_internal.cuh -- layouts and device helpers shared by the zdec kernels.
+//
+// Repacked Q4_K layout ("tile blocks").  A matrix of N rows x K columns is cut
+// into row tiles of 16 rows; each (row tile, super-block of 256 columns) is one
+// 2304-byte tile block (= 16 canonical 144-byte blocks), stored row tile major:
+//   offset(rt, sb) = (rt * nsb + sb) * 2304,  nsb = K / 256.
+// Inside a tile block the bytes are arranged for the warp that multiplies it
+// with mma.sync.m16n8k16 (lane = 4*g + tig, g = lane/4, tig = lane%4):
+//   [0, 2048)    codes: 4 chunks of 512 B; chunk c, lane l -> 16 bytes at
+//                c*512 + 16*l, i.e. one uint4 load per lane per chunk.
+//   [2048, 2304) meta: one uint64 per lane at 2048 + 8*l.
+// Lane (g, tig) owns rows g and g+8 of the tile and, in every super-block,
+// the two 32-weight sub-blocks j1 = 2*tig and j2 = 2*tig+1 of both rows.
+// Within sub-block j = 2*tig + h the lane's 32 weights are 4 groups of 8
+// (p = 0..3): k = 256*sb + 32*j + 8*p + o, o = 0..7.  Group (h, p) of row
+// rho (0: row g, 1: row g+8) is one 32-bit word; chunk c = 2*h + (p >> 1),
+// word index (p & 1)*2 + rho.  Nibble n of the word (bits 4n..4n+3) holds
+// offset o = {0,4,2,6,1,5,3,7}[n].  With the masks 0x000F000F / 0x00F000F0
+// (and the same after >> 8) one lop3 yields the half2 pairs the mma A
+// fragment wants: offsets (0,1) and (2,3) as 1024+q, offsets (4,5) and (6,7)
+// as 1024+16q.  The activation operand stores the elements at offsets 4..7
+// divided by 16 so both kinds of pair multiply to q*x.
+// Meta uint64 of lane (g, tig): low word = row g, high word = row g+8, each
+//   bits 0-5 sc[j1], 16-21 sc[j2], 6-11 m[j1], 22-27 m[j2],
+//   bits 12-15, 28-31 (both words): four nibbles of one fp16 value: tig 0 ->
+//   d of row g, 1 -> dmin of row g, 2 -> d of row g+8, 3 -> dmin of row g+8
+//   (value bits 0-3 low word 12-15, 4-7 low 28-31, 8-11 high 12-15, 12-15 high 28-31).
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace zdec {
+
+constexpr int QK = 256;                 // weights per super-block
+constexpr int CANON_BLOCK = 144;        // canonical bytes per super-block
+constexpr int TILE_BYTES = 2304;        // 16 rows x 144
+constexpr int TILE_CODE_BYTES = 2048;
+constexpr int HD = 128;                 // head_dim the attention kernel implements
+constexpr int GROUP = 4;                // query heads per kv head the kernel implements
+constexpr int ATT_CHUNK = 64;           // tokens per attention smem chunk
+constexpr int MAX_B = 32;
+
+// offset -> nibble position inside a lane word, and back
+__host__ __device__ constexpr int nib_of_off(int o) {
+    return o == 0 ? 0 : o == 4 ? 1 : o == 2 ? 2 : o == 6 ? 3 : o == 1 ? 4 : o == 5 ? 5 : o == 3 ? 6 : 7;
+}
+__host__ __device__ constexpr int off_of_nib(int n) {
+    return n == 0 ? 0 : n == 1 ? 4 : n == 2 ? 2 : n == 3 ? 6 : n == 4 ? 1 : n == 5 ? 5 : n == 6 ? 3 : 7;
+}
+
+// ----------------------------------------------------------------- PTX ---
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Hint: bring [p, p+bytes) into L2.  p 16-byte aligned, bytes multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream_u2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_u4(const void *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+    uint32_t r;
+    // (a & mask) | orv
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));
+    return r;
+}
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C(16x8 f32)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
+          "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// ------------------------------------------------------- device status ---
+enum : uint32_t { STATUS_POSITION = 1u, STATUS_CAPACITY = 2u, STATUS_TIMEOUT = 4u, STATUS_TOKEN = 8u };
+
+// ------------------------------------------------------------ launchers ---
+struct GemmArgs;   // defined in zdec_kernels.cuh
+
+}  // namespace zdec

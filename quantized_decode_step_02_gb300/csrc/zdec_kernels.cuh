@@ -1,0 +1,120 @@
+// zdec_kernels.cuh -- host-side launchers of the zdec kernels.  Every launcher
+// enqueues on `stream`; `pdl` asks for programmatic dependent launch (the
+// kernel may start while its predecessor drains and waits in-kernel with
+// griddepcontrol.wait before touching the predecessor's outputs).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <utility>
+
+#include "zdec_internal.cuh"
+
+namespace zdec {
+
+// ------------------------------------------------------------- repack.cu
+// Canonical rows -> tile blocks.  interleave8 == 0: tile row r of row tile rt
+// is source row 16*rt + r of src0.  interleave8 == 1: rows 0-7 of tile rt are
+// rows 8*rt..8*rt+7 of src0 and rows 8-15 the same rows of src1 (gate/up).
+// Source rows >= src_rows are zero blocks (padding).
+cudaError_t launch_repack(const uint8_t *src0, const uint8_t *src1, int interleave8, int src_rows,
+                          int n_rowtiles, int nsb, uint8_t *dst, cudaStream_t stream);
+// Tile blocks -> canonical blocks for logical rows [row0, row0+nrows) of a
+// matrix stored at `tiles`.  row_map: 0 plain rows, 1 the gate half and 2 the
+// up half of a gate/up interleaved matrix.
+cudaError_t launch_export_canonical(const uint8_t *tiles, int row_map, int nsb, int row0,
+                                    int nrows, uint8_t *dst, cudaStream_t stream);
+cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int row0, int nrows,
+                                float *dst, cudaStream_t stream);
+// x[b][:] = dequant(E[tokens[b]]) for b < B; also checks positions against
+// the device lengths (status bit STATUS_POSITION on mismatch).
+cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
+                         const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
+                         float *x, int ldx, bool pdl, cudaStream_t stream);
+
+// --------------------------------------------------------------- gemm.cu
+enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LMHEAD = 3 };
+
+struct GemmParams {
+    const uint8_t *W;      // tile blocks
+    int N;                 // valid output rows (<= 16 * nrt); SWIGLU: ffn rows
+    int nrt;               // row tiles
+    int nsb;               // K / 256
+    const __half *x16;     // [Bp][K] fp16, offsets 4..7 of every 8 divided by 16
+    const uint2 *sx;       // [Bp][nsb][4] sub-block sums (hi, lo) pairs
+    int B;                 // valid batch rows
+    float *out;            // STORE: y[b*ldo + n]; RESID: x[b*ldo + n] += y; SWIGLU: a[b*ldo + f]
+    int ldo;
+    float *amax_val;       // LMHEAD: per-CTA argmax partials [grid][MAX_B]
+    int *amax_idx;
+    int rt_per_cta;        // row tiles per CTA (RT)
+    int ksplit;            // K splits per CTA (KS); RT*KS == 8 warps
+};
+// impl 1: CUDA-core dequant-matvec (B <= 4); impl 2: mma.sync swap-AB GEMM.
+cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream);
+int gemm_grid(const GemmParams &p);
+
+// prep: fp32 rows -> fp16 operand + sub-block sums.  gain != nullptr applies
+// RMSNorm (x * rsqrt(mean x^2 + eps) * gain).  Rows B..Bp-1 are zeroed.
+cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B,
+                        int Bp, __half *x16, uint2 *sx, bool pdl, cudaStream_t stream);
+// ids[b] = argmax over the per-CTA partials (lowest index on ties); also
+// advances the device lengths: len_dev[b] = positions[b] + 1.
+cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
+                                int32_t *ids, const int32_t *positions, int32_t *len_dev,
+                                bool pdl, cudaStream_t stream);
+
+// ---------------------------------------------------------- attention.cu
+struct KvArena {
+    int kv_dtype;          // 0 fp16, 1 Q8_0
+    int n_layers, n_kv, Lp;
+    uint8_t *k;            // fp16: [slot][layer][g][Lp][128] half;  Q8: int8 codes, same shape
+    uint8_t *v;            // fp16: [slot][layer][g][128][Lp] half (V transposed); Q8: int8 codes
+    uint8_t *ks;           // Q8: [slot][layer][g][Lp][4] half   (K scales)
+    uint8_t *vs;           // Q8: [slot][layer][g][4][Lp] half   (V scales, transposed)
+};
+struct AttnParams {
+    KvArena kv;
+    int layer;
+    int nq;                // query heads (= 4 * n_kv)
+    const int32_t *positions;
+    const float *qkv;      // [B][qkv_ld]: q (nq*128), k (n_kv*128), v (n_kv*128)
+    int qkv_ld;
+    const float2 *rope;    // [max_L][64] (cos, sin)
+    int append;            // 1: rotate q/k at pos and append k, v; 0: q already rotated, no append
+    int S;                 // splits per (b, kv head)
+    float *part;           // [B][n_kv][S][4][130]
+    int *tickets;          // [B][n_kv]
+    float *o;              // [B][nq*128]
+    int B;
+    int max_L;             // positions >= max_L are ignored (the step is flagged elsewhere)
+};
+cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream);
+// Raise the attention kernel's dynamic shared-memory limit (once, before capture).
+cudaError_t attention_setup(int kv_dtype);
+size_t attention_smem_bytes(int kv_dtype);
+// Bulk append of fp16 K/V [n_layers][n][n_kv][128] (device) at tokens t0.. of slot.
+cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const uint16_t *k16,
+                             const uint16_t *v16, cudaStream_t stream);
+// Canonical read-back: [n][n_kv][128] (+ scales [n][n_kv][4]) for one layer.
+cudaError_t launch_kv_read(const KvArena &a, int slot, int layer, int t0, int n, uint8_t *k,
+                           uint8_t *v, uint16_t *ks, uint16_t *vs, cudaStream_t stream);
+
+// Launch helper with the programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, bool pdl,
+                     cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace zdec
