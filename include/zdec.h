@@ -196,18 +196,22 @@ zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, const float *q
  * The dense Q4_K projection on its own (used for kernel-level parity and the
  * GEMM roofline).  N multiple of 16, K multiple of 512, 1 <= B <= 32. */
 
-/* Bytes of the repacked layout of an N x K matrix (== canonical bytes). */
+/* Bytes of the repacked layout of an N x K matrix: the canonical bytes with
+ * the row count rounded up to a multiple of 128 (zero blocks pad the last
+ * group of eight 16-row tiles). */
 size_t zdec_q4k_repacked_bytes(int N, int K);
 /* canonical_dev (N*K/256 blocks, row-major) -> repacked_dev.  Device memory. */
 zdec_status zdec_q4k_repack(const void *canonical_dev, int N, int K, void *repacked_dev,
                             void *stream);
-/* Scratch bytes zdec_q4k_gemm needs for B rows of length K. */
+/* Scratch bytes zdec_q4k_gemm needs for B rows of length K: fp16 high and
+ * low parts of the activations (padded to a multiple of 8 rows) and their
+ * per-32 sub-block sums. */
 size_t zdec_q4k_gemm_workspace_bytes(int K, int B);
 /* y[b][n] = sum_k W[n][k] x[b][k] for b < B.  x_dev fp32 [B][K], y_dev fp32
  * [B][N], workspace_dev >= zdec_q4k_gemm_workspace_bytes(K, B) bytes, 16-byte
  * aligned, owned by the caller.  impl: 1 = dequant-matvec (B <= 4),
- * 2 = mma.sync GEMM.  Activations are rounded to fp16 on the way in; weights
- * are exact; accumulation is fp32. */
+ * 2 = mma.sync GEMM.  Activations enter as fp16 high + low parts (about 22
+ * significant bits); weights are exact; accumulation is fp32. */
 zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B,
                           float *y_dev, int impl, void *workspace_dev, size_t workspace_bytes,
                           void *stream);

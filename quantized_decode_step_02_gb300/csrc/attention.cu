@@ -8,10 +8,11 @@
 // KV cache pushes an RDNA4 swarm crossover...", "Why Q8 is close to free and
 // where the sharp edges are"), which is what the Q8_0 instantiation does.
 //
-// Grid: (split s, kv head g, sequence b); 128 threads.  The 4 query heads of
-// a kv head share one read of its K/V tiles.  A split covers Ts tokens
-// (a multiple of 64, Ts = ceil(ceil((pos+1)/S) / 64) * 64), streamed through
-// two shared-memory stages of 64 tokens with cp.async.  Both products run on
+// Grid: (cluster rank r, kv head g, sequence b); 128 threads; the CS CTAs of
+// one (b, g) form a thread-block cluster.  The 4 query heads of a kv head
+// share one read of its K/V tiles.  The pos+1 tokens are cut into 64-token
+// chunks; rank r takes chunks [r*nch/CS, (r+1)*nch/CS), streamed through two
+// shared-memory stages with cp.async.  Both products run on
 // mma.sync.m16n8k16 with fp32 accumulation:
 //   scores: A = q (rows 0-3 the fp16 high parts of the 4 heads, rows 8-11 the
 //           low parts, so q keeps ~22 bits), B = K^T (8 tokens per MMA);
@@ -19,9 +20,14 @@
 //           V^T tile, whose layout makes each thread's four tokens adjacent.
 // Q8_0: codes become exact fp16 integers in registers; K scales multiply the
 // per-32-dim partial scores, V scales are folded into p per 32-dim block.
-// The last CTA of each (b, g) (atomic ticket, no waiting) merges the splits'
-// (max, sum, unnormalised output) partials.
+// Each CTA reduces its warps to one (max, sum, unnormalised output) partial in
+// shared memory; rank 0 of the cluster merges the ranks' partials through
+// distributed shared memory (fixed rank order) and writes the output.
+#include <cooperative_groups.h>
+
 #include "zdec_kernels.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace zdec {
 
@@ -140,24 +146,24 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ __align__(16) uint8_t s_newk[HD * 2], s_newv[HD * 2];   // new token (fp16 or codes)
     __shared__ uint16_t s_newks[4], s_newvs[4];
-    __shared__ int s_last;
+    __shared__ float s_part[GROUP][HD + 4];   // this CTA's (max, sum, output) per head
 
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int rank = blockIdx.x, g = blockIdx.y, b = blockIdx.z, CS = p.cs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int pos = p.positions[b];       // staged before the step: not a predecessor output
-    if (pos < 0 || pos >= p.max_L) return;   // bad device input: flagged by the embedding kernel
+    if (pos < 0 || pos >= p.max_L) return;   // bad device input (whole cluster); flagged by the embedding kernel
     const int ntok = pos + 1;
-    const int Ts = (((ntok + p.S - 1) / p.S) + ATT_CHUNK - 1) / ATT_CHUNK * ATT_CHUNK;
-    const int T0 = s * Ts;
-    if (T0 >= ntok) return;               // empty split; the combiner does not wait for it
-    const int T1 = min(T0 + Ts, ntok);
+    const int nch = (ntok + ATT_CHUNK - 1) / ATT_CHUNK;
+    const int c_lo = rank * nch / CS, c_hi = (rank + 1) * nch / CS;
+    const int T0 = c_lo * ATT_CHUNK;
+    const int T1 = min(c_hi * ATT_CHUNK, ntok);
+    const bool empty = c_lo >= c_hi;       // still takes part in the cluster merge
     const int H = p.append ? min(T1, pos) : T1;   // tokens read from the arena
-    const int nchunks = (T1 - T0 + ATT_CHUNK - 1) / ATT_CHUNK;
-    const int n_used = (ntok + Ts - 1) / Ts;
-    const bool has_new = p.append && T1 == ntok;
+    const int nchunks = c_hi - c_lo;
+    const bool has_new = p.append && !empty && T1 == ntok;
 
     uint8_t *stage0 = smem, *stage1 = smem + Lay::STAGE;
-    issue_chunk<KVT>(p, stage0, b, g, T0, H);
+    if (!empty) issue_chunk<KVT>(p, stage0, b, g, T0, H);
     cp_async_commit();
     if (nchunks > 1) issue_chunk<KVT>(p, stage1, b, g, T0 + ATT_CHUNK, H);
     cp_async_commit();
@@ -437,51 +443,94 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             L += f * wl[w * 4 + head];
             for (int e = 0; e < 4; e++) O[e] += f * wo[(w * 4 + head) * HD + d0 + e];
         }
-        float *pp = p.part + ((((size_t)b * p.kv.n_kv + g) * p.S + s) * 4 + head) * (HD + 2);
-        if ((threadIdx.x & 31) == 0) { pp[0] = M; pp[1] = L; }
-        for (int e = 0; e < 4; e++) pp[2 + d0 + e] = O[e];
+        if ((threadIdx.x & 31) == 0) { s_part[head][0] = M; s_part[head][1] = L; }
+        for (int e = 0; e < 4; e++) s_part[head][4 + d0 + e] = O[e];
     }
-    // ---- last CTA of (b, g) merges the splits
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int t = atomicAdd(&p.tickets[b * p.kv.n_kv + g], 1);
-        s_last = (t == n_used - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    {
-        const float *base = p.part + (((size_t)b * p.kv.n_kv + g) * p.S) * 4 * (HD + 2);
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < n_used; s2++) M = fmaxf(M, __ldcg(base + ((size_t)s2 * 4 + head) * (HD + 2)));
-        float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int s2 = 0; s2 < n_used; s2++) {
-            const float *ps = base + ((size_t)s2 * 4 + head) * (HD + 2);
-            float ms = __ldcg(ps);
-            float f = ms == -INFINITY ? 0.0f : expf(ms - M);
-            L += f * __ldcg(ps + 1);
-            for (int e = 0; e < 4; e++) O[e] += f * __ldcg(ps + 2 + d0 + e);
+    // ---- rank 0 merges the cluster's partials through distributed shared memory
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (rank == 0) {
+        // issue every peer's loads before using any (distributed shared memory
+        // latency is paid once, not once per rank)
+        float mr[16], lr[16];
+        float4 orr[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            mr[r] = -INFINITY;
+            lr[r] = 0.0f;
+            orr[r] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (r < CS) {
+                const float *ps = cluster.map_shared_rank(&s_part[0][0], r) + head * (HD + 4);
+                mr[r] = ps[0];
+                lr[r] = ps[1];
+                orr[r] = *reinterpret_cast<const float4 *>(ps + 4 + d0);
+            }
         }
-        float inv = 1.0f / L;
-        float *o = p.o + (size_t)b * p.nq * HD + (size_t)(GROUP * g + head) * HD + d0;
-        for (int e = 0; e < 4; e++) o[e] = O[e] * inv;
-        if (threadIdx.x == 0) p.tickets[b * p.kv.n_kv + g] = 0;
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < 16; r++) M = fmaxf(M, mr[r]);
+        float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            const float f = mr[r] == -INFINITY ? 0.0f : expf(mr[r] - M);
+            L += f * lr[r];
+            O[0] += f * orr[r].x; O[1] += f * orr[r].y; O[2] += f * orr[r].z; O[3] += f * orr[r].w;
+        }
+        const float inv = 1.0f / L;
+        const int qd = p.nq * HD;
+        const int kcol = (GROUP * g + head) * HD + d0;   // column of o, the O projection's input
+        float y[4];
+        for (int e = 0; e < 4; e++) y[e] = O[e] * inv;
+        float *o = p.o + (size_t)b * qd + kcol;
+        for (int e = 0; e < 4; e++) o[e] = y[e];
+        // the O projection's operand as fp16 hi + lo parts (elements 4..7 of every
+        // 8 stored /16) and the per-32 sub-block sums, as the GEMM prep writes them
+        __half h[4], hl[4];
+        float part = 0.0f;
+        for (int e = 0; e < 4; e++) {
+            h[e] = __float2half_rn(y[e]);
+            hl[e] = __float2half_rn((y[e] - __half2float(h[e])) * LO_SCALE);
+            part += y[e];
+        }
+        if (d0 & 4)
+            for (int e = 0; e < 4; e++) {
+                h[e] = __hmul(h[e], __float2half(0.0625f));
+                hl[e] = __hmul(hl[e], __float2half(0.0625f));
+            }
+        const size_t ai = act_chunk(kcol >> 8, b, (kcol & 255) >> 3, p.oBp) + (kcol & 7);
+        *reinterpret_cast<uint2 *>(p.o16 + ai) =
+            make_uint2(h2_as_u32(__halves2half2(h[0], h[1])), h2_as_u32(__halves2half2(h[2], h[3])));
+        *reinterpret_cast<uint2 *>(p.o16lo + ai) =
+            make_uint2(h2_as_u32(__halves2half2(hl[0], hl[1])), h2_as_u32(__halves2half2(hl[2], hl[3])));
+        part += __shfl_xor_sync(AFULL, part, 1);
+        part += __shfl_xor_sync(AFULL, part, 2);
+        part += __shfl_xor_sync(AFULL, part, 4);
+        if ((lane & 7) == 0) store_sum(p.osx, kcol >> 8, b, (kcol >> 5) & 7, p.oBp, part);
     }
+    cluster.sync();   // peers keep their partials alive until rank 0 has read them
 }
 
 cudaError_t attention_setup(int kv_dtype) {
     int smem = (int)attention_smem_bytes(kv_dtype);
-    if (kv_dtype == 0)
-        return cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    return cudaFuncSetAttribute(attention_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e;
+    if (kv_dtype == 0) {
+        e = cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    } else {
+        e = cudaFuncSetAttribute(attention_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attention_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
+    return e;
 }
 
 cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream) {
-    dim3 grid(p.S, p.kv.n_kv, p.B), block(128);
+    if (p.cs < 1 || p.cs > 16) return cudaErrorInvalidValue;
+    dim3 grid(p.cs, p.kv.n_kv, p.B), block(128);
     size_t smem = attention_smem_bytes(p.kv.kv_dtype);
-    if (p.kv.kv_dtype == 0) return launch_k(attention_kernel<0>, grid, block, smem, pdl, stream, p);
-    return launch_k(attention_kernel<1>, grid, block, smem, pdl, stream, p);
+    if (p.kv.kv_dtype == 0) return launch_k(attention_kernel<0>, grid, block, smem, pdl, p.cs, stream, p);
+    return launch_k(attention_kernel<1>, grid, block, smem, pdl, p.cs, stream, p);
 }
 
 // ------------------------------------------------------------ bulk append ---

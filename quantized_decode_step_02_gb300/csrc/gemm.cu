@@ -3,48 +3,55 @@
 // One read of every weight per decode step, multiplied against all B hidden
 // states ("The weight read is the only term that does not scale": a step that
 // advances eight sequences loads each weight tile once and multiplies eight
-// hidden states against it).  Two kernels do this:
-//   * gemm_mma_kernel: mma.sync.m16n8k16 with the weight rows in the MMA M
-//     slot (16 rows per tile) and the batch in N (8 per tile, zero padded);
-//     the dense-matrix-core path the pages switch to past about four
-//     sequences ("RDNA4 pads the batch dimension to 16").
-//   * gemm_matvec_kernel: the same tile blocks through CUDA-core fp32 FMAs,
-//     the dequant-matvec of the batch-one path.
-// Both dequantize in registers: one lop3 turns two 4-bit codes into the fp16
-// pair (1024+q, 1024+q') (or 1024+16q for the high nibbles), one HFMA2 with
-// (sc, sc) and (-1024 sc, -1024 sc) turns that into the exact integers q*sc
-// (or 16*q*sc).  Sub-block scales therefore live in the A operand, a whole
-// 256-column super-block accumulates in fp32 inside the tensor core, and the
-// epilogue applies d and the min term: y += d*acc_q - dmin*acc_m, where
-// acc_m = sum_j m_j * S_j comes from one more MMA against the per-sub-block
-// activation sums S_j (split as hi + lo fp16).
+// hidden states against it).
+//
+// Kernel structure (gemm_kernel): a CTA owns one group of 8 row tiles
+// (128 rows) and a range of 256-column super-blocks; warp w multiplies row
+// tile w.  Stages of the range stream through a ring of shared-memory buffers
+// with 1-D bulk copies (TMA) completing on one mbarrier per stage: each stage
+// is the group's 18,432 contiguous bytes of tile blocks plus that
+// super-block's activation rows.  Weight copies are issued before the
+// programmatic-launch dependency wait (weights never depend on the previous
+// kernel), activation copies after it.  Small matrices split K across a
+// thread-block cluster and reduce the partial tiles through distributed
+// shared memory (fixed order, no atomics).
+//
+// Arithmetic, per warp and super-block:
+//   * dequant: one lop3 puts two 4-bit codes under the fp16 exponent of 1024;
+//     one HFMA2 with (sc, sc) and (-1024 sc, -1024 sc) yields the exact
+//     integers q*sc (16*q*sc for the high nibbles, whose activations are stored
+//     divided by 16), so the sub-block scale lives in the A operand;
+//   * IMPL 2: mma.sync.m16n8k16 with weight rows in M (16 per tile) and the
+//     batch in N (8 per tile), fp32 accumulation over the whole super-block;
+//     the batch is zero padded to 8 (the pages' 16-wide WMMA tile pads the
+//     batch the same way, "RDNA4 pads the batch dimension to 16");
+//     IMPL 1: the same operands through CUDA-core fp32 FMAs (the batch-one
+//     dequant-matvec);
+//   * epilogue: y += d*acc_q - dmin*acc_m, acc_m = sum_j m_j*S_j from one more
+//     MMA against the per-sub-block activation sums S_j (hi + lo fp16).
+// Activations arrive as fp16 hi + lo planes (~22 significant bits).
+#include <cooperative_groups.h>
+
 #include "zdec_kernels.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace zdec {
 
 constexpr uint32_t FULL = 0xFFFFFFFFu;
+constexpr uint32_t LO_SKEW = 64;   // bytes between the hi and lo planes of a stage
 
 // ------------------------------------------------------------------ prep ---
-// Block b converts fp32 row b into the GEMM operand: fp16 values (offsets 4..7
-// of every group of 8 divided by 16, matching the tile-block nibble layout) and
-// per-32 sub-block sums of the fp16 values, stored as hi + lo fp16 at
-// sx[b][sb][tig] = {(hi_2tig, hi_2tig+1), (lo_2tig, lo_2tig+1)}.
+// Block b converts fp32 row b into the act planes (hi, lo) and sub-block sums.
+// gain != nullptr applies RMSNorm: x * rsqrt(mean x^2 + eps) * gain.
 template <bool NORM>
 __global__ __launch_bounds__(512) void prep_kernel(const float *__restrict__ src, int lds, int K,
-                                                   const float *__restrict__ gain, float eps, int B,
-                                                   __half *__restrict__ x16, __half *__restrict__ sxh) {
+                                                   const float *__restrict__ gain, float eps, int Bp,
+                                                   __half *__restrict__ hi, __half *__restrict__ lo,
+                                                   __half *__restrict__ sums) {
     pdl_launch_dependents();
     pdl_wait();
-    int b = blockIdx.x;
-    int nsb = K / QK, nchunks = K / 8;
-    __half *xo = x16 + (size_t)b * K;
-    __half *so = sxh + (size_t)b * nsb * 16;
-    if (b >= B) {   // padding row of the MMA N tile
-        for (int c = threadIdx.x; c < nchunks; c += blockDim.x)
-            *reinterpret_cast<uint4 *>(xo + 8 * c) = make_uint4(0, 0, 0, 0);
-        for (int i = threadIdx.x; i < nsb * 16; i += blockDim.x) so[i] = __ushort_as_half(0);
-        return;
-    }
+    const int b = blockIdx.x, nchunks = K / 8;
     const float *xr = src + (size_t)b * lds;
     float r = 1.0f;
     if (NORM) {
@@ -62,48 +69,32 @@ __global__ __launch_bounds__(512) void prep_kernel(const float *__restrict__ src
         __syncthreads();
         r = 1.0f / sqrtf(red[0] / (float)K + eps);
     }
-    const __half sixteenth = __float2half(0.0625f);
     for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {   // nchunks % 32 == 0: warp-uniform
         float4 v0 = *reinterpret_cast<const float4 *>(xr + 8 * c);
         float4 v1 = *reinterpret_cast<const float4 *>(xr + 8 * c + 4);
         float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        __half h[8];
-        float part = 0.0f;
+        float y[8], part = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            float y = NORM ? (v[i] * r) * gain[8 * c + i] : v[i];
-            h[i] = __float2half_rn(y);
-            part += __half2float(h[i]);
+            y[i] = NORM ? (v[i] * r) * gain[8 * c + i] : v[i];
+            part += y[i];
         }
-#pragma unroll
-        for (int i = 4; i < 8; i++) h[i] = __hmul(h[i], sixteenth);
-        uint4 out;
-        out.x = h2_as_u32(__halves2half2(h[0], h[1]));
-        out.y = h2_as_u32(__halves2half2(h[2], h[3]));
-        out.z = h2_as_u32(__halves2half2(h[4], h[5]));
-        out.w = h2_as_u32(__halves2half2(h[6], h[7]));
-        *reinterpret_cast<uint4 *>(xo + 8 * c) = out;
+        const int sb = c >> 5, cl = c & 31;
+        store_act8(hi, lo, act_chunk(sb, b, cl, Bp), y);
         part += __shfl_xor_sync(FULL, part, 1);
         part += __shfl_xor_sync(FULL, part, 2);
-        if ((c & 3) == 0) {
-            int sb = c >> 5, j = (c & 31) >> 2, tig = j >> 1, hh = j & 1;
-            __half hi = __float2half_rn(part);
-            __half lo = __float2half_rn(part - __half2float(hi));
-            so[(sb * 4 + tig) * 4 + hh] = hi;
-            so[(sb * 4 + tig) * 4 + 2 + hh] = lo;
-        }
+        if ((c & 3) == 0) store_sum(sums, sb, b, cl >> 2, Bp, part);
     }
 }
 
-cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B,
-                        int Bp, __half *x16, uint2 *sx, bool pdl, cudaStream_t stream) {
+cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B, int Bp,
+                        __half *hi, __half *lo, __half *sums, bool pdl, cudaStream_t stream) {
     int threads = K / 8 < 512 ? K / 8 : 512;
-    __half *sxh = reinterpret_cast<__half *>(sx);
     if (gain)
-        return launch_k(prep_kernel<true>, dim3(Bp), dim3(threads), 0, pdl, stream, src, lds, K,
-                        gain, eps, B, x16, sxh);
-    return launch_k(prep_kernel<false>, dim3(Bp), dim3(threads), 0, pdl, stream, src, lds, K,
-                    gain, eps, B, x16, sxh);
+        return launch_k(prep_kernel<true>, dim3(B), dim3(threads), 0, pdl, 1, stream, src, lds, K, gain,
+                        eps, Bp, hi, lo, sums);
+    return launch_k(prep_kernel<false>, dim3(B), dim3(threads), 0, pdl, 1, stream, src, lds, K, gain, eps,
+                    Bp, hi, lo, sums);
 }
 
 // ------------------------------------------------------- tile decoding ---
@@ -148,331 +139,489 @@ __device__ __forceinline__ void decode_word(uint32_t w, __half2 c, __half2 o, ui
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-// ------------------------------------------------------------ epilogue ---
-// acc[nt][i] follows the mma C fragment: i = 0,1 -> row g, cols 2tig, 2tig+1;
-// i = 2,3 -> row g+8.  Row tile rt, column tile nt covers batch rows 8nt..8nt+7.
-template <int NT, int EPI>
-__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&acc)[NT][4], bool active,
-                                              int rt, int warp, int lane, float *s_amax_v,
-                                              int *s_amax_i) {
-    int g = lane >> 2, tig = lane & 3;
-    if (EPI == EPI_STORE || EPI == EPI_RESID) {
-        if (!active) return;
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                int row = rt * 16 + g + (i >= 2 ? 8 : 0), col = 8 * nt + 2 * tig + (i & 1);
-                if (col < p.B && row < p.N) {
-                    float *o = p.out + (size_t)col * p.ldo + row;
-                    if (EPI == EPI_STORE) *o = acc[nt][i];
-                    else *o += acc[nt][i];
-                }
-            }
-    } else if (EPI == EPI_SWIGLU) {
-        if (!active) return;
-        int f = rt * 8 + g;
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                int col = 8 * nt + 2 * tig + e;
-                if (col < p.B && f < p.N)
-                    p.out[(size_t)col * p.ldo + f] = silu_f(acc[nt][e]) * acc[nt][2 + e];
-            }
-    } else {   // EPI_LMHEAD: logits and the CTA's argmax partial per batch row
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                int col = 8 * nt + 2 * tig + e;
-                int r0 = rt * 16 + g, r1 = r0 + 8;
-                float v0 = (active && r0 < p.N) ? acc[nt][e] : -INFINITY;
-                float v1 = (active && r1 < p.N) ? acc[nt][2 + e] : -INFINITY;
-                if (active && p.out && col < p.B) {
-                    if (r0 < p.N) p.out[(size_t)col * p.ldo + r0] = acc[nt][e];
-                    if (r1 < p.N) p.out[(size_t)col * p.ldo + r1] = acc[nt][2 + e];
-                }
-                float bv = v0;
-                int bi = r0;
-                if (v1 > bv) { bv = v1; bi = r1; }
-                for (int o = 4; o < 32; o <<= 1) {   // across g, lowest index on ties
-                    float ov = __shfl_xor_sync(FULL, bv, o);
-                    int oi = __shfl_xor_sync(FULL, bi, o);
-                    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-                }
-                if (g == 0) {
-                    s_amax_v[warp * (NT * 8) + col] = bv;
-                    s_amax_i[warp * (NT * 8) + col] = bi;
-                }
-            }
-    }
-}
-
-// K-split reduction through shared memory, then the epilogue on split 0.
-template <int NT, int EPI>
-__device__ __forceinline__ void gemm_finish(const GemmParams &p, float (&acc)[NT][4], bool valid,
-                                            int rt) {
-    __shared__ float red[8][NT][4][32];
-    __shared__ float s_amax_v[8 * NT * 8];
-    __shared__ int s_amax_i[8 * NT * 8];
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int RT = p.rt_per_cta, KS = p.ksplit;
-    int rtl = warp % RT, ks = warp / RT;
-    if (KS > 1) {
-        if (ks > 0)
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-                for (int i = 0; i < 4; i++) red[warp][nt][i][lane] = acc[nt][i];
-        __syncthreads();
-        if (ks == 0)
-            for (int k2 = 1; k2 < KS; k2++) {
-                int w2 = rtl + k2 * RT;
-#pragma unroll
-                for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-                    for (int i = 0; i < 4; i++) acc[nt][i] += red[w2][nt][i][lane];
-            }
-    }
-    gemm_epilogue<NT, EPI>(p, acc, valid && ks == 0, rt, warp, lane, s_amax_v, s_amax_i);
-    if (EPI == EPI_LMHEAD) {
-        __syncthreads();
-        if ((int)threadIdx.x < NT * 8) {
-            int col = threadIdx.x;
-            float bv = -INFINITY;
-            int bi = 0x7FFFFFFF;
-            for (int w = 0; w < RT; w++) {   // split-0 warps, increasing rows
-                float v = s_amax_v[w * (NT * 8) + col];
-                int i = s_amax_i[w * (NT * 8) + col];
-                if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
-            }
-            if (col < p.B) {
-                p.amax_val[blockIdx.x * MAX_B + col] = bv;
-                p.amax_idx[blockIdx.x * MAX_B + col] = bi;
-            }
-        }
-    }
-}
-
-// L2 prefetch of the CTA's contiguous run of tile blocks.  Weights never
-// change during a step, so this is issued before the dependency wait.
-__device__ __forceinline__ void prefetch_cta_weights(const GemmParams &p) {
-    int rt0 = blockIdx.x * p.rt_per_cta;
-    int n = min(p.rt_per_cta, p.nrt - rt0);
-    const uint8_t *base = p.W + (size_t)rt0 * p.nsb * TILE_BYTES;
-    size_t bytes = (size_t)n * p.nsb * TILE_BYTES;
-    for (size_t off = (size_t)threadIdx.x * 4096; off < bytes; off += (size_t)blockDim.x * 4096)
-        prefetch_l2(base + off, (uint32_t)min((size_t)4096, bytes - off));
-}
-
-// ---------------------------------------------------------- mma kernel ---
-template <int NT, int EPI>
-__global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_mma_kernel(const GemmParams p) {
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int g = lane >> 2, tig = lane & 3;
-    int RT = p.rt_per_cta, KS = p.ksplit;
-    int rtl = warp % RT, ks = warp / RT;
-    int rt = blockIdx.x * RT + rtl;
-    bool valid = rt < p.nrt;
-    prefetch_cta_weights(p);
-    pdl_launch_dependents();
-    pdl_wait();
-
-    const int K = p.nsb * QK;
-    int sb0 = ks * p.nsb / KS, sb1 = (ks + 1) * p.nsb / KS;
-    float acc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) acc[nt][i] = 0.0f;
-    const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-
-    if (valid && sb0 < sb1) {
-        const uint8_t *tile = p.W + ((size_t)rt * p.nsb + sb0) * TILE_BYTES;
-        uint4 q[4];
-        uint2 mt;
-#pragma unroll
-        for (int c = 0; c < 4; c++) q[c] = ld_stream_u4(tile + c * 512 + 16 * lane);
-        mt = ld_stream_u2(tile + TILE_CODE_BYTES + 8 * lane);
-        for (int sb = sb0; sb < sb1; sb++) {
-            // issue the next tile block's loads before working on this one
-            uint4 qn[4];
-            uint2 mtn;
-            if (sb + 1 < sb1) {
-                const uint8_t *tn = tile + TILE_BYTES;
-#pragma unroll
-                for (int c = 0; c < 4; c++) qn[c] = ld_stream_u4(tn + c * 512 + 16 * lane);
-                mtn = ld_stream_u2(tn + TILE_CODE_BYTES + 8 * lane);
-            }
-            TileMeta tm;
-            decode_meta(mt, tig, tm);
-            float tq[NT][4], tmin[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-                for (int i = 0; i < 4; i++) tq[nt][i] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                const int h = c >> 1;
-                const __half2 cg = h ? tm.cg1 : tm.cg0, og = h ? tm.og1 : tm.og0;
-                const __half2 c8 = h ? tm.c81 : tm.c80, o8 = h ? tm.o81 : tm.o80;
-#pragma unroll
-                for (int pp = 0; pp < 2; pp++) {
-                    const int pidx = (c & 1) * 2 + pp;
-                    uint32_t w0 = pp ? q[c].z : q[c].x, w1 = pp ? q[c].w : q[c].y;
-                    uint32_t at[4], at16[4];
-                    decode_word(w0, cg, og, at[0], at16[0], at[2], at16[2]);
-                    decode_word(w1, c8, o8, at[1], at16[1], at[3], at16[3]);
-                    const int koff = sb * QK + 32 * (2 * tig + h) + 8 * pidx;
-#pragma unroll
-                    for (int nt = 0; nt < NT; nt++) {
-                        uint4 xv = ld_u4(p.x16 + (size_t)(8 * nt + g) * K + koff);
-                        mma16816(tq[nt], at, xv.x, xv.y, tq[nt]);
-                        mma16816(tq[nt], at16, xv.z, xv.w, tq[nt]);
-                    }
-                }
-            }
-            const uint32_t am[4] = {tm.mg, tm.m8, tm.mg, tm.m8};
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++) {
-                uint2 s = p.sx[((size_t)(8 * nt + g) * p.nsb + sb) * 4 + tig];
-                mma16816(tmin[nt], am, s.x, s.y, zero4);
-                acc[nt][0] += tm.dg * tq[nt][0] - tm.dming * tmin[nt][0];
-                acc[nt][1] += tm.dg * tq[nt][1] - tm.dming * tmin[nt][1];
-                acc[nt][2] += tm.d8 * tq[nt][2] - tm.dmin8 * tmin[nt][2];
-                acc[nt][3] += tm.d8 * tq[nt][3] - tm.dmin8 * tmin[nt][3];
-            }
-            if (sb + 1 < sb1) {
-#pragma unroll
-                for (int c = 0; c < 4; c++) q[c] = qn[c];
-                mt = mtn;
-                tile += TILE_BYTES;
-            }
-        }
-    }
-    gemm_finish<NT, EPI>(p, acc, valid, rt);
-}
-
-// ------------------------------------------------------- matvec kernel ---
 __device__ __forceinline__ float dot2(uint32_t a, uint32_t x) {
     float2 fa = __half22float2(u32_as_h2(a)), fx = __half22float2(u32_as_h2(x));
     return fmaf(fa.x, fx.x, fa.y * fx.y);
 }
 
-template <int NB, int EPI>
-__global__ __launch_bounds__(256, 2) void gemm_matvec_kernel(const GemmParams p) {
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int tig = lane & 3;
-    int RT = p.rt_per_cta, KS = p.ksplit;
-    int rtl = warp % RT, ks = warp / RT;
-    int rt = blockIdx.x * RT + rtl;
-    bool valid = rt < p.nrt;
-    prefetch_cta_weights(p);
+// ------------------------------------------------------- stage compute ---
+// Stage layout: [GROUP_BYTES tile blocks][hi rows B x 512][lo rows][sums B x 32].
+//
+// MMA columns are "virtual": column 2c of n-tile nt multiplies the hi plane of
+// batch row b = 4nt + c, column 2c+1 its lo plane, so one 8-wide N tile carries
+// four batch rows at full (hi + lo) precision and the lane holding C-fragment
+// columns (2tig, 2tig+1) owns both halves of batch row 4nt + tig.
+// acc[nt][0..3] = (row g, hi), (row g, lo), (row g+8, hi), (row g+8, lo).
+template <int NT>
+__device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane, int B,
+                                          uint32_t abytes, float (&acc)[NT][4]) {
+    const int g = lane >> 2, tig = lane & 3;
+    const uint8_t *tile = st + warp * TILE_BYTES;
+    // this lane's B column: hi plane, or the lo plane (placed 64 bytes further so
+    // that a hi lane and a lo lane of the same batch row use different banks)
+    const uint8_t *plane = st + GROUP_BYTES + ((g & 1) ? abytes + LO_SKEW : 0u);
+    const uint8_t *sums = st + GROUP_BYTES + 2 * abytes + LO_SKEW;
+    uint4 q[4];
+#pragma unroll
+    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
+    TileMeta tm;
+    decode_meta(*reinterpret_cast<const uint2 *>(tile + TILE_CODE_BYTES + 8 * lane), tig, tm);
+    // two independent accumulator chains per n-tile (x1 and x16 nibbles)
+    float tq[NT][4], t16[NT][4], tmin[NT][4];
+    const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) tq[nt][i] = t16[nt][i] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const int h = c >> 1;
+        const __half2 cg = h ? tm.cg1 : tm.cg0, og = h ? tm.og1 : tm.og0;
+        const __half2 c8 = h ? tm.c81 : tm.c80, o8 = h ? tm.o81 : tm.o80;
+#pragma unroll
+        for (int pp = 0; pp < 2; pp++) {
+            const int pidx = (c & 1) * 2 + pp;
+            uint32_t w0 = pp ? q[c].z : q[c].x, w1 = pp ? q[c].w : q[c].y;
+            uint32_t at[4], at16[4];
+            decode_word(w0, cg, og, at[0], at16[0], at[2], at16[2]);
+            decode_word(w1, c8, o8, at[1], at16[1], at[3], at16[3]);
+            const int chunk = tig * 8 + h * 4 + pidx;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const int b = 4 * nt + (g >> 1);
+                uint4 xv = make_uint4(0, 0, 0, 0);
+                if (b < B)
+                    xv = *reinterpret_cast<const uint4 *>(plane + b * 512 +
+                                                          ((chunk ^ (tig | ((b & 1) << 2))) * 16));
+                mma16816(tq[nt], at, xv.x, xv.y, tq[nt]);
+                mma16816(t16[nt], at16, xv.z, xv.w, t16[nt]);
+            }
+        }
+    }
+    const uint32_t am[4] = {tm.mg, tm.m8, tm.mg, tm.m8};
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        const int b = 4 * nt + (g >> 1);
+        uint2 s = make_uint2(0, 0);   // the min term goes to the hi column only
+        if (b < B && !(g & 1)) s = *reinterpret_cast<const uint2 *>(sums + b * 32 + tig * 8);
+        mma16816(tmin[nt], am, s.x, s.y, zero4);
+        acc[nt][0] += tm.dg * (tq[nt][0] + t16[nt][0]) - tm.dming * tmin[nt][0];
+        acc[nt][1] += tm.dg * (tq[nt][1] + t16[nt][1]) - tm.dming * tmin[nt][1];
+        acc[nt][2] += tm.d8 * (tq[nt][2] + t16[nt][2]) - tm.dmin8 * tmin[nt][2];
+        acc[nt][3] += tm.d8 * (tq[nt][3] + t16[nt][3]) - tm.dmin8 * tmin[nt][3];
+    }
+}
+
+// CUDA-core dequant-matvec on the same stage (B <= 4); accr[col][rho] partial
+// over this lane's quarter of the row (summed across tig at the end).
+template <int NB>
+__device__ __forceinline__ void stage_fma(const uint8_t *st, int warp, int lane, uint32_t abytes,
+                                          float (&accr)[NB][2]) {
+    const int tig = lane & 3;
+    const uint8_t *tile = st + warp * TILE_BYTES;
+    const uint8_t *ahi = st + GROUP_BYTES, *alo = ahi + abytes + LO_SKEW;
+    const uint8_t *sums = ahi + 2 * abytes + LO_SKEW;
+    uint4 q[4];
+#pragma unroll
+    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
+    TileMeta tm;
+    decode_meta(*reinterpret_cast<const uint2 *>(tile + TILE_CODE_BYTES + 8 * lane), tig, tm);
+    float sq[NB][2], sl[NB][2];
+#pragma unroll
+    for (int c = 0; c < NB; c++) sq[c][0] = sq[c][1] = sl[c][0] = sl[c][1] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const int h = c >> 1;
+        const __half2 cg = h ? tm.cg1 : tm.cg0, og = h ? tm.og1 : tm.og0;
+        const __half2 c8 = h ? tm.c81 : tm.c80, o8 = h ? tm.o81 : tm.o80;
+#pragma unroll
+        for (int pp = 0; pp < 2; pp++) {
+            const int pidx = (c & 1) * 2 + pp;
+            uint32_t w0 = pp ? q[c].z : q[c].x, w1 = pp ? q[c].w : q[c].y;
+            uint32_t a0, a016, a0h, a0h16, a1, a116, a1h, a1h16;
+            decode_word(w0, cg, og, a0, a016, a0h, a0h16);
+            decode_word(w1, c8, o8, a1, a116, a1h, a1h16);
+            const int chunk = tig * 8 + h * 4 + pidx;
+#pragma unroll
+            for (int col = 0; col < NB; col++) {
+                const int off = (chunk ^ (tig | ((col & 1) << 2))) * 16;
+                uint4 xv = *reinterpret_cast<const uint4 *>(ahi + col * 512 + off);
+                uint4 xl = *reinterpret_cast<const uint4 *>(alo + col * 512 + off);
+                sq[col][0] += dot2(a0, xv.x) + dot2(a0h, xv.y) + dot2(a016, xv.z) + dot2(a0h16, xv.w);
+                sq[col][1] += dot2(a1, xv.x) + dot2(a1h, xv.y) + dot2(a116, xv.z) + dot2(a1h16, xv.w);
+                sl[col][0] += dot2(a0, xl.x) + dot2(a0h, xl.y) + dot2(a016, xl.z) + dot2(a0h16, xl.w);
+                sl[col][1] += dot2(a1, xl.x) + dot2(a1h, xl.y) + dot2(a116, xl.z) + dot2(a1h16, xl.w);
+            }
+        }
+    }
+    float2 mg = __half22float2(u32_as_h2(tm.mg)), m8 = __half22float2(u32_as_h2(tm.m8));
+#pragma unroll
+    for (int col = 0; col < NB; col++) {
+        uint2 s = *reinterpret_cast<const uint2 *>(sums + col * 32 + tig * 8);
+        float2 shi = __half22float2(u32_as_h2(s.x)), slo = __half22float2(u32_as_h2(s.y));
+        float s1 = shi.x + slo.x, s2 = shi.y + slo.y;
+        accr[col][0] += tm.dg * (sq[col][0] + sl[col][0] * LO_UNSCALE) - tm.dming * (mg.x * s1 + mg.y * s2);
+        accr[col][1] += tm.d8 * (sq[col][1] + sl[col][1] * LO_UNSCALE) - tm.dmin8 * (m8.x * s1 + m8.y * s2);
+    }
+}
+
+// ------------------------------------------------------------ epilogue ---
+// y[nt][rho]: output row rt*16 + g + 8*rho, batch row b = 4nt + tig.
+template <int NT, int EPI>
+__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT][2], int grp) {
+    constexpr int NB = 4 * NT;   // batch rows this instance covers
+    // SWIGLU: a[col][64 rows]; RESID with a next operand: x[col][128 rows]
+    __shared__ float s_v[EPI == EPI_SWIGLU ? NB * 64 : (EPI == EPI_RESID ? NB * 128 : GT * NB)];
+    __shared__ int s_i[GT * NB];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    const int rt = grp * GT + warp;
+    const bool active = rt < p.nrt;
+    if (EPI == EPI_STORE) {
+        if (!active) return;
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int row = rt * 16 + g + 8 * r, b = 4 * nt + tig;
+                if (b < p.B && row < p.N) p.out[(size_t)b * p.ldo + row] = y[nt][r];
+            }
+    } else if (EPI == EPI_RESID) {
+        // x += y; with next_gain set, the group's 128 updated rows also become the
+        // next projection's operand g*x (act planes + sub-block sums) and one
+        // partial sum of x^2 per column for that projection's RMSNorm scale
+        if (active)
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    const int row = rt * 16 + g + 8 * r, b = 4 * nt + tig;
+                    if (b < p.B && row < p.N) {
+                        float *o = p.out + (size_t)b * p.ldo + row;
+                        const float xn = *o + y[nt][r];
+                        *o = xn;
+                        if (p.next_gain) s_v[b * 128 + warp * 16 + 8 * r + g] = xn;
+                    }
+                }
+        if (!p.next_gain) return;
+        __syncthreads();
+        for (int task = threadIdx.x; task < NB * 16; task += blockDim.x) {   // (col, chunk of 8 rows)
+            const int col = task >> 4, ch = task & 15;
+            const int r0 = grp * 128 + ch * 8;
+            const bool live = col < p.B && r0 < p.N;
+            float part = 0.0f, sq = 0.0f;
+            if (live) {
+                float yy[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const float xv = s_v[col * 128 + ch * 8 + i];
+                    sq = fmaf(xv, xv, sq);
+                    yy[i] = xv * p.next_gain[r0 + i];
+                    part += yy[i];
+                }
+                store_act8(p.out16, p.out16lo, act_chunk(r0 >> 8, col, (r0 & 255) >> 3, p.out_Bp), yy);
+            }
+            part += __shfl_xor_sync(FULL, part, 1);   // four chunks = one sub-block
+            part += __shfl_xor_sync(FULL, part, 2);
+            if (live && (ch & 3) == 0) store_sum(p.out_sx, r0 >> 8, col, (r0 & 255) >> 5, p.out_Bp, part);
+            // the 16 chunks of one column are 16 consecutive lanes
+            sq += __shfl_xor_sync(FULL, sq, 1);
+            sq += __shfl_xor_sync(FULL, sq, 2);
+            sq += __shfl_xor_sync(FULL, sq, 4);
+            sq += __shfl_xor_sync(FULL, sq, 8);
+            if (live && ch == 0) p.part_out[grp * MAX_B + col] = sq;
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        // tile rows 0-7 gate, 8-15 up of ffn rows 8*rt .. 8*rt+7: a = silu(gate) * up,
+        // then the group's 64 consecutive rows become the down projection's act planes
+        if (active)
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const int b = 4 * nt + tig;
+                s_v[b * 64 + warp * 8 + g] = silu_f(y[nt][0]) * y[nt][1];
+            }
+        __syncthreads();
+        for (int task = threadIdx.x; task < NB * 8; task += blockDim.x) {   // 8 chunks of 8 rows per column
+            const int col = task >> 3, ch = task & 7;
+            const int f = grp * 64 + ch * 8;
+            const bool live = col < p.B && f < p.N;
+            float part = 0.0f;
+            if (live) {
+                float yy[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    yy[i] = s_v[col * 64 + ch * 8 + i];
+                    part += yy[i];
+                }
+                store_act8(p.out16, p.out16lo, act_chunk(f >> 8, col, (f & 255) >> 3, p.out_Bp), yy);
+            }
+            part += __shfl_xor_sync(FULL, part, 1);   // four chunks = one 32-row sub-block
+            part += __shfl_xor_sync(FULL, part, 2);
+            if (live && (ch & 3) == 0) store_sum(p.out_sx, f >> 8, col, (f & 255) >> 5, p.out_Bp, part);
+        }
+    } else {   // EPI_LMHEAD: logits and the CTA's argmax partial per batch row
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            const int b = 4 * nt + tig;
+            const int r0 = rt * 16 + g, r1 = r0 + 8;
+            const float v0 = (active && r0 < p.N) ? y[nt][0] : -INFINITY;
+            const float v1 = (active && r1 < p.N) ? y[nt][1] : -INFINITY;
+            if (active && p.out && b < p.B) {
+                if (r0 < p.N) p.out[(size_t)b * p.ldo + r0] = y[nt][0];
+                if (r1 < p.N) p.out[(size_t)b * p.ldo + r1] = y[nt][1];
+            }
+            float bv = v0;
+            int bi = r0;
+            if (v1 > bv) { bv = v1; bi = r1; }
+            for (int o = 4; o < 32; o <<= 1) {   // across g, lowest index on ties
+                const float ov = __shfl_xor_sync(FULL, bv, o);
+                const int oi = __shfl_xor_sync(FULL, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            if (g == 0) {
+                s_v[warp * NB + b] = bv;
+                s_i[warp * NB + b] = bi;
+            }
+        }
+        __syncthreads();
+        if ((int)threadIdx.x < NB) {
+            const int b = threadIdx.x;
+            float bv = -INFINITY;
+            int bi = 0x7FFFFFFF;
+            for (int w = 0; w < GT; w++) {   // increasing rows
+                const float v = s_v[w * NB + b];
+                const int i = s_i[w * NB + b];
+                if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+            }
+            if (b < p.B) {
+                p.amax_val[grp * MAX_B + b] = bv;
+                p.amax_idx[grp * MAX_B + b] = bi;
+            }
+        }
+    }
+}
+
+// Bounded wait on a stage's mbarrier; on timeout the status word records it.
+__device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (1LL << 32)) {   // ~2 s: a copy that never lands
+            if (status) atomicOr(status, STATUS_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+
+__host__ __device__ __forceinline__ uint32_t stage_bytes_of(int B) {
+    uint32_t raw = GROUP_BYTES + (uint32_t)B * 1024u + LO_SKEW + (uint32_t)B * 32u;
+    return (raw + 127u) & ~127u;
+}
+
+// ------------------------------------------------------------- kernel ---
+// NT n-tiles of 4 batch rows each (IMPL 2), or NT batch rows (IMPL 1, NT <= 4).
+template <int NT, int EPI, int IMPL>
+__global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const GemmParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_bad;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
+    const int cs = p.cs, rank = blockIdx.x % cs, grp = blockIdx.x / cs;
+    const int rt = grp * GT + warp;
+    const int s0 = rank * p.nsb / cs, s1 = (rank + 1) * p.nsb / cs, n = s1 - s0;
+    const int B = p.B, D = p.stages;
+    const uint32_t abytes = (uint32_t)B * 512u, sbytes = (uint32_t)B * 32u;
+    const uint32_t tx = GROUP_BYTES + 2 * abytes + sbytes;
+    const uint32_t sbyt = stage_bytes_of(B);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)D * sbyt);
+    const uint8_t *gW = p.W + (size_t)grp * p.nsb * GROUP_BYTES;
+    auto stage = [&](int i) { return smem + (size_t)(i % D) * sbyt; };
+    auto issue_w = [&](int i) {
+        mbar_expect_tx(&full[i % D], tx);
+        bulk_g2s(stage(i), gW + (size_t)(s0 + i) * GROUP_BYTES, GROUP_BYTES, &full[i % D]);
+    };
+    auto issue_act = [&](int i) {
+        uint8_t *st = stage(i) + GROUP_BYTES;
+        const size_t sb = (size_t)(s0 + i);
+        bulk_g2s(st, p.x16 + sb * p.Bp * 256, abytes, &full[i % D]);
+        bulk_g2s(st + abytes + LO_SKEW, p.x16lo + sb * p.Bp * 256, abytes, &full[i % D]);
+        bulk_g2s(st + 2 * abytes + LO_SKEW, p.sx + sb * p.Bp * 16, sbytes, &full[i % D]);
+    };
+    if (threadIdx.x == 0) {
+        s_bad = 0;
+        for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int pre = min(D, n);
+    if (threadIdx.x == 0)
+        for (int i = 0; i < pre; i++) issue_w(i);
+    // warm L2 with this CTA's slice of the next kernel's read-only bytes, so the
+    // HBM keeps streaming while this grid drains and the next one ramps up
+    if (p.pf_ptr && p.pf_bytes) {
+        const size_t per = ((p.pf_bytes + gridDim.x - 1) / gridDim.x + 4095) & ~(size_t)4095;
+        const size_t beg = (size_t)blockIdx.x * per;
+        const size_t end = min(p.pf_bytes, beg + per);
+        for (size_t off = beg + (size_t)threadIdx.x * 4096; off < end; off += (size_t)blockDim.x * 4096)
+            prefetch_l2(p.pf_ptr + off, (uint32_t)min((size_t)4096, end - off));
+    }
     pdl_launch_dependents();
     pdl_wait();
+    if (threadIdx.x == 0)
+        for (int i = 0; i < pre; i++) issue_act(i);
 
-    const int K = p.nsb * QK;
-    int sb0 = ks * p.nsb / KS, sb1 = (ks + 1) * p.nsb / KS;
+    constexpr int NA = IMPL == 2 ? NT : 1;   // mma accumulator tiles
+    constexpr int NB = IMPL == 1 ? NT : 1;   // matvec columns
+    float acc[NA][4];
+#pragma unroll
+    for (int nt = 0; nt < NA; nt++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) acc[nt][i] = 0.0f;
     float accr[NB][2];
 #pragma unroll
     for (int c = 0; c < NB; c++) accr[c][0] = accr[c][1] = 0.0f;
-    if (valid) {
-        for (int sb = sb0; sb < sb1; sb++) {
-            const uint8_t *tile = p.W + ((size_t)rt * p.nsb + sb) * TILE_BYTES;
-            uint4 q[4];
-#pragma unroll
-            for (int c = 0; c < 4; c++) q[c] = ld_stream_u4(tile + c * 512 + 16 * lane);
-            TileMeta tm;
-            decode_meta(ld_stream_u2(tile + TILE_CODE_BYTES + 8 * lane), tig, tm);
-            float sq[NB][2];
-#pragma unroll
-            for (int c = 0; c < NB; c++) sq[c][0] = sq[c][1] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                const int h = c >> 1;
-                const __half2 cg = h ? tm.cg1 : tm.cg0, og = h ? tm.og1 : tm.og0;
-                const __half2 c8 = h ? tm.c81 : tm.c80, o8 = h ? tm.o81 : tm.o80;
-#pragma unroll
-                for (int pp = 0; pp < 2; pp++) {
-                    const int pidx = (c & 1) * 2 + pp;
-                    uint32_t w0 = pp ? q[c].z : q[c].x, w1 = pp ? q[c].w : q[c].y;
-                    uint32_t a0, a016, a0h, a0h16, a1, a116, a1h, a1h16;
-                    decode_word(w0, cg, og, a0, a016, a0h, a0h16);
-                    decode_word(w1, c8, o8, a1, a116, a1h, a1h16);
-                    const int koff = sb * QK + 32 * (2 * tig + h) + 8 * pidx;
-#pragma unroll
-                    for (int col = 0; col < NB; col++) {
-                        uint4 xv = ld_u4(p.x16 + (size_t)col * K + koff);
-                        sq[col][0] += dot2(a0, xv.x) + dot2(a0h, xv.y) + dot2(a016, xv.z) + dot2(a0h16, xv.w);
-                        sq[col][1] += dot2(a1, xv.x) + dot2(a1h, xv.y) + dot2(a116, xv.z) + dot2(a1h16, xv.w);
-                    }
-                }
+    // two stages per step: their loads, dequant and MMAs are independent, which
+    // gives each warp two dependency chains to interleave, and halves the
+    // block-wide syncs that release stages for refilling
+    bool ok = true;
+    for (int i = 0; i < n; i += 2) {
+        const bool two = i + 1 < n;
+        if (ok && !wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, p.status)) { ok = false; s_bad = 1; }
+        if (two && ok && !wait_stage(&full[(i + 1) % D], (uint32_t)((i + 1) / D) & 1u, p.status)) {
+            ok = false;
+            s_bad = 1;
+        }
+        if (ok && rt < p.nrt) {
+            if (IMPL == 2) {
+                stage_mma<NA>(stage(i), warp, lane, B, abytes, acc);
+                if (two) stage_mma<NA>(stage(i + 1), warp, lane, B, abytes, acc);
+            } else {
+                stage_fma<NB>(stage(i), warp, lane, abytes, accr);
+                if (two) stage_fma<NB>(stage(i + 1), warp, lane, abytes, accr);
             }
-            float2 mg = __half22float2(u32_as_h2(tm.mg)), m8 = __half22float2(u32_as_h2(tm.m8));
-#pragma unroll
-            for (int col = 0; col < NB; col++) {
-                uint2 s = p.sx[((size_t)col * p.nsb + sb) * 4 + tig];
-                float2 hi = __half22float2(u32_as_h2(s.x)), lo = __half22float2(u32_as_h2(s.y));
-                float s1 = hi.x + lo.x, s2 = hi.y + lo.y;
-                accr[col][0] += tm.dg * sq[col][0] - tm.dming * (mg.x * s1 + mg.y * s2);
-                accr[col][1] += tm.d8 * sq[col][1] - tm.dmin8 * (m8.x * s1 + m8.y * s2);
-            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && !s_bad) {
+            if (i + D < n) { issue_w(i + D); issue_act(i + D); }
+            if (two && i + 1 + D < n) { issue_w(i + 1 + D); issue_act(i + 1 + D); }
         }
     }
-    // every lane of a quad holds a quarter of each row's sum: butterfly over tig
+    const bool bad = s_bad != 0;
+    if (bad) {   // drain what may still be in flight (bounded); the result is abandoned
+        if (threadIdx.x == 0)
+            for (int i = max(0, n - D); i < n; i++) wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, nullptr);
+        __syncthreads();
+        if (cs == 1) return;   // cluster members still meet the two cluster barriers below
+    }
+    // per-lane outputs: y[nt][rho] for output row g + 8 rho, batch row 4nt + tig
+    constexpr int NY = IMPL == 2 ? NT : 1;
+    float y[NY][2];
+    if (IMPL == 2) {
 #pragma unroll
-    for (int c = 0; c < NB; c++)
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            accr[c][r] += __shfl_xor_sync(FULL, accr[c][r], 1);
-            accr[c][r] += __shfl_xor_sync(FULL, accr[c][r], 2);
+        for (int nt = 0; nt < NY; nt++) {
+            y[nt][0] = acc[nt < NA ? nt : 0][0] + acc[nt < NA ? nt : 0][1] * LO_UNSCALE;
+            y[nt][1] = acc[nt < NA ? nt : 0][2] + acc[nt < NA ? nt : 0][3] * LO_UNSCALE;
         }
-    // into the mma C-fragment layout so the epilogue is shared
-    float acc[1][4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        int col = 2 * tig + (i & 1), r = i >> 1;
-        float v = 0.0f;
+    } else {   // quad butterfly, then batch row tig
 #pragma unroll
         for (int c = 0; c < NB; c++)
-            if (c == col) v = accr[c][r];
-        acc[0][i] = v;
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                accr[c][r] += __shfl_xor_sync(FULL, accr[c][r], 1);
+                accr[c][r] += __shfl_xor_sync(FULL, accr[c][r], 2);
+            }
+        y[0][0] = y[0][1] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NB; c++)
+            if (c == tig) { y[0][0] = accr[c][0]; y[0][1] = accr[c][1]; }
     }
-    gemm_finish<1, EPI>(p, acc, valid, rt);
+    if (cs > 1) {   // K split across the cluster: rank 0 sums the partial tiles in rank order
+        cg::cluster_group cluster = cg::this_cluster();
+        float *red = reinterpret_cast<float *>(smem);   // every stage has been consumed
+#pragma unroll
+        for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+            for (int r = 0; r < 2; r++) red[((warp * NY + nt) * 2 + r) * 32 + lane] = y[nt][r];
+        cluster.sync();
+        if (rank == 0)
+            for (int rr = 1; rr < cs; rr++) {
+                const float *peer = cluster.map_shared_rank(red, rr);
+#pragma unroll
+                for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+                    for (int r = 0; r < 2; r++) y[nt][r] += peer[((warp * NY + nt) * 2 + r) * 32 + lane];
+            }
+        cluster.sync();
+        if (rank != 0 || bad) return;
+    }
+    if (p.rms_part) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
+        __shared__ float s_r[4 * NY];
+        if (warp == 0)
+            for (int b = 0; b < 4 * NY; b++) {
+                float ss = 0.0f;
+                if (b < B)
+                    for (int i = lane; i < p.rms_nparts; i += 32) ss += p.rms_part[i * MAX_B + b];
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+                if (lane == 0) s_r[b] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
+            }
+        __syncthreads();
+#pragma unroll
+        for (int nt = 0; nt < NY; nt++) {
+            y[nt][0] *= s_r[4 * nt + tig];
+            y[nt][1] *= s_r[4 * nt + tig];
+        }
+    }
+    gemm_epilogue<NY, EPI>(p, y, grp);
 }
 
 // ------------------------------------------------------------ dispatch ---
-int gemm_grid(const GemmParams &p) { return (p.nrt + p.rt_per_cta - 1) / p.rt_per_cta; }
+int gemm_grid(const GemmParams &p) { return n_groups(p.nrt) * p.cs; }
+
+int gemm_stages(int B) {
+    const uint32_t budget = B <= 8 ? 110u * 1024u : 200u * 1024u;   // two CTAs per SM up to B = 8
+    int d = (int)(budget / stage_bytes_of(B));
+    return d < 2 ? 2 : (d > 6 ? 6 : d);
+}
+
+template <int NT, int EPI, int IMPL>
+static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
+    p.stages = gemm_stages(p.B);
+    const size_t smem = (size_t)p.stages * stage_bytes_of(p.B) + 8 * 8;
+    static bool configured = false;   // raise the dynamic shared-memory limit once per instance
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_k(gemm_kernel<NT, EPI, IMPL>, dim3(gemm_grid(p)), dim3(256), smem, pdl, p.cs, s, p);
+}
 
 template <int EPI>
-static cudaError_t launch_gemm_epi(const GemmParams &p, int impl, bool pdl, cudaStream_t s) {
-    dim3 grid(gemm_grid(p)), block(256);
+static cudaError_t launch_epi(const GemmParams &p, int impl, bool pdl, cudaStream_t s) {
     if (impl == 1) {
         switch (p.B) {
-            case 1: return launch_k(gemm_matvec_kernel<1, EPI>, grid, block, 0, pdl, s, p);
-            case 2: return launch_k(gemm_matvec_kernel<2, EPI>, grid, block, 0, pdl, s, p);
-            case 3: return launch_k(gemm_matvec_kernel<3, EPI>, grid, block, 0, pdl, s, p);
-            case 4: return launch_k(gemm_matvec_kernel<4, EPI>, grid, block, 0, pdl, s, p);
+            case 1: return launch_one<1, EPI, 1>(p, pdl, s);
+            case 2: return launch_one<2, EPI, 1>(p, pdl, s);
+            case 3: return launch_one<3, EPI, 1>(p, pdl, s);
+            case 4: return launch_one<4, EPI, 1>(p, pdl, s);
             default: return cudaErrorInvalidValue;
         }
     }
-    switch ((p.B + 7) / 8) {
-        case 1: return launch_k(gemm_mma_kernel<1, EPI>, grid, block, 0, pdl, s, p);
-        case 2: return launch_k(gemm_mma_kernel<2, EPI>, grid, block, 0, pdl, s, p);
-        case 3: return launch_k(gemm_mma_kernel<3, EPI>, grid, block, 0, pdl, s, p);
-        case 4: return launch_k(gemm_mma_kernel<4, EPI>, grid, block, 0, pdl, s, p);
-        default: return cudaErrorInvalidValue;
-    }
+    if (p.B <= 4) return launch_one<1, EPI, 2>(p, pdl, s);
+    if (p.B <= 8) return launch_one<2, EPI, 2>(p, pdl, s);
+    if (p.B <= 16) return launch_one<4, EPI, 2>(p, pdl, s);
+    return launch_one<8, EPI, 2>(p, pdl, s);
 }
 
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream) {
-    if (p.rt_per_cta * p.ksplit != 8) return cudaErrorInvalidValue;
+    if (p.cs != 1 && p.cs != 2 && p.cs != 4 && p.cs != 8) return cudaErrorInvalidValue;
+    if (p.B < 1 || p.B > MAX_B || p.B > p.Bp || !p.x16 || !p.x16lo || !p.sx) return cudaErrorInvalidValue;
     switch (epi) {
-        case EPI_STORE: return launch_gemm_epi<EPI_STORE>(p, impl, pdl, stream);
-        case EPI_RESID: return launch_gemm_epi<EPI_RESID>(p, impl, pdl, stream);
-        case EPI_SWIGLU: return launch_gemm_epi<EPI_SWIGLU>(p, impl, pdl, stream);
-        case EPI_LMHEAD: return launch_gemm_epi<EPI_LMHEAD>(p, impl, pdl, stream);
+        case EPI_STORE: return launch_epi<EPI_STORE>(p, impl, pdl, stream);
+        case EPI_RESID: return launch_epi<EPI_RESID>(p, impl, pdl, stream);
+        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(p, impl, pdl, stream);
+        case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(p, impl, pdl, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -512,7 +661,7 @@ __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *_
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
                                 int32_t *ids, const int32_t *positions, int32_t *len_dev,
                                 bool pdl, cudaStream_t stream) {
-    return launch_k(argmax_final_kernel, dim3(B), dim3(256), 0, pdl, stream, amax_val, amax_idx,
+    return launch_k(argmax_final_kernel, dim3(B), dim3(256), 0, pdl, 1, stream, amax_val, amax_idx,
                     nparts, B, ids, positions, len_dev);
 }
 

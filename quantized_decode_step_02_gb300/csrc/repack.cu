@@ -65,7 +65,7 @@ __global__ void repack_kernel(const uint8_t *__restrict__ src0, const uint8_t *_
     parse_canon(blk[0], cb[0]);
     parse_canon(blk[1], cb[1]);
 
-    uint8_t *tile = dst + ((size_t)rt * nsb + sb) * TILE_BYTES;
+    uint8_t *tile = dst + tile_offset(rt, sb, nsb);
     int j1 = 2 * tig, j2 = 2 * tig + 1;
     for (int c = 0; c < 4; c++) {
         int h = c >> 1;
@@ -95,6 +95,7 @@ __global__ void repack_kernel(const uint8_t *__restrict__ src0, const uint8_t *_
 
 cudaError_t launch_repack(const uint8_t *src0, const uint8_t *src1, int interleave8, int src_rows,
                           int n_rowtiles, int nsb, uint8_t *dst, cudaStream_t stream) {
+    n_rowtiles = n_groups(n_rowtiles) * GT;   // pad to whole groups with zero blocks
     long warps = (long)n_rowtiles * nsb;
     int threads = 256;
     long blocks = (warps * 32 + threads - 1) / threads;
@@ -156,7 +157,7 @@ __global__ void export_canonical_kernel(const uint8_t *__restrict__ tiles, int r
     int r = (int)(t / nsb), sb = (int)(t % nsb);
     int rt, lr;
     map_row(row_map, row0 + r, rt, lr);
-    const uint8_t *tile = tiles + ((size_t)rt * nsb + sb) * TILE_BYTES;
+    const uint8_t *tile = tiles + tile_offset(rt, sb, nsb);
     uint16_t d, dmin;
     int sc[8], m[8];
     tile_row_fields(tile, lr, d, dmin, sc, m);
@@ -193,7 +194,7 @@ __global__ void dequant_rows_kernel(const uint8_t *__restrict__ tiles, int row_m
     int sb = rem >> 3, j = rem & 7;
     int rt, lr;
     map_row(row_map, row0 + r, rt, lr);
-    const uint8_t *tile = tiles + ((size_t)rt * nsb + sb) * TILE_BYTES;
+    const uint8_t *tile = tiles + tile_offset(rt, sb, nsb);
     uint16_t dbits, mbits;
     int sc[8], m[8];
     tile_row_fields(tile, lr, dbits, mbits, sc, m);
@@ -215,9 +216,11 @@ cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int 
 __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
                              const int32_t *tokens, const int32_t *positions,
                              const int32_t *len_dev, uint32_t *status, int B,
-                             float *__restrict__ x, int ldx) {
+                             float *__restrict__ x, int ldx, const float *__restrict__ gain,
+                             __half *u, __half *ulo, __half *usx, int Bp, float *part) {
     pdl_launch_dependents();
     pdl_wait();
+    __shared__ float red[32];
     int b = blockIdx.x;
     if (b >= B) return;
     int tok = tokens[b];
@@ -227,23 +230,46 @@ __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
         tok = 0;
     }
     int rt = tok >> 4, lr = tok & 15;
+    float ss = 0.0f;
     for (int t = threadIdx.x; t < nsb * 8; t += blockDim.x) {
         int sb = t >> 3, j = t & 7;
-        const uint8_t *tile = E + ((size_t)rt * nsb + sb) * TILE_BYTES;
+        const uint8_t *tile = E + tile_offset(rt, sb, nsb);
         uint16_t dbits, mbits;
         int sc[8], m[8];
         tile_row_fields(tile, lr, dbits, mbits, sc, m);
         float d = __half2float(__ushort_as_half(dbits)), dmin = __half2float(__ushort_as_half(mbits));
         float *o = x + (size_t)b * ldx + sb * 256 + 32 * j;
-        for (int i = 0; i < 32; i++) o[i] = dq_value(d, sc[j], dmin, m[j], tile_q(tile, lr, 32 * j + i));
+        float usum = 0.0f;
+        for (int c = 0; c < 4; c++) {
+            float y[8];
+            for (int i = 0; i < 8; i++) {
+                const int k = 32 * j + 8 * c + i;
+                float w = dq_value(d, sc[j], dmin, m[j], tile_q(tile, lr, k));
+                o[8 * c + i] = w;
+                ss = fmaf(w, w, ss);
+                y[i] = w * gain[sb * 256 + k];
+                usum += y[i];
+            }
+            store_act8(u, ulo, act_chunk(sb, b, 4 * j + c, Bp), y);
+        }
+        store_sum(usx, sb, b, j, Bp, usum);
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.0f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += red[w];
+        part[b] = tot;
     }
 }
 
 cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
                          const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
-                         float *x, int ldx, bool pdl, cudaStream_t stream) {
-    return launch_k(embed_kernel, dim3(B), dim3(128), 0, pdl, stream, E, nsb, vocab, tokens,
-                    positions, len_dev, status, B, x, ldx);
+                         float *x, int ldx, const float *gain, __half *u, __half *ulo, __half *usx,
+                         int Bp, float *part, bool pdl, cudaStream_t stream) {
+    return launch_k(embed_kernel, dim3(B), dim3(128), 0, pdl, 1, stream, E, nsb, vocab, tokens,
+                    positions, len_dev, status, B, x, ldx, gain, u, ulo, usx, Bp, part);
 }
 
 }  // namespace zdec

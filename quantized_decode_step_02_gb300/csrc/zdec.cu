@@ -24,7 +24,16 @@ namespace {
 thread_local std::string g_global_error;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-size_t tile_bytes(int rows16, int nsb) { return (size_t)rows16 * nsb * TILE_BYTES; }
+// Bytes of a matrix of rows16 row tiles in the grouped layout (padded to whole groups).
+size_t tile_bytes(int rows16, int nsb) { return (size_t)n_groups(rows16) * nsb * GROUP_BYTES; }
+
+// K split (cluster size) for a projection: grow it until the grid covers the
+// GPU, keeping at least two super-blocks per CTA.
+int pick_cs(int groups, int nsb, int num_sms) {
+    int cs = 1;
+    while (cs < 8 && groups * cs < num_sms && nsb / (cs * 2) >= 2) cs *= 2;
+    return cs;
+}
 
 struct LayerW {
     uint8_t *qkv, *o, *gu, *down;
@@ -60,8 +69,13 @@ struct zdec_ctx {
     float *x = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *logits = nullptr;
     float *part = nullptr, *amax_v = nullptr;
     int *amax_i = nullptr, *tickets = nullptr;
-    __half *x16 = nullptr;
-    uint2 *sx = nullptr;
+    float *rms_part = nullptr;          // per-group sums of x^2 feeding the next RMSNorm scale
+    // GEMM act planes (hi, lo) and sub-block sums: x* for the normed residual,
+    // o* for the attention output, a* for the SwiGLU output
+    __half *x16 = nullptr, *x16lo = nullptr, *sx = nullptr;
+    __half *o16 = nullptr, *o16lo = nullptr, *osx = nullptr;
+    __half *a16 = nullptr, *a16lo = nullptr, *asx = nullptr;
+    int cs_qkv = 1, cs_o = 1, cs_gu = 1, cs_down = 1, cs_lm = 1;
     int32_t *tok_dev = nullptr, *pos_dev = nullptr, *ids_dev = nullptr, *len_dev = nullptr;
     uint32_t *status = nullptr;
     int32_t *pinned_io = nullptr;      // [2*max_B] staging of host tokens/positions
@@ -296,7 +310,7 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     {
         const int Bm = max_B, Bp = ctx->Bp_max;
         const int Kmax = std::max({H, F, ctx->qd});
-        int lm_grid = (ctx->nrt_vocab + 7) / 8;
+        int lm_grid = n_groups(ctx->nrt_vocab) * 8;   // any cluster split of the LM head
         size_t w = 0;
         auto t = [&](size_t bytes) { size_t o = w; w = align_up(w + bytes, 256); return o; };
         size_t ox = t((size_t)Bm * H * 4), oqkv = t((size_t)Bm * ctx->qkv_ld * 4), oo2 = t((size_t)Bm * ctx->qd * 4);
@@ -304,7 +318,13 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
         size_t opart = t((size_t)Bm * d.n_kv_heads * 64 * 4 * (HD + 2) * 4);
         size_t oav = t((size_t)lm_grid * MAX_B * 4), oai = t((size_t)lm_grid * MAX_B * 4);
         size_t otk = t((size_t)Bm * d.n_kv_heads * 4);
-        size_t ox16 = t((size_t)Bp * Kmax * 2), osx = t((size_t)Bp * (Kmax / QK) * 4 * 8);
+        size_t orms = t((size_t)(n_groups(H / 16) + 1) * MAX_B * 4);
+        auto plane = [&](int K) { return (size_t)(K / QK) * Bp * 256 * 2; };
+        auto sums = [&](int K) { return (size_t)(K / QK) * Bp * 16 * 2; };
+        size_t ox16 = t(plane(H)), ox16lo = t(plane(H)), osx = t(sums(H));
+        size_t oo16 = t(plane(ctx->qd)), oo16lo = t(plane(ctx->qd)), oosx = t(sums(ctx->qd));
+        size_t oa16 = t(plane(F)), oa16lo = t(plane(F)), oasx = t(sums(F));
+        (void)Kmax;
         size_t otok = t(Bm * 4), opos = t(Bm * 4), oids = t(Bm * 4), olen = t(Bm * 4), ost = t(4);
         ctx->ws_bytes = w;
         if (cudaMalloc(&ctx->ws, w) != cudaSuccess) {
@@ -315,7 +335,10 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
         ctx->x = (float *)(b + ox); ctx->qkv = (float *)(b + oqkv); ctx->o = (float *)(b + oo2);
         ctx->act = (float *)(b + oact); ctx->logits = (float *)(b + olog); ctx->part = (float *)(b + opart);
         ctx->amax_v = (float *)(b + oav); ctx->amax_i = (int *)(b + oai); ctx->tickets = (int *)(b + otk);
-        ctx->x16 = (__half *)(b + ox16); ctx->sx = (uint2 *)(b + osx);
+        ctx->rms_part = (float *)(b + orms);
+        ctx->x16 = (__half *)(b + ox16); ctx->x16lo = (__half *)(b + ox16lo); ctx->sx = (__half *)(b + osx);
+        ctx->o16 = (__half *)(b + oo16); ctx->o16lo = (__half *)(b + oo16lo); ctx->osx = (__half *)(b + oosx);
+        ctx->a16 = (__half *)(b + oa16); ctx->a16lo = (__half *)(b + oa16lo); ctx->asx = (__half *)(b + oasx);
         ctx->tok_dev = (int32_t *)(b + otok); ctx->pos_dev = (int32_t *)(b + opos);
         ctx->ids_dev = (int32_t *)(b + oids); ctx->len_dev = (int32_t *)(b + olen);
         ctx->status = (uint32_t *)(b + ost);
@@ -323,6 +346,14 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
             return bail(fail(nullptr, ZDEC_ERR_CUDA, "workspace memset failed"));
         if (cudaMallocHost(&ctx->pinned_io, 2 * Bm * sizeof(int32_t)) != cudaSuccess)
             return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate pinned staging"));
+    }
+    {
+        const int nsm = ctx->num_sms > 0 ? ctx->num_sms : 148;
+        ctx->cs_qkv = pick_cs(n_groups(ctx->qkv_ld / 16), ctx->nsb_h, nsm);
+        ctx->cs_o = pick_cs(n_groups(H / 16), ctx->nsb_q, nsm);
+        ctx->cs_gu = pick_cs(n_groups(F / 8), ctx->nsb_h, nsm);
+        ctx->cs_down = pick_cs(n_groups(H / 16), ctx->nsb_f, nsm);
+        ctx->cs_lm = pick_cs(n_groups(ctx->nrt_vocab), ctx->nsb_h, nsm);
     }
     if (attention_setup(kv_dtype) != cudaSuccess)
         return bail(fail(nullptr, ZDEC_ERR_CUDA, "attention smem attribute failed"));
@@ -406,10 +437,12 @@ extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
 }
 
 // --------------------------------------------------------------- step ---
-static int attn_splits(const zdec_ctx *ctx, int B) {
-    int per = B * ctx->d.n_kv_heads;
-    int s = (4 * ctx->num_sms + per - 1) / per;
-    return std::max(1, std::min(64, s));
+// CTAs per (sequence, kv head) for the attention cluster: a power of two that
+// gives about two CTAs per SM, at most 16.
+static int attn_cluster(const zdec_ctx *ctx, int B) {
+    int per = B * ctx->d.n_kv_heads, want = (2 * ctx->num_sms + per - 1) / per, cs = 1;
+    while (cs < want && cs < 16) cs *= 2;
+    return cs;
 }
 
 static int pick_impl(const zdec_ctx *ctx, int B) {
@@ -422,7 +455,7 @@ static int pick_impl(const zdec_ctx *ctx, int B) {
 // Enqueue the whole step for rows 0..B-1.  logits_out may be null.
 static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pdl) {
     const zdec_model_desc &d = ctx->d;
-    const int H = d.hidden, F = d.ffn, Bp = (int)align_up((size_t)B, 8);
+    const int H = d.hidden, F = d.ffn;
     const int impl = pick_impl(ctx, B);
     cudaStream_t s = ctx->stream;
     int nk = 0;
@@ -453,13 +486,31 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         nk++;                            \
     } while (0)
 
+    const int Bp0 = ctx->Bp_max;
     STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev,
-                                         ctx->len_dev, ctx->status, B, ctx->x, H, pdl, s));
+                                         ctx->len_dev, ctx->status, B, ctx->x, H, ctx->L[0].attn_norm,
+                                         ctx->x16, ctx->x16lo, ctx->sx, Bp0, ctx->rms_part, pdl, s));
     if ((e = capture_x(0)) != cudaSuccess) return e;
+    const int Bp = ctx->Bp_max;   // row pitch of every act plane
     GemmParams gp{};
-    gp.x16 = ctx->x16;
-    gp.sx = ctx->sx;
     gp.B = B;
+    gp.Bp = Bp;
+    gp.out_Bp = Bp;
+    gp.status = ctx->status;
+    // Every projection takes its activation as fp16 hi + lo planes (~22 bits):
+    // the new K/V rows are rounded and quantized, and over dozens of layers a
+    // single fp16 operand would drift past the parity tolerance.
+    auto operand = [&](__half *hi, __half *lo, __half *sums) { gp.x16 = hi; gp.x16lo = lo; gp.sx = sums; };
+    auto matrix = [&](const uint8_t *W, int N, int nrt, int nsb, int cs) {
+        gp.W = W; gp.N = N; gp.nrt = nrt; gp.nsb = nsb; gp.cs = cs;
+        gp.pf_ptr = nullptr; gp.pf_bytes = 0;
+    };
+    // the next weight matrix to warm in L2 while a GEMM runs (capped so the
+    // prefetched bytes and the running kernel's stream fit in L2 together)
+    auto prefetch = [&](const uint8_t *W, int nrt, int nsb) {
+        gp.pf_ptr = W;
+        gp.pf_bytes = std::min(tile_bytes(nrt, nsb), (size_t)64 << 20);
+    };
     AttnParams ap{};
     ap.kv = ctx->arena;
     ap.nq = d.n_q_heads;
@@ -468,44 +519,70 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     ap.qkv_ld = ctx->qkv_ld;
     ap.rope = ctx->rope;
     ap.append = 1;
-    ap.S = attn_splits(ctx, B);
-    ap.part = ctx->part;
-    ap.tickets = ctx->tickets;
+    ap.cs = attn_cluster(ctx, B);
     ap.o = ctx->o;
+    ap.o16 = ctx->o16;
+    ap.o16lo = ctx->o16lo;
+    ap.osx = ctx->osx;
+    ap.oBp = Bp;
     ap.B = B;
     ap.max_L = ctx->max_L;
+    // RMSNorm never runs as its own kernel: the producer of the residual (the
+    // embedding gather, the O and down projections) writes gain*x as the next
+    // projection's operand plus per-group sums of x^2, and the consumer scales
+    // its outputs by r = 1/sqrt(mean x^2 + eps).
+    const int resid_groups = n_groups(H / 16);
+    auto normed_input = [&](int nparts) {
+        operand(ctx->x16, ctx->x16lo, ctx->sx);
+        gp.rms_part = ctx->rms_part; gp.rms_nparts = nparts; gp.rms_K = H; gp.rms_eps = d.rms_eps;
+    };
+    auto plain_input = [&](__half *hi, __half *lo, __half *sums) {
+        operand(hi, lo, sums);
+        gp.rms_part = nullptr;
+    };
     for (int l = 0; l < d.n_layers; l++) {
         const LayerW &lw = ctx->L[l];
-        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->x, H, H, lw.attn_norm, d.rms_eps, B, Bp, ctx->x16, ctx->sx, pdl, s));
-        gp.W = lw.qkv; gp.N = ctx->qkv_ld; gp.nrt = ctx->qkv_ld / 16; gp.nsb = ctx->nsb_h;
-        gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld; gp.rt_per_cta = 2; gp.ksplit = 4;
+        normed_input(l == 0 ? 1 : resid_groups);
+        matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, ctx->cs_qkv);
+        prefetch(lw.o, H / 16, ctx->nsb_q);
+        gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld;
         STEP(ZDEC_KERNEL_GEMM_QKV, launch_gemm(gp, EPI_STORE, impl, pdl, s));
         ap.layer = l;
         STEP(ZDEC_KERNEL_ATTENTION, launch_attention(ap, pdl, s));
-        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->o, ctx->qd, ctx->qd, nullptr, 0.0f, B, Bp, ctx->x16, ctx->sx, pdl, s));
-        gp.W = lw.o; gp.N = H; gp.nrt = H / 16; gp.nsb = ctx->nsb_q;
-        gp.out = ctx->x; gp.ldo = H; gp.rt_per_cta = 1; gp.ksplit = 8;
+        plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention combine
+        matrix(lw.o, H, H / 16, ctx->nsb_q, ctx->cs_o);
+        prefetch(lw.gu, F / 8, ctx->nsb_h);
+        gp.out = ctx->x; gp.ldo = H;
+        gp.next_gain = lw.ffn_norm; gp.part_out = ctx->rms_part;
+        gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
         STEP(ZDEC_KERNEL_GEMM_O, launch_gemm(gp, EPI_RESID, impl, pdl, s));
-        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->x, H, H, lw.ffn_norm, d.rms_eps, B, Bp, ctx->x16, ctx->sx, pdl, s));
-        gp.W = lw.gu; gp.N = F; gp.nrt = F / 8; gp.nsb = ctx->nsb_h;
-        gp.out = ctx->act; gp.ldo = F; gp.rt_per_cta = 4; gp.ksplit = 2;
+        normed_input(resid_groups);
+        matrix(lw.gu, F, F / 8, ctx->nsb_h, ctx->cs_gu);
+        prefetch(lw.down, H / 16, ctx->nsb_f);
+        gp.out = nullptr; gp.ldo = F;
+        gp.out16 = ctx->a16; gp.out16lo = ctx->a16lo; gp.out_sx = ctx->asx;
         STEP(ZDEC_KERNEL_GEMM_GATEUP, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s));
-        STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->act, F, F, nullptr, 0.0f, B, Bp, ctx->x16, ctx->sx, pdl, s));
-        gp.W = lw.down; gp.N = H; gp.nrt = H / 16; gp.nsb = ctx->nsb_f;
-        gp.out = ctx->x; gp.ldo = H; gp.rt_per_cta = 1; gp.ksplit = 8;
+        plain_input(ctx->a16, ctx->a16lo, ctx->asx);   // written by the gate/up epilogue
+        matrix(lw.down, H, H / 16, ctx->nsb_f, ctx->cs_down);
+        if (l + 1 < d.n_layers) prefetch(ctx->L[l + 1].qkv, ctx->qkv_ld / 16, ctx->nsb_h);
+        else prefetch(ctx->embed, ctx->nrt_vocab, ctx->nsb_h);
+        gp.out = ctx->x; gp.ldo = H;
+        gp.next_gain = l + 1 < d.n_layers ? ctx->L[l + 1].attn_norm : ctx->final_norm;
+        gp.part_out = ctx->rms_part;
+        gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
         STEP(ZDEC_KERNEL_GEMM_DOWN, launch_gemm(gp, EPI_RESID, impl, pdl, s));
         if ((e = capture_x(l + 1)) != cudaSuccess) return e;
     }
-    STEP(ZDEC_KERNEL_PREP, launch_prep(ctx->x, H, H, ctx->final_norm, d.rms_eps, B, Bp, ctx->x16, ctx->sx, pdl, s));
-    gp.W = ctx->embed; gp.N = d.vocab; gp.nrt = ctx->nrt_vocab; gp.nsb = ctx->nsb_h;
-    gp.out = logits_out; gp.ldo = d.vocab; gp.rt_per_cta = 8; gp.ksplit = 1;
+    normed_input(resid_groups);
+    matrix(ctx->embed, d.vocab, ctx->nrt_vocab, ctx->nsb_h, ctx->cs_lm);
+    gp.out = logits_out; gp.ldo = d.vocab;
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
     STEP(ZDEC_KERNEL_GEMM_LMHEAD, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s));
     STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, gemm_grid(gp), B, ctx->ids_dev,
                                                  ctx->pos_dev, ctx->len_dev, pdl, s));
 #undef STEP
     ctx->last_kernels = nk;
-    ctx->last_splits = ap.S;
+    ctx->last_splits = ap.cs;
     return cudaSuccess;
 }
 
@@ -777,10 +854,12 @@ extern "C" zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, con
     ap.qkv_ld = ctx->qkv_ld;
     ap.rope = ctx->rope;
     ap.append = 0;
-    ap.S = attn_splits(ctx, B);
-    ap.part = ctx->part;
-    ap.tickets = ctx->tickets;
+    ap.cs = attn_cluster(ctx, B);
     ap.o = ctx->o;
+    ap.o16 = ctx->o16;
+    ap.o16lo = ctx->o16lo;
+    ap.osx = ctx->osx;
+    ap.oBp = ctx->Bp_max;
     ap.B = B;
     ap.max_L = ctx->max_L;
     CK(launch_attention(ap, false, ctx->stream));
@@ -792,7 +871,7 @@ extern "C" zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, con
 // ---------------------------------------------------------- stateless ---
 extern "C" size_t zdec_q4k_repacked_bytes(int N, int K) {
     if (N <= 0 || K <= 0 || N % 16 || K % QK) return 0;
-    return (size_t)N * (K / QK) * CANON_BLOCK;
+    return tile_bytes(N / 16, K / QK);
 }
 
 extern "C" zdec_status zdec_q4k_repack(const void *canonical_dev, int N, int K, void *repacked_dev, void *stream) {
@@ -806,8 +885,8 @@ extern "C" zdec_status zdec_q4k_repack(const void *canonical_dev, int N, int K, 
 
 extern "C" size_t zdec_q4k_gemm_workspace_bytes(int K, int B) {
     if (K <= 0 || K % QK || B < 1 || B > MAX_B) return 0;
-    size_t Bp = align_up((size_t)B, 8);
-    return align_up(Bp * K * 2, 256) + Bp * (K / QK) * 4 * 8;
+    const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
+    return 2 * plane + (size_t)(K / QK) * B * 16 * 2 + 256;
 }
 
 extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B, float *y_dev,
@@ -820,23 +899,28 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
     if (workspace_bytes < zdec_q4k_gemm_workspace_bytes(K, B)) return fail(ctx, ZDEC_ERR_ARG, "workspace too small");
     if ((uintptr_t)workspace_dev % 16 || (uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "pointers must be 16-byte aligned");
-    size_t Bp = align_up((size_t)B, 8);
-    __half *x16 = (__half *)workspace_dev;
-    uint2 *sx = (uint2 *)((uint8_t *)workspace_dev + align_up(Bp * K * 2, 256));
+    const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
+    __half *hi = (__half *)workspace_dev;
+    __half *lo = (__half *)((uint8_t *)workspace_dev + plane);
+    __half *sums = (__half *)((uint8_t *)workspace_dev + 2 * plane);
     cudaStream_t s = (cudaStream_t)stream;
-    CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, (int)Bp, x16, sx, false, s));
+    CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, B, hi, lo, sums, false, s));
+    int dev = 0, nsm = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     GemmParams gp{};
     gp.W = (const uint8_t *)repacked_dev;
     gp.N = N;
     gp.nrt = N / 16;
     gp.nsb = K / QK;
-    gp.x16 = x16;
-    gp.sx = sx;
+    gp.x16 = hi;
+    gp.x16lo = lo;
+    gp.sx = sums;
     gp.B = B;
+    gp.Bp = B;
     gp.out = y_dev;
     gp.ldo = N;
-    gp.rt_per_cta = 2;
-    gp.ksplit = 4;
+    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm);
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
 }

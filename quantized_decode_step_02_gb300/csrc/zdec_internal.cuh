@@ -2,8 +2,11 @@
 //
 // Repacked Q4_K layout ("tile blocks").  A matrix of N rows x K columns is cut
 // into row tiles of 16 rows; each (row tile, super-block of 256 columns) is one
-// 2304-byte tile block (= 16 canonical 144-byte blocks), stored row tile major:
-//   offset(rt, sb) = (rt * nsb + sb) * 2304,  nsb = K / 256.
+// 2304-byte tile block (= 16 canonical 144-byte blocks).  Eight consecutive row
+// tiles form a group (128 rows); the eight tile blocks of one (group,
+// super-block) are adjacent, so a GEMM stage is one 18,432-byte bulk copy:
+//   offset(rt, sb) = ((rt / 8) * nsb + sb) * 18432 + (rt % 8) * 2304,
+// nsb = K / 256.  The row count is padded to a whole group with zero blocks.
 // Inside a tile block the bytes are arranged for the warp that multiplies it
 // with mma.sync.m16n8k16 (lane = 4*g + tig, g = lane/4, tig = lane%4):
 //   [0, 2048)    codes: 4 chunks of 512 B; chunk c, lane l -> 16 bytes at
@@ -39,6 +42,30 @@ constexpr int HD = 128;                 // head_dim the attention kernel impleme
 constexpr int GROUP = 4;                // query heads per kv head the kernel implements
 constexpr int ATT_CHUNK = 64;           // tokens per attention smem chunk
 constexpr int MAX_B = 32;
+constexpr int GT = 8;                   // row tiles per group (one per GEMM warp)
+constexpr int GROUP_BYTES = GT * TILE_BYTES;
+
+__host__ __device__ __forceinline__ size_t tile_offset(int rt, int sb, int nsb) {
+    return ((size_t)(rt >> 3) * nsb + sb) * GROUP_BYTES + (size_t)(rt & 7) * TILE_BYTES;
+}
+__host__ __device__ __forceinline__ int n_groups(int n_rowtiles) { return (n_rowtiles + GT - 1) / GT; }
+
+// GEMM activation operand ("act planes").  For every super-block sb the rows
+// b = 0..Bp-1 hold that super-block's 256 values as fp16, elements 4..7 of
+// every 8 divided by 16 (matching the nibble layout), in 32 chunks of 8.  Chunk
+// c of row b sits at chunk position c ^ ((c >> 3) | ((b & 1) << 2)) so that the
+// eight lanes of a shared-memory phase (two rows, four tigs) hit eight
+// different bank groups.  A plane is [nsb][Bp][256] halves; the hi and lo
+// parts of a split operand are two planes.  The sub-block sums are
+// [nsb][Bp][4 tig][4] halves: (hi_2tig, hi_2tig+1, lo_2tig, lo_2tig+1) where
+// hi + lo is the fp32 sum of the 32 values of sub-block j.
+__host__ __device__ __forceinline__ size_t act_chunk(int sb, int b, int c, int Bp) {
+    int pc = c ^ ((c >> 3) | ((b & 1) << 2));
+    return ((size_t)sb * Bp + b) * 256 + (size_t)pc * 8;
+}
+__host__ __device__ __forceinline__ size_t act_sum(int sb, int b, int j, int lo, int Bp) {
+    return (((size_t)sb * Bp + b) * 4 + (j >> 1)) * 4 + (lo ? 2 : 0) + (j & 1);
+}
 
 // offset -> nibble position inside a lane word, and back
 __host__ __device__ constexpr int nib_of_off(int o) {
@@ -83,7 +110,7 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
 // D = A(16x16 f16, row) * B(16x8 f16, col) + C(16x8 f32)
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1, const float (&c)[4]) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -98,13 +125,84 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// ------------------------------------------------- mbarrier + bulk copy ---
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// The lo plane holds (y - fp16(y)) * LO_SCALE: the residual is ~2^-11 |y|, and
+// scaling it by 2^10 keeps it out of the fp16 subnormal range for small
+// activations (the GEMM divides its lo accumulator by the same power of two).
+constexpr float LO_SCALE = 1024.0f;
+constexpr float LO_UNSCALE = 1.0f / 1024.0f;
+
+// fp16 hi + lo of eight values into act planes at element index idx (a chunk
+// start); elements 4..7 are stored divided by 16.  lo may be null.
+__device__ __forceinline__ void store_act8(__half *hi, __half *lo, size_t idx, const float (&y)[8]) {
+    __half h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        h[i] = __float2half_rn(y[i]);
+        l[i] = __float2half_rn((y[i] - __half2float(h[i])) * LO_SCALE);
+    }
+    const __half sixteenth = __float2half(0.0625f);
+#pragma unroll
+    for (int i = 4; i < 8; i++) {
+        h[i] = __hmul(h[i], sixteenth);
+        l[i] = __hmul(l[i], sixteenth);
+    }
+    uint4 v;
+    v.x = h2_as_u32(__halves2half2(h[0], h[1]));
+    v.y = h2_as_u32(__halves2half2(h[2], h[3]));
+    v.z = h2_as_u32(__halves2half2(h[4], h[5]));
+    v.w = h2_as_u32(__halves2half2(h[6], h[7]));
+    *reinterpret_cast<uint4 *>(hi + idx) = v;
+    if (lo) {
+        v.x = h2_as_u32(__halves2half2(l[0], l[1]));
+        v.y = h2_as_u32(__halves2half2(l[2], l[3]));
+        v.z = h2_as_u32(__halves2half2(l[4], l[5]));
+        v.w = h2_as_u32(__halves2half2(l[6], l[7]));
+        *reinterpret_cast<uint4 *>(lo + idx) = v;
+    }
+}
+// Sub-block sum `part` (fp32) of sub-block j of super-block sb, row b.
+__device__ __forceinline__ void store_sum(__half *sums, int sb, int b, int j, int Bp, float part) {
+    __half hi = __float2half_rn(part);
+    __half lo = __float2half_rn(part - __half2float(hi));
+    sums[act_sum(sb, b, j, 0, Bp)] = hi;
+    sums[act_sum(sb, b, j, 1, Bp)] = lo;
+}
 
 // ------------------------------------------------------- device status ---
 enum : uint32_t { STATUS_POSITION = 1u, STATUS_CAPACITY = 2u, STATUS_TIMEOUT = 4u, STATUS_TOKEN = 8u };
 
-// ------------------------------------------------------------ launchers ---
-struct GemmArgs;   // defined in zdec_kernels.cuh
 
 }  // namespace zdec

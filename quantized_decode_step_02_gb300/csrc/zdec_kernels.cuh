@@ -28,36 +28,55 @@ cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int 
                                 float *dst, cudaStream_t stream);
 // x[b][:] = dequant(E[tokens[b]]) for b < B; also checks positions against
 // the device lengths (status bit STATUS_POSITION on mismatch).
+// It also writes the first projection's operand gain*x (act planes, row pitch
+// Bp) and the sum of x^2 of each row into part[b] (one partial per row).
 cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
                          const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
-                         float *x, int ldx, bool pdl, cudaStream_t stream);
+                         float *x, int ldx, const float *gain, __half *u, __half *ulo, __half *usx,
+                         int Bp, float *part, bool pdl, cudaStream_t stream);
 
 // --------------------------------------------------------------- gemm.cu
 enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LMHEAD = 3 };
 
 struct GemmParams {
-    const uint8_t *W;      // tile blocks
-    int N;                 // valid output rows (<= 16 * nrt); SWIGLU: ffn rows
-    int nrt;               // row tiles
+    const uint8_t *W;      // grouped tile blocks
+    int N;                 // valid output rows (SWIGLU: ffn rows)
+    int nrt;               // row tiles (16 rows each; the storage is padded to groups of 8)
     int nsb;               // K / 256
-    const __half *x16;     // [Bp][K] fp16, offsets 4..7 of every 8 divided by 16
-    const uint2 *sx;       // [Bp][nsb][4] sub-block sums (hi, lo) pairs
-    int B;                 // valid batch rows
-    float *out;            // STORE: y[b*ldo + n]; RESID: x[b*ldo + n] += y; SWIGLU: a[b*ldo + f]
+    const __half *x16;     // act plane (hi) [nsb][Bp][256]
+    const __half *x16lo;   // act plane (lo) or nullptr
+    const __half *sx;      // sub-block sums [nsb][Bp][4][4]
+    int B;                 // batch rows used
+    int Bp;                // row pitch of the act planes
+    float *out;            // STORE: y[b*ldo + n]; RESID: x[b*ldo + n] += y; LMHEAD: logits or null
     int ldo;
+    __half *out16;         // SWIGLU, RESID with next_gain: act planes of the next
+    __half *out16lo;       //   projection (hi, lo) and its sub-block sums
+    __half *out_sx;
+    int out_Bp;
+    const float *next_gain;   // RESID: RMSNorm gain of the next projection (nullptr: none)
+    float *part_out;          // RESID: per-group sum of x^2 per column [grid][MAX_B]
+    const float *rms_part;    // consumer: partial sums of x^2 of its operand (nullptr: no norm)
+    int rms_nparts;
+    int rms_K;
+    float rms_eps;
     float *amax_val;       // LMHEAD: per-CTA argmax partials [grid][MAX_B]
     int *amax_idx;
-    int rt_per_cta;        // row tiles per CTA (RT)
-    int ksplit;            // K splits per CTA (KS); RT*KS == 8 warps
+    int cs;                // K split over a cluster of cs CTAs (1, 2, 4, 8)
+    int stages;            // pipeline depth (set by the launcher)
+    const uint8_t *pf_ptr; // read-only bytes the next kernel streams (L2 prefetch), or null
+    size_t pf_bytes;       // multiple of 16, pf_ptr 16-byte aligned
+    uint32_t *status;      // device status word (bounded-wait timeouts)
 };
 // impl 1: CUDA-core dequant-matvec (B <= 4); impl 2: mma.sync swap-AB GEMM.
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream);
 int gemm_grid(const GemmParams &p);
+int gemm_stages(int B);
 
 // prep: fp32 rows -> fp16 operand + sub-block sums.  gain != nullptr applies
 // RMSNorm (x * rsqrt(mean x^2 + eps) * gain).  Rows B..Bp-1 are zeroed.
-cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B,
-                        int Bp, __half *x16, uint2 *sx, bool pdl, cudaStream_t stream);
+cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B, int Bp,
+                        __half *hi, __half *lo, __half *sums, bool pdl, cudaStream_t stream);
 // ids[b] = argmax over the per-CTA partials (lowest index on ties); also
 // advances the device lengths: len_dev[b] = positions[b] + 1.
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
@@ -82,10 +101,12 @@ struct AttnParams {
     int qkv_ld;
     const float2 *rope;    // [max_L][64] (cos, sin)
     int append;            // 1: rotate q/k at pos and append k, v; 0: q already rotated, no append
-    int S;                 // splits per (b, kv head)
-    float *part;           // [B][n_kv][S][4][130]
-    int *tickets;          // [B][n_kv]
+    int cs;                // CTAs per (b, kv head): one thread-block cluster (1..16)
     float *o;              // [B][nq*128]
+    __half *o16;           // act planes (hi, lo) and sums of the O projection's input
+    __half *o16lo;
+    __half *osx;
+    int oBp;               // their row pitch
     int B;
     int max_L;             // positions >= max_L are ignored (the step is flagged elsewhere)
 };
@@ -101,19 +122,32 @@ cudaError_t launch_kv_read(const KvArena &a, int slot, int layer, int t0, int n,
                            uint8_t *v, uint16_t *ks, uint16_t *vs, cudaStream_t stream);
 
 // Launch helper with the programmatic-stream-serialization attribute.
+// Launch helper: optional programmatic stream serialization and a 1-D cluster
+// of `cluster` CTAs along x (1 = no cluster).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, bool pdl,
-                     cudaStream_t stream, Args &&...args) {
+                     int cluster, cudaStream_t stream, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        n++;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        n++;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

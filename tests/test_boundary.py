@@ -32,8 +32,9 @@ def test_size_queries():
     assert z.q4k_repacked_bytes(4095, 4096) == 0          # N must be a multiple of 16
     assert z.q4k_repacked_bytes(4096, 100) == 0
     ws = z.q4k_gemm_workspace_bytes(4096, 1)
-    assert ws >= 8 * 4096 * 2 + 8 * 16 * 4 * 8              # batch padded to 8 rows
+    assert ws >= 2 * 1 * 4096 * 2 + 16 * 16 * 2           # hi + lo planes of one row, sums
     assert z.q4k_gemm_workspace_bytes(4096, 33) == 0
+    assert z.q4k_repacked_bytes(144, 512) == 128 * 2 * 2 * 144   # rows padded to 128
 
 
 def _create(desc_kw, max_B=1, max_L=16):

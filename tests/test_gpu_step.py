@@ -176,7 +176,7 @@ def test_profile_step_reports_every_launch():
     ids = torch.empty(1, dtype=torch.int32, device=dev)
     rec = dec.profile_step(toks, pos, None, ids)
     kinds = [k for k, _ in rec]
-    assert len(rec) == dec.info()["kernels_per_step"] == 4 + 9 * d.n_layers
+    assert len(rec) == dec.info()["kernels_per_step"] == 3 + 5 * d.n_layers
     assert kinds.count("attention") == d.n_layers and kinds[-1] == "argmax"
     assert all(ms > 0 for _, ms in rec)
     dec.close()
