@@ -41,6 +41,23 @@ namespace zdec {
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 constexpr uint32_t LO_SKEW = 64;   // bytes between the hi and lo planes of a stage
 
+// Stage layout for a kernel covering BR = 4*NT batch rows (B of them real):
+//   [0, GROUP_BYTES)                 tile blocks of the group
+//   hi plane  BR x 512 bytes, LO_SKEW gap, lo plane BR x 512 bytes,
+//   sums BR x 32 bytes, then BR x 32 zero bytes (the lo lanes' min-term slots).
+// The bulk copies fill the first B rows of each plane; rows B..BR-1 are zeroed
+// once per stage buffer, so every lane reads its rows unconditionally.
+struct StageLayout {
+    uint32_t hi, lo, sums, zero, bytes;
+    __host__ __device__ StageLayout(int BR) {
+        hi = GROUP_BYTES;
+        lo = hi + (uint32_t)BR * 512u + LO_SKEW;
+        sums = lo + (uint32_t)BR * 512u;
+        zero = sums + (uint32_t)BR * 32u;
+        bytes = (zero + (uint32_t)BR * 32u + 127u) & ~127u;
+    }
+};
+
 // ------------------------------------------------------------------ prep ---
 // Block b converts fp32 row b into the act planes (hi, lo) and sub-block sums.
 // gain != nullptr applies RMSNorm: x * rsqrt(mean x^2 + eps) * gain.
@@ -153,14 +170,11 @@ __device__ __forceinline__ float dot2(uint32_t a, uint32_t x) {
 // columns (2tig, 2tig+1) owns both halves of batch row 4nt + tig.
 // acc[nt][0..3] = (row g, hi), (row g, lo), (row g+8, hi), (row g+8, lo).
 template <int NT>
-__device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane, int B,
-                                          uint32_t abytes, float (&acc)[NT][4]) {
-    const int g = lane >> 2, tig = lane & 3;
+__device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane, uint32_t act_off,
+                                          uint32_t sum_off, uint32_t swz, float (&acc)[NT][4]) {
+    const int tig = lane & 3;
     const uint8_t *tile = st + warp * TILE_BYTES;
-    // this lane's B column: hi plane, or the lo plane (placed 64 bytes further so
-    // that a hi lane and a lo lane of the same batch row use different banks)
-    const uint8_t *plane = st + GROUP_BYTES + ((g & 1) ? abytes + LO_SKEW : 0u);
-    const uint8_t *sums = st + GROUP_BYTES + 2 * abytes + LO_SKEW;
+    const uint8_t *act = st + act_off;   // this lane's B column of n-tile 0 (see gemm_kernel)
     uint4 q[4];
 #pragma unroll
     for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
@@ -185,14 +199,10 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
             uint32_t at[4], at16[4];
             decode_word(w0, cg, og, at[0], at16[0], at[2], at16[2]);
             decode_word(w1, c8, o8, at[1], at16[1], at[3], at16[3]);
-            const int chunk = tig * 8 + h * 4 + pidx;
+            const uint32_t off = ((uint32_t)(h * 4 + pidx) ^ swz) * 16;
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
-                const int b = 4 * nt + (g >> 1);
-                uint4 xv = make_uint4(0, 0, 0, 0);
-                if (b < B)
-                    xv = *reinterpret_cast<const uint4 *>(plane + b * 512 +
-                                                          ((chunk ^ (tig | ((b & 1) << 2))) * 16));
+                const uint4 xv = *reinterpret_cast<const uint4 *>(act + nt * 2048 + off);
                 mma16816(tq[nt], at, xv.x, xv.y, tq[nt]);
                 mma16816(t16[nt], at16, xv.z, xv.w, t16[nt]);
             }
@@ -201,9 +211,8 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
     const uint32_t am[4] = {tm.mg, tm.m8, tm.mg, tm.m8};
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
-        const int b = 4 * nt + (g >> 1);
-        uint2 s = make_uint2(0, 0);   // the min term goes to the hi column only
-        if (b < B && !(g & 1)) s = *reinterpret_cast<const uint2 *>(sums + b * 32 + tig * 8);
+        // the min term goes to the hi column only: lo lanes read a zero slot
+        const uint2 s = *reinterpret_cast<const uint2 *>(st + sum_off + nt * 128);
         mma16816(tmin[nt], am, s.x, s.y, zero4);
         acc[nt][0] += tm.dg * (tq[nt][0] + t16[nt][0]) - tm.dming * tmin[nt][0];
         acc[nt][1] += tm.dg * (tq[nt][1] + t16[nt][1]) - tm.dming * tmin[nt][1];
@@ -215,12 +224,12 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
 // CUDA-core dequant-matvec on the same stage (B <= 4); accr[col][rho] partial
 // over this lane's quarter of the row (summed across tig at the end).
 template <int NB>
-__device__ __forceinline__ void stage_fma(const uint8_t *st, int warp, int lane, uint32_t abytes,
+__device__ __forceinline__ void stage_fma(const uint8_t *st, int warp, int lane, const StageLayout &L,
                                           float (&accr)[NB][2]) {
     const int tig = lane & 3;
     const uint8_t *tile = st + warp * TILE_BYTES;
-    const uint8_t *ahi = st + GROUP_BYTES, *alo = ahi + abytes + LO_SKEW;
-    const uint8_t *sums = ahi + 2 * abytes + LO_SKEW;
+    const uint8_t *ahi = st + L.hi, *alo = st + L.lo;
+    const uint8_t *sums = st + L.sums;
     uint4 q[4];
 #pragma unroll
     for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
@@ -414,10 +423,7 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, uint3
 }
 
 
-__host__ __device__ __forceinline__ uint32_t stage_bytes_of(int B) {
-    uint32_t raw = GROUP_BYTES + (uint32_t)B * 1024u + LO_SKEW + (uint32_t)B * 32u;
-    return (raw + 127u) & ~127u;
-}
+
 
 // ------------------------------------------------------------- kernel ---
 // NT n-tiles of 4 batch rows each (IMPL 2), or NT batch rows (IMPL 1, NT <= 4).
@@ -430,9 +436,11 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
     const int rt = grp * GT + warp;
     const int s0 = rank * p.nsb / cs, s1 = (rank + 1) * p.nsb / cs, n = s1 - s0;
     const int B = p.B, D = p.stages;
+    constexpr int BR = IMPL == 2 ? 4 * NT : 4;   // batch rows held per stage
+    const StageLayout lay(BR);
     const uint32_t abytes = (uint32_t)B * 512u, sbytes = (uint32_t)B * 32u;
     const uint32_t tx = GROUP_BYTES + 2 * abytes + sbytes;
-    const uint32_t sbyt = stage_bytes_of(B);
+    const uint32_t sbyt = lay.bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)D * sbyt);
     const uint8_t *gW = p.W + (size_t)grp * p.nsb * GROUP_BYTES;
     auto stage = [&](int i) { return smem + (size_t)(i % D) * sbyt; };
@@ -443,16 +451,37 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
     auto issue_act = [&](int i) {
         uint8_t *st = stage(i) + GROUP_BYTES;
         const size_t sb = (size_t)(s0 + i);
-        bulk_g2s(st, p.x16 + sb * p.Bp * 256, abytes, &full[i % D]);
-        bulk_g2s(st + abytes + LO_SKEW, p.x16lo + sb * p.Bp * 256, abytes, &full[i % D]);
-        bulk_g2s(st + 2 * abytes + LO_SKEW, p.sx + sb * p.Bp * 16, sbytes, &full[i % D]);
+        bulk_g2s(st + (lay.hi - GROUP_BYTES), p.x16 + sb * p.Bp * 256, abytes, &full[i % D]);
+        bulk_g2s(st + (lay.lo - GROUP_BYTES), p.x16lo + sb * p.Bp * 256, abytes, &full[i % D]);
+        bulk_g2s(st + (lay.sums - GROUP_BYTES), p.sx + sb * p.Bp * 16, sbytes, &full[i % D]);
     };
     if (threadIdx.x == 0) {
         s_bad = 0;
         for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
         mbar_fence_init();
     }
+    // zero the batch rows the copies never write (rows B..BR-1 and the lo lanes'
+    // min-term slots) in every stage buffer
+    for (int i = threadIdx.x; i < D * BR * 8; i += blockDim.x) {
+        const int st = i / (BR * 8), r = (i / 8) % BR, w = i % 8;   // 8 x 16 bytes per 128-byte unit
+        uint8_t *base = smem + (size_t)st * sbyt;
+        if (r >= B) {
+            for (int k = 0; k < 4; k++) {
+                *reinterpret_cast<uint4 *>(base + lay.hi + r * 512 + (w * 4 + k) * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(base + lay.lo + r * 512 + (w * 4 + k) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            if (w < 2) *reinterpret_cast<uint4 *>(base + lay.sums + r * 32 + w * 16) = make_uint4(0, 0, 0, 0);
+        }
+        if (w < 2) *reinterpret_cast<uint4 *>(base + lay.zero + r * 32 + w * 16) = make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
+    // this lane's fixed offsets into a stage: virtual column g of n-tile 0 is the
+    // hi (g even) or lo (g odd) plane of batch row g/2
+    const int g = lane >> 2;
+    const uint32_t act_off = ((g & 1) ? lay.lo : lay.hi) + (uint32_t)(g >> 1) * 512u + (uint32_t)tig * 128u;
+    const uint32_t swz = (uint32_t)tig | ((uint32_t)((g >> 1) & 1) << 2);
+    const uint32_t sum_off = (g & 1) ? lay.zero + (uint32_t)tig * 8u
+                                     : lay.sums + (uint32_t)(g >> 1) * 32u + (uint32_t)tig * 8u;
     const int pre = min(D, n);
     if (threadIdx.x == 0)
         for (int i = 0; i < pre; i++) issue_w(i);
@@ -493,11 +522,11 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
         }
         if (ok && rt < p.nrt) {
             if (IMPL == 2) {
-                stage_mma<NA>(stage(i), warp, lane, B, abytes, acc);
-                if (two) stage_mma<NA>(stage(i + 1), warp, lane, B, abytes, acc);
+                stage_mma<NA>(stage(i), warp, lane, act_off, sum_off, swz, acc);
+                if (two) stage_mma<NA>(stage(i + 1), warp, lane, act_off, sum_off, swz, acc);
             } else {
-                stage_fma<NB>(stage(i), warp, lane, abytes, accr);
-                if (two) stage_fma<NB>(stage(i + 1), warp, lane, abytes, accr);
+                stage_fma<NB>(stage(i), warp, lane, lay, accr);
+                if (two) stage_fma<NB>(stage(i + 1), warp, lane, lay, accr);
             }
         }
         __syncthreads();
@@ -577,16 +606,19 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
 // ------------------------------------------------------------ dispatch ---
 int gemm_grid(const GemmParams &p) { return n_groups(p.nrt) * p.cs; }
 
-int gemm_stages(int B) {
+static int stages_for(uint32_t stage_bytes, int B) {
     const uint32_t budget = B <= 8 ? 110u * 1024u : 200u * 1024u;   // two CTAs per SM up to B = 8
-    int d = (int)(budget / stage_bytes_of(B));
+    int d = (int)(budget / stage_bytes);
     return d < 2 ? 2 : (d > 6 ? 6 : d);
 }
 
+int gemm_stages(int B) { return stages_for(StageLayout(4 * ((B + 3) / 4)).bytes, B); }
+
 template <int NT, int EPI, int IMPL>
 static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
-    p.stages = gemm_stages(p.B);
-    const size_t smem = (size_t)p.stages * stage_bytes_of(p.B) + 8 * 8;
+    const StageLayout lay(IMPL == 2 ? 4 * NT : 4);
+    p.stages = stages_for(lay.bytes, p.B);
+    const size_t smem = (size_t)p.stages * lay.bytes + 8 * 8;
     static bool configured = false;   // raise the dynamic shared-memory limit once per instance
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>,

@@ -82,6 +82,7 @@ struct zdec_ctx {
     // host state
     std::vector<int> len_host;
     int gemm_impl = 0, matvec_max_B = 0;
+    size_t prefetch_cap = 0;   // bytes of the next matrix a GEMM warms in L2 (0: off; ZDEC_L2_PREFETCH_MB)
     std::map<std::tuple<int, const void *, int>, cudaGraphExec_t> graphs;
     std::string err;
     int last_kernels = 0, last_splits = 0;
@@ -225,6 +226,7 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     ctx->L.resize(d.n_layers);
     ctx->len_host.assign(max_B, 0);
     if (const char *e = getenv("ZDEC_MATVEC_MAX_B")) ctx->matvec_max_B = std::max(0, std::min(4, atoi(e)));
+    if (const char *e = getenv("ZDEC_L2_PREFETCH_MB")) ctx->prefetch_cap = (size_t)std::max(0, atoi(e)) << 20;
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -440,8 +442,8 @@ extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
 // CTAs per (sequence, kv head) for the attention cluster: a power of two that
 // gives about two CTAs per SM, at most 16.
 static int attn_cluster(const zdec_ctx *ctx, int B) {
-    int per = B * ctx->d.n_kv_heads, want = (2 * ctx->num_sms + per - 1) / per, cs = 1;
-    while (cs < want && cs < 16) cs *= 2;
+    int per = B * ctx->d.n_kv_heads, cs = 1;   // largest power of two keeping one wave of 2 CTAs/SM
+    while (cs < 16 && per * cs * 2 <= 2 * ctx->num_sms) cs *= 2;
     return cs;
 }
 
@@ -509,7 +511,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     // prefetched bytes and the running kernel's stream fit in L2 together)
     auto prefetch = [&](const uint8_t *W, int nrt, int nsb) {
         gp.pf_ptr = W;
-        gp.pf_bytes = std::min(tile_bytes(nrt, nsb), (size_t)64 << 20);
+        gp.pf_bytes = std::min(tile_bytes(nrt, nsb), ctx->prefetch_cap);
     };
     AttnParams ap{};
     ap.kv = ctx->arena;
