@@ -216,6 +216,28 @@ zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x
                           float *y_dev, int impl, void *workspace_dev, size_t workspace_bytes,
                           void *stream);
 
+/* ---------------------------------------------- allocation-free variant ---
+ * The pages have no counterpart to this call: it is zdec_q4k_gemm without a
+ * workspace argument, for callers that cannot provide device memory (a plain
+ * C host with no device allocator of its own, or code that must not call
+ * cudaMalloc/cudaFree, which waits for the whole device).  It allocates
+ * nothing: its scratch is one array of 1,081,600 bytes per device that the
+ * library's module image holds, sized for K*B <= ZDEC_Q4K_GEMM_STATIC_MAX_KB.
+ * Arguments, layouts and results are those of zdec_q4k_gemm (the same
+ * kernels, so the outputs are bitwise equal).  Errors: K*B above the limit
+ * returns ZDEC_ERR_ARG, with the limit in zdec_last_global_error(), before
+ * any CUDA call; the other checks are zdec_q4k_gemm's.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, which may load the module); make that first call
+ *   before any stream capture begins on that device.
+ * - Calls whose kernels may overlap in time (different streams with no
+ *   ordering between them, or different host threads) share the array and
+ *   race on it: order them, e.g. on one stream or with events.  Consecutive
+ *   calls on one stream are safe. */
+#define ZDEC_Q4K_GEMM_STATIC_MAX_KB 262144
+zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int K, const float *x_dev, int B,
+                                 float *y_dev, int impl, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

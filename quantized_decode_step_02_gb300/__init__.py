@@ -16,10 +16,12 @@ import numpy as np
 from . import _build
 
 __all__ = ["ModelDesc", "Decoder", "ZdecError", "load_library", "q4k_repacked_bytes",
-           "q4k_repack", "q4k_gemm", "q4k_gemm_workspace_bytes", "KV_F16", "KV_Q8_0",
+           "q4k_repack", "q4k_gemm", "q4k_gemm_workspace_bytes", "q4k_gemm_static",
+           "Q4K_GEMM_STATIC_MAX_KB", "KV_F16", "KV_Q8_0",
            "KERNEL_KINDS", "T_EMBED", "T_WQ", "T_WK", "T_WV", "T_WO", "T_GATE", "T_UP", "T_DOWN"]
 
 KV_F16, KV_Q8_0 = 0, 1
+Q4K_GEMM_STATIC_MAX_KB = 262144   # K*B limit of q4k_gemm_static (ZDEC_Q4K_GEMM_STATIC_MAX_KB)
 STEP_HOST_IO, STEP_EAGER = 1, 2
 T_EMBED, T_WQ, T_WK, T_WV, T_WO, T_GATE, T_UP, T_DOWN = range(8)
 KERNEL_KINDS = ["embed", "prep", "gemm_qkv", "attention", "gemm_o", "gemm_gateup", "gemm_down",
@@ -33,7 +35,7 @@ EXPORTS = ["zdec_create", "zdec_destroy", "zdec_append_kv", "zdec_decode_step", 
            "zdec_set_gemm_impl", "zdec_get_info", "zdec_profile_step", "zdec_debug_export_q4k",
            "zdec_debug_dequant", "zdec_debug_read_kv", "zdec_debug_capture_hidden",
            "zdec_debug_attention", "zdec_q4k_repacked_bytes", "zdec_q4k_repack",
-           "zdec_q4k_gemm_workspace_bytes", "zdec_q4k_gemm"]
+           "zdec_q4k_gemm_workspace_bytes", "zdec_q4k_gemm", "zdec_q4k_gemm_static"]
 
 
 class ZdecError(RuntimeError):
@@ -108,6 +110,7 @@ def load_library(build_if_missing: bool = True):
         "zdec_q4k_repack": (i, [vp, i, i, vp, vp]),
         "zdec_q4k_gemm_workspace_bytes": (sz, [i, i]),
         "zdec_q4k_gemm": (i, [vp, i, i, vp, i, vp, i, vp, sz, vp]),
+        "zdec_q4k_gemm_static": (i, [vp, i, i, vp, i, vp, i, vp]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -354,3 +357,11 @@ def q4k_gemm(repacked_dev, N: int, K: int, x_dev, y_dev, impl: int, workspace_de
     _glob_check(load_library().zdec_q4k_gemm(_ptr(repacked_dev), N, K, _ptr(x_dev), B, _ptr(y_dev), impl,
                                              _ptr(workspace_dev), workspace_dev.numel() * workspace_dev.element_size(),
                                              ctypes.c_void_p(stream) if stream else None))
+
+
+def q4k_gemm_static(repacked_dev, N: int, K: int, x_dev, y_dev, impl: int, stream=None):
+    """q4k_gemm without a workspace: the library's own per-device scratch
+    (K*B <= Q4K_GEMM_STATIC_MAX_KB); calls that may overlap in time race on it."""
+    B = x_dev.shape[0]
+    _glob_check(load_library().zdec_q4k_gemm_static(_ptr(repacked_dev), N, K, _ptr(x_dev), B, _ptr(y_dev), impl,
+                                                    ctypes.c_void_p(stream) if stream else None))

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -910,6 +911,73 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     int dev = 0, nsm = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    GemmParams gp{};
+    gp.W = (const uint8_t *)repacked_dev;
+    gp.N = N;
+    gp.nrt = N / 16;
+    gp.nsb = K / QK;
+    gp.x16 = hi;
+    gp.x16lo = lo;
+    gp.sx = sums;
+    gp.B = B;
+    gp.Bp = B;
+    gp.out = y_dev;
+    gp.ldo = N;
+    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm);
+    CK(launch_gemm(gp, EPI_STORE, impl, false, s));
+    return ZDEC_OK;
+}
+
+// ------------------------------------------------- allocation-free GEMM ---
+// The stateless projection for callers that cannot hand over device memory:
+// a plain C host with no device allocator of its own, or a caller inside a
+// section that must not call cudaMalloc/cudaFree (cudaFree waits for the
+// whole device, stalling every other stream).  The activation planes that
+// zdec_q4k_gemm keeps in the caller's workspace live here in one file-scope
+// device array, sized for K*B <= ZDEC_Q4K_GEMM_STATIC_MAX_KB, with the same
+// layout (hi plane, lo plane, sub-block sums).  Nothing in it has to start at
+// zero: each call's prep kernel writes every byte its GEMM then reads.
+namespace {
+constexpr size_t kStaticPlaneBytes = (size_t)ZDEC_Q4K_GEMM_STATIC_MAX_KB * 2;   // a multiple of 256
+constexpr size_t kStaticScratchBytes =
+    2 * kStaticPlaneBytes + (size_t)ZDEC_Q4K_GEMM_STATIC_MAX_KB / QK * 16 * 2 + 256;
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_addr[kStaticMaxDevices];   // device address of the array, looked up once per device
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int K, const float *x_dev, int B,
+                                            float *y_dev, int impl, void *stream) {
+    zdec_ctx *ctx = nullptr;
+    if (!repacked_dev || !x_dev || !y_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
+    if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
+    if (B < 1 || B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "B must be in [1, %d]", MAX_B);
+    if (impl != 1 && impl != 2) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1 or 2");
+    if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
+    if ((long long)K * B > ZDEC_Q4K_GEMM_STATIC_MAX_KB)
+        return fail(ctx, ZDEC_ERR_ARG,
+                    "K*B = %lld exceeds the static scratch of zdec_q4k_gemm_static (K*B <= %d); "
+                    "use zdec_q4k_gemm with a caller workspace",
+                    (long long)K * B, ZDEC_Q4K_GEMM_STATIC_MAX_KB);
+    if ((uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "x_dev must be 16-byte aligned");
+    int dev = 0, nsm = 148;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kStaticMaxDevices) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    void *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_addr[dev]) CK(cudaGetSymbolAddress(&g_static_addr[dev], g_static_scratch));
+        base = g_static_addr[dev];
+    }
+    CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+    const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
+    __half *hi = (__half *)base;
+    __half *lo = (__half *)((uint8_t *)base + plane);
+    __half *sums = (__half *)((uint8_t *)base + 2 * plane);
+    cudaStream_t s = (cudaStream_t)stream;
+    CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, B, hi, lo, sums, false, s));
     GemmParams gp{};
     gp.W = (const uint8_t *)repacked_dev;
     gp.N = N;
