@@ -141,6 +141,36 @@ const char *zdec_last_global_error(void);
  * next step (cached CUDA graphs are rebuilt). */
 zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl);
 
+/* Which engine runs a step.  ZDEC_ENGINE_PERSISTENT: the whole step is one
+ * persistent cooperative kernel (two CTAs per SM, each streaming weight tiles
+ * and KV units through a shared-memory ring while counters in global memory
+ * order the phases); available for B <= 8 when the device supports
+ * cooperative launch and n_q_heads*head_dim == hidden.  ZDEC_ENGINE_KERNELS:
+ * one kernel per operation (embedding, per layer QKV, attention, O, gate/up,
+ * down; LM head, argmax).  ZDEC_ENGINE_AUTO (the default) runs the kernel
+ * engine, the faster of the two in every configuration measured so far.
+ * Forcing PERSISTENT where it is unavailable fails with ZDEC_ERR_UNSUPPORTED
+ * (here, or at the step).  Takes effect at the next step. */
+enum { ZDEC_ENGINE_AUTO = 0, ZDEC_ENGINE_KERNELS = 1, ZDEC_ENGINE_PERSISTENT = 2 };
+zdec_status zdec_set_engine(zdec_ctx *ctx, int engine);
+
+/* Phase timeline of the persistent engine (tracing).  on = 1 allocates a
+ * buffer of step_ctas * (2 + 5*n_layers) * 8 uint64 entries and makes every
+ * later step run without graph replay and record, per CTA c and phase ph
+ * (0 embedding; 1 + 5l + {0 QKV, 1 attention, 2 O, 3 gate/up, 4 down} of
+ * layer l; 1 + 5*n_layers LM head), at entry (c*phases + ph)*8 + k the GPU
+ * global timer in ns: k = 0 the consumer warps enter the phase, 1 its inputs
+ * are released, 2 the first item has landed, 3 the last item is consumed,
+ * 4 the phase's reductions and epilogues are done, 5 the producer issues the
+ * phase's first copy, 6 its first activation copy, and 7 = the number of
+ * items of the phase on that CTA (zero where a CTA has no work).  on = 0
+ * frees it.  ZDEC_ERR_UNSUPPORTED without the persistent engine. */
+zdec_status zdec_set_trace(zdec_ctx *ctx, int on);
+/* Copy the trace of the last traced step (waits for the stream).  *n gets the
+ * entry count (0 when tracing is off); out_host needs that many uint64
+ * (out_host = NULL: only the size query). */
+zdec_status zdec_debug_step_trace(zdec_ctx *ctx, uint64_t *out_host, size_t cap, size_t *n);
+
 typedef struct {
     size_t weight_bytes;      /* repacked weights on the device              */
     size_t arena_bytes;       /* KV arena                                    */
@@ -149,6 +179,8 @@ typedef struct {
     int kernels_per_step;     /* kernel launches of one step (last B used)   */
     int attn_splits;          /* split-K factor of the attention (last B)    */
     int matvec_max_B;         /* switch point in use                         */
+    int engine;               /* engine of the last step (ZDEC_ENGINE_*)     */
+    int step_ctas;            /* CTAs of the persistent kernel (0: unavailable) */
 } zdec_info;
 zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info);
 
@@ -158,7 +190,8 @@ zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info);
  * the number of launches.  The step is a real step (lengths advance). */
 enum { ZDEC_KERNEL_EMBED = 0, ZDEC_KERNEL_PREP = 1, ZDEC_KERNEL_GEMM_QKV = 2,
        ZDEC_KERNEL_ATTENTION = 3, ZDEC_KERNEL_GEMM_O = 4, ZDEC_KERNEL_GEMM_GATEUP = 5,
-       ZDEC_KERNEL_GEMM_DOWN = 6, ZDEC_KERNEL_GEMM_LMHEAD = 7, ZDEC_KERNEL_ARGMAX = 8 };
+       ZDEC_KERNEL_GEMM_DOWN = 6, ZDEC_KERNEL_GEMM_LMHEAD = 7, ZDEC_KERNEL_ARGMAX = 8,
+       ZDEC_KERNEL_STEP = 9 /* persistent engine: input check + the step kernel */ };
 zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *tokens_dev,
                               const int32_t *positions_dev, float *logits_dev, int32_t *ids_dev,
                               int *kind, float *ms, int cap, int *n);

@@ -18,21 +18,22 @@ from . import _build
 __all__ = ["ModelDesc", "Decoder", "ZdecError", "load_library", "q4k_repacked_bytes",
            "q4k_repack", "q4k_gemm", "q4k_gemm_workspace_bytes", "q4k_gemm_static",
            "Q4K_GEMM_STATIC_MAX_KB", "KV_F16", "KV_Q8_0",
-           "KERNEL_KINDS", "T_EMBED", "T_WQ", "T_WK", "T_WV", "T_WO", "T_GATE", "T_UP", "T_DOWN"]
+           "KERNEL_KINDS", "ENGINE_AUTO", "ENGINE_KERNELS", "ENGINE_PERSISTENT", "T_EMBED", "T_WQ", "T_WK", "T_WV", "T_WO", "T_GATE", "T_UP", "T_DOWN"]
 
 KV_F16, KV_Q8_0 = 0, 1
 Q4K_GEMM_STATIC_MAX_KB = 262144   # K*B limit of q4k_gemm_static (ZDEC_Q4K_GEMM_STATIC_MAX_KB)
 STEP_HOST_IO, STEP_EAGER = 1, 2
 T_EMBED, T_WQ, T_WK, T_WV, T_WO, T_GATE, T_UP, T_DOWN = range(8)
 KERNEL_KINDS = ["embed", "prep", "gemm_qkv", "attention", "gemm_o", "gemm_gateup", "gemm_down",
-                "gemm_lmhead", "argmax"]
+                "gemm_lmhead", "argmax", "step"]
+ENGINE_AUTO, ENGINE_KERNELS, ENGINE_PERSISTENT = 0, 1, 2
 STATUS = {0: "ok", -1: "bad argument", -2: "out of memory", -3: "capacity", -4: "position",
           -5: "unsupported", -6: "cuda error", -7: "timeout", -8: "device check"}
 
 # Every symbol include/zdec.h declares; load_library() checks they are exported.
 EXPORTS = ["zdec_create", "zdec_destroy", "zdec_append_kv", "zdec_decode_step", "zdec_sync",
            "zdec_reset_seq", "zdec_seq_len", "zdec_last_error", "zdec_last_global_error",
-           "zdec_set_gemm_impl", "zdec_get_info", "zdec_profile_step", "zdec_debug_export_q4k",
+           "zdec_set_gemm_impl", "zdec_set_engine", "zdec_set_trace", "zdec_debug_step_trace", "zdec_get_info", "zdec_profile_step", "zdec_debug_export_q4k",
            "zdec_debug_dequant", "zdec_debug_read_kv", "zdec_debug_capture_hidden",
            "zdec_debug_attention", "zdec_q4k_repacked_bytes", "zdec_q4k_repack",
            "zdec_q4k_gemm_workspace_bytes", "zdec_q4k_gemm", "zdec_q4k_gemm_static"]
@@ -63,7 +64,7 @@ class _Info(ctypes.Structure):
     _fields_ = [("weight_bytes", ctypes.c_size_t), ("arena_bytes", ctypes.c_size_t),
                 ("workspace_bytes", ctypes.c_size_t), ("kv_bytes_per_token", ctypes.c_size_t),
                 ("kernels_per_step", ctypes.c_int), ("attn_splits", ctypes.c_int),
-                ("matvec_max_B", ctypes.c_int)]
+                ("matvec_max_B", ctypes.c_int), ("engine", ctypes.c_int), ("step_ctas", ctypes.c_int)]
 
 
 _lib = None
@@ -100,6 +101,9 @@ def load_library(build_if_missing: bool = True):
         "zdec_last_global_error": (ctypes.c_char_p, []),
         "zdec_set_gemm_impl": (i, [vp, i]),
         "zdec_get_info": (i, [vp, ctypes.POINTER(_Info)]),
+        "zdec_set_engine": (i, [vp, i]),
+        "zdec_set_trace": (i, [vp, i]),
+        "zdec_debug_step_trace": (i, [vp, vp, sz, ctypes.POINTER(sz)]),
         "zdec_profile_step": (i, [vp, i, vp, vp, vp, vp, vp, vp, i, ctypes.POINTER(i)]),
         "zdec_debug_export_q4k": (i, [vp, i, i, i, i, vp]),
         "zdec_debug_dequant": (i, [vp, i, i, i, i, vp]),
@@ -267,6 +271,26 @@ class Decoder:
 
     def set_gemm_impl(self, impl: int):
         self._check(self.lib.zdec_set_gemm_impl(self.h, impl))
+
+    def set_engine(self, engine: int):
+        """ENGINE_AUTO (persistent step kernel where available), ENGINE_KERNELS or
+        ENGINE_PERSISTENT."""
+        self._check(self.lib.zdec_set_engine(self.h, engine))
+
+    def set_trace(self, on: bool):
+        """Record the phase timeline of the following persistent steps."""
+        self._check(self.lib.zdec_set_trace(self.h, int(bool(on))))
+
+    def step_trace(self) -> np.ndarray:
+        """[ctas][phases][8] uint64 timeline of the last traced step (see zdec.h)."""
+        n = ctypes.c_size_t()
+        self._check(self.lib.zdec_debug_step_trace(self.h, None, 0, ctypes.byref(n)))
+        if n.value == 0:
+            return np.zeros((0, 0, 8), np.uint64)
+        out = np.empty(n.value, np.uint64)
+        self._check(self.lib.zdec_debug_step_trace(self.h, _ptr(out), n.value, ctypes.byref(n)))
+        phases = 2 + 5 * self.desc.n_layers
+        return out.reshape(-1, phases, 8)
 
     def info(self) -> dict:
         inf = _Info()

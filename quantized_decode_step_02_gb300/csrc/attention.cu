@@ -78,38 +78,40 @@ __device__ __forceinline__ void issue_chunk(const AttnParams &p, uint8_t *stage,
     const int Lp = p.kv.Lp;
     uint8_t *sK = stage, *sV = stage + Lay::K_BYTES;
     if (KVT == 0) {
-        const uint8_t *gK = p.kv.k + (pi * Lp + c0) * (HD * 2);
-        const uint8_t *gV = p.kv.v + pi * HD * (size_t)Lp * 2 + (size_t)c0 * 2;
+        // the arena's 16-byte segments are swizzled (kv_*_off); the padded
+        // stage rows hold them in natural order
+        const uint8_t *gK = p.kv.k + pi * Lp * (HD * 2);
+        const uint8_t *gV = p.kv.v + pi * Lp * (HD * 2);
         for (int i = threadIdx.x; i < nt * 16; i += blockDim.x) {
             int t = i >> 4, sg = i & 15;
-            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + (size_t)t * 256 + sg * 16);
+            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + kv_k16_off(c0 + t, 8 * sg));
         }
         int vseg = (nt + 7) >> 3;   // 8 tokens per 16 bytes
         for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
             int d = i / vseg, sg = i % vseg;
-            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + (size_t)d * Lp * 2 + sg * 16);
+            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v16_off(d, c0 + 8 * sg));
         }
     } else {
         uint8_t *sKs = stage + Lay::K_BYTES + Lay::V_BYTES, *sVs = sKs + Lay::KS_BYTES;
-        const uint8_t *gK = p.kv.k + (pi * Lp + c0) * HD;
+        const uint8_t *gK = p.kv.k + pi * Lp * HD;
         const uint8_t *gKs = p.kv.ks + (pi * Lp + c0) * 8;
-        const uint8_t *gV = p.kv.v + pi * HD * (size_t)Lp + c0;
-        const uint8_t *gVs = p.kv.vs + pi * 4 * (size_t)Lp * 2 + (size_t)c0 * 2;
+        const uint8_t *gV = p.kv.v + pi * Lp * HD;
+        const uint8_t *gVs = p.kv.vs + pi * Lp * 8;
         for (int i = threadIdx.x; i < nt * 8; i += blockDim.x) {
             int t = i >> 3, sg = i & 7;
-            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + (size_t)t * HD + sg * 16);
+            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + kv_k8_off(c0 + t, 16 * sg));
         }
         for (int i = threadIdx.x; i < (nt + 1) / 2; i += blockDim.x)   // 2 tokens of scales per 16 B
             cp_async16(sKs + i * 16, gKs + (size_t)i * 16);
         int vseg = (nt + 15) >> 4;   // 16 tokens per 16 bytes
         for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
             int d = i / vseg, sg = i % vseg;
-            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + (size_t)d * Lp + sg * 16);
+            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v8_off(d, c0 + 16 * sg));
         }
         int sseg = (nt + 7) >> 3;    // 8 tokens of one scale row per 16 B
         for (int i = threadIdx.x; i < 4 * sseg; i += blockDim.x) {
             int bl = i / sseg, sg = i % sseg;
-            cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + (size_t)bl * Lp * 2 + sg * 16);
+            cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + kv_vs_off(bl, c0 + 8 * sg));
         }
     }
 }
@@ -226,20 +228,20 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             int d = lane + 32 * i;
             __half kh = __float2half_rn(kr[i]), vh = __float2half_rn(vx[i]);
             if (KVT == 0) {
-                reinterpret_cast<__half *>(p.kv.k)[(pi * Lp + pos) * HD + d] = kh;
-                reinterpret_cast<__half *>(p.kv.v)[(pi * HD + d) * (size_t)Lp + pos] = vh;
+                *reinterpret_cast<__half *>(p.kv.k + pi * Lp * (HD * 2) + kv_k16_off(pos, d)) = kh;
+                *reinterpret_cast<__half *>(p.kv.v + pi * Lp * (HD * 2) + kv_v16_off(d, pos)) = vh;
                 reinterpret_cast<__half *>(s_newk)[d] = kh;
                 reinterpret_cast<__half *>(s_newv)[d] = vh;
             } else {
                 uint16_t ksb, vsb;
                 int8_t kc = q8_0_lane(kh, ksb), vc = q8_0_lane(vh, vsb);
-                reinterpret_cast<int8_t *>(p.kv.k)[(pi * Lp + pos) * HD + d] = kc;
-                reinterpret_cast<int8_t *>(p.kv.v)[(pi * HD + d) * (size_t)Lp + pos] = vc;
+                *reinterpret_cast<int8_t *>(p.kv.k + pi * Lp * HD + kv_k8_off(pos, d)) = kc;
+                *reinterpret_cast<int8_t *>(p.kv.v + pi * Lp * HD + kv_v8_off(d, pos)) = vc;
                 reinterpret_cast<int8_t *>(s_newk)[d] = kc;
                 reinterpret_cast<int8_t *>(s_newv)[d] = vc;
                 if (lane == 0) {
-                    reinterpret_cast<uint16_t *>(p.kv.ks)[(pi * Lp + pos) * 4 + i] = ksb;
-                    reinterpret_cast<uint16_t *>(p.kv.vs)[(pi * 4 + i) * (size_t)Lp + pos] = vsb;
+                    *reinterpret_cast<uint16_t *>(p.kv.ks + pi * Lp * 8 + kv_ks_off(pos, i)) = ksb;
+                    *reinterpret_cast<uint16_t *>(p.kv.vs + pi * Lp * 8 + kv_vs_off(i, pos)) = vsb;
                     s_newks[i] = ksb;
                     s_newvs[i] = vsb;
                 }
@@ -552,17 +554,17 @@ __global__ void kv_append_kernel(const KvArena a, int slot, int t0, int n,
         int d = lane + 32 * i;
         uint16_t kb = ks[d], vb = vs[d];
         if (a.kv_dtype == 0) {
-            reinterpret_cast<uint16_t *>(a.k)[(pi * a.Lp + pos) * HD + d] = kb;
-            reinterpret_cast<uint16_t *>(a.v)[(pi * HD + d) * (size_t)a.Lp + pos] = vb;
+            *reinterpret_cast<uint16_t *>(a.k + pi * a.Lp * (HD * 2) + kv_k16_off(pos, d)) = kb;
+            *reinterpret_cast<uint16_t *>(a.v + pi * a.Lp * (HD * 2) + kv_v16_off(d, pos)) = vb;
         } else {
             uint16_t ksb, vsb;
             int8_t kc = q8_0_lane(__ushort_as_half(kb), ksb);
             int8_t vc = q8_0_lane(__ushort_as_half(vb), vsb);
-            reinterpret_cast<int8_t *>(a.k)[(pi * a.Lp + pos) * HD + d] = kc;
-            reinterpret_cast<int8_t *>(a.v)[(pi * HD + d) * (size_t)a.Lp + pos] = vc;
+            *reinterpret_cast<int8_t *>(a.k + pi * a.Lp * HD + kv_k8_off(pos, d)) = kc;
+            *reinterpret_cast<int8_t *>(a.v + pi * a.Lp * HD + kv_v8_off(d, pos)) = vc;
             if (lane == 0) {
-                reinterpret_cast<uint16_t *>(a.ks)[(pi * a.Lp + pos) * 4 + i] = ksb;
-                reinterpret_cast<uint16_t *>(a.vs)[(pi * 4 + i) * (size_t)a.Lp + pos] = vsb;
+                *reinterpret_cast<uint16_t *>(a.ks + pi * a.Lp * 8 + kv_ks_off(pos, i)) = ksb;
+                *reinterpret_cast<uint16_t *>(a.vs + pi * a.Lp * 8 + kv_vs_off(i, pos)) = vsb;
             }
         }
     }
@@ -585,15 +587,15 @@ __global__ void kv_read_kernel(const KvArena a, int slot, int layer, int t0, int
     size_t pi = plane_index(a, slot, layer, g);
     int pos = t0 + t;
     if (a.kv_dtype == 0) {
-        reinterpret_cast<uint16_t *>(k)[i] = reinterpret_cast<const uint16_t *>(a.k)[(pi * a.Lp + pos) * HD + d];
-        reinterpret_cast<uint16_t *>(v)[i] = reinterpret_cast<const uint16_t *>(a.v)[(pi * HD + d) * (size_t)a.Lp + pos];
+        reinterpret_cast<uint16_t *>(k)[i] = *reinterpret_cast<const uint16_t *>(a.k + pi * a.Lp * (HD * 2) + kv_k16_off(pos, d));
+        reinterpret_cast<uint16_t *>(v)[i] = *reinterpret_cast<const uint16_t *>(a.v + pi * a.Lp * (HD * 2) + kv_v16_off(d, pos));
     } else {
-        k[i] = a.k[(pi * a.Lp + pos) * HD + d];
-        v[i] = a.v[(pi * HD + d) * (size_t)a.Lp + pos];
+        k[i] = a.k[pi * a.Lp * HD + kv_k8_off(pos, d)];
+        v[i] = a.v[pi * a.Lp * HD + kv_v8_off(d, pos)];
         if ((d & 31) == 0) {
             size_t o = ((size_t)t * a.n_kv + g) * 4 + (d >> 5);
-            ks[o] = reinterpret_cast<const uint16_t *>(a.ks)[(pi * a.Lp + pos) * 4 + (d >> 5)];
-            vs[o] = reinterpret_cast<const uint16_t *>(a.vs)[(pi * 4 + (d >> 5)) * (size_t)a.Lp + pos];
+            ks[o] = *reinterpret_cast<const uint16_t *>(a.ks + pi * a.Lp * 8 + kv_ks_off(pos, d >> 5));
+            vs[o] = *reinterpret_cast<const uint16_t *>(a.vs + pi * a.Lp * 8 + kv_vs_off(d >> 5, pos));
         }
     }
 }

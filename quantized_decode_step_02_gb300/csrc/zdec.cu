@@ -91,6 +91,21 @@ struct zdec_ctx {
     std::vector<Launch> *prof = nullptr;
     float *capture_dev_host = nullptr;   // pinned [L+1][B][H] while a capture is armed
     float *capture_user = nullptr;       // [B][L+1][H]
+    // persistent step kernel (step.cu)
+    int engine = ZDEC_ENGINE_AUTO, last_engine = ZDEC_ENGINE_KERNELS;
+    int step_grid = 0;                   // CTAs (0: the persistent kernel is unavailable)
+    int step_slots[2] = {0, 0};          // ring slots for B <= 4 and B <= 8
+    void *step_buf = nullptr;            // its buffers (one allocation)
+    StepLayerW *d_layers = nullptr;
+    float *s_q = nullptr, *s_gpart = nullptr, *s_apart = nullptr, *s_rms_ffn = nullptr, *s_capture = nullptr;
+    __half *g16 = nullptr, *g16lo = nullptr, *gsx = nullptr;
+    int *s_cnt = nullptr, *s_ok = nullptr, *s_abort = nullptr;
+    int s_ncnt = 0;
+    bool persistent_eager = false;       // its CUDA graph capture failed: launch it directly
+    int step_pf_items = 0;               // L2 prefetch distance (items per CTA; ZDEC_STEP_PF_ITEMS)
+    int step_att_min = 8;                // attention units per CTA at least (ZDEC_STEP_ATT_MIN)
+    unsigned long long *trace = nullptr; // phase timeline of the last persistent step, or null
+    size_t trace_entries = 0;
 };
 
 static zdec_status fail(zdec_ctx *c, zdec_status s, const char *fmt, ...) {
@@ -136,6 +151,8 @@ static void free_ctx(zdec_ctx *ctx) {
     for (void *p : ctx->arena_allocs) cudaFree(p);
     cudaFree(ctx->rope);
     cudaFree(ctx->ws);
+    cudaFree(ctx->step_buf);
+    cudaFree(ctx->trace);
     cudaFreeHost(ctx->pinned_io);
     cudaFreeHost(ctx->capture_dev_host);
     if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
@@ -191,6 +208,85 @@ static zdec_status upload_weights(zdec_ctx *ctx, const zdec_weights *w) {
         if (!ok) return done(fail(ctx, ZDEC_ERR_CUDA, "layer %d upload: %s", l, cudaGetErrorString(e)));
     }
     return done(ZDEC_OK);
+}
+
+// Ring slots and CTAs of the persistent step kernel, and its buffers.  The
+// kernel runs two CTAs per SM when they fit (one otherwise); it is left
+// unavailable (step_grid = 0) when the device cannot launch it cooperatively,
+// or when the attention output width differs from the hidden size.
+static zdec_status step_configure(zdec_ctx *ctx) {
+    const zdec_model_desc &d = ctx->d;
+    int dev = 0, coop = 0, smem_sm = 0, reserved = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (getenv("ZDEC_NO_PERSISTENT") || !coop || ctx->qd != d.hidden || ctx->num_sms < 1) return ZDEC_OK;
+    if (const char *e = getenv("ZDEC_STEP_PF_ITEMS")) ctx->step_pf_items = std::max(0, atoi(e));
+    if (const char *e = getenv("ZDEC_STEP_ATT_MIN")) ctx->step_att_min = std::max(1, atoi(e));
+    int per_sm = 2;
+    for (int v = 0; v < 2; v++) {
+        const int B = v ? STEP_MAX_B : 4;
+        const size_t static_smem = 11 * 1024;   // the kernel's own __shared__ state
+        int slots = (int)(((size_t)smem_sm / 2 - reserved - static_smem) / (step_slot_bytes(B) + 16));
+        // the attention's warp pairs need a slot count divisible by their number (<= 4)
+        slots = std::max(2, std::min(8, slots));
+        if (slots == 5) slots = 4;
+        if (slots == 7) slots = 6;
+        int fit = 0;
+        while (true) {
+            if (step_setup(B, ctx->kv_dtype, slots, &fit) != cudaSuccess) {
+                cudaGetLastError();
+                return ZDEC_OK;
+            }
+            if (fit >= 2 || slots <= 2) break;
+            slots = slots == 6 ? 4 : slots - 1;
+        }
+        if (fit < 1) return ZDEC_OK;
+        per_sm = std::min(per_sm, fit);
+        ctx->step_slots[v] = slots;
+    }
+    const int grid = per_sm * ctx->num_sms;
+    const int H = d.hidden, NL = d.n_layers, Bm = std::min(ctx->max_B, STEP_MAX_B);
+    ctx->s_ncnt = step_counter_count(NL, H, d.ffn, d.vocab, d.n_q_heads, d.n_kv_heads);
+    size_t w = 0;
+    auto t = [&](size_t bytes) { size_t o = w; w = align_up(w + bytes, 256); return o; };
+    auto plane = [&](int K) { return (size_t)(K / QK) * Bm * 256 * 2; };
+    const size_t o_layers = t(sizeof(StepLayerW) * NL);
+    const size_t o_q = t((size_t)Bm * ctx->qd * 4);
+    const size_t o_gp = t(step_gpart_floats(H, d.ffn, d.vocab, d.n_q_heads, d.n_kv_heads, Bm, grid) * 4);
+    const size_t o_ap = t(step_apart_floats(d.n_kv_heads, Bm, grid) * 4);
+    const size_t o_rf = t((size_t)(H / 128) * MAX_B * 4);
+    const size_t o_cap = t((size_t)(NL + 1) * Bm * H * 4);
+    const size_t o_g = t(plane(H)), o_glo = t(plane(H)), o_gsx = t((size_t)(H / QK) * Bm * 16 * 2);
+    const size_t o_cnt = t((size_t)ctx->s_ncnt * 4), o_ok = t(4), o_ab = t(4);
+    if (cudaMalloc(&ctx->step_buf, w) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(nullptr, ZDEC_ERR_OOM, "cannot allocate %zu bytes for the step kernel", w);
+    }
+    uint8_t *b = (uint8_t *)ctx->step_buf;
+    ctx->d_layers = (StepLayerW *)(b + o_layers);
+    ctx->s_q = (float *)(b + o_q);
+    ctx->s_gpart = (float *)(b + o_gp);
+    ctx->s_apart = (float *)(b + o_ap);
+    ctx->s_rms_ffn = (float *)(b + o_rf);
+    ctx->s_capture = (float *)(b + o_cap);
+    ctx->g16 = (__half *)(b + o_g);
+    ctx->g16lo = (__half *)(b + o_glo);
+    ctx->gsx = (__half *)(b + o_gsx);
+    ctx->s_cnt = (int *)(b + o_cnt);
+    ctx->s_ok = (int *)(b + o_ok);
+    ctx->s_abort = (int *)(b + o_ab);
+    std::vector<StepLayerW> lw(NL);
+    for (int l = 0; l < NL; l++)
+        lw[l] = {ctx->L[l].qkv, ctx->L[l].o, ctx->L[l].gu, ctx->L[l].down, ctx->L[l].attn_norm, ctx->L[l].ffn_norm};
+    if (cudaMemsetAsync(ctx->step_buf, 0, w, ctx->stream) != cudaSuccess ||
+        cudaMemcpyAsync(ctx->d_layers, lw.data(), sizeof(StepLayerW) * NL, cudaMemcpyHostToDevice, ctx->stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(ctx->stream) != cudaSuccess)
+        return fail(nullptr, ZDEC_ERR_CUDA, "step kernel buffers: %s", cudaGetErrorString(cudaGetLastError()));
+    ctx->step_grid = grid;
+    return ZDEC_OK;
 }
 
 extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights,
@@ -360,6 +456,10 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     }
     if (attention_setup(kv_dtype) != cudaSuccess)
         return bail(fail(nullptr, ZDEC_ERR_CUDA, "attention smem attribute failed"));
+    {
+        zdec_status ss = step_configure(ctx);
+        if (ss != ZDEC_OK) return bail(ss);
+    }
 
     zdec_status us = upload_weights(ctx, weights);
     if (us != ZDEC_OK) {
@@ -589,6 +689,87 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     return cudaSuccess;
 }
 
+// The persistent kernel runs this step?
+static bool use_persistent(const zdec_ctx *ctx, int B) {
+    return ctx->engine == ZDEC_ENGINE_PERSISTENT && ctx->step_grid > 0 && B <= STEP_MAX_B;
+}
+
+// The whole step as the prep kernel + the persistent step kernel.
+static cudaError_t enqueue_step_persistent(zdec_ctx *ctx, int B, float *logits_out) {
+    const zdec_model_desc &d = ctx->d;
+    StepParams p{};
+    p.n_layers = d.n_layers;
+    p.hidden = d.hidden;
+    p.ffn = d.ffn;
+    p.vocab = d.vocab;
+    p.n_q = d.n_q_heads;
+    p.n_kv = d.n_kv_heads;
+    p.eps = d.rms_eps;
+    p.layers = ctx->d_layers;
+    p.embed = ctx->embed;
+    p.lm = ctx->embed;
+    p.final_norm = ctx->final_norm;
+    p.rope = ctx->rope;
+    p.kv = ctx->arena;
+    p.max_L = ctx->max_L;
+    p.B = B;
+    p.tokens = ctx->tok_dev;
+    p.positions = ctx->pos_dev;
+    p.logits = logits_out;
+    p.ids = ctx->ids_dev;
+    p.capture = ctx->capture_dev_host ? ctx->s_capture : nullptr;
+    p.x = ctx->x;
+    p.u16 = ctx->x16; p.u16lo = ctx->x16lo; p.usx = ctx->sx;
+    p.g16 = ctx->g16; p.g16lo = ctx->g16lo; p.gsx = ctx->gsx;
+    p.o16 = ctx->o16; p.o16lo = ctx->o16lo; p.osx = ctx->osx;
+    p.a16 = ctx->a16; p.a16lo = ctx->a16lo; p.asx = ctx->asx;
+    p.rms_attn = ctx->rms_part;
+    p.rms_ffn = ctx->s_rms_ffn;
+    p.q = ctx->s_q;
+    p.gpart = ctx->s_gpart;
+    p.apart = ctx->s_apart;
+    p.amax_val = ctx->amax_v;
+    p.amax_idx = ctx->amax_i;
+    p.cnt = ctx->s_cnt;
+    p.n_cnt = ctx->s_ncnt;
+    p.step_ok = ctx->s_ok;
+    p.abort_flag = ctx->s_abort;
+    p.status = ctx->status;
+    p.slots = ctx->step_slots[B <= 4 ? 0 : 1];
+    p.slot_bytes = step_slot_bytes(B);
+    p.pf_items = ctx->step_pf_items;
+    p.att_min_units = ctx->step_att_min;
+    p.trace = ctx->trace;
+    cudaStream_t s = ctx->stream;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (ctx->prof) {
+        cudaEventCreate(&e0);
+        cudaEventCreate(&e1);
+        cudaEventRecord(e0, s);
+    }
+    cudaError_t e = launch_step(p, ctx->step_grid, ctx->len_dev, s);
+    if (ctx->prof) {
+        cudaEventRecord(e1, s);
+        ctx->prof->push_back(Launch{ZDEC_KERNEL_STEP, e0, e1});
+    }
+    if (e != cudaSuccess) return e;
+    if (ctx->capture_dev_host)
+        e = cudaMemcpyAsync(ctx->capture_dev_host, ctx->s_capture, (size_t)(d.n_layers + 1) * B * d.hidden * 4,
+                            cudaMemcpyDeviceToHost, s);
+    ctx->last_kernels = 2;
+    ctx->last_splits = 0;
+    return e;
+}
+
+static cudaError_t enqueue_any(zdec_ctx *ctx, int B, float *logits_out, bool pdl) {
+    if (use_persistent(ctx, B)) {
+        ctx->last_engine = ZDEC_ENGINE_PERSISTENT;
+        return enqueue_step_persistent(ctx, B, logits_out);
+    }
+    ctx->last_engine = ZDEC_ENGINE_KERNELS;
+    return enqueue_step(ctx, B, logits_out, pdl);
+}
+
 static zdec_status check_step_args(zdec_ctx *ctx, int B, const int32_t *tokens, const int32_t *positions,
                                    int32_t *ids) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
@@ -597,6 +778,8 @@ static zdec_status check_step_args(zdec_ctx *ctx, int B, const int32_t *tokens, 
     for (int b = 0; b < B; b++)
         if (ctx->len_host[b] + 1 > ctx->max_L)
             return fail(ctx, ZDEC_ERR_CAPACITY, "sequence %d is full (%d tokens)", b, ctx->max_L);
+    if (ctx->engine == ZDEC_ENGINE_PERSISTENT && !use_persistent(ctx, B))
+        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the persistent step kernel is unavailable for B=%d", B);
     return ZDEC_OK;
 }
 
@@ -627,21 +810,30 @@ extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tok
     zdec_status st = check_step_args(ctx, B, tokens, positions, ids);
     if (st != ZDEC_OK) return st;
     const bool host = flags & ZDEC_STEP_HOST_IO;
-    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host;
+    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host || ctx->trace ||
+                       (ctx->persistent_eager && use_persistent(ctx, B));
     st = stage_inputs(ctx, B, tokens, positions, host);
     if (st != ZDEC_OK) return st;
     float *lg = host ? (logits ? ctx->logits : nullptr) : logits;
-    const int impl = pick_impl(ctx, B);
+    const int impl = use_persistent(ctx, B) ? 3 : pick_impl(ctx, B);
     if (eager) {
-        CK(enqueue_step(ctx, B, lg, true));
+        CK(enqueue_any(ctx, B, lg, true));
     } else {
         auto key = std::make_tuple(B, (const void *)lg, impl);
         auto it = ctx->graphs.find(key);
         if (it == ctx->graphs.end()) {
             cudaGraph_t graph;
             CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
-            cudaError_t e = enqueue_step(ctx, B, lg, true);
+            cudaError_t e = enqueue_any(ctx, B, lg, true);
             cudaError_t e2 = cudaStreamEndCapture(ctx->stream, &graph);
+            if ((e != cudaSuccess || e2 != cudaSuccess) && impl == 3) {
+                // a cooperative launch that cannot be captured: run the persistent engine without graphs
+                if (e2 == cudaSuccess) cudaGraphDestroy(graph);
+                cudaGetLastError();
+                ctx->persistent_eager = true;
+                CK(enqueue_any(ctx, B, lg, true));
+                goto launched;
+            }
             if (e != cudaSuccess || e2 != cudaSuccess) {
                 if (e2 == cudaSuccess) cudaGraphDestroy(graph);
                 return fail(ctx, ZDEC_ERR_CUDA, "step capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
@@ -654,6 +846,7 @@ extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tok
         }
         CK(cudaGraphLaunch(it->second, ctx->stream));
     }
+launched:
     if (host) {
         if (logits)
             CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)B * ctx->d.vocab * 4, cudaMemcpyDeviceToHost, ctx->stream));
@@ -712,6 +905,48 @@ extern "C" zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info) {
     info->kernels_per_step = ctx->last_kernels;
     info->attn_splits = ctx->last_splits;
     info->matvec_max_B = ctx->matvec_max_B;
+    info->engine = ctx->last_engine;
+    info->step_ctas = ctx->step_grid;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_set_trace(zdec_ctx *ctx, int on) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (!on) {
+        CK(cudaStreamSynchronize(ctx->stream));
+        cudaFree(ctx->trace);
+        ctx->trace = nullptr;
+        ctx->trace_entries = 0;
+        return ZDEC_OK;
+    }
+    if (ctx->step_grid == 0) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the persistent step kernel is unavailable");
+    if (ctx->trace) return ZDEC_OK;
+    const size_t n = (size_t)ctx->step_grid * (2 + 5 * ctx->d.n_layers) * 8;
+    if (cudaMalloc(&ctx->trace, n * 8) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ctx, ZDEC_ERR_OOM, "cannot allocate the step trace");
+    }
+    CK(cudaMemsetAsync(ctx->trace, 0, n * 8, ctx->stream));
+    ctx->trace_entries = n;
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_debug_step_trace(zdec_ctx *ctx, uint64_t *out_host, size_t cap, size_t *n) {
+    if (!ctx || !n) return fail(nullptr, ZDEC_ERR_ARG, "null argument");
+    *n = ctx->trace_entries;
+    if (!ctx->trace || !out_host) return ZDEC_OK;   // size query
+    if (cap < ctx->trace_entries) return fail(ctx, ZDEC_ERR_ARG, "trace needs %zu entries", ctx->trace_entries);
+    CK(cudaStreamSynchronize(ctx->stream));
+    CK(cudaMemcpy(out_host, ctx->trace, ctx->trace_entries * 8, cudaMemcpyDeviceToHost));
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_set_engine(zdec_ctx *ctx, int engine) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (engine < ZDEC_ENGINE_AUTO || engine > ZDEC_ENGINE_PERSISTENT) return fail(ctx, ZDEC_ERR_ARG, "bad engine %d", engine);
+    if (engine == ZDEC_ENGINE_PERSISTENT && ctx->step_grid == 0)
+        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the persistent step kernel is unavailable on this device/model");
+    ctx->engine = engine;
     return ZDEC_OK;
 }
 
@@ -725,7 +960,7 @@ extern "C" zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *to
     if (st != ZDEC_OK) return st;
     std::vector<Launch> launches;
     ctx->prof = &launches;
-    cudaError_t e = enqueue_step(ctx, B, logits_dev, false);
+    cudaError_t e = enqueue_any(ctx, B, logits_dev, false);
     ctx->prof = nullptr;
     if (e == cudaSuccess) e = cudaMemcpyAsync(ids_dev, ctx->ids_dev, B * 4, cudaMemcpyDeviceToDevice, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);

@@ -87,10 +87,12 @@ cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int 
 struct KvArena {
     int kv_dtype;          // 0 fp16, 1 Q8_0
     int n_layers, n_kv, Lp;
-    uint8_t *k;            // fp16: [slot][layer][g][Lp][128] half;  Q8: int8 codes, same shape
-    uint8_t *v;            // fp16: [slot][layer][g][128][Lp] half (V transposed); Q8: int8 codes
-    uint8_t *ks;           // Q8: [slot][layer][g][Lp][4] half   (K scales)
-    uint8_t *vs;           // Q8: [slot][layer][g][4][Lp] half   (V scales, transposed)
+    // one plane per (slot, layer, kv head), plane index (slot*n_layers + layer)*n_kv + g;
+    // the layout inside a plane is given by kv_*_off (zdec_internal.cuh)
+    uint8_t *k;            // fp16 Lp*256 bytes per plane; Q8: int8 codes, Lp*128
+    uint8_t *v;            // fp16 Lp*256 bytes (unit-tiled V^T); Q8: Lp*128
+    uint8_t *ks;           // Q8: Lp*8 bytes per plane (K scales)
+    uint8_t *vs;           // Q8: Lp*8 bytes per plane (V scales, unit-tiled)
 };
 struct AttnParams {
     KvArena kv;
@@ -120,6 +122,64 @@ cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const ui
 // Canonical read-back: [n][n_kv][128] (+ scales [n][n_kv][4]) for one layer.
 cudaError_t launch_kv_read(const KvArena &a, int slot, int layer, int t0, int n, uint8_t *k,
                            uint8_t *v, uint16_t *ks, uint16_t *vs, cudaStream_t stream);
+
+// ---------------------------------------------------------------- step.cu
+// The whole decode step as one persistent kernel (B <= STEP_MAX_B).
+constexpr int STEP_MAX_B = 8;
+struct StepLayerW {
+    const uint8_t *qkv, *o, *gu, *down;   // grouped tile blocks
+    const float *attn_norm, *ffn_norm;
+};
+struct StepParams {
+    int n_layers, hidden, ffn, vocab, n_q, n_kv;
+    float eps;
+    const StepLayerW *layers;   // device [n_layers]
+    const uint8_t *embed, *lm;
+    const float *final_norm;
+    const float2 *rope;         // [max_L][64] (cos, sin)
+    KvArena kv;
+    int max_L;
+    int B;
+    const int32_t *tokens, *positions;
+    float *logits;              // [B][vocab] or null
+    int32_t *ids;               // [B]
+    float *capture;             // [n_layers+1][B][hidden] or null
+    // workspace
+    float *x;                   // [B][hidden] residual stream
+    __half *u16, *u16lo, *usx;  // gain*x planes: QKV and LM head input
+    __half *g16, *g16lo, *gsx;  // ffn-gain*x planes: gate/up input
+    __half *o16, *o16lo, *osx;  // attention output planes: O input
+    __half *a16, *a16lo, *asx;  // SwiGLU planes: down input
+    float *rms_attn, *rms_ffn;  // [hidden/128][MAX_B] partial sums of x^2
+    float *q;                   // [B][n_q][128] rotated, scaled queries
+    float *gpart;               // GEMM piece partials [(groups + grid)][B][128]
+    float *apart;               // attention piece partials [(B*n_kv + grid)][4][HD + 4]
+    float *amax_val;            // [lm groups][MAX_B]
+    int *amax_idx;
+    int *cnt;                   // step counters (zeroed by the prep kernel)
+    int n_cnt;
+    const int *step_ok;         // set by the prep kernel
+    int *abort_flag;
+    uint32_t *status;
+    int slots;                  // ring slots per CTA
+    int slot_bytes;
+    int pf_items;               // items each CTA prefetches into L2 ahead of its ring (0: none)
+    int att_min_units;          // attention units per CTA at least (fewer CTAs for short work)
+    unsigned long long *trace;  // [grid][phases][8] timestamps (null: off), see step.cu
+};
+int step_counter_count(int n_layers, int hidden, int ffn, int vocab, int n_q, int n_kv);
+size_t step_gpart_floats(int hidden, int ffn, int vocab, int n_q, int n_kv, int B, int grid);
+size_t step_apart_floats(int n_kv, int B, int grid);
+int step_lm_groups(int vocab);
+// Shared memory per CTA for `slots` ring slots at batch B.
+size_t step_smem_bytes(int B, int slots);
+int step_slot_bytes(int B);
+// Validate inputs, zero the counters, advance the lengths (prep kernel), then
+// the persistent kernel over `grid` CTAs (cooperative launch).
+cudaError_t launch_step(const StepParams &p, int grid, int32_t *len_dev, cudaStream_t stream);
+// Configure the kernels (shared-memory limit) and report how many CTAs of the
+// step kernel fit on one SM for `slots` ring slots at batch B.
+cudaError_t step_setup(int B, int kv_dtype, int slots, int *ctas_per_sm);
 
 // Launch helper with the programmatic-stream-serialization attribute.
 // Launch helper: optional programmatic stream serialization and a 1-D cluster

@@ -88,6 +88,7 @@ def test_matvec_and_mma_paths_both_match(impl):
     w = cached_model(d, 102)
     lengths = [40, 9]
     dec, om, kvs = setup_pair(d, w, 102, lengths, 0, 64)
+    dec.set_engine(z.ENGINE_KERNELS)   # the projection kernel choice applies to that engine
     dec.set_gemm_impl(impl)
     check_step(dec, om, kvs, make_tokens(d, 300, 2), np.array(lengths, np.int32), f"impl {impl}")
     dec.close()
@@ -172,14 +173,91 @@ def test_profile_step_reports_every_launch():
     dec, _, _ = setup_pair(d, w, 106, [5], 0, 16)
     dev = torch.device("cuda")
     toks = torch.from_numpy(make_tokens(d, 106, 1)).to(dev)
-    pos = torch.tensor([5], dtype=torch.int32, device=dev)
     ids = torch.empty(1, dtype=torch.int32, device=dev)
-    rec = dec.profile_step(toks, pos, None, ids)
+    dec.set_engine(z.ENGINE_KERNELS)
+    rec = dec.profile_step(toks, torch.tensor([5], dtype=torch.int32, device=dev), None, ids)
     kinds = [k for k, _ in rec]
     assert len(rec) == dec.info()["kernels_per_step"] == 3 + 5 * d.n_layers
     assert kinds.count("attention") == d.n_layers and kinds[-1] == "argmax"
     assert all(ms > 0 for _, ms in rec)
+    assert dec.info()["engine"] == z.ENGINE_KERNELS
+    dec.set_engine(z.ENGINE_PERSISTENT)
+    rec = dec.profile_step(toks, torch.tensor([6], dtype=torch.int32, device=dev), None, ids)
+    assert [k for k, _ in rec] == ["step"] and rec[0][1] > 0
+    assert dec.info()["kernels_per_step"] == 2 and dec.info()["engine"] == z.ENGINE_PERSISTENT
+    assert dec.info()["step_ctas"] >= torch.cuda.get_device_properties(0).multi_processor_count
     dec.close()
+
+
+@pytest.mark.parametrize("kv_dtype", [0, 1])
+def test_persistent_and_kernel_engines_agree(kv_dtype):
+    """The same three steps through both engines: each matches the oracle
+    (check_step), and the two agree to far below the tolerance."""
+    d = SMALL
+    w = cached_model(d, 107)
+    lengths = [0, 31, 32, 100]
+    out = {}
+    for eng in (z.ENGINE_KERNELS, z.ENGINE_PERSISTENT):
+        dec, om, kvs = setup_pair(d, w, 107, lengths, kv_dtype, 128)
+        dec.set_engine(eng)
+        pos = np.array(lengths, np.int32)
+        res = []
+        for step in range(3):
+            lg, ids, rl, _ = check_step(dec, om, kvs, make_tokens(d, 700 + step, 4), pos, f"engine {eng} step {step}")
+            res.append((lg, ids, top2_gap(rl)))
+            pos += 1
+        assert dec.info()["engine"] == eng
+        out[eng] = res
+        dec.close()
+    for (la, ia, gap), (lb, ib, _) in zip(out[z.ENGINE_KERNELS], out[z.ENGINE_PERSISTENT]):
+        for b in range(4):
+            assert normwise(la[b], lb[b]) < 1e-4
+            if gap[b] > 1e-3:
+                assert ia[b] == ib[b]
+
+
+@pytest.mark.parametrize("kv_dtype", [0, 1])
+@pytest.mark.parametrize("B", [4, 8])
+def test_persistent_engine_long_contexts(kv_dtype, B):
+    """Contexts long enough that every CTA of the persistent kernel takes
+    several 32-token units of one (sequence, kv head), so all warp pairs run
+    and the ring slots cycle within an attention piece."""
+    d = SMALL
+    w = cached_model(d, 109)
+    lengths = [1900 + 97 * b for b in range(B)]
+    dec, om, kvs = setup_pair(d, w, 109, lengths, kv_dtype, 2700)
+    dec.set_engine(z.ENGINE_PERSISTENT)
+    pos = np.array(lengths, np.int32)
+    for step in range(2):
+        check_step(dec, om, kvs, make_tokens(d, 900 + step, B), pos, f"B={B} kv{kv_dtype} step {step}")
+        pos += 1
+    assert dec.info()["engine"] == z.ENGINE_PERSISTENT
+    dec.close()
+
+
+def test_persistent_engine_batch_of_eight_and_fallback_above():
+    """B = 8 (the largest batch of the persistent kernel) runs it and matches
+    the oracle; forcing it at B = 9 is refused before anything runs, and the
+    default engine takes B = 9."""
+    d = SMALL
+    w = cached_model(d, 108)
+    for B in (8, 9):
+        lengths = [(37 * b) % 90 for b in range(B)]
+        dec, om, kvs = setup_pair(d, w, 108, lengths, 1, 96)
+        dec.set_engine(z.ENGINE_PERSISTENT)
+        toks = make_tokens(d, 800 + B, B)
+        if B <= 8:
+            check_step(dec, om, kvs, toks, np.array(lengths, np.int32), f"B={B}")
+            assert dec.info()["engine"] == z.ENGINE_PERSISTENT
+        else:
+            with pytest.raises(z.ZdecError) as e:
+                dec.step_host(toks, np.array(lengths, np.int32))
+            assert e.value.status == -5
+            assert [dec.seq_len(b) for b in range(B)] == lengths
+            dec.set_engine(z.ENGINE_AUTO)
+            check_step(dec, om, kvs, toks, np.array(lengths, np.int32), f"B={B}")
+            assert dec.info()["engine"] == z.ENGINE_KERNELS
+        dec.close()
 
 
 # ------------------------------------------------------------ full-size configs
