@@ -135,10 +135,14 @@ zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len);
 const char *zdec_last_error(const zdec_ctx *ctx);
 const char *zdec_last_global_error(void);
 
-/* Which dense kernel runs the Q4_K projections: 0 = by measured switch point
- * (B <= switch uses the dequant-matvec, else the mma.sync GEMM), 1 = always
- * the matvec (B <= 4 only), 2 = always the mma.sync GEMM.  Takes effect at the
- * next step (cached CUDA graphs are rebuilt). */
+/* Which dense kernel runs the Q4_K projections of the kernel engine:
+ * 0 = default (B = 1: the sub-block-column mma matvec, impl 3; 2 <= B <= 4 by
+ * the measured switch point between the CUDA-core matvec and the GEMM),
+ * 1 = always the CUDA-core dequant-matvec (B <= 4 only), 2 = always the
+ * mma.sync GEMM (batch in the mma N dimension, sub-block scales folded into
+ * the A operand), 3 = the sub-block-column mma matvec at B = 1 (raw codes as
+ * the A operand, one mma column per sub-block; the GEMM above B = 1).  Takes
+ * effect at the next step (cached CUDA graphs are rebuilt). */
 zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl);
 
 /* Which engine runs a step.  ZDEC_ENGINE_PERSISTENT: the whole step is one
@@ -243,7 +247,7 @@ size_t zdec_q4k_gemm_workspace_bytes(int K, int B);
 /* y[b][n] = sum_k W[n][k] x[b][k] for b < B.  x_dev fp32 [B][K], y_dev fp32
  * [B][N], workspace_dev >= zdec_q4k_gemm_workspace_bytes(K, B) bytes, 16-byte
  * aligned, owned by the caller.  impl: 1 = dequant-matvec (B <= 4),
- * 2 = mma.sync GEMM.  Activations enter as fp16 high + low parts (about 22
+ * 2 = mma.sync GEMM, 3 = sub-block-column mma matvec (B = 1).  Activations enter as fp16 high + low parts (about 22
  * significant bits); weights are exact; accumulation is fp32. */
 zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B,
                           float *y_dev, int impl, void *workspace_dev, size_t workspace_bytes,

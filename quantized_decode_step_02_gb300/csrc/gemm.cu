@@ -300,8 +300,12 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, uint3
 
 // ------------------------------------------------------------- kernel ---
 // NT n-tiles of 4 batch rows each (IMPL 2), or NT batch rows (IMPL 1, NT <= 4).
+// Residency: three CTAs per SM for the one-tile mma kernel (B <= 4; <= 80
+// registers), two up to B = 8, one above.
+template <int NT, int IMPL> struct GemmOcc { static constexpr int v = (IMPL >= 2 && NT == 1) ? 3 : (NT <= 2 ? 2 : 1); };
+
 template <int NT, int EPI, int IMPL>
-__global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const GemmParams p) {
+__global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const GemmParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_bad;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
@@ -309,7 +313,7 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
     const int rt = grp * GT + warp;
     const int s0 = rank * p.nsb / cs, s1 = (rank + 1) * p.nsb / cs, n = s1 - s0;
     const int B = p.B, D = p.stages;
-    constexpr int BR = IMPL == 2 ? 4 * NT : 4;   // batch rows held per stage
+    constexpr int BR = IMPL == 2 ? 4 * NT : 4;   // batch rows held per stage (IMPL 3: B = 1, rows 1-3 zero)
     const StageLayout lay(BR);
     const uint32_t abytes = (uint32_t)B * 512u, sbytes = (uint32_t)B * 32u;
     const uint32_t tx = GROUP_BYTES + 2 * abytes + sbytes;
@@ -351,10 +355,14 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
     // this lane's fixed offsets into a stage: virtual column g of n-tile 0 is the
     // hi (g even) or lo (g odd) plane of batch row g/2
     const int g = lane >> 2;
-    const uint32_t act_off = ((g & 1) ? lay.lo : lay.hi) + (uint32_t)(g >> 1) * 512u + (uint32_t)tig * 128u;
+    uint32_t act_off = ((g & 1) ? lay.lo : lay.hi) + (uint32_t)(g >> 1) * 512u + (uint32_t)tig * 128u;
     const uint32_t swz = (uint32_t)tig | ((uint32_t)((g >> 1) & 1) << 2);
-    const uint32_t sum_off = (g & 1) ? lay.zero + (uint32_t)tig * 8u
-                                     : lay.sums + (uint32_t)(g >> 1) * 32u + (uint32_t)tig * 8u;
+    uint32_t sum_off = (g & 1) ? lay.zero + (uint32_t)tig * 8u
+                               : lay.sums + (uint32_t)(g >> 1) * 32u + (uint32_t)tig * 8u;
+    if (IMPL == 3) {   // B column g carries sub-block data only in lane group tig = g/2 (see stage_mv)
+        act_off = (g == 2 * tig ? lay.hi : (g == 2 * tig + 1 ? lay.lo : lay.hi + 512u)) + (uint32_t)tig * 128u;
+        sum_off = lay.sums + (uint32_t)tig * 8u;
+    }
     const int pre = min(D, n);
     if (threadIdx.x == 0)
         for (int i = 0; i < pre; i++) issue_w(i);
@@ -382,6 +390,7 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
     float accr[NB][2];
 #pragma unroll
     for (int c = 0; c < NB; c++) accr[c][0] = accr[c][1] = 0.0f;
+    float ymv[2] = {0.0f, 0.0f};
     // two stages per step: their loads, dequant and MMAs are independent, which
     // gives each warp two dependency chains to interleave, and halves the
     // block-wide syncs that release stages for refilling
@@ -397,6 +406,9 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
             if (IMPL == 2) {
                 stage_mma<NA>(stage(i), warp, lane, act_off, sum_off, swz, acc);
                 if (two) stage_mma<NA>(stage(i + 1), warp, lane, act_off, sum_off, swz, acc);
+            } else if (IMPL == 3) {
+                stage_mv(stage(i), warp, lane, act_off, sum_off, ymv);
+                if (two) stage_mv(stage(i + 1), warp, lane, act_off, sum_off, ymv);
             } else {
                 stage_fma<NB>(stage(i), warp, lane, lay, accr);
                 if (two) stage_fma<NB>(stage(i + 1), warp, lane, lay, accr);
@@ -424,6 +436,14 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
             y[nt][0] = acc[nt < NA ? nt : 0][0] + acc[nt < NA ? nt : 0][1] * LO_UNSCALE;
             y[nt][1] = acc[nt < NA ? nt : 0][2] + acc[nt < NA ? nt : 0][3] * LO_UNSCALE;
         }
+    } else if (IMPL == 3) {   // the row's four lanes, then batch row 0 in lane tig 0
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            ymv[r] += __shfl_xor_sync(FULL, ymv[r], 1);
+            ymv[r] += __shfl_xor_sync(FULL, ymv[r], 2);
+        }
+        y[0][0] = tig == 0 ? ymv[0] : 0.0f;
+        y[0][1] = tig == 0 ? ymv[1] : 0.0f;
     } else {   // quad butterfly, then batch row tig
 #pragma unroll
         for (int c = 0; c < NB; c++)
@@ -479,18 +499,18 @@ __global__ __launch_bounds__(256, (NT <= 2 ? 2 : 1)) void gemm_kernel(const Gemm
 // ------------------------------------------------------------ dispatch ---
 int gemm_grid(const GemmParams &p) { return n_groups(p.nrt) * p.cs; }
 
-static int stages_for(uint32_t stage_bytes, int B) {
-    const uint32_t budget = B <= 8 ? 110u * 1024u : 200u * 1024u;   // two CTAs per SM up to B = 8
+static int stages_for(uint32_t stage_bytes, int occ) {
+    const uint32_t budget = occ >= 3 ? 70u * 1024u : (occ == 2 ? 110u * 1024u : 200u * 1024u);
     int d = (int)(budget / stage_bytes);
     return d < 2 ? 2 : (d > 6 ? 6 : d);
 }
 
-int gemm_stages(int B) { return stages_for(StageLayout(4 * ((B + 3) / 4)).bytes, B); }
+int gemm_ctas_per_sm(int B, int impl) { return impl == 2 && B <= 4 ? 3 : (B <= 8 ? 2 : 1); }
 
 template <int NT, int EPI, int IMPL>
 static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
     const StageLayout lay(IMPL == 2 ? 4 * NT : 4);
-    p.stages = stages_for(lay.bytes, p.B);
+    p.stages = stages_for(lay.bytes, GemmOcc<NT, IMPL>::v);
     const size_t smem = (size_t)p.stages * lay.bytes + 8 * 8;
     static bool configured = false;   // raise the dynamic shared-memory limit once per instance
     if (!configured) {
@@ -504,6 +524,10 @@ static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
 
 template <int EPI>
 static cudaError_t launch_epi(const GemmParams &p, int impl, bool pdl, cudaStream_t s) {
+    if (impl == 3) {
+        if (p.B != 1) return cudaErrorInvalidValue;
+        return launch_one<1, EPI, 3>(p, pdl, s);
+    }
     if (impl == 1) {
         switch (p.B) {
             case 1: return launch_one<1, EPI, 1>(p, pdl, s);

@@ -140,5 +140,74 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
     }
 }
 
+// ------------------------------------------------------ batch of one ---
+// B = 1: the mma as a dot-product engine with one column per sub-block.
+//   A: the raw codes as fp16 subnormals, q * 2^-24 (one AND per two codes;
+//      the high nibbles give 16q * 2^-24, their activations being stored
+//      divided by 16), so no bias and no scale enter the operand;
+//   B: column n = 2t + e of an mma carries the activations of sub-block
+//      2t + h (e = 0: hi plane, 1: lo plane) in the k-slots of lane group
+//      tig = t and zeros elsewhere.  A lane (g, tig) loads real activations
+//      only when g = 2 tig (hi) or g = 2 tig + 1 (lo); the other lanes read a
+//      zero row (act_off, see the kernels).
+// D[row][2t + e] is then 2^-24 times the code-times-activation sum of one
+// sub-block, and the C fragment hands lane (g, tig) exactly its own two
+// sub-blocks for rows g and g + 8, which it scales by d*sc and offsets by
+// dmin*m*S in fp32: y[rho] += d sc 2^24 D - dmin m S_j.
+// y holds this lane's share of rows g, g + 8 (sub-blocks 2tig, 2tig+1 of
+// every super-block); the four lanes of a row are summed by the caller.
+__device__ __forceinline__ void stage_mv(const uint8_t *st, int warp, int lane, uint32_t act_off, uint32_t sum_off,
+                                         float (&y)[2]) {
+    const int tig = lane & 3;
+    const uint8_t *tile = st + warp * TILE_BYTES;
+    const uint8_t *act = st + act_off;
+    uint4 q[4];
+#pragma unroll
+    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
+    const uint2 mt = *reinterpret_cast<const uint2 *>(tile + TILE_CODE_BYTES + 8 * lane);
+    // d, dmin of rows g, g+8 (four nibble quarters spread over the tig lanes)
+    uint32_t dq = ((mt.x >> 12) & 0xFu) | ((mt.x >> 24) & 0xF0u) | ((mt.y >> 4) & 0xF00u) | ((mt.y >> 16) & 0xF000u);
+    const uint32_t other = __shfl_xor_sync(FULL, dq, 1);
+    const uint32_t pair = (tig & 1) ? (other | (dq << 16)) : (dq | (other << 16));
+    const uint32_t pair2 = __shfl_xor_sync(FULL, pair, 2);
+    const float2 fg = __half22float2(u32_as_h2(tig < 2 ? pair : pair2));
+    const float2 f8 = __half22float2(u32_as_h2(tig < 2 ? pair2 : pair));
+    float D[2][2][4];   // [sub-block h][chain][c fragment]
+#pragma unroll
+    for (int h = 0; h < 2; h++)
+#pragma unroll
+        for (int k = 0; k < 2; k++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) D[h][k][i] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const int h = c >> 1;
+#pragma unroll
+        for (int pp = 0; pp < 2; pp++) {
+            const int pidx = (c & 1) * 2 + pp;
+            const uint32_t w0 = pp ? q[c].z : q[c].x, w1 = pp ? q[c].w : q[c].y;
+            const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
+            const uint32_t a[4] = {w0 & 0x000F000Fu, w1 & 0x000F000Fu, s0 & 0x000F000Fu, s1 & 0x000F000Fu};
+            const uint32_t a16[4] = {w0 & 0x00F000F0u, w1 & 0x00F000F0u, s0 & 0x00F000F0u, s1 & 0x00F000F0u};
+            const uint4 xv = *reinterpret_cast<const uint4 *>(act + (((uint32_t)(h * 4 + pidx) ^ (uint32_t)tig) << 4));
+            mma16816(D[h][c & 1], a, xv.x, xv.y, D[h][c & 1]);
+            mma16816(D[h][c & 1], a16, xv.z, xv.w, D[h][c & 1]);
+        }
+    }
+    const uint2 sv = *reinterpret_cast<const uint2 *>(st + sum_off);   // (S hi 2tig, 2tig+1, S lo 2tig, 2tig+1)
+    const float2 shi = __half22float2(u32_as_h2(sv.x)), slo = __half22float2(u32_as_h2(sv.y));
+    const float S[2] = {shi.x + slo.x, shi.y + slo.y};
+    const float dg = fg.x * 16777216.0f, d8 = f8.x * 16777216.0f;   // the codes carry 2^-24
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const int sh = 16 * h;   // sub-block 2tig + h: fields at bits 0 / 16 (sc) and 6 / 22 (m)
+        const float scg = (float)((mt.x >> sh) & 63u), sc8 = (float)((mt.y >> sh) & 63u);
+        const float mg = (float)((mt.x >> (sh + 6)) & 63u), m8 = (float)((mt.y >> (sh + 6)) & 63u);
+        const float vg = (D[h][0][0] + D[h][1][0]) + (D[h][0][1] + D[h][1][1]) * LO_UNSCALE;
+        const float v8 = (D[h][0][2] + D[h][1][2]) + (D[h][0][3] + D[h][1][3]) * LO_UNSCALE;
+        y[0] += (dg * scg) * vg - (fg.y * mg) * S[h];
+        y[1] += (d8 * sc8) * v8 - (f8.y * m8) * S[h];
+    }
+}
 
 }  // namespace zdec

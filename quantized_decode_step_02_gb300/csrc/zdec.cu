@@ -30,9 +30,9 @@ size_t tile_bytes(int rows16, int nsb) { return (size_t)n_groups(rows16) * nsb *
 
 // K split (cluster size) for a projection: grow it until the grid covers the
 // GPU, keeping at least two super-blocks per CTA.
-int pick_cs(int groups, int nsb, int num_sms) {
+int pick_cs(int groups, int nsb, int target_ctas) {
     int cs = 1;
-    while (cs < 8 && groups * cs < num_sms && nsb / (cs * 2) >= 2) cs *= 2;
+    while (cs < 8 && groups * cs * 2 <= target_ctas && nsb / (cs * 2) >= 2) cs *= 2;
     return cs;
 }
 
@@ -76,13 +76,14 @@ struct zdec_ctx {
     __half *x16 = nullptr, *x16lo = nullptr, *sx = nullptr;
     __half *o16 = nullptr, *o16lo = nullptr, *osx = nullptr;
     __half *a16 = nullptr, *a16lo = nullptr, *asx = nullptr;
-    int cs_qkv = 1, cs_o = 1, cs_gu = 1, cs_down = 1, cs_lm = 1;
+    int cs_qkv[2] = {1, 1}, cs_o[2] = {1, 1}, cs_gu[2] = {1, 1}, cs_down[2] = {1, 1}, cs_lm[2] = {1, 1};  // B<=4, B>4
     int32_t *tok_dev = nullptr, *pos_dev = nullptr, *ids_dev = nullptr, *len_dev = nullptr;
     uint32_t *status = nullptr;
     int32_t *pinned_io = nullptr;      // [2*max_B] staging of host tokens/positions
     // host state
     std::vector<int> len_host;
     int gemm_impl = 0, matvec_max_B = 0;
+    int b1_impl = 3;                   // projection kernel at B = 1 (ZDEC_B1_IMPL)
     size_t prefetch_cap = 0;   // bytes of the next matrix a GEMM warms in L2 (0: off; ZDEC_L2_PREFETCH_MB)
     std::map<std::tuple<int, const void *, int>, cudaGraphExec_t> graphs;
     std::string err;
@@ -323,6 +324,7 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     ctx->L.resize(d.n_layers);
     ctx->len_host.assign(max_B, 0);
     if (const char *e = getenv("ZDEC_MATVEC_MAX_B")) ctx->matvec_max_B = std::max(0, std::min(4, atoi(e)));
+    if (const char *e = getenv("ZDEC_B1_IMPL")) ctx->b1_impl = std::max(1, std::min(3, atoi(e)));
     if (const char *e = getenv("ZDEC_L2_PREFETCH_MB")) ctx->prefetch_cap = (size_t)std::max(0, atoi(e)) << 20;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -448,11 +450,14 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     }
     {
         const int nsm = ctx->num_sms > 0 ? ctx->num_sms : 148;
-        ctx->cs_qkv = pick_cs(n_groups(ctx->qkv_ld / 16), ctx->nsb_h, nsm);
-        ctx->cs_o = pick_cs(n_groups(H / 16), ctx->nsb_q, nsm);
-        ctx->cs_gu = pick_cs(n_groups(F / 8), ctx->nsb_h, nsm);
-        ctx->cs_down = pick_cs(n_groups(H / 16), ctx->nsb_f, nsm);
-        ctx->cs_lm = pick_cs(n_groups(ctx->nrt_vocab), ctx->nsb_h, nsm);
+        for (int v = 0; v < 2; v++) {   // split factors filling the kernel's CTAs per SM
+            const int target = nsm * gemm_ctas_per_sm(v ? 8 : 4, 2);
+            ctx->cs_qkv[v] = pick_cs(n_groups(ctx->qkv_ld / 16), ctx->nsb_h, target);
+            ctx->cs_o[v] = pick_cs(n_groups(H / 16), ctx->nsb_q, target);
+            ctx->cs_gu[v] = pick_cs(n_groups(F / 8), ctx->nsb_h, target);
+            ctx->cs_down[v] = pick_cs(n_groups(H / 16), ctx->nsb_f, target);
+            ctx->cs_lm[v] = pick_cs(n_groups(ctx->nrt_vocab), ctx->nsb_h, target);
+        }
     }
     if (attention_setup(kv_dtype) != cudaSuccess)
         return bail(fail(nullptr, ZDEC_ERR_CUDA, "attention smem attribute failed"));
@@ -552,6 +557,8 @@ static int pick_impl(const zdec_ctx *ctx, int B) {
     if (B > 4) return 2;
     if (ctx->gemm_impl == 1) return 1;
     if (ctx->gemm_impl == 2) return 2;
+    if (ctx->gemm_impl == 3) return B == 1 ? 3 : 2;
+    if (B == 1) return ctx->b1_impl;
     return B <= ctx->matvec_max_B ? 1 : 2;
 }
 
@@ -590,6 +597,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     } while (0)
 
     const int Bp0 = ctx->Bp_max;
+    const int cv = B <= 4 ? 0 : 1;   // split-factor set
     STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev,
                                          ctx->len_dev, ctx->status, B, ctx->x, H, ctx->L[0].attn_norm,
                                          ctx->x16, ctx->x16lo, ctx->sx, Bp0, ctx->rms_part, pdl, s));
@@ -646,27 +654,27 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     for (int l = 0; l < d.n_layers; l++) {
         const LayerW &lw = ctx->L[l];
         normed_input(l == 0 ? 1 : resid_groups);
-        matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, ctx->cs_qkv);
+        matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, ctx->cs_qkv[cv]);
         prefetch(lw.o, H / 16, ctx->nsb_q);
         gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld;
         STEP(ZDEC_KERNEL_GEMM_QKV, launch_gemm(gp, EPI_STORE, impl, pdl, s));
         ap.layer = l;
         STEP(ZDEC_KERNEL_ATTENTION, launch_attention(ap, pdl, s));
         plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention combine
-        matrix(lw.o, H, H / 16, ctx->nsb_q, ctx->cs_o);
+        matrix(lw.o, H, H / 16, ctx->nsb_q, ctx->cs_o[cv]);
         prefetch(lw.gu, F / 8, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
         gp.next_gain = lw.ffn_norm; gp.part_out = ctx->rms_part;
         gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
         STEP(ZDEC_KERNEL_GEMM_O, launch_gemm(gp, EPI_RESID, impl, pdl, s));
         normed_input(resid_groups);
-        matrix(lw.gu, F, F / 8, ctx->nsb_h, ctx->cs_gu);
+        matrix(lw.gu, F, F / 8, ctx->nsb_h, ctx->cs_gu[cv]);
         prefetch(lw.down, H / 16, ctx->nsb_f);
         gp.out = nullptr; gp.ldo = F;
         gp.out16 = ctx->a16; gp.out16lo = ctx->a16lo; gp.out_sx = ctx->asx;
         STEP(ZDEC_KERNEL_GEMM_GATEUP, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s));
         plain_input(ctx->a16, ctx->a16lo, ctx->asx);   // written by the gate/up epilogue
-        matrix(lw.down, H, H / 16, ctx->nsb_f, ctx->cs_down);
+        matrix(lw.down, H, H / 16, ctx->nsb_f, ctx->cs_down[cv]);
         if (l + 1 < d.n_layers) prefetch(ctx->L[l + 1].qkv, ctx->qkv_ld / 16, ctx->nsb_h);
         else prefetch(ctx->embed, ctx->nrt_vocab, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
@@ -677,7 +685,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         if ((e = capture_x(l + 1)) != cudaSuccess) return e;
     }
     normed_input(resid_groups);
-    matrix(ctx->embed, d.vocab, ctx->nrt_vocab, ctx->nsb_h, ctx->cs_lm);
+    matrix(ctx->embed, d.vocab, ctx->nrt_vocab, ctx->nsb_h, ctx->cs_lm[cv]);
     gp.out = logits_out; gp.ldo = d.vocab;
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
     STEP(ZDEC_KERNEL_GEMM_LMHEAD, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s));
@@ -890,7 +898,7 @@ extern "C" zdec_status zdec_sync(zdec_ctx *ctx) {
 
 extern "C" zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
-    if (impl < 0 || impl > 2) return fail(ctx, ZDEC_ERR_ARG, "impl must be 0, 1 or 2");
+    if (impl < 0 || impl > 3) return fail(ctx, ZDEC_ERR_ARG, "impl must be 0, 1, 2 or 3");
     ctx->gemm_impl = impl;
     return ZDEC_OK;
 }
@@ -1133,8 +1141,9 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     if (!repacked_dev || !x_dev || !y_dev || !workspace_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
     if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
     if (B < 1 || B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "B must be in [1, %d]", MAX_B);
-    if (impl != 1 && impl != 2) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1 or 2");
+    if (impl < 1 || impl > 3) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1, 2 or 3");
     if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
+    if (impl == 3 && B != 1) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "impl 3 handles B = 1");
     if (workspace_bytes < zdec_q4k_gemm_workspace_bytes(K, B)) return fail(ctx, ZDEC_ERR_ARG, "workspace too small");
     if ((uintptr_t)workspace_dev % 16 || (uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "pointers must be 16-byte aligned");
     const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
@@ -1158,7 +1167,7 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     gp.Bp = B;
     gp.out = y_dev;
     gp.ldo = N;
-    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm);
+    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm * gemm_ctas_per_sm(B, impl));
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
 }
@@ -1189,8 +1198,9 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
     if (!repacked_dev || !x_dev || !y_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
     if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
     if (B < 1 || B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "B must be in [1, %d]", MAX_B);
-    if (impl != 1 && impl != 2) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1 or 2");
+    if (impl < 1 || impl > 3) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1, 2 or 3");
     if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
+    if (impl == 3 && B != 1) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "impl 3 handles B = 1");
     if ((long long)K * B > ZDEC_Q4K_GEMM_STATIC_MAX_KB)
         return fail(ctx, ZDEC_ERR_ARG,
                     "K*B = %lld exceeds the static scratch of zdec_q4k_gemm_static (K*B <= %d); "
@@ -1225,7 +1235,7 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
     gp.Bp = B;
     gp.out = y_dev;
     gp.ldo = N;
-    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm);
+    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm * gemm_ctas_per_sm(B, impl));
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
 }

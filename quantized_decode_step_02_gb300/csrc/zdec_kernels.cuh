@@ -71,7 +71,9 @@ struct GemmParams {
 // impl 1: CUDA-core dequant-matvec (B <= 4); impl 2: mma.sync swap-AB GEMM.
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream);
 int gemm_grid(const GemmParams &p);
-int gemm_stages(int B);
+// CTAs per SM the projection kernel is built for at batch B (its split
+// factor targets that many CTAs per SM).
+int gemm_ctas_per_sm(int B, int impl);
 
 // prep: fp32 rows -> fp16 operand + sub-block sums.  gain != nullptr applies
 // RMSNorm (x * rsqrt(mean x^2 + eps) * gain).  Rows B..Bp-1 are zeroed.

@@ -68,7 +68,8 @@ def test_null_context_calls_fail_cleanly():
 def test_stateless_gemm_validates_arguments():
     lib = z.load_library()
     dummy = ctypes.c_void_p(16)
-    assert lib.zdec_q4k_gemm(dummy, 4096, 4096, dummy, 1, dummy, 3, dummy, 1 << 20, None) == -1
+    assert lib.zdec_q4k_gemm(dummy, 4096, 4096, dummy, 1, dummy, 4, dummy, 1 << 20, None) == -1
+    assert lib.zdec_q4k_gemm(dummy, 4096, 4096, dummy, 2, dummy, 3, dummy, 1 << 20, None) == -5
     assert lib.zdec_q4k_gemm(dummy, 4096, 4096, dummy, 5, dummy, 1, dummy, 1 << 20, None) == -5
     assert lib.zdec_q4k_gemm(dummy, 4008, 4096, dummy, 1, dummy, 2, dummy, 1 << 20, None) == -5
     assert lib.zdec_q4k_gemm(dummy, 4096, 4096, dummy, 1, dummy, 2, dummy, 16, None) == -1

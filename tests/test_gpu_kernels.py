@@ -78,11 +78,20 @@ def _gemm_case(N, K, B, impl, seed):
     return got
 
 
-def test_gemm_4096_square_batch1_both_kernels():
+def test_gemm_4096_square_batch1_all_kernels():
     # single-layer tiny step: Q4_K GEMV 4096 x 4096, N(0, 0.02) weights, x ~ N(0,1), seed 0
     a = _gemm_case(4096, 4096, 1, 2, 0)
     b = _gemm_case(4096, 4096, 1, 1, 0)
-    assert normwise(a, b) < 1e-4
+    c = _gemm_case(4096, 4096, 1, 3, 0)
+    assert normwise(a, b) < 1e-4 and normwise(a, c) < 1e-4
+
+
+@pytest.mark.parametrize("N,K", [(16, 512), (48, 1024), (4096, 14336), (151936 // 16 * 16, 512), (2048, 4096)])
+def test_gemm_subblock_column_matvec_batch1(N, K):
+    """impl 3 (raw codes as fp16 subnormal mma operands, one column per
+    sub-block): ragged row tiles, long K, a split-K cluster and a grid of
+    thousands of CTAs."""
+    _gemm_case(N, K, 1, 3, N + K)
 
 
 @pytest.mark.parametrize("N,K,B", [(16, 512, 1), (48, 1024, 3), (4096, 14336, 2), (6144, 4096, 8),

@@ -82,7 +82,7 @@ def test_small_model_multi_step_ragged(kv_dtype):
     dec.close()
 
 
-@pytest.mark.parametrize("impl", [1, 2])
+@pytest.mark.parametrize("impl", [1, 2, 3])
 def test_matvec_and_mma_paths_both_match(impl):
     d = SMALL
     w = cached_model(d, 102)
@@ -91,6 +91,12 @@ def test_matvec_and_mma_paths_both_match(impl):
     dec.set_engine(z.ENGINE_KERNELS)   # the projection kernel choice applies to that engine
     dec.set_gemm_impl(impl)
     check_step(dec, om, kvs, make_tokens(d, 300, 2), np.array(lengths, np.int32), f"impl {impl}")
+    dec.close()
+    # batch of one (impl 3 runs its own kernel only there)
+    dec, om, kvs = setup_pair(d, w, 102, lengths[:1], 0, 64)
+    dec.set_engine(z.ENGINE_KERNELS)
+    dec.set_gemm_impl(impl)
+    check_step(dec, om, kvs, make_tokens(d, 301, 1), np.array(lengths[:1], np.int32), f"impl {impl} B=1")
     dec.close()
 
 

@@ -25,6 +25,7 @@ def test_static_gemm_rejects_oversize_before_any_cuda_call():
     assert "exceeds" in msg and str(z.Q4K_GEMM_STATIC_MAX_KB) in msg
     assert lib.zdec_q4k_gemm_static(None, 4096, 4096, dummy, 1, dummy, 2, None) == -1
     assert lib.zdec_q4k_gemm_static(dummy, 4096, 4096, dummy, 5, dummy, 1, None) == -5
+    assert lib.zdec_q4k_gemm_static(dummy, 4096, 4096, dummy, 1, dummy, 4, None) == -1
     assert lib.zdec_q4k_gemm_static(dummy, 4096, 4000, dummy, 1, dummy, 2, None) == -5
 
 
@@ -38,7 +39,7 @@ def _matrix(N, K, seed, dev, torch):
 
 @gpu
 @needs_cuda
-@pytest.mark.parametrize("N,K,B,impl", [(4096, 4096, 1, 1), (2048, 4096, 3, 1), (4096, 4096, 1, 2),
+@pytest.mark.parametrize("N,K,B,impl", [(4096, 4096, 1, 1), (2048, 4096, 3, 1), (4096, 4096, 1, 2), (4096, 4096, 1, 3),
                                         (1024, 4096, 13, 2), (512, 8192, 32, 2)])
 def test_static_gemm_equals_workspace_gemm_on_consecutive_calls(N, K, B, impl):
     torch = pytest.importorskip("torch")
