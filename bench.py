@@ -63,6 +63,33 @@ def args_parse():
     return p.parse_args()
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The job's time is its slowest rank's: all-reduce MAX over the ranks."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tok_s(B: int, world: int, ms_per_step: float) -> float:
+    """Replicas: every rank decodes its own batch of B, so the job advances
+    B * world sequences per step of the slowest rank."""
+    return B * world * 1000.0 / ms_per_step
+
+
+def ncu_traffic(engine: str, kind: str, B: int, kv: str, impl: int):
+    """DRAM bytes per launch of a kernel kind from a committed ncu capture
+    (profiles/ncu_traffic.json), or None when no capture matches."""
+    try:
+        tab = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))["kernels"]
+    except Exception:
+        return None
+    key = f"{engine}/{kind}/B{B}/" + (kv if kind == "attention" else f"impl{impl}")
+    return tab.get(key, {}).get("bytes")
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -247,14 +274,11 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True):
         ev1.record(stream)
         torch.cuda.synchronize()
     dec.sync()
-    ms = ev0.elapsed_time(ev1) / a.steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / a.steps, world, "cuda")
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.barrier()
-        ms = float(t.item())
     Lmid = L + a.warmup + a.steps / 2
-    res = {"B": B, "L": L, "kv": kv, "ms_per_step": ms, "tok_s": B * world * 1000.0 / ms,
+    res = {"B": B, "L": L, "kv": kv, "ms_per_step": ms, "tok_s": aggregate_tok_s(B, world, ms),
            "step_bytes": step_bytes(desc, B, Lmid, kv), "kernels_per_step": dec.info()["kernels_per_step"],
            "engine": ["auto", "kernels", "persistent"][dec.info()["engine"]],
            "clocks": clk.summary()}
@@ -283,12 +307,8 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True):
         t0 = time.perf_counter()
         for j in range(a.warmup, n_total):
             dec.step_host(ht[j], hp[j])
-        el = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([el], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            el = float(t.item())
-        res["e2e"] = {"value": B * world * a.steps / el, "unit": "tok/s",
+        el = max_over_ranks(time.perf_counter() - t0, world, "cuda")
+        res["e2e"] = {"value": aggregate_tok_s(B, world, 1000.0 * el / a.steps), "unit": "tok/s",
                       "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B}
     dec.close()
     return res
@@ -337,8 +357,10 @@ def main():
         Lmid = a.L + a.warmup + a.steps + 0.5
     kb = kernel_bytes(desc, dom, a.B, Lmid, a.kv)
     achieved = kb / (launch_ms * 1e-3) / 1e9
+    impl = a.gemm_impl or (3 if a.B == 1 else 2)
     roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "peak_source": peak_src, "traffic": None,
+            "frac": achieved / hbm_peak, "peak_source": peak_src,
+            "traffic": ncu_traffic(r["engine"], dom, a.B, a.kv, impl),
             "bytes_per_launch": kb, "avg_launch_ms": launch_ms, "launches_per_step": launches}
     cpu = None
     if not a.no_cpu_baseline and world == 1:
