@@ -638,6 +638,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     ap.oBp = Bp;
     ap.B = B;
     ap.max_L = ctx->max_L;
+    ap.status = ctx->status;
     // RMSNorm never runs as its own kernel: the producer of the residual (the
     // embedding gather, the O and down projections) writes gain*x as the next
     // projection's operand plus per-group sums of x^2, and the consumer scales
@@ -1108,6 +1109,7 @@ extern "C" zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, con
     ap.oBp = ctx->Bp_max;
     ap.B = B;
     ap.max_L = ctx->max_L;
+    ap.status = ctx->status;
     CK(launch_attention(ap, false, ctx->stream));
     CK(cudaMemcpyAsync(o_host, ctx->o, (size_t)B * qd * 4, cudaMemcpyDeviceToHost, ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));

@@ -113,6 +113,7 @@ struct AttnParams {
     int oBp;               // their row pitch
     int B;
     int max_L;             // positions >= max_L are ignored (the step is flagged elsewhere)
+    uint32_t *status;      // device status word (bounded-wait timeouts)
 };
 cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream);
 // Raise the attention kernel's dynamic shared-memory limit (once, before capture).
