@@ -263,11 +263,12 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         const int c0 = T0 + ci * ATT_CHUNK;
         cp_async_wait<1>();
         __syncthreads();
-        // fix-up: zero V columns past the loaded history, insert the new token
-        {
-            const int zfrom = max(H, c0) - c0, cend = min(ATT_CHUNK, T1 - c0 + 0);
+        // fix-up (only the chunk at the end of the loaded history): zero V columns
+        // past it and insert the new token; whole-history chunks skip both barriers
+        const int zfrom = max(H, c0) - c0;
+        if (zfrom < ATT_CHUNK) {
             uint8_t *sV = st + Lay::K_BYTES;
-            if (zfrom < ATT_CHUNK) {
+            {
                 for (int i = threadIdx.x; i < HD * (ATT_CHUNK - zfrom); i += blockDim.x) {
                     int d = i / (ATT_CHUNK - zfrom), t = zfrom + i % (ATT_CHUNK - zfrom);
                     if (KVT == 0) reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE)[t] = __ushort_as_half(0);
@@ -299,7 +300,6 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
                 }
             }
             __syncthreads();
-            (void)cend;
         }
 
         const int tb = c0 + 16 * warp;   // this warp's 16 tokens

@@ -150,7 +150,8 @@ __device__ __forceinline__ void stage_fma(const uint8_t *st, int warp, int lane,
 // ------------------------------------------------------------ epilogue ---
 // y[nt][rho]: output row rt*16 + g + 8*rho, batch row b = 4nt + tig.
 template <int NT, int EPI>
-__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT][2], int grp) {
+__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT][2], int grp,
+                                              const float (&xin)[NT][2]) {
     constexpr int NB = 4 * NT;   // batch rows this instance covers
     // SWIGLU: a[col][64 rows]; RESID with a next operand: x[col][128 rows]
     __shared__ float s_v[EPI == EPI_SWIGLU ? NB * 64 : (EPI == EPI_RESID ? NB * 128 : GT * NB)];
@@ -179,7 +180,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT
                     const int row = rt * 16 + g + 8 * r, b = 4 * nt + tig;
                     if (b < p.B && row < p.N) {
                         float *o = p.out + (size_t)b * p.ldo + row;
-                        const float xn = *o + y[nt][r];
+                        const float xn = xin[nt][r] + y[nt][r];   // x fetched at the kernel's start
                         *o = xn;
                         if (p.next_gain) s_v[b * 128 + warp * 16 + 8 * r + g] = xn;
                     }
@@ -379,6 +380,27 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     pdl_wait();
     if (threadIdx.x == 0)
         for (int i = 0; i < pre; i++) issue_act(i);
+    // the epilogue's inputs from earlier kernels, fetched now so that their
+    // latency hides behind the K loop: this lane's partial sums of x^2 per
+    // batch row (RMSNorm scale) and the residual rows it will update
+    constexpr int NY = IMPL == 2 ? NT : 1;
+    constexpr bool EARLY = NY <= 2;   // registers allow the early fetch and the batched reduction
+    float rms_pre[4 * NY];
+#pragma unroll
+    for (int b = 0; b < 4 * NY; b++) {
+        rms_pre[b] = 0.0f;
+        if (EARLY && p.rms_part && b < B)
+            for (int i = lane; i < p.rms_nparts; i += 32) rms_pre[b] += p.rms_part[i * MAX_B + b];
+    }
+    float xin[NY][2];
+#pragma unroll
+    for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            const int row = rt * 16 + (lane >> 2) + 8 * r, b = 4 * nt + tig;
+            xin[nt][r] = (EPI == EPI_RESID && rank == 0 && rt < p.nrt && b < B && row < p.N)
+                             ? p.out[(size_t)b * p.ldo + row] : 0.0f;
+        }
 
     constexpr int NA = IMPL == 2 ? NT : 1;   // mma accumulator tiles
     constexpr int NB = IMPL == 1 ? NT : 1;   // matvec columns
@@ -428,7 +450,6 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         if (cs == 1) return;   // cluster members still meet the two cluster barriers below
     }
     // per-lane outputs: y[nt][rho] for output row g + 8 rho, batch row 4nt + tig
-    constexpr int NY = IMPL == 2 ? NT : 1;
     float y[NY][2];
     if (IMPL == 2) {
 #pragma unroll
@@ -465,7 +486,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
 #pragma unroll
             for (int r = 0; r < 2; r++) red[((warp * NY + nt) * 2 + r) * 32 + lane] = y[nt][r];
         cluster.sync();
-        if (rank == 0)
+        if (rank == 0 && !EARLY) {
             for (int rr = 1; rr < cs; rr++) {
                 const float *peer = cluster.map_shared_rank(red, rr);
 #pragma unroll
@@ -473,27 +494,47 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
 #pragma unroll
                     for (int r = 0; r < 2; r++) y[nt][r] += peer[((warp * NY + nt) * 2 + r) * 32 + lane];
             }
+        } else if (rank == 0) {   // every peer's loads in flight before the sums (rank order kept)
+            float pv[7][NY][2];
+#pragma unroll
+            for (int rr = 1; rr < 8; rr++) {
+                const float *peer = rr < cs ? cluster.map_shared_rank(red, rr) : nullptr;
+#pragma unroll
+                for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+                    for (int r = 0; r < 2; r++)
+                        pv[rr - 1][nt][r] = rr < cs ? peer[((warp * NY + nt) * 2 + r) * 32 + lane] : 0.0f;
+            }
+#pragma unroll
+            for (int rr = 1; rr < 8; rr++)
+#pragma unroll
+                for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+                    for (int r = 0; r < 2; r++)
+                        if (rr < cs) y[nt][r] += pv[rr - 1][nt][r];
+        }
         cluster.sync();
         if (rank != 0 || bad) return;
     }
     if (p.rms_part) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
-        __shared__ float s_r[4 * NY];
-        if (warp == 0)
-            for (int b = 0; b < 4 * NY; b++) {
-                float ss = 0.0f;
-                if (b < B)
-                    for (int i = lane; i < p.rms_nparts; i += 32) ss += p.rms_part[i * MAX_B + b];
-                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-                if (lane == 0) s_r[b] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
-            }
-        __syncthreads();
 #pragma unroll
         for (int nt = 0; nt < NY; nt++) {
-            y[nt][0] *= s_r[4 * nt + tig];
-            y[nt][1] *= s_r[4 * nt + tig];
+            float rr[4];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {   // every lane reduces the four rows of n-tile nt
+                float ss = rms_pre[4 * nt + c];
+                if (!EARLY && 4 * nt + c < B)
+                    for (int i = lane; i < p.rms_nparts; i += 32) ss += p.rms_part[i * MAX_B + 4 * nt + c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+                rr[c] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
+            }
+            const float r_b = tig == 0 ? rr[0] : (tig == 1 ? rr[1] : (tig == 2 ? rr[2] : rr[3]));
+            y[nt][0] *= r_b;
+            y[nt][1] *= r_b;
         }
     }
-    gemm_epilogue<NY, EPI>(p, y, grp);
+    gemm_epilogue<NY, EPI>(p, y, grp, xin);
 }
 
 // ------------------------------------------------------------ dispatch ---
