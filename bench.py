@@ -284,7 +284,7 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True):
            "clocks": clk.summary()}
     res["step_gbs"] = res["step_bytes"] / (ms * 1e-3) / 1e9
     i = n_total
-    if a.trace and dec.info()["step_ctas"] > 0:   # one traced step (not timed)
+    if a.trace:   # one traced step (not timed)
         dec.set_trace(True)
         dec.step(toks[i], pos[i], None, ids)
         np.save(a.trace, dec.step_trace())

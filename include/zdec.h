@@ -158,19 +158,23 @@ zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl);
 enum { ZDEC_ENGINE_AUTO = 0, ZDEC_ENGINE_KERNELS = 1, ZDEC_ENGINE_PERSISTENT = 2 };
 zdec_status zdec_set_engine(zdec_ctx *ctx, int engine);
 
-/* Phase timeline of the persistent engine (tracing).  on = 1 allocates a
- * buffer of step_ctas * (2 + 5*n_layers) * 8 uint64 entries and makes every
- * later step run without graph replay and record, per CTA c and phase ph
+/* Tracing.  on = 1 makes every later step run without graph replay and
+ * record a timeline of the GPU global timer (ns); on = 0 stops and frees it.
+ * Kernel engine: [launches][8] entries per step: the first CTA's start, the
+ * first CTA past its dependency wait, the last CTA's end, the launch's kind
+ * (ZDEC_KERNEL_*), then the latest CTA to reach the kernel's milestones (for
+ * the projections: past the wait, first stage landed, K loop done, cluster
+ * reduction done; zero where a kernel records none).  Persistent engine: per CTA c and phase ph
  * (0 embedding; 1 + 5l + {0 QKV, 1 attention, 2 O, 3 gate/up, 4 down} of
- * layer l; 1 + 5*n_layers LM head), at entry (c*phases + ph)*8 + k the GPU
- * global timer in ns: k = 0 the consumer warps enter the phase, 1 its inputs
- * are released, 2 the first item has landed, 3 the last item is consumed,
- * 4 the phase's reductions and epilogues are done, 5 the producer issues the
- * phase's first copy, 6 its first activation copy, and 7 = the number of
- * items of the phase on that CTA (zero where a CTA has no work).  on = 0
- * frees it.  ZDEC_ERR_UNSUPPORTED without the persistent engine. */
+ * layer l; 1 + 5*n_layers LM head), at entry (c*phases + ph)*8 + k: k = 0 the
+ * consumer warps enter the phase, 1 its inputs are released, 2 the first item
+ * has landed, 3 the last item is consumed, 4 the phase's reductions and
+ * epilogues are done, 5 the producer issues the phase's first copy, 6 its
+ * first activation copy, and 7 = the number of items of the phase on that CTA
+ * (zero where a CTA has no work). */
 zdec_status zdec_set_trace(zdec_ctx *ctx, int on);
-/* Copy the trace of the last traced step (waits for the stream).  *n gets the
+/* Copy the trace of the last traced step (waits for the stream), in the
+ * layout of the engine that ran it (zdec_get_info().engine).  *n gets the
  * entry count (0 when tracing is off); out_host needs that many uint64
  * (out_host = NULL: only the size query). */
 zdec_status zdec_debug_step_trace(zdec_ctx *ctx, uint64_t *out_host, size_t cap, size_t *n);

@@ -282,15 +282,17 @@ class Decoder:
         self._check(self.lib.zdec_set_trace(self.h, int(bool(on))))
 
     def step_trace(self) -> np.ndarray:
-        """[ctas][phases][8] uint64 timeline of the last traced step (see zdec.h)."""
+        """Timeline of the last traced step (see zdec.h): persistent engine
+        [ctas][phases][8], kernel engine [launches][8] uint64."""
         n = ctypes.c_size_t()
         self._check(self.lib.zdec_debug_step_trace(self.h, None, 0, ctypes.byref(n)))
         if n.value == 0:
-            return np.zeros((0, 0, 8), np.uint64)
+            return np.zeros((0, 8), np.uint64)
         out = np.empty(n.value, np.uint64)
         self._check(self.lib.zdec_debug_step_trace(self.h, _ptr(out), n.value, ctypes.byref(n)))
-        phases = 2 + 5 * self.desc.n_layers
-        return out.reshape(-1, phases, 8)
+        if self.info()["engine"] == ENGINE_PERSISTENT:
+            return out.reshape(-1, 2 + 5 * self.desc.n_layers, 8)
+        return out.reshape(-1, 8)
 
     def info(self) -> dict:
         inf = _Info()

@@ -152,6 +152,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
 
     const int rank = blockIdx.x, g = blockIdx.y, b = blockIdx.z, CS = p.cs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    tl_min(p.tl, 0);
     const int pos = p.positions[b];       // staged before the step: not a predecessor output
     if (pos < 0 || pos >= p.max_L) return;   // bad device input (whole cluster); flagged by the embedding kernel
     const int ntok = pos + 1;
@@ -172,10 +173,22 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
 
     pdl_launch_dependents();
     pdl_wait();
+    tl_min(p.tl, 1);
+    tl_max(p.tl, 4);
 
     // ---- query fragments: head 4g+gid (gid < 4), dims 16s' + 4tig + {0..3}
     uint32_t qa[8][4];
-    {
+    if (p.q_frag) {   // prepared by the QKV projection's epilogue (rotated, scaled, hi/lo)
+        const uint4 *qf = p.q_frag + ((size_t)b * p.nq + GROUP * g + (gid < GROUP ? gid : 0)) * 32 + tig;
+#pragma unroll
+        for (int st = 0; st < 8; st++) {
+            const uint4 f = gid < GROUP ? qf[st * 4] : make_uint4(0, 0, 0, 0);
+            qa[st][0] = f.x;
+            qa[st][1] = f.y;
+            qa[st][2] = f.z;
+            qa[st][3] = f.w;
+        }
+    } else {
         const float qscale = 0.08838834764831845f;   // 1/sqrt(128)
         const int hq = GROUP * g + gid;
         const float *qrow = p.qkv + (size_t)b * p.qkv_ld + (size_t)hq * HD;
@@ -206,6 +219,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         }
     }
 
+    tl_max(p.tl, 5);
     // ---- the new token: rotate k, round to fp16, quantize (Q8_0), append
     if (has_new && warp == 0) {
         const float *krow = p.qkv + (size_t)b * p.qkv_ld + (size_t)(p.nq + g) * HD;
@@ -268,16 +282,19 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         const int zfrom = max(H, c0) - c0;
         if (zfrom < ATT_CHUNK) {
             uint8_t *sV = st + Lay::K_BYTES;
-            {
-                for (int i = threadIdx.x; i < HD * (ATT_CHUNK - zfrom); i += blockDim.x) {
-                    int d = i / (ATT_CHUNK - zfrom), t = zfrom + i % (ATT_CHUNK - zfrom);
-                    if (KVT == 0) reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE)[t] = __ushort_as_half(0);
-                    else sV[d * Lay::V_STRIDE + t] = 0;
-                }
-                if (KVT == 1) {
-                    uint16_t *sVs = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES);
-                    for (int i = threadIdx.x; i < 4 * (ATT_CHUNK - zfrom); i += blockDim.x)
-                        sVs[(i / (ATT_CHUNK - zfrom)) * ATT_CHUNK + zfrom + i % (ATT_CHUNK - zfrom)] = 0;
+            {   // thread d clears row d of V^T from column zfrom on (128 threads, 128 rows)
+                const int d = threadIdx.x;
+                if (KVT == 0) {
+                    __half *row = reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE);
+                    for (int t = zfrom; t < ATT_CHUNK; t++) row[t] = __ushort_as_half(0);
+                } else {
+                    uint8_t *row = sV + d * Lay::V_STRIDE;
+                    for (int t = zfrom; t < ATT_CHUNK; t++) row[t] = 0;
+                    if (d < 4) {
+                        uint16_t *srow = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES) +
+                                         d * ATT_CHUNK;
+                        for (int t = zfrom; t < ATT_CHUNK; t++) srow[t] = 0;
+                    }
                 }
             }
             __syncthreads();
@@ -416,6 +433,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         cp_async_commit();
     }
     cp_async_wait<0>();
+    tl_max(p.tl, 6);
 
     // ---- merge the 4 warps of this CTA (smem reused after the stages)
     float *wm = reinterpret_cast<float *>(smem);          // [4 warps][4 heads]
@@ -509,7 +527,9 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         part += __shfl_xor_sync(AFULL, part, 4);
         if ((lane & 7) == 0) store_sum(p.osx, kcol >> 8, b, (kcol >> 5) & 7, p.oBp, part);
     }
+    tl_max(p.tl, 7);
     cluster.sync();   // peers keep their partials alive until rank 0 has read them
+    tl_end(p.tl);
 }
 
 cudaError_t attention_setup(int kv_dtype) {

@@ -154,20 +154,48 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT
                                               const float (&xin)[NT][2]) {
     constexpr int NB = 4 * NT;   // batch rows this instance covers
     // SWIGLU: a[col][64 rows]; RESID with a next operand: x[col][128 rows]
-    __shared__ float s_v[EPI == EPI_SWIGLU ? NB * 64 : (EPI == EPI_RESID ? NB * 128 : GT * NB)];
+    __shared__ float s_v[EPI == EPI_LMHEAD ? GT * NB : NB * 128];
     __shared__ int s_i[GT * NB];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
     const int rt = grp * GT + warp;
     const bool active = rt < p.nrt;
     if (EPI == EPI_STORE) {
-        if (!active) return;
+        const bool qhead = p.q_frag && grp < p.q_heads;   // CTA-uniform
+        if (active)
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++)
+            for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-            for (int r = 0; r < 2; r++) {
-                const int row = rt * 16 + g + 8 * r, b = 4 * nt + tig;
-                if (b < p.B && row < p.N) p.out[(size_t)b * p.ldo + row] = y[nt][r];
+                for (int r = 0; r < 2; r++) {
+                    const int row = rt * 16 + g + 8 * r, b = 4 * nt + tig;
+                    if (b < p.B && row < p.N) {
+                        p.out[(size_t)b * p.ldo + row] = y[nt][r];
+                        if (qhead) s_v[b * 128 + warp * 16 + g + 8 * r] = y[nt][r];
+                    }
+                }
+        if (!qhead) return;
+        // query head grp: rotate at its position, scale, split hi/lo, fragment order
+        __syncthreads();
+        const float qscale = 0.08838834764831845f;   // 1/sqrt(128)
+        for (int task = threadIdx.x; task < p.B * 32; task += blockDim.x) {
+            const int b = task >> 5, st = (task >> 2) & 7, tq = task & 3;
+            const float2 *cs = p.q_rope + (size_t)p.q_pos[b] * 64;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int d = 16 * st + 4 * tq + e;
+                const float x = s_v[b * 128 + d];
+                const float2 c = cs[d & 63];
+                v[e] = (d < 64 ? x * c.x - s_v[b * 128 + d + 64] * c.y : x * c.x + s_v[b * 128 + d - 64] * c.y) * qscale;
             }
+            const __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            uint4 f;
+            f.x = h2_as_u32(h01);
+            f.y = h2_as_u32(__floats2half2_rn(v[0] - f01.x, v[1] - f01.y));
+            f.z = h2_as_u32(h23);
+            f.w = h2_as_u32(__floats2half2_rn(v[2] - f23.x, v[3] - f23.y));
+            p.q_frag[(((size_t)b * p.q_heads + grp) * 8 + st) * 4 + tq] = f;
+        }
     } else if (EPI == EPI_RESID) {
         // x += y; with next_gain set, the group's 128 updated rows also become the
         // next projection's operand g*x (act planes + sub-block sums) and one
@@ -333,6 +361,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         bulk_g2s(st + (lay.lo - GROUP_BYTES), p.x16lo + sb * p.Bp * 256, abytes, &full[i % D]);
         bulk_g2s(st + (lay.sums - GROUP_BYTES), p.sx + sb * p.Bp * 16, sbytes, &full[i % D]);
     };
+    tl_min(p.tl, 0);
     if (threadIdx.x == 0) {
         s_bad = 0;
         for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
@@ -378,6 +407,8 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     }
     pdl_launch_dependents();
     pdl_wait();
+    tl_min(p.tl, 1);
+    tl_max(p.tl, 4);
     if (threadIdx.x == 0)
         for (int i = 0; i < pre; i++) issue_act(i);
     // the epilogue's inputs from earlier kernels, fetched now so that their
@@ -420,6 +451,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     for (int i = 0; i < n; i += 2) {
         const bool two = i + 1 < n;
         if (ok && !wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, p.status)) { ok = false; s_bad = 1; }
+        if (i == 0) tl_max(p.tl, 5);
         if (two && ok && !wait_stage(&full[(i + 1) % D], (uint32_t)((i + 1) / D) & 1u, p.status)) {
             ok = false;
             s_bad = 1;
@@ -442,6 +474,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
             if (two && i + 1 + D < n) { issue_w(i + 1 + D); issue_act(i + 1 + D); }
         }
     }
+    tl_max(p.tl, 6);
     const bool bad = s_bad != 0;
     if (bad) {   // drain what may still be in flight (bounded); the result is abandoned
         if (threadIdx.x == 0)
@@ -495,9 +528,9 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
                     for (int r = 0; r < 2; r++) y[nt][r] += peer[((warp * NY + nt) * 2 + r) * 32 + lane];
             }
         } else if (rank == 0) {   // every peer's loads in flight before the sums (rank order kept)
-            float pv[7][NY][2];
+            float pv[15][NY][2];
 #pragma unroll
-            for (int rr = 1; rr < 8; rr++) {
+            for (int rr = 1; rr < 16; rr++) {
                 const float *peer = rr < cs ? cluster.map_shared_rank(red, rr) : nullptr;
 #pragma unroll
                 for (int nt = 0; nt < NY; nt++)
@@ -506,7 +539,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
                         pv[rr - 1][nt][r] = rr < cs ? peer[((warp * NY + nt) * 2 + r) * 32 + lane] : 0.0f;
             }
 #pragma unroll
-            for (int rr = 1; rr < 8; rr++)
+            for (int rr = 1; rr < 16; rr++)
 #pragma unroll
                 for (int nt = 0; nt < NY; nt++)
 #pragma unroll
@@ -514,7 +547,11 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
                         if (rr < cs) y[nt][r] += pv[rr - 1][nt][r];
         }
         cluster.sync();
-        if (rank != 0 || bad) return;
+        if (rank != 0 || bad) {
+            tl_end(p.tl);
+            return;
+        }
+        tl_max(p.tl, 7);
     }
     if (p.rms_part) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
 #pragma unroll
@@ -535,6 +572,10 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         }
     }
     gemm_epilogue<NY, EPI>(p, y, grp, xin);
+    if (p.tl) {
+        __syncthreads();
+        tl_end(p.tl);
+    }
 }
 
 // ------------------------------------------------------------ dispatch ---
@@ -557,6 +598,8 @@ static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -585,7 +628,7 @@ static cudaError_t launch_epi(const GemmParams &p, int impl, bool pdl, cudaStrea
 }
 
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream) {
-    if (p.cs != 1 && p.cs != 2 && p.cs != 4 && p.cs != 8) return cudaErrorInvalidValue;
+    if (p.cs != 1 && p.cs != 2 && p.cs != 4 && p.cs != 8 && p.cs != 16) return cudaErrorInvalidValue;
     if (p.B < 1 || p.B > MAX_B || p.B > p.Bp || !p.x16 || !p.x16lo || !p.sx) return cudaErrorInvalidValue;
     switch (epi) {
         case EPI_STORE: return launch_epi<EPI_STORE>(p, impl, pdl, stream);
@@ -599,9 +642,11 @@ cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaSt
 // --------------------------------------------------------- argmax final ---
 __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *__restrict__ idxs,
                                     int nparts, int B, int32_t *ids, const int32_t *positions,
-                                    int32_t *len_dev) {
+                                    int32_t *len_dev, unsigned long long *tl) {
+    tl_min(tl, 0);
     pdl_launch_dependents();
     pdl_wait();
+    tl_min(tl, 1);
     int b = blockIdx.x;
     __shared__ float sv[32];
     __shared__ int si[32];
@@ -625,14 +670,15 @@ __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *_
             if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
         ids[b] = bi == 0x7FFFFFFF ? 0 : bi;
         len_dev[b] = positions[b] + 1;
+        tl_end(tl);
     }
 }
 
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
                                 int32_t *ids, const int32_t *positions, int32_t *len_dev,
-                                bool pdl, cudaStream_t stream) {
+                                bool pdl, cudaStream_t stream, unsigned long long *tl) {
     return launch_k(argmax_final_kernel, dim3(B), dim3(256), 0, pdl, 1, stream, amax_val, amax_idx,
-                    nparts, B, ids, positions, len_dev);
+                    nparts, B, ids, positions, len_dev, tl);
 }
 
 }  // namespace zdec

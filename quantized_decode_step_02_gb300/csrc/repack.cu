@@ -172,9 +172,12 @@ __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
                              const int32_t *tokens, const int32_t *positions,
                              const int32_t *len_dev, uint32_t *status, int B,
                              float *__restrict__ x, int ldx, const float *__restrict__ gain,
-                             __half *u, __half *ulo, __half *usx, int Bp, float *part) {
+                             __half *u, __half *ulo, __half *usx, int Bp, float *part,
+                             unsigned long long *tl) {
+    tl_min(tl, 0);
     pdl_launch_dependents();
     pdl_wait();
+    tl_min(tl, 1);
     __shared__ float red[32];
     int b = blockIdx.x;
     if (b >= B) return;
@@ -216,15 +219,16 @@ __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
         float tot = 0.0f;
         for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += red[w];
         part[b] = tot;
+        tl_end(tl);
     }
 }
 
 cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
                          const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
                          float *x, int ldx, const float *gain, __half *u, __half *ulo, __half *usx,
-                         int Bp, float *part, bool pdl, cudaStream_t stream) {
+                         int Bp, float *part, bool pdl, cudaStream_t stream, unsigned long long *tl) {
     return launch_k(embed_kernel, dim3(B), dim3(128), 0, pdl, 1, stream, E, nsb, vocab, tokens,
-                    positions, len_dev, status, B, x, ldx, gain, u, ulo, usx, Bp, part);
+                    positions, len_dev, status, B, x, ldx, gain, u, ulo, usx, Bp, part, tl);
 }
 
 }  // namespace zdec

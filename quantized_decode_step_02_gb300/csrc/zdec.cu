@@ -30,9 +30,9 @@ size_t tile_bytes(int rows16, int nsb) { return (size_t)n_groups(rows16) * nsb *
 
 // K split (cluster size) for a projection: grow it until the grid covers the
 // GPU, keeping at least two super-blocks per CTA.
-int pick_cs(int groups, int nsb, int target_ctas) {
+int pick_cs(int groups, int nsb, int target_ctas, int max_cs = 8) {
     int cs = 1;
-    while (cs < 8 && groups * cs * 2 <= target_ctas && nsb / (cs * 2) >= 2) cs *= 2;
+    while (cs < max_cs && groups * cs * 2 <= target_ctas && nsb / (cs * 2) >= 2) cs *= 2;
     return cs;
 }
 
@@ -79,6 +79,7 @@ struct zdec_ctx {
     int cs_qkv[2] = {1, 1}, cs_o[2] = {1, 1}, cs_gu[2] = {1, 1}, cs_down[2] = {1, 1}, cs_lm[2] = {1, 1};  // B<=4, B>4
     int32_t *tok_dev = nullptr, *pos_dev = nullptr, *ids_dev = nullptr, *len_dev = nullptr;
     uint32_t *status = nullptr;
+    uint4 *qfrag = nullptr;            // [max_B][n_q][32] query fragments (QKV epilogue -> attention)
     int32_t *pinned_io = nullptr;      // [2*max_B] staging of host tokens/positions
     // host state
     std::vector<int> len_host;
@@ -107,6 +108,11 @@ struct zdec_ctx {
     int step_att_min = 8;                // attention units per CTA at least (ZDEC_STEP_ATT_MIN)
     unsigned long long *trace = nullptr; // phase timeline of the last persistent step, or null
     size_t trace_entries = 0;
+    bool trace_on = false;               // tracing requested (zdec_set_trace)
+    unsigned long long *ktl = nullptr;   // kernel engine: [launches][4] timeline of the last step
+    unsigned long long *ktl_init = nullptr;   // pinned: its initial values
+    size_t ktl_entries = 0;
+    std::vector<int> ktl_kinds;          // kernel kind of each launch of the last traced step
 };
 
 static zdec_status fail(zdec_ctx *c, zdec_status s, const char *fmt, ...) {
@@ -154,6 +160,8 @@ static void free_ctx(zdec_ctx *ctx) {
     cudaFree(ctx->ws);
     cudaFree(ctx->step_buf);
     cudaFree(ctx->trace);
+    cudaFree(ctx->ktl);
+    cudaFreeHost(ctx->ktl_init);
     cudaFreeHost(ctx->pinned_io);
     cudaFreeHost(ctx->capture_dev_host);
     if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
@@ -427,6 +435,7 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
         size_t oa16 = t(plane(F)), oa16lo = t(plane(F)), oasx = t(sums(F));
         (void)Kmax;
         size_t otok = t(Bm * 4), opos = t(Bm * 4), oids = t(Bm * 4), olen = t(Bm * 4), ost = t(4);
+        size_t oqf = t((size_t)Bm * d.n_q_heads * 32 * 16);
         ctx->ws_bytes = w;
         if (cudaMalloc(&ctx->ws, w) != cudaSuccess) {
             cudaGetLastError();
@@ -443,6 +452,7 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
         ctx->tok_dev = (int32_t *)(b + otok); ctx->pos_dev = (int32_t *)(b + opos);
         ctx->ids_dev = (int32_t *)(b + oids); ctx->len_dev = (int32_t *)(b + olen);
         ctx->status = (uint32_t *)(b + ost);
+        ctx->qfrag = (uint4 *)(b + oqf);
         if (cudaMemsetAsync(ctx->ws, 0, w, ctx->stream) != cudaSuccess)
             return bail(fail(nullptr, ZDEC_ERR_CUDA, "workspace memset failed"));
         if (cudaMallocHost(&ctx->pinned_io, 2 * Bm * sizeof(int32_t)) != cudaSuccess)
@@ -450,13 +460,18 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     }
     {
         const int nsm = ctx->num_sms > 0 ? ctx->num_sms : 148;
+        // ZDEC_CS_TARGET: CTAs per SM x 10 that the split factors aim at (default:
+        // the kernel's residency); ZDEC_CS_MAX: largest split (8, or 16 with
+        // non-portable clusters)
+        const int tgt10 = getenv("ZDEC_CS_TARGET") ? atoi(getenv("ZDEC_CS_TARGET")) : 0;
+        const int csmax = getenv("ZDEC_CS_MAX") ? atoi(getenv("ZDEC_CS_MAX")) : 8;
         for (int v = 0; v < 2; v++) {   // split factors filling the kernel's CTAs per SM
-            const int target = nsm * gemm_ctas_per_sm(v ? 8 : 4, 2);
-            ctx->cs_qkv[v] = pick_cs(n_groups(ctx->qkv_ld / 16), ctx->nsb_h, target);
-            ctx->cs_o[v] = pick_cs(n_groups(H / 16), ctx->nsb_q, target);
-            ctx->cs_gu[v] = pick_cs(n_groups(F / 8), ctx->nsb_h, target);
-            ctx->cs_down[v] = pick_cs(n_groups(H / 16), ctx->nsb_f, target);
-            ctx->cs_lm[v] = pick_cs(n_groups(ctx->nrt_vocab), ctx->nsb_h, target);
+            const int target = tgt10 > 0 ? nsm * tgt10 / 10 : nsm * gemm_ctas_per_sm(v ? 8 : 4, 2);
+            ctx->cs_qkv[v] = pick_cs(n_groups(ctx->qkv_ld / 16), ctx->nsb_h, target, csmax);
+            ctx->cs_o[v] = pick_cs(n_groups(H / 16), ctx->nsb_q, target, csmax);
+            ctx->cs_gu[v] = pick_cs(n_groups(F / 8), ctx->nsb_h, target, csmax);
+            ctx->cs_down[v] = pick_cs(n_groups(H / 16), ctx->nsb_f, target, csmax);
+            ctx->cs_lm[v] = pick_cs(n_groups(ctx->nrt_vocab), ctx->nsb_h, target, csmax);
         }
     }
     if (attention_setup(kv_dtype) != cudaSuccess)
@@ -587,20 +602,29 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         return cudaMemcpyAsync(ctx->capture_dev_host + (size_t)slot * B * H, ctx->x, (size_t)B * H * 4,
                                cudaMemcpyDeviceToHost, s);
     };
-#define STEP(kind, call)                 \
-    do {                                 \
-        mark(kind, true);                \
-        if ((e = (call)) != cudaSuccess) \
-            return e;                    \
-        mark(kind, false);               \
-        nk++;                            \
+    // launch timeline (tracing): slot nk of ctx->ktl for launch nk
+    unsigned long long *tlb = ctx->trace_on ? ctx->ktl : nullptr, *tlk = nullptr;
+    if (tlb) {
+        ctx->ktl_kinds.clear();
+        if ((e = cudaMemcpyAsync(tlb, ctx->ktl_init, ctx->ktl_entries * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return e;
+    }
+#define STEP(kind, call)                        \
+    do {                                        \
+        tlk = tlb ? tlb + 8 * nk : nullptr;     \
+        if (tlb) ctx->ktl_kinds.push_back(kind); \
+        mark(kind, true);                       \
+        if ((e = (call)) != cudaSuccess)        \
+            return e;                           \
+        mark(kind, false);                      \
+        nk++;                                   \
     } while (0)
 
     const int Bp0 = ctx->Bp_max;
     const int cv = B <= 4 ? 0 : 1;   // split-factor set
     STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev,
                                          ctx->len_dev, ctx->status, B, ctx->x, H, ctx->L[0].attn_norm,
-                                         ctx->x16, ctx->x16lo, ctx->sx, Bp0, ctx->rms_part, pdl, s));
+                                         ctx->x16, ctx->x16lo, ctx->sx, Bp0, ctx->rms_part, pdl, s, tlk));
     if ((e = capture_x(0)) != cudaSuccess) return e;
     const int Bp = ctx->Bp_max;   // row pitch of every act plane
     GemmParams gp{};
@@ -639,6 +663,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     ap.B = B;
     ap.max_L = ctx->max_L;
     ap.status = ctx->status;
+    ap.q_frag = ctx->qfrag;   // written by the QKV projection's epilogue
     // RMSNorm never runs as its own kernel: the producer of the residual (the
     // embedding gather, the O and down projections) writes gain*x as the next
     // projection's operand plus per-group sums of x^2, and the consumer scales
@@ -658,22 +683,24 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, ctx->cs_qkv[cv]);
         prefetch(lw.o, H / 16, ctx->nsb_q);
         gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld;
-        STEP(ZDEC_KERNEL_GEMM_QKV, launch_gemm(gp, EPI_STORE, impl, pdl, s));
+        gp.q_frag = ctx->qfrag; gp.q_pos = ctx->pos_dev; gp.q_rope = ctx->rope; gp.q_heads = d.n_q_heads;
+        STEP(ZDEC_KERNEL_GEMM_QKV, (gp.tl = tlk, launch_gemm(gp, EPI_STORE, impl, pdl, s)));
+        gp.q_frag = nullptr;
         ap.layer = l;
-        STEP(ZDEC_KERNEL_ATTENTION, launch_attention(ap, pdl, s));
+        STEP(ZDEC_KERNEL_ATTENTION, (ap.tl = tlk, launch_attention(ap, pdl, s)));
         plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention combine
         matrix(lw.o, H, H / 16, ctx->nsb_q, ctx->cs_o[cv]);
         prefetch(lw.gu, F / 8, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
         gp.next_gain = lw.ffn_norm; gp.part_out = ctx->rms_part;
         gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
-        STEP(ZDEC_KERNEL_GEMM_O, launch_gemm(gp, EPI_RESID, impl, pdl, s));
+        STEP(ZDEC_KERNEL_GEMM_O, (gp.tl = tlk, launch_gemm(gp, EPI_RESID, impl, pdl, s)));
         normed_input(resid_groups);
         matrix(lw.gu, F, F / 8, ctx->nsb_h, ctx->cs_gu[cv]);
         prefetch(lw.down, H / 16, ctx->nsb_f);
         gp.out = nullptr; gp.ldo = F;
         gp.out16 = ctx->a16; gp.out16lo = ctx->a16lo; gp.out_sx = ctx->asx;
-        STEP(ZDEC_KERNEL_GEMM_GATEUP, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s));
+        STEP(ZDEC_KERNEL_GEMM_GATEUP, (gp.tl = tlk, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s)));
         plain_input(ctx->a16, ctx->a16lo, ctx->asx);   // written by the gate/up epilogue
         matrix(lw.down, H, H / 16, ctx->nsb_f, ctx->cs_down[cv]);
         if (l + 1 < d.n_layers) prefetch(ctx->L[l + 1].qkv, ctx->qkv_ld / 16, ctx->nsb_h);
@@ -682,16 +709,16 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         gp.next_gain = l + 1 < d.n_layers ? ctx->L[l + 1].attn_norm : ctx->final_norm;
         gp.part_out = ctx->rms_part;
         gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
-        STEP(ZDEC_KERNEL_GEMM_DOWN, launch_gemm(gp, EPI_RESID, impl, pdl, s));
+        STEP(ZDEC_KERNEL_GEMM_DOWN, (gp.tl = tlk, launch_gemm(gp, EPI_RESID, impl, pdl, s)));
         if ((e = capture_x(l + 1)) != cudaSuccess) return e;
     }
     normed_input(resid_groups);
     matrix(ctx->embed, d.vocab, ctx->nrt_vocab, ctx->nsb_h, ctx->cs_lm[cv]);
     gp.out = logits_out; gp.ldo = d.vocab;
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
-    STEP(ZDEC_KERNEL_GEMM_LMHEAD, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s));
+    STEP(ZDEC_KERNEL_GEMM_LMHEAD, (gp.tl = tlk, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s)));
     STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, gemm_grid(gp), B, ctx->ids_dev,
-                                                 ctx->pos_dev, ctx->len_dev, pdl, s));
+                                                 ctx->pos_dev, ctx->len_dev, pdl, s, tlk));
 #undef STEP
     ctx->last_kernels = nk;
     ctx->last_splits = ap.cs;
@@ -748,7 +775,7 @@ static cudaError_t enqueue_step_persistent(zdec_ctx *ctx, int B, float *logits_o
     p.slot_bytes = step_slot_bytes(B);
     p.pf_items = ctx->step_pf_items;
     p.att_min_units = ctx->step_att_min;
-    p.trace = ctx->trace;
+    p.trace = ctx->trace_on ? ctx->trace : nullptr;
     cudaStream_t s = ctx->stream;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (ctx->prof) {
@@ -819,7 +846,7 @@ extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tok
     zdec_status st = check_step_args(ctx, B, tokens, positions, ids);
     if (st != ZDEC_OK) return st;
     const bool host = flags & ZDEC_STEP_HOST_IO;
-    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host || ctx->trace ||
+    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host || ctx->trace_on ||
                        (ctx->persistent_eager && use_persistent(ctx, B));
     st = stage_inputs(ctx, B, tokens, positions, host);
     if (st != ZDEC_OK) return st;
@@ -921,32 +948,50 @@ extern "C" zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info) {
 
 extern "C" zdec_status zdec_set_trace(zdec_ctx *ctx, int on) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    CK(cudaStreamSynchronize(ctx->stream));
     if (!on) {
-        CK(cudaStreamSynchronize(ctx->stream));
         cudaFree(ctx->trace);
+        cudaFree(ctx->ktl);
+        cudaFreeHost(ctx->ktl_init);
         ctx->trace = nullptr;
-        ctx->trace_entries = 0;
+        ctx->ktl = nullptr;
+        ctx->ktl_init = nullptr;
+        ctx->trace_entries = ctx->ktl_entries = 0;
+        ctx->trace_on = false;
         return ZDEC_OK;
     }
-    if (ctx->step_grid == 0) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the persistent step kernel is unavailable");
-    if (ctx->trace) return ZDEC_OK;
-    const size_t n = (size_t)ctx->step_grid * (2 + 5 * ctx->d.n_layers) * 8;
-    if (cudaMalloc(&ctx->trace, n * 8) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(ctx, ZDEC_ERR_OOM, "cannot allocate the step trace");
+    if (ctx->trace_on) return ZDEC_OK;
+    if (ctx->step_grid > 0) {   // persistent engine: [ctas][phases][8]
+        const size_t n = (size_t)ctx->step_grid * (2 + 5 * ctx->d.n_layers) * 8;
+        if (cudaMalloc(&ctx->trace, n * 8) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, ZDEC_ERR_OOM, "cannot allocate the step trace");
+        }
+        CK(cudaMemsetAsync(ctx->trace, 0, n * 8, ctx->stream));
+        ctx->trace_entries = n;
     }
-    CK(cudaMemsetAsync(ctx->trace, 0, n * 8, ctx->stream));
-    ctx->trace_entries = n;
+    // kernel engine: [launches][8] = (first start, first past the wait, last end, kind, milestones)
+    const size_t nk = (size_t)(3 + 5 * ctx->d.n_layers) * 8;
+    if (cudaMalloc(&ctx->ktl, nk * 8) != cudaSuccess || cudaMallocHost(&ctx->ktl_init, nk * 8) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ctx, ZDEC_ERR_OOM, "cannot allocate the launch timeline");
+    }
+    for (size_t i = 0; i < nk; i++) ctx->ktl_init[i] = (i % 8 < 2) ? ~0ULL : 0ULL;
+    ctx->ktl_entries = nk;
+    ctx->trace_on = true;
     return ZDEC_OK;
 }
 
 extern "C" zdec_status zdec_debug_step_trace(zdec_ctx *ctx, uint64_t *out_host, size_t cap, size_t *n) {
     if (!ctx || !n) return fail(nullptr, ZDEC_ERR_ARG, "null argument");
-    *n = ctx->trace_entries;
-    if (!ctx->trace || !out_host) return ZDEC_OK;   // size query
-    if (cap < ctx->trace_entries) return fail(ctx, ZDEC_ERR_ARG, "trace needs %zu entries", ctx->trace_entries);
+    const bool pers = ctx->last_engine == ZDEC_ENGINE_PERSISTENT;
+    *n = !ctx->trace_on ? 0 : (pers ? ctx->trace_entries : ctx->ktl_entries);
+    if (!ctx->trace_on || !out_host || *n == 0) return ZDEC_OK;   // size query
+    if (cap < *n) return fail(ctx, ZDEC_ERR_ARG, "trace needs %zu entries", *n);
     CK(cudaStreamSynchronize(ctx->stream));
-    CK(cudaMemcpy(out_host, ctx->trace, ctx->trace_entries * 8, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(out_host, pers ? ctx->trace : ctx->ktl, *n * 8, cudaMemcpyDeviceToHost));
+    if (!pers)
+        for (size_t i = 0; i < *n / 8; i++) out_host[8 * i + 3] = i < ctx->ktl_kinds.size() ? ctx->ktl_kinds[i] : 0;
     return ZDEC_OK;
 }
 

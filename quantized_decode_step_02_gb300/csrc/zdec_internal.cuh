@@ -235,6 +235,29 @@ __device__ __forceinline__ void store_sum(__half *sums, int sb, int b, int j, in
     sums[act_sum(sb, b, j, 1, Bp)] = lo;
 }
 
+// ------------------------------------------------------ launch timeline ---
+// Optional per-launch timestamps (%globaltimer, ns): tl[0] earliest CTA start,
+// tl[1] earliest CTA past the dependency wait, tl[2] latest CTA end, tl[3] the
+// launch's kind (written by the host), tl[4..7] the latest CTA to reach a
+// kernel's own milestones (projection: past the wait, first stage landed, K
+// loop done, cluster reduction done).  Null: off.  Recorded by thread 0 of
+// every CTA with atomic min / max.
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void tl_min(unsigned long long *tl, int k) {
+    if (tl && threadIdx.x == 0) atomicMin(tl + k, gtimer());
+}
+__device__ __forceinline__ void tl_end(unsigned long long *tl) {
+    if (tl && threadIdx.x == 0) atomicMax(tl + 2, gtimer());
+}
+// Latest CTA to reach milestone k (4..7; what each means is up to the kernel).
+__device__ __forceinline__ void tl_max(unsigned long long *tl, int k) {
+    if (tl && threadIdx.x == 0) atomicMax(tl + k, gtimer());
+}
+
 // ------------------------------------------------------- device status ---
 enum : uint32_t { STATUS_POSITION = 1u, STATUS_CAPACITY = 2u, STATUS_TIMEOUT = 4u, STATUS_TOKEN = 8u };
 

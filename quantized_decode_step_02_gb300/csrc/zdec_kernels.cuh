@@ -33,7 +33,7 @@ cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int 
 cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
                          const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
                          float *x, int ldx, const float *gain, __half *u, __half *ulo, __half *usx,
-                         int Bp, float *part, bool pdl, cudaStream_t stream);
+                         int Bp, float *part, bool pdl, cudaStream_t stream, unsigned long long *tl = nullptr);
 
 // --------------------------------------------------------------- gemm.cu
 enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LMHEAD = 3 };
@@ -62,11 +62,21 @@ struct GemmParams {
     float rms_eps;
     float *amax_val;       // LMHEAD: per-CTA argmax partials [grid][MAX_B]
     int *amax_idx;
-    int cs;                // K split over a cluster of cs CTAs (1, 2, 4, 8)
+    int cs;                // K split over a cluster of cs CTAs (1, 2, 4, 8, 16)
     int stages;            // pipeline depth (set by the launcher)
     const uint8_t *pf_ptr; // read-only bytes the next kernel streams (L2 prefetch), or null
     size_t pf_bytes;       // multiple of 16, pf_ptr 16-byte aligned
     uint32_t *status;      // device status word (bounded-wait timeouts)
+    unsigned long long *tl;   // launch timeline slot (zdec_internal.cuh) or null
+    // STORE of a QKV projection: the query heads (groups < q_heads, one 128-row
+    // group each) also go out rotated (RoPE at q_pos[b]), scaled by 1/sqrt(128)
+    // and split into fp16 hi + lo, in the attention's mma A-fragment order:
+    // q_frag[((b * q_heads + head) * 8 + st) * 4 + tig] = (hi, lo) of dims
+    // 16 st + 4 tig + {0,1} and (hi, lo) of dims + {2,3} (null: off)
+    uint4 *q_frag;
+    const int32_t *q_pos;
+    const float2 *q_rope;
+    int q_heads;
 };
 // impl 1: CUDA-core dequant-matvec (B <= 4); impl 2: mma.sync swap-AB GEMM.
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream);
@@ -83,7 +93,7 @@ cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, flo
 // advances the device lengths: len_dev[b] = positions[b] + 1.
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
                                 int32_t *ids, const int32_t *positions, int32_t *len_dev,
-                                bool pdl, cudaStream_t stream);
+                                bool pdl, cudaStream_t stream, unsigned long long *tl = nullptr);
 
 // ---------------------------------------------------------- attention.cu
 struct KvArena {
@@ -114,6 +124,8 @@ struct AttnParams {
     int B;
     int max_L;             // positions >= max_L are ignored (the step is flagged elsewhere)
     uint32_t *status;      // device status word (bounded-wait timeouts)
+    unsigned long long *tl;   // launch timeline slot (zdec_internal.cuh) or null
+    const uint4 *q_frag;   // query fragments prepared by the QKV projection (GemmParams), or null
 };
 cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream);
 // Raise the attention kernel's dynamic shared-memory limit (once, before capture).

@@ -309,3 +309,33 @@ def test_full_step_b8_l2400_fp16_and_batch_invariance():
 @pytest.mark.parametrize("kv_dtype", [0, 1])
 def test_full_step_b8_long_context(kv_dtype):
     _full_config(3, 8, [6900, 8192, 6900, 8192, 7000, 8000, 6900, 8192], kv_dtype)
+
+
+def test_trace_timelines_of_both_engines():
+    """Tracing records every launch of the kernel engine (start <= release from
+    the dependency wait <= end, each release after the previous launch's end)
+    and the persistent engine's per-CTA phase timeline; traced steps still
+    match the oracle."""
+    d = SMALL
+    w = cached_model(d, 110)
+    dec, om, kvs = setup_pair(d, w, 110, [20, 7], 0, 64)
+    dec.set_engine(z.ENGINE_KERNELS)
+    dec.set_trace(True)
+    check_step(dec, om, kvs, make_tokens(d, 1100, 2), np.array([20, 7], np.int32), "traced kernels")
+    tr = dec.step_trace().astype(np.int64)
+    assert tr.shape == (3 + 5 * d.n_layers, 8)
+    kinds = [z.KERNEL_KINDS[k] for k in tr[:, 3]]
+    assert kinds[0] == "embed" and kinds[-2] == "gemm_lmhead" and kinds[-1] == "argmax"
+    assert kinds.count("attention") == d.n_layers
+    assert np.all(tr[:, 0] <= tr[:, 1]) and np.all(tr[:, 1] <= tr[:, 2])
+    assert np.all(tr[1:, 1] >= tr[:-1, 2])
+    if dec.info()["step_ctas"] > 0:
+        dec.set_engine(z.ENGINE_PERSISTENT)
+        check_step(dec, om, kvs, make_tokens(d, 1101, 2), np.array([21, 8], np.int32), "traced persistent")
+        tp = dec.step_trace()
+        assert tp.shape == (dec.info()["step_ctas"], 2 + 5 * d.n_layers, 8)
+        busy = tp[:, :, 4] > 0
+        assert busy[:, 0].any() and busy[:, -1].any()   # the embedding and the LM head ran
+    dec.set_trace(False)
+    assert dec.step_trace().size == 0
+    dec.close()
