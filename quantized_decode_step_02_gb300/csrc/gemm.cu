@@ -337,6 +337,7 @@ template <int NT, int EPI, int IMPL>
 __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const GemmParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_bad;
+    __shared__ uint64_t red_bar;   // rank 0 of a cluster: the peers' partial tiles have landed
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
     const int cs = p.cs, rank = blockIdx.x % cs, grp = blockIdx.x / cs;
     const int rt = grp * GT + warp;
@@ -365,8 +366,11 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     if (threadIdx.x == 0) {
         s_bad = 0;
         for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
+        if (cs > 1 && rank == 0) mbar_init(&red_bar, cs - 1);
         mbar_fence_init();
     }
+    // rank 0 receives the peers' partial tiles after the barriers (see the end)
+    const uint32_t red_off = (uint32_t)D * sbyt + 64u;
     // zero the batch rows the copies never write (rows B..BR-1 and the lo lanes'
     // min-term slots) in every stage buffer
     for (int i = threadIdx.x; i < D * BR * 8; i += blockDim.x) {
@@ -382,6 +386,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         if (w < 2) *reinterpret_cast<uint4 *>(base + lay.zero + r * 32 + w * 16) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
+    if (cs > 1) cluster_arrive_release();   // publishes red_bar's initialisation (waited on at the end)
     // this lane's fixed offsets into a stage: virtual column g of n-tile 0 is the
     // hi (g even) or lo (g odd) plane of batch row g/2
     const int g = lane >> 2;
@@ -511,46 +516,43 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         for (int c = 0; c < NB; c++)
             if (c == tig) { y[0][0] = accr[c][0]; y[0][1] = accr[c][1]; }
     }
-    if (cs > 1) {   // K split across the cluster: rank 0 sums the partial tiles in rank order
-        cg::cluster_group cluster = cg::this_cluster();
-        float *red = reinterpret_cast<float *>(smem);   // every stage has been consumed
+    if (cs > 1) {   // K split across the cluster: the peers push their partial tiles to rank 0
+        cluster_wait_acquire();   // every CTA of the cluster has initialised its barriers
+        constexpr int SLOT = GT * NY * 2 * 32;   // floats of one peer's partial tile set
+        const uint32_t red_local = smem_u32(smem + red_off);
+        if (rank != 0) {
+            const uint32_t dst = map_to_rank(red_local, 0) + (uint32_t)((rank - 1) * SLOT) * 4u;
 #pragma unroll
-        for (int nt = 0; nt < NY; nt++)
+            for (int nt = 0; nt < NY; nt++)
 #pragma unroll
-            for (int r = 0; r < 2; r++) red[((warp * NY + nt) * 2 + r) * 32 + lane] = y[nt][r];
-        cluster.sync();
-        if (rank == 0 && !EARLY) {
-            for (int rr = 1; rr < cs; rr++) {
-                const float *peer = cluster.map_shared_rank(red, rr);
-#pragma unroll
-                for (int nt = 0; nt < NY; nt++)
-#pragma unroll
-                    for (int r = 0; r < 2; r++) y[nt][r] += peer[((warp * NY + nt) * 2 + r) * 32 + lane];
+                for (int r = 0; r < 2; r++)
+                    st_cluster_f32(dst + (uint32_t)(((warp * NY + nt) * 2 + r) * 32 + lane) * 4u, y[nt][r]);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                mbar_remote_arrive(map_to_rank(smem_u32(&red_bar), 0));
             }
-        } else if (rank == 0) {   // every peer's loads in flight before the sums (rank order kept)
-            float pv[15][NY][2];
-#pragma unroll
-            for (int rr = 1; rr < 16; rr++) {
-                const float *peer = rr < cs ? cluster.map_shared_rank(red, rr) : nullptr;
-#pragma unroll
-                for (int nt = 0; nt < NY; nt++)
-#pragma unroll
-                    for (int r = 0; r < 2; r++)
-                        pv[rr - 1][nt][r] = rr < cs ? peer[((warp * NY + nt) * 2 + r) * 32 + lane] : 0.0f;
-            }
-#pragma unroll
-            for (int rr = 1; rr < 16; rr++)
-#pragma unroll
-                for (int nt = 0; nt < NY; nt++)
-#pragma unroll
-                    for (int r = 0; r < 2; r++)
-                        if (rr < cs) y[nt][r] += pv[rr - 1][nt][r];
-        }
-        cluster.sync();
-        if (rank != 0 || bad) {
             tl_end(p.tl);
             return;
         }
+        // rank 0: wait (bounded) for the cs - 1 pushes, then sum them in rank order
+        if (!mbar_try_wait_cluster(&red_bar, 0)) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait_cluster(&red_bar, 0))
+                if (clock64() - t0 > (1LL << 32)) {
+                    if (threadIdx.x == 0) atomicOr(p.status, STATUS_TIMEOUT);
+                    s_bad = 1;
+                    break;
+                }
+        }
+        const float *red = reinterpret_cast<const float *>(smem + red_off);
+        for (int rr = 1; rr < cs; rr++)
+#pragma unroll
+            for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+                for (int r = 0; r < 2; r++) y[nt][r] += red[(rr - 1) * SLOT + ((warp * NY + nt) * 2 + r) * 32 + lane];
+        __syncthreads();
+        if (bad || s_bad) return;
         tl_max(p.tl, 7);
     }
     if (p.rms_part) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
@@ -581,8 +583,9 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
 // ------------------------------------------------------------ dispatch ---
 int gemm_grid(const GemmParams &p) { return n_groups(p.nrt) * p.cs; }
 
-static int stages_for(uint32_t stage_bytes, int occ) {
-    const uint32_t budget = occ >= 3 ? 70u * 1024u : (occ == 2 ? 110u * 1024u : 200u * 1024u);
+static int stages_for(uint32_t stage_bytes, int occ, uint32_t reserved) {
+    uint32_t budget = occ >= 3 ? 70u * 1024u : (occ == 2 ? 110u * 1024u : 200u * 1024u);
+    budget = budget > reserved + 2 * stage_bytes ? budget - reserved : 2 * stage_bytes;
     int d = (int)(budget / stage_bytes);
     return d < 2 ? 2 : (d > 6 ? 6 : d);
 }
@@ -592,8 +595,13 @@ int gemm_ctas_per_sm(int B, int impl) { return impl == 2 && B <= 4 ? 3 : (B <= 8
 template <int NT, int EPI, int IMPL>
 static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
     const StageLayout lay(IMPL == 2 ? 4 * NT : 4);
-    p.stages = stages_for(lay.bytes, GemmOcc<NT, IMPL>::v);
-    const size_t smem = (size_t)p.stages * lay.bytes + 8 * 8;
+    // rank 0 of a cluster holds the cs - 1 peers' partial tiles; a split whose
+    // tiles do not fit next to two stages is halved
+    constexpr uint32_t NYB = GT * (IMPL == 2 ? NT : 1) * 2 * 32 * 4;
+    while (p.cs > 1 && (uint32_t)(p.cs - 1) * NYB + 2 * lay.bytes > 180u * 1024u) p.cs >>= 1;
+    const uint32_t red_bytes = p.cs > 1 ? (uint32_t)(p.cs - 1) * NYB : 0u;
+    p.stages = stages_for(lay.bytes, GemmOcc<NT, IMPL>::v, red_bytes);
+    const size_t smem = (size_t)p.stages * lay.bytes + 64 + red_bytes;
     static bool configured = false;   // raise the dynamic shared-memory limit once per instance
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>,

@@ -717,7 +717,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     gp.out = logits_out; gp.ldo = d.vocab;
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
     STEP(ZDEC_KERNEL_GEMM_LMHEAD, (gp.tl = tlk, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s)));
-    STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, gemm_grid(gp), B, ctx->ids_dev,
+    STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, n_groups(ctx->nrt_vocab), B, ctx->ids_dev,
                                                  ctx->pos_dev, ctx->len_dev, pdl, s, tlk));
 #undef STEP
     ctx->last_kernels = nk;
