@@ -242,7 +242,10 @@ def run_reference(a, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True):
+def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=None):
+    """One measured configuration.  dev_hist: (k, v) fp16 CUDA tensors
+    [n_layers][>= L][n_kv][hd] appended to every sequence instead of the seeded
+    host history (the sweep's large points; timing does not depend on values)."""
     import torch
     import quantized_decode_step_02_gb300 as z
     dev = torch.cuda.current_device()
@@ -253,9 +256,17 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True):
     if a.gemm_impl:
         dec.set_gemm_impl(a.gemm_impl)
     dec.set_engine({"auto": z.ENGINE_AUTO, "kernels": z.ENGINE_KERNELS, "persistent": z.ENGINE_PERSISTENT}[a.engine])
-    for b in range(B):
-        k, v = make_kv_history(desc, a.seed, b, L)
-        dec.append_kv(b, k, v)
+    if dev_hist is not None:   # one contiguous copy, alive until the appends have run
+        k, v = dev_hist[0][:, :L].contiguous(), dev_hist[1][:, :L].contiguous()
+        torch.cuda.synchronize()
+        for b in range(B):
+            dec.append_kv(b, k, v)
+        dec.sync()
+        del k, v
+    else:
+        for b in range(B):
+            k, v = make_kv_history(desc, a.seed, b, L)
+            dec.append_kv(b, k, v)
     n_total = a.warmup + a.steps
     toks = [torch.from_numpy(make_tokens(desc, a.seed * 1000 + i, B)).cuda() for i in range(n_total + 4)]
     pos = [torch.full((B,), L + i, dtype=torch.int32, device="cuda") for i in range(n_total + 4)]
@@ -330,13 +341,28 @@ def main():
     w = make_model(desc, a.seed)
     gen_s = time.time() - t0
     if a.sweep:
+        # B x L x kv grid on a seeded device-side N(0,1) history (one per L,
+        # shared by the sequences), then the projection-kernel switch point
+        import torch
+        gen = torch.Generator(device="cuda").manual_seed(10)
+        shape = (desc.n_layers, 32768, desc.n_kv_heads, desc.head_dim)
+        hist = (torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16),
+                torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16))
         for kv in ("f16", "q8_0"):
             for B in (1, 4, 8, 16, 32):
                 for L in (2048, 8192, 16384, 32768):
-                    r = bench_point(a, desc, w, B, L, kv, rank, world)
+                    r = bench_point(a, desc, w, B, L, kv, rank, world, dev_hist=hist)
                     if rank == 0:
                         print(json.dumps({"sweep": True, **{k: v for k, v in r.items() if k != "profile_ms"},
                                           "profile_ms": r["profile_ms"]}), flush=True)
+        for B in (1, 2, 3, 4):
+            for impl in ((1, 2, 3) if B == 1 else (1, 2)):
+                a.gemm_impl = impl
+                r = bench_point(a, desc, w, B, 2048, "f16", rank, world, dev_hist=hist)
+                if rank == 0:
+                    print(json.dumps({"switch": True, "impl": impl, **{k: v for k, v in r.items() if k != "profile_ms"},
+                                      "profile_ms": r["profile_ms"]}), flush=True)
+        a.gemm_impl = 0
         return
     r = bench_point(a, desc, w, a.B, a.L, a.kv, rank, world)
     if rank != 0:
