@@ -58,6 +58,8 @@ def args_parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--sweep", action="store_true", help="B x L x kv grid, one JSON line per point")
+    p.add_argument("--device-history", action="store_true",
+                   help="one seeded device-side N(0,1) KV history shared by the sequences (fast setup)")
     p.add_argument("--layers", type=int, default=None, help="smaller model (profiling runs only)")
     p.add_argument("--trace", default=None, help="save the phase timeline of one persistent step (.npy)")
     return p.parse_args()
@@ -340,14 +342,17 @@ def main():
     t0 = time.time()
     w = make_model(desc, a.seed)
     gen_s = time.time() - t0
+    def device_history(L):
+        import torch
+        gen = torch.Generator(device="cuda").manual_seed(10)
+        shape = (desc.n_layers, L, desc.n_kv_heads, desc.head_dim)
+        return (torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16),
+                torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16))
+
     if a.sweep:
         # B x L x kv grid on a seeded device-side N(0,1) history (one per L,
         # shared by the sequences), then the projection-kernel switch point
-        import torch
-        gen = torch.Generator(device="cuda").manual_seed(10)
-        shape = (desc.n_layers, 32768, desc.n_kv_heads, desc.head_dim)
-        hist = (torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16),
-                torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16))
+        hist = device_history(32768)
         for kv in ("f16", "q8_0"):
             for B in (1, 4, 8, 16, 32):
                 for L in (2048, 8192, 16384, 32768):
@@ -364,7 +369,8 @@ def main():
                                       "profile_ms": r["profile_ms"]}), flush=True)
         a.gemm_impl = 0
         return
-    r = bench_point(a, desc, w, a.B, a.L, a.kv, rank, world)
+    r = bench_point(a, desc, w, a.B, a.L, a.kv, rank, world,
+                    dev_hist=device_history(a.L) if a.device_history else None)
     if rank != 0:
         return
     pk = peaks() or {}

@@ -52,8 +52,16 @@ template <> struct AttnLayout<1> {          // Q8_0
     static constexpr int STAGE = K_BYTES + V_BYTES + KS_BYTES + VS_BYTES;
 };
 
-size_t attention_smem_bytes(int kv_dtype) {
-    size_t stages = kv_dtype ? 2 * AttnLayout<1>::STAGE : 2 * AttnLayout<0>::STAGE;
+// A CTA keeps `stages` chunks in flight.  With few CTAs per SM the chunk
+// latency, not the SM's arithmetic, bounds a shallow ring: at two stages a
+// Q8_0 cache ran at half the fp16 cache's bandwidth (the same chunks per
+// latency, half the bytes).
+constexpr int ATT_MAX_STAGES = 8;
+static int att_max_stages(int kv_dtype) { return kv_dtype ? ATT_MAX_STAGES : 5; }   // <= 200 KB
+int attention_default_stages(int kv_dtype) { return kv_dtype ? 4 : 2; }
+size_t attention_smem_bytes(int kv_dtype, int ns) {
+    if (ns < 2 || ns > att_max_stages(kv_dtype)) ns = attention_default_stages(kv_dtype);
+    size_t stages = kv_dtype ? (size_t)ns * AttnLayout<1>::STAGE : (size_t)ns * AttnLayout<0>::STAGE;
     size_t merge = (4 * 4 * 2 + 4 * 4 * HD) * sizeof(float);
     return stages > merge ? stages : merge;
 }
@@ -86,10 +94,17 @@ __device__ __forceinline__ void issue_chunk(const AttnParams &p, uint8_t *stage,
             int t = i >> 4, sg = i & 15;
             cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + kv_k16_off(c0 + t, 8 * sg));
         }
-        int vseg = (nt + 7) >> 3;   // 8 tokens per 16 bytes
-        for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
-            int d = i / vseg, sg = i % vseg;
-            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v16_off(d, c0 + 8 * sg));
+        if (nt == ATT_CHUNK) {   // whole chunk: 8 segments per head-dim row
+            for (int i = threadIdx.x; i < HD * 8; i += blockDim.x) {
+                const int d = i >> 3, sg = i & 7;
+                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v16_off(d, c0 + 8 * sg));
+            }
+        } else {
+            const int vseg = (nt + 7) >> 3;   // 8 tokens per 16 bytes
+            for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
+                const int d = i / vseg, sg = i % vseg;
+                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v16_off(d, c0 + 8 * sg));
+            }
         }
     } else {
         uint8_t *sKs = stage + Lay::K_BYTES + Lay::V_BYTES, *sVs = sKs + Lay::KS_BYTES;
@@ -103,18 +118,99 @@ __device__ __forceinline__ void issue_chunk(const AttnParams &p, uint8_t *stage,
         }
         for (int i = threadIdx.x; i < (nt + 1) / 2; i += blockDim.x)   // 2 tokens of scales per 16 B
             cp_async16(sKs + i * 16, gKs + (size_t)i * 16);
-        int vseg = (nt + 15) >> 4;   // 16 tokens per 16 bytes
-        for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
-            int d = i / vseg, sg = i % vseg;
-            cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v8_off(d, c0 + 16 * sg));
-        }
-        int sseg = (nt + 7) >> 3;    // 8 tokens of one scale row per 16 B
-        for (int i = threadIdx.x; i < 4 * sseg; i += blockDim.x) {
-            int bl = i / sseg, sg = i % sseg;
-            cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + kv_vs_off(bl, c0 + 8 * sg));
+        if (nt == ATT_CHUNK) {   // whole chunk: 4 code segments per head-dim row, 8 per scale row
+            for (int i = threadIdx.x; i < HD * 4; i += blockDim.x) {
+                const int d = i >> 2, sg = i & 3;
+                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v8_off(d, c0 + 16 * sg));
+            }
+            if (threadIdx.x < 32) {
+                const int bl = threadIdx.x >> 3, sg = threadIdx.x & 7;
+                cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + kv_vs_off(bl, c0 + 8 * sg));
+            }
+        } else {
+            const int vseg = (nt + 15) >> 4;   // 16 tokens per 16 bytes
+            for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
+                const int d = i / vseg, sg = i % vseg;
+                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v8_off(d, c0 + 16 * sg));
+            }
+            const int sseg = (nt + 7) >> 3;    // 8 tokens of one scale row per 16 B
+            for (int i = threadIdx.x; i < 4 * sseg; i += blockDim.x) {
+                const int bl = i / sseg, sg = i % sseg;
+                cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + kv_vs_off(bl, c0 + 8 * sg));
+            }
         }
     }
 }
+
+// Whole-chunk staging with the index arithmetic hoisted out of the chunk loop.
+// A chunk starts at a multiple of 64 tokens, so every swizzle term depends on
+// the thread alone and the arena offset of each 16-byte segment is
+// c0 * (bytes per token) + a per-thread constant + an unrolled-copy constant.
+// Thread tid copies segments i = tid + 128 j of each tensor (see issue_chunk
+// for the segment order); ks / vs: threads 0-31 copy one scale segment each.
+template <int KVT> struct ChunkPlan {
+    const uint8_t *gK, *gV, *gS, *gT;   // plane bases: K, V codes, K scales, V scales
+    uint32_t k_src, k_dst, v_src, v_dst, s_src, s_dst, t_src, t_dst;
+
+    __device__ ChunkPlan(const AttnParams &p, int b, int g) {
+        using Lay = AttnLayout<KVT>;
+        const uint32_t tid = threadIdx.x;
+        const size_t pi = plane_index(p.kv, b, p.layer, g);
+        const int Lp = p.kv.Lp;
+        if (KVT == 0) {
+            gK = p.kv.k + pi * Lp * (HD * 2);
+            gV = p.kv.v + pi * Lp * (HD * 2);
+            gS = gT = nullptr;
+            const uint32_t t = tid >> 4, sg = tid & 15;          // K: 16 segments per token
+            k_src = t * 256 + ((sg ^ (t & 7)) << 4);
+            k_dst = t * Lay::K_STRIDE + sg * 16;
+            const uint32_t d = tid >> 3, vs = tid & 7;           // V^T: 8 segments per dim row
+            v_src = ((vs >> 2) * HD + d) * 64 + (((vs & 3) ^ ((tid >> 4) & 3)) << 4);
+            v_dst = Lay::K_BYTES + d * Lay::V_STRIDE + vs * 16;
+            s_src = s_dst = t_src = t_dst = 0;
+        } else {
+            gK = p.kv.k + pi * Lp * HD;
+            gV = p.kv.v + pi * Lp * HD;
+            gS = p.kv.ks + pi * Lp * 8;
+            gT = p.kv.vs + pi * Lp * 8;
+            const uint32_t t = tid >> 3, sg = tid & 7;           // K: 8 segments per token
+            k_src = t * 128 + ((sg ^ (t & 7)) << 4);
+            k_dst = t * Lay::K_STRIDE + sg * 16;
+            const uint32_t d = tid >> 2, vs = tid & 3;           // V^T: 4 segments per dim row
+            v_src = ((vs >> 1) * HD + d) * 32 + (((vs & 1) ^ ((tid >> 4) & 1)) << 4);
+            v_dst = Lay::K_BYTES + d * Lay::V_STRIDE + vs * 16;
+            s_src = (tid & 31) * 16;                              // K scales: 512 contiguous bytes
+            s_dst = Lay::K_BYTES + Lay::V_BYTES + (tid & 31) * 16;
+            const uint32_t bl = (tid >> 3) & 3, ss = tid & 7;     // V scales: 4 rows of 8 segments
+            t_src = (((ss >> 2) * 4 + bl) * KU + 8 * (ss & 3)) * 2;
+            t_dst = Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES + bl * ATT_CHUNK * 2 + ss * 16;
+        }
+    }
+
+    // tokens [c0, c0 + 64) of the plane into the stage at shared address st
+    __device__ __forceinline__ void issue(uint32_t st, int c0) const {
+        using Lay = AttnLayout<KVT>;
+        if (KVT == 0) {
+            const uint8_t *k = gK + (size_t)c0 * 256 + k_src, *v = gV + (size_t)c0 * 256 + v_src;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {   // tokens t + 8 j; dims d + 16 j
+                cp_async16_s(st + k_dst + j * 8 * Lay::K_STRIDE, k + j * 8 * 256);
+                cp_async16_s(st + v_dst + j * 16 * Lay::V_STRIDE, v + j * 16 * 64);
+            }
+        } else {
+            const uint8_t *k = gK + (size_t)c0 * 128 + k_src, *v = gV + (size_t)c0 * 128 + v_src;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {   // tokens t + 16 j; dims d + 32 j
+                cp_async16_s(st + k_dst + j * 16 * Lay::K_STRIDE, k + j * 16 * 128);
+                cp_async16_s(st + v_dst + j * 32 * Lay::V_STRIDE, v + j * 32 * 32);
+            }
+            if (threadIdx.x < 32) {
+                cp_async16_s(st + s_dst, gS + (size_t)c0 * 8 + s_src);
+                cp_async16_s(st + t_dst, gT + (size_t)c0 * 8 + t_src);
+            }
+        }
+    }
+};
 
 __device__ __forceinline__ void codes4_to_h2(uint32_t w, uint32_t &lo, uint32_t &hi) {
     // bytes b0..b3 (int8) -> (b0, b1), (b2, b3) as exact fp16 integers:
@@ -165,11 +261,23 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     const int nchunks = c_hi - c_lo;
     const bool has_new = p.append && !empty && T1 == ntok;
 
-    uint8_t *stage0 = smem, *stage1 = smem + Lay::STAGE;
-    if (!empty) issue_chunk<KVT>(p, stage0, b, g, T0, H);
-    cp_async_commit();
-    if (nchunks > 1) issue_chunk<KVT>(p, stage1, b, g, T0 + ATT_CHUNK, H);
-    cp_async_commit();
+    const int NS = p.stages;   // 2..ATT_MAX_STAGES (checked at launch)
+    const ChunkPlan<KVT> plan(p, b, g);
+    const uint32_t smem_s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    // whole chunks through the plan, the history's ragged end through issue_chunk
+    auto load_chunk = [&](int slot, int c0) {
+        if (H - c0 >= ATT_CHUNK) plan.issue(smem_s + (uint32_t)(slot * Lay::STAGE), c0);
+        else issue_chunk<KVT>(p, smem + slot * Lay::STAGE, b, g, c0, H);
+    };
+    // ring of NS slots: chunks 0..NS-2 now (the history is no predecessor's
+    // output: loaded before the wait); chunk ci + NS - 1 goes out at the top of
+    // iteration ci, into the slot chunk ci - 1 has just freed, so that one
+    // block barrier per chunk covers both the landing and the reuse
+#pragma unroll 1
+    for (int s = 0; s < NS - 1; s++) {
+        if (s < nchunks) load_chunk(s, T0 + s * ATT_CHUNK);
+        cp_async_commit();
+    }
 
     pdl_launch_dependents();
     pdl_wait();
@@ -189,7 +297,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             qa[st][3] = f.w;
         }
     } else {
-        const float qscale = 0.08838834764831845f;   // 1/sqrt(128)
+        const float qscale = 0.12751743082459868f;   // log2(e)/sqrt(128): scores in log2 units
         const int hq = GROUP * g + gid;
         const float *qrow = p.qkv + (size_t)b * p.qkv_ld + (size_t)hq * HD;
         const float2 *cs = p.rope + (size_t)pos * (HD / 2);
@@ -272,11 +380,23 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         for (int i = 0; i < 4; i++) oacc[dn][i] = 0.0f;
     const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 
+    int slot = 0, rslot = NS - 1;
     for (int ci = 0; ci < nchunks; ci++) {
-        uint8_t *st = (ci & 1) ? stage1 : stage0;
+        uint8_t *st = smem + slot * Lay::STAGE;
         const int c0 = T0 + ci * ATT_CHUNK;
-        cp_async_wait<1>();
-        __syncthreads();
+        switch (NS) {   // NS - 1 + ci groups committed; chunk ci's is group ci
+            case 2: cp_async_wait<0>(); break;
+            case 3: cp_async_wait<1>(); break;
+            case 4: cp_async_wait<2>(); break;
+            case 5: cp_async_wait<3>(); break;
+            case 6: cp_async_wait<4>(); break;
+            case 7: cp_async_wait<5>(); break;
+            default: cp_async_wait<6>(); break;
+        }
+        __syncthreads();   // chunk ci has landed; every warp is done with chunk ci - 1
+        if (ci + NS - 1 < nchunks) load_chunk(rslot, T0 + (ci + NS - 1) * ATT_CHUNK);
+        cp_async_commit();
+        rslot = rslot + 1 == NS ? 0 : rslot + 1;
         // fix-up (only the chunk at the end of the loaded history): zero V columns
         // past it and insert the new token; whole-history chunks skip both barriers
         const int zfrom = max(H, c0) - c0;
@@ -339,6 +459,13 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
                 } else {
                     const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES);
                     const int ta = 16 * warp + 4 * tig + 2 * nt;   // tokens of columns 2tig, 2tig+1
+                    // the four block scales of tokens ta and ta + 1
+                    const uint2 ksa = *reinterpret_cast<const uint2 *>(sKs + ta * 4);
+                    const uint2 ksb = *reinterpret_cast<const uint2 *>(sKs + (ta + 1) * 4);
+                    const float2 ka01 = __half22float2(u32_as_h2(ksa.x)), ka23 = __half22float2(u32_as_h2(ksa.y));
+                    const float2 kb01 = __half22float2(u32_as_h2(ksb.x)), kb23 = __half22float2(u32_as_h2(ksb.y));
+                    const float kas[4] = {ka01.x, ka01.y, ka23.x, ka23.y};
+                    const float kbs[4] = {kb01.x, kb01.y, kb23.x, kb23.y};
 #pragma unroll
                     for (int bl = 0; bl < 4; bl++) {
                         float tmp[4];
@@ -351,8 +478,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
                             if (hs) mma16816(tmp, qa[st8], b0, b1, tmp);
                             else mma16816(tmp, qa[st8], b0, b1, zero4);
                         }
-                        float ka = __half2float(__ushort_as_half(sKs[ta * 4 + bl]));
-                        float kb = __half2float(__ushort_as_half(sKs[(ta + 1) * 4 + bl]));
+                        const float ka = kas[bl], kb = kbs[bl];
                         S[nt][0] += ka * tmp[0];
                         S[nt][1] += kb * tmp[1];
                         S[nt][2] += ka * tmp[2];
@@ -366,27 +492,32 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             sc[1] = S[0][1] + S[0][3];
             sc[2] = S[1][0] + S[1][2];
             sc[3] = S[1][1] + S[1][3];
+            if (gid >= GROUP) sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;   // zero A rows: no head
+            if (tb + 16 > T1)   // the range's last tile may end early
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                int t = tb + 4 * tig + e;
-                if (t >= T1 || gid >= GROUP) sc[e] = -INFINITY;
-            }
+                for (int e = 0; e < 4; e++)
+                    if (tb + 4 * tig + e >= T1) sc[e] = -INFINITY;
             float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
             mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 1));
             mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 2));
+            // scores are in log2 units (q carries log2(e)/sqrt(128)); the output
+            // is rescaled only when some head's running max grew (alpha = 1
+            // exactly otherwise), which after the first tiles is rare
             const float m_new = fmaxf(m_run, mt);
-            float alpha = 1.0f, pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const bool grow = m_new > m_run;
+            const float alpha = grow ? exp2f(m_run - m_new) : 1.0f;   // m_run = -inf -> 0
+            float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (m_new != -INFINITY) {
-                alpha = expf(m_run - m_new);   // m_run = -inf -> 0
 #pragma unroll
-                for (int e = 0; e < 4; e++) pr[e] = expf(sc[e] - m_new);
+                for (int e = 0; e < 4; e++) pr[e] = exp2f(sc[e] - m_new);
             }
             m_run = m_new;
             l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+            if (__any_sync(AFULL, grow))
 #pragma unroll
-            for (int dn = 0; dn < 16; dn++)
+                for (int dn = 0; dn < 16; dn++)
 #pragma unroll
-                for (int i = 0; i < 4; i++) oacc[dn][i] *= alpha;
+                    for (int i = 0; i < 4; i++) oacc[dn][i] *= alpha;
             // ---- output += P V
             if (KVT == 0) {
                 uint32_t pa[4];
@@ -407,9 +538,9 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
                 const int tl = 16 * warp + 4 * tig;
 #pragma unroll
                 for (int bl = 0; bl < 4; bl++) {
-                    float q4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) q4[e] = pr[e] * __half2float(__ushort_as_half(sVs[bl * ATT_CHUNK + tl + e]));
+                    const uint2 vsc = *reinterpret_cast<const uint2 *>(sVs + bl * ATT_CHUNK + tl);   // tokens tl..tl+3
+                    const float2 v01 = __half22float2(u32_as_h2(vsc.x)), v23 = __half22float2(u32_as_h2(vsc.y));
+                    const float q4[4] = {pr[0] * v01.x, pr[1] * v01.y, pr[2] * v23.x, pr[3] * v23.y};
                     uint32_t pa[4];
                     __half2 h01 = __floats2half2_rn(q4[0], q4[1]), h23 = __floats2half2_rn(q4[2], q4[3]);
                     float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
@@ -428,9 +559,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
                 }
             }
         }
-        __syncthreads();   // everyone is done with this stage
-        if (ci + 2 < nchunks) issue_chunk<KVT>(p, st, b, g, T0 + (ci + 2) * ATT_CHUNK, H);
-        cp_async_commit();
+        slot = slot + 1 == NS ? 0 : slot + 1;
     }
     cp_async_wait<0>();
     tl_max(p.tl, 6);
@@ -459,7 +588,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int w = 0; w < 4; w++) {
             float mw = wm[w * 4 + head];
-            float f = mw == -INFINITY ? 0.0f : expf(mw - M);
+            float f = mw == -INFINITY ? 0.0f : exp2f(mw - M);
             L += f * wl[w * 4 + head];
             for (int e = 0; e < 4; e++) O[e] += f * wo[(w * 4 + head) * HD + d0 + e];
         }
@@ -492,7 +621,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int r = 0; r < 16; r++) {
-            const float f = mr[r] == -INFINITY ? 0.0f : expf(mr[r] - M);
+            const float f = mr[r] == -INFINITY ? 0.0f : exp2f(mr[r] - M);
             L += f * lr[r];
             O[0] += f * orr[r].x; O[1] += f * orr[r].y; O[2] += f * orr[r].z; O[3] += f * orr[r].w;
         }
@@ -533,7 +662,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
 }
 
 cudaError_t attention_setup(int kv_dtype) {
-    int smem = (int)attention_smem_bytes(kv_dtype);
+    int smem = (int)attention_smem_bytes(kv_dtype, att_max_stages(kv_dtype));
     cudaError_t e;
     if (kv_dtype == 0) {
         e = cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -547,10 +676,13 @@ cudaError_t attention_setup(int kv_dtype) {
     return e;
 }
 
-cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnParams &p0, bool pdl, cudaStream_t stream) {
+    AttnParams p = p0;
     if (p.cs < 1 || p.cs > 16) return cudaErrorInvalidValue;
+    if (p.stages == 0) p.stages = attention_default_stages(p.kv.kv_dtype);
+    if (p.stages < 2 || p.stages > att_max_stages(p.kv.kv_dtype)) return cudaErrorInvalidValue;
     dim3 grid(p.cs, p.kv.n_kv, p.B), block(128);
-    size_t smem = attention_smem_bytes(p.kv.kv_dtype);
+    size_t smem = attention_smem_bytes(p.kv.kv_dtype, p.stages);
     if (p.kv.kv_dtype == 0) return launch_k(attention_kernel<0>, grid, block, smem, pdl, p.cs, stream, p);
     return launch_k(attention_kernel<1>, grid, block, smem, pdl, p.cs, stream, p);
 }

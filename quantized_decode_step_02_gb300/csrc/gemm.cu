@@ -151,7 +151,7 @@ __device__ __forceinline__ void stage_fma(const uint8_t *st, int warp, int lane,
 // y[nt][rho]: output row rt*16 + g + 8*rho, batch row b = 4nt + tig.
 template <int NT, int EPI>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT][2], int grp,
-                                              const float (&xin)[NT][2]) {
+                                              const float (&xin)[NT][2], const float *sgain) {
     constexpr int NB = 4 * NT;   // batch rows this instance covers
     // SWIGLU: a[col][64 rows]; RESID with a next operand: x[col][128 rows]
     __shared__ float s_v[EPI == EPI_LMHEAD ? GT * NB : NB * 128];
@@ -175,16 +175,22 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT
         if (!qhead) return;
         // query head grp: rotate at its position, scale, split hi/lo, fragment order
         __syncthreads();
-        const float qscale = 0.08838834764831845f;   // 1/sqrt(128)
+        const float qscale = 0.12751743082459868f;   // log2(e)/sqrt(128): the attention works in log2 units
         for (int task = threadIdx.x; task < p.B * 32; task += blockDim.x) {
             const int b = task >> 5, st = (task >> 2) & 7, tq = task & 3;
-            const float2 *cs = p.q_rope + (size_t)p.q_pos[b] * 64;
+            // cos/sin of dims 16 st + 4 tq + {0..3} (mod 64); the row was
+            // prefetched into L1 at the kernel's start
+            const float4 *cs4 = reinterpret_cast<const float4 *>(p.q_rope + (size_t)p.q_pos[b] * 64 +
+                                                                 ((16 * st + 4 * tq) & 63));
+            const float4 r4[2] = {cs4[0], cs4[1]};
+            const float2 cpair[4] = {make_float2(r4[0].x, r4[0].y), make_float2(r4[0].z, r4[0].w),
+                                     make_float2(r4[1].x, r4[1].y), make_float2(r4[1].z, r4[1].w)};
             float v[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 const int d = 16 * st + 4 * tq + e;
                 const float x = s_v[b * 128 + d];
-                const float2 c = cs[d & 63];
+                const float2 c = cpair[e];
                 v[e] = (d < 64 ? x * c.x - s_v[b * 128 + d + 64] * c.y : x * c.x + s_v[b * 128 + d - 64] * c.y) * qscale;
             }
             const __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
@@ -226,7 +232,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT
                 for (int i = 0; i < 8; i++) {
                     const float xv = s_v[col * 128 + ch * 8 + i];
                     sq = fmaf(xv, xv, sq);
-                    yy[i] = xv * p.next_gain[r0 + i];
+                    yy[i] = xv * sgain[ch * 8 + i];
                     part += yy[i];
                 }
                 store_act8(p.out16, p.out16lo, act_chunk(r0 >> 8, col, (r0 & 255) >> 3, p.out_Bp), yy);
@@ -329,21 +335,37 @@ __device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, uint3
 
 // ------------------------------------------------------------- kernel ---
 // NT n-tiles of 4 batch rows each (IMPL 2), or NT batch rows (IMPL 1, NT <= 4).
-// Residency: three CTAs per SM for the one-tile mma kernel (B <= 4; <= 80
-// registers), two up to B = 8, one above.
-template <int NT, int IMPL> struct GemmOcc { static constexpr int v = (IMPL >= 2 && NT == 1) ? 3 : (NT <= 2 ? 2 : 1); };
+// Residency: three CTAs per SM for the mma kernels up to two n-tiles (B <= 8;
+// <= 80 registers), one above.
+template <int NT, int IMPL> struct GemmOcc { static constexpr int v = (IMPL >= 2 && NT <= 2) ? 3 : (NT <= 2 ? 2 : 1); };
+// MMA accumulator chains per n-tile (stage_mma): all four where registers
+// allow, one at NT = 2 (three CTAs per SM in 80 registers), two at NT = 8.
+template <int NT> struct GemmChains { static constexpr int v = NT == 2 ? 1 : (NT == 8 ? 2 : 4); };
+// Batch rows a stage holds: 4 per n-tile (IMPL 2), the four matvec columns
+// (IMPL 1), or batch row 0 plus the zero row 1 that the idle B columns read
+// (IMPL 3).
+template <int NT, int IMPL> struct GemmBR { static constexpr int v = IMPL == 2 ? 4 * NT : (IMPL == 3 ? 2 : 4); };
+// Bytes of one peer's partial tiles in rank 0's reduction area: every lane's
+// y (IMPL 1, 2), or only the tig = 0 lanes, which hold the rows' sums (IMPL 3).
+template <int NT, int IMPL> struct GemmRed {
+    static constexpr uint32_t v = IMPL == 3 ? GT * 2 * 8 * 4 : GT * (IMPL == 2 ? NT : 1) * 2 * 32 * 4;
+};
 
 template <int NT, int EPI, int IMPL>
 __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const GemmParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_bad;
     __shared__ uint64_t red_bar;   // rank 0 of a cluster: the peers' partial tiles have landed
+    __shared__ uint32_t s_done[8];  // pipe 1: warps done with each ring slot (running count)
+    __shared__ int s_issued;        // stages whose copies have been issued
+    __shared__ float s_gain[128];   // RESID with next_gain: the group's gain rows
+    __shared__ float s_rms[MAX_B];  // RMSNorm scale per batch row (consumers of a folded norm)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
     const int cs = p.cs, rank = blockIdx.x % cs, grp = blockIdx.x / cs;
     const int rt = grp * GT + warp;
     const int s0 = rank * p.nsb / cs, s1 = (rank + 1) * p.nsb / cs, n = s1 - s0;
     const int B = p.B, D = p.stages;
-    constexpr int BR = IMPL == 2 ? 4 * NT : 4;   // batch rows held per stage (IMPL 3: B = 1, rows 1-3 zero)
+    constexpr int BR = GemmBR<NT, IMPL>::v;   // batch rows held per stage
     const StageLayout lay(BR);
     const uint32_t abytes = (uint32_t)B * 512u, sbytes = (uint32_t)B * 32u;
     const uint32_t tx = GROUP_BYTES + 2 * abytes + sbytes;
@@ -363,14 +385,16 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         bulk_g2s(st + (lay.sums - GROUP_BYTES), p.sx + sb * p.Bp * 16, sbytes, &full[i % D]);
     };
     tl_min(p.tl, 0);
+    if (threadIdx.x < 8) s_done[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         s_bad = 0;
         for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
         if (cs > 1 && rank == 0) mbar_init(&red_bar, cs - 1);
         mbar_fence_init();
     }
-    // rank 0 receives the peers' partial tiles after the barriers (see the end)
-    const uint32_t red_off = (uint32_t)D * sbyt + 64u;
+    // rank 0 receives the peers' partial tiles after the barriers (see the end):
+    // behind the stage ring, or in it (red_alias) once rank 0's K loop is done
+    const uint32_t red_off = p.red_off;
     // zero the batch rows the copies never write (rows B..BR-1 and the lo lanes'
     // min-term slots) in every stage buffer
     for (int i = threadIdx.x; i < D * BR * 8; i += blockDim.x) {
@@ -386,7 +410,9 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         if (w < 2) *reinterpret_cast<uint4 *>(base + lay.zero + r * 32 + w * 16) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    if (cs > 1) cluster_arrive_release();   // publishes red_bar's initialisation (waited on at the end)
+    // publishes red_bar's initialisation (waited on after the K loop); with an
+    // aliased reduction area rank 0 arrives only when its stages are free
+    if (cs > 1 && !(p.red_alias && rank == 0)) cluster_arrive_release();
     // this lane's fixed offsets into a stage: virtual column g of n-tile 0 is the
     // hi (g even) or lo (g odd) plane of batch row g/2
     const int g = lane >> 2;
@@ -399,8 +425,16 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         sum_off = lay.sums + (uint32_t)tig * 8u;
     }
     const int pre = min(D, n);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         for (int i = 0; i < pre; i++) issue_w(i);
+        s_issued = pre;
+    }
+    // epilogue inputs that no earlier kernel of the step writes (weights, the
+    // rotary table, the step's positions), fetched before the dependency wait
+    if (EPI == EPI_RESID && p.next_gain && threadIdx.x < 128)
+        s_gain[threadIdx.x] = grp * 128 + (int)threadIdx.x < p.N ? p.next_gain[grp * 128 + threadIdx.x] : 0.0f;
+    if (EPI == EPI_STORE && p.q_frag && grp < p.q_heads && (int)threadIdx.x < B * 4)   // 4 lines of 128 B per row
+        prefetch_l1(p.q_rope + (size_t)p.q_pos[threadIdx.x >> 2] * 64 + (threadIdx.x & 3) * 16);
     // warm L2 with this CTA's slice of the next kernel's read-only bytes, so the
     // HBM keeps streaming while this grid drains and the next one ramps up
     if (p.pf_ptr && p.pf_bytes) {
@@ -420,23 +454,30 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     // latency hides behind the K loop: this lane's partial sums of x^2 per
     // batch row (RMSNorm scale) and the residual rows it will update
     constexpr int NY = IMPL == 2 ? NT : 1;
-    constexpr bool EARLY = NY <= 2;   // registers allow the early fetch and the batched reduction
-    float rms_pre[4 * NY];
+    constexpr bool EARLY = NY == 1 || (NY == 2 && GemmOcc<NT, IMPL>::v < 3);   // registers hold the residual
+    // RMSNorm scale of every batch row, one warp per row, into shared memory
+    if (p.rms_part)
+        for (int b = warp; b < B && b < 4 * NY; b += 8) {
+            float ss = 0.0f;
+            for (int i = lane; i < p.rms_nparts; i += 32) ss += p.rms_part[i * MAX_B + b];
 #pragma unroll
-    for (int b = 0; b < 4 * NY; b++) {
-        rms_pre[b] = 0.0f;
-        if (EARLY && p.rms_part && b < B)
-            for (int i = lane; i < p.rms_nparts; i += 32) rms_pre[b] += p.rms_part[i * MAX_B + b];
-    }
-    float xin[NY][2];
-#pragma unroll
-    for (int nt = 0; nt < NY; nt++)
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            const int row = rt * 16 + (lane >> 2) + 8 * r, b = 4 * nt + tig;
-            xin[nt][r] = (EPI == EPI_RESID && rank == 0 && rt < p.nrt && b < B && row < p.N)
-                             ? p.out[(size_t)b * p.ldo + row] : 0.0f;
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+            if (lane == 0) s_rms[b] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
         }
+    float xin[NY][2];
+    auto fetch_xin = [&]() {
+#pragma unroll
+        for (int nt = 0; nt < NY; nt++)
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int row = rt * 16 + (lane >> 2) + 8 * r, b = 4 * nt + tig;
+                xin[nt][r] = (EPI == EPI_RESID && rank == 0 && rt < p.nrt && b < B && row < p.N)
+                                 ? p.out[(size_t)b * p.ldo + row] : 0.0f;
+            }
+    };
+    if (EARLY) fetch_xin();
+    else if (EPI == EPI_RESID && rank == 0 && (int)threadIdx.x < 4 * B)   // the group's rows: 4 lines per batch row
+        prefetch_l1(p.out + (size_t)(threadIdx.x >> 2) * p.ldo + grp * 128 + (threadIdx.x & 3) * 32);
 
     constexpr int NA = IMPL == 2 ? NT : 1;   // mma accumulator tiles
     constexpr int NB = IMPL == 1 ? NT : 1;   // matvec columns
@@ -453,6 +494,31 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     // gives each warp two dependency chains to interleave, and halves the
     // block-wide syncs that release stages for refilling
     bool ok = true;
+    if (p.pipe == 1) {
+        // each warp takes the stages in order; the last warp done with a stage
+        // refills its slot, so no block-wide barrier stalls the ring
+        for (int i = 0; i < n; i++) {
+            if (ok && !wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, p.status)) { ok = false; s_bad = 1; }
+            if (i == 0) tl_max(p.tl, 5);
+            if (ok && rt < p.nrt) {
+                if (IMPL == 2) stage_mma<NA, GemmChains<NT>::v>(stage(i), warp, lane, act_off, sum_off, swz, acc);
+                else if (IMPL == 3) stage_mv(stage(i), warp, lane, act_off, sum_off, ymv);
+                else stage_fma<NB>(stage(i), warp, lane, lay, accr);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();   // this warp's reads of the slot precede its refill
+                const uint32_t prev = atomicAdd(&s_done[i % D], 1u);
+                if ((prev & 7u) == 7u && i + D < n && !*((volatile int *)&s_bad)) {
+                    __threadfence_block();
+                    issue_w(i + D);
+                    issue_act(i + D);
+                    atomicMax(&s_issued, i + D + 1);
+                }
+            }
+        }
+        __syncthreads();
+    } else
     for (int i = 0; i < n; i += 2) {
         const bool two = i + 1 < n;
         if (ok && !wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, p.status)) { ok = false; s_bad = 1; }
@@ -463,8 +529,8 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         }
         if (ok && rt < p.nrt) {
             if (IMPL == 2) {
-                stage_mma<NA>(stage(i), warp, lane, act_off, sum_off, swz, acc);
-                if (two) stage_mma<NA>(stage(i + 1), warp, lane, act_off, sum_off, swz, acc);
+                stage_mma<NA, GemmChains<NT>::v>(stage(i), warp, lane, act_off, sum_off, swz, acc);
+                if (two) stage_mma<NA, GemmChains<NT>::v>(stage(i + 1), warp, lane, act_off, sum_off, swz, acc);
             } else if (IMPL == 3) {
                 stage_mv(stage(i), warp, lane, act_off, sum_off, ymv);
                 if (two) stage_mv(stage(i + 1), warp, lane, act_off, sum_off, ymv);
@@ -475,15 +541,15 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         }
         __syncthreads();
         if (threadIdx.x == 0 && !s_bad) {
-            if (i + D < n) { issue_w(i + D); issue_act(i + D); }
-            if (two && i + 1 + D < n) { issue_w(i + 1 + D); issue_act(i + 1 + D); }
+            if (i + D < n) { issue_w(i + D); issue_act(i + D); s_issued = i + D + 1; }
+            if (two && i + 1 + D < n) { issue_w(i + 1 + D); issue_act(i + 1 + D); s_issued = i + D + 2; }
         }
     }
     tl_max(p.tl, 6);
     const bool bad = s_bad != 0;
-    if (bad) {   // drain what may still be in flight (bounded); the result is abandoned
+    if (bad) {   // drain the last D issued stages, which may still be in flight (bounded); the result is abandoned
         if (threadIdx.x == 0)
-            for (int i = max(0, n - D); i < n; i++) wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, nullptr);
+            for (int i = max(0, s_issued - D); i < s_issued; i++) wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, nullptr);
         __syncthreads();
         if (cs == 1) return;   // cluster members still meet the two cluster barriers below
     }
@@ -517,11 +583,18 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
             if (c == tig) { y[0][0] = accr[c][0]; y[0][1] = accr[c][1]; }
     }
     if (cs > 1) {   // K split across the cluster: the peers push their partial tiles to rank 0
+        if (p.red_alias && rank == 0) cluster_arrive_release();   // every copy into the ring has landed
         cluster_wait_acquire();   // every CTA of the cluster has initialised its barriers
-        constexpr int SLOT = GT * NY * 2 * 32;   // floats of one peer's partial tile set
+        constexpr int SLOT = GemmRed<NT, IMPL>::v / 4;   // floats of one peer's partial tile set
         const uint32_t red_local = smem_u32(smem + red_off);
         if (rank != 0) {
             const uint32_t dst = map_to_rank(red_local, 0) + (uint32_t)((rank - 1) * SLOT) * 4u;
+            if (IMPL == 3) {
+                if (tig == 0)
+#pragma unroll
+                    for (int r = 0; r < 2; r++)
+                        st_cluster_f32(dst + (uint32_t)((warp * 2 + r) * 8 + (lane >> 2)) * 4u, y[0][r]);
+            } else
 #pragma unroll
             for (int nt = 0; nt < NY; nt++)
 #pragma unroll
@@ -546,6 +619,12 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
                 }
         }
         const float *red = reinterpret_cast<const float *>(smem + red_off);
+        if (IMPL == 3) {
+            if (tig == 0)
+                for (int rr = 1; rr < cs; rr++)
+#pragma unroll
+                    for (int r = 0; r < 2; r++) y[0][r] += red[(rr - 1) * SLOT + (warp * 2 + r) * 8 + (lane >> 2)];
+        } else
         for (int rr = 1; rr < cs; rr++)
 #pragma unroll
             for (int nt = 0; nt < NY; nt++)
@@ -558,22 +637,14 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     if (p.rms_part) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
 #pragma unroll
         for (int nt = 0; nt < NY; nt++) {
-            float rr[4];
-#pragma unroll
-            for (int c = 0; c < 4; c++) {   // every lane reduces the four rows of n-tile nt
-                float ss = rms_pre[4 * nt + c];
-                if (!EARLY && 4 * nt + c < B)
-                    for (int i = lane; i < p.rms_nparts; i += 32) ss += p.rms_part[i * MAX_B + 4 * nt + c];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-                rr[c] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
-            }
-            const float r_b = tig == 0 ? rr[0] : (tig == 1 ? rr[1] : (tig == 2 ? rr[2] : rr[3]));
+            const int b = 4 * nt + tig;   // computed before the K loop
+            const float r_b = b < B ? s_rms[b] : 1.0f;
             y[nt][0] *= r_b;
             y[nt][1] *= r_b;
         }
     }
-    gemm_epilogue<NY, EPI>(p, y, grp, xin);
+    if (!EARLY) fetch_xin();
+    gemm_epilogue<NY, EPI>(p, y, grp, xin, s_gain);
     if (p.tl) {
         __syncthreads();
         tl_end(p.tl);
@@ -583,24 +654,47 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
 // ------------------------------------------------------------ dispatch ---
 int gemm_grid(const GemmParams &p) { return n_groups(p.nrt) * p.cs; }
 
+// Dynamic shared memory a CTA may take at `occ` CTAs per SM: its share of the
+// SM's 228 KB (1 KB reserved per CTA) less the static arrays.
+static uint32_t occ_budget(int occ) { return occ >= 3 ? 72u * 1024u : (occ == 2 ? 110u * 1024u : 200u * 1024u); }
+
 static int stages_for(uint32_t stage_bytes, int occ, uint32_t reserved) {
-    uint32_t budget = occ >= 3 ? 70u * 1024u : (occ == 2 ? 110u * 1024u : 200u * 1024u);
+    uint32_t budget = occ_budget(occ);
     budget = budget > reserved + 2 * stage_bytes ? budget - reserved : 2 * stage_bytes;
     int d = (int)(budget / stage_bytes);
     return d < 2 ? 2 : (d > 6 ? 6 : d);
 }
 
-int gemm_ctas_per_sm(int B, int impl) { return impl == 2 && B <= 4 ? 3 : (B <= 8 ? 2 : 1); }
+// CTAs per SM of the kernel launch_epi picks for (B, impl): GemmOcc of its NT
+int gemm_ctas_per_sm(int B, int impl) {
+    if (impl == 1) return B <= 2 ? 2 : 1;
+    if (impl == 3) return 3;
+    return B <= 8 ? 3 : 1;
+}
 
 template <int NT, int EPI, int IMPL>
 static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
-    const StageLayout lay(IMPL == 2 ? 4 * NT : 4);
+    const StageLayout lay(GemmBR<NT, IMPL>::v);
     // rank 0 of a cluster holds the cs - 1 peers' partial tiles; a split whose
     // tiles do not fit next to two stages is halved
-    constexpr uint32_t NYB = GT * (IMPL == 2 ? NT : 1) * 2 * 32 * 4;
-    while (p.cs > 1 && (uint32_t)(p.cs - 1) * NYB + 2 * lay.bytes > 180u * 1024u) p.cs >>= 1;
-    const uint32_t red_bytes = p.cs > 1 ? (uint32_t)(p.cs - 1) * NYB : 0u;
-    p.stages = stages_for(lay.bytes, GemmOcc<NT, IMPL>::v, red_bytes);
+    constexpr uint32_t NYB = GemmRed<NT, IMPL>::v;
+    constexpr int OCC = GemmOcc<NT, IMPL>::v;
+    // the peers' tiles go behind the ring when ring and tiles fit the CTA's
+    // share of the SM together, else into the ring itself (rank 0 frees it
+    // first); a split whose tiles fit neither way is halved
+    const int d_plain = stages_for(lay.bytes, OCC, 0);
+    while (p.cs > 1 && (uint32_t)(p.cs - 1) * NYB > (uint32_t)d_plain * lay.bytes &&
+           (uint32_t)(p.cs - 1) * NYB + 2 * lay.bytes > 180u * 1024u)
+        p.cs >>= 1;
+    uint32_t red_bytes = p.cs > 1 ? (uint32_t)(p.cs - 1) * NYB : 0u;
+    p.red_alias = 0;
+    if (red_bytes && (size_t)d_plain * lay.bytes + 64 + red_bytes > occ_budget(OCC) &&
+        red_bytes <= (uint32_t)d_plain * lay.bytes) {
+        p.red_alias = 1;
+        red_bytes = 0;
+    }
+    p.stages = p.red_alias ? d_plain : stages_for(lay.bytes, OCC, red_bytes);
+    p.red_off = p.red_alias ? 0u : (uint32_t)p.stages * lay.bytes + 64u;
     const size_t smem = (size_t)p.stages * lay.bytes + 64 + red_bytes;
     static bool configured = false;   // raise the dynamic shared-memory limit once per instance
     if (!configured) {

@@ -82,7 +82,10 @@ __device__ __forceinline__ float dot2(uint32_t a, uint32_t x) {
 // four batch rows at full (hi + lo) precision and the lane holding C-fragment
 // columns (2tig, 2tig+1) owns both halves of batch row 4nt + tig.
 // acc[nt][0..3] = (row g, hi), (row g, lo), (row g+8, hi), (row g+8, lo).
-template <int NT>
+// CHAINS: independent MMA accumulator chains per n-tile: 4 (two word pairs,
+// and the x1 and x16 nibbles apart), 2 (word pairs) or 1; fewer chains free
+// registers for more CTAs per SM, where the n-tiles already interleave.
+template <int NT, int CHAINS = 4>
 __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane, uint32_t act_off,
                                           uint32_t sum_off, uint32_t swz, float (&acc)[NT][4]) {
     const int tig = lane & 3;
@@ -93,16 +96,24 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
     for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
     TileMeta tm;
     decode_meta(*reinterpret_cast<const uint2 *>(tile + TILE_CODE_BYTES + 8 * lane), tig, tm);
-    // four independent accumulator chains per n-tile (x1 and x16 nibbles, two
-    // word pairs), so a warp always has MMAs whose inputs are ready
-    float tq[2][NT][4], t16[2][NT][4], tmin[NT][4];
+    // independent accumulator chains per n-tile, so a warp always has MMAs
+    // whose inputs are ready
+    constexpr int PP = CHAINS >= 2 ? 2 : 1;
+    constexpr bool S16 = CHAINS >= 4;
+    float tq[PP][NT][4], t16[S16 ? PP : 1][NT][4], tmin[NT][4];
     const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int k = 0; k < 2; k++)
+    for (int k = 0; k < PP; k++)
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-            for (int i = 0; i < 4; i++) tq[k][nt][i] = t16[k][nt][i] = 0.0f;
+            for (int i = 0; i < 4; i++) tq[k][nt][i] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < (S16 ? PP : 1); k++)
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) t16[k][nt][i] = 0.0f;
 #pragma unroll
     for (int c = 0; c < 4; c++) {
         const int h = c >> 1;
@@ -116,11 +127,13 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
             decode_word(w0, cg, og, at[0], at16[0], at[2], at16[2]);
             decode_word(w1, c8, o8, at[1], at16[1], at[3], at16[3]);
             const uint32_t off = ((uint32_t)(h * 4 + pidx) ^ swz) * 16;
+            const int k = PP == 2 ? pp : 0;
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
                 const uint4 xv = *reinterpret_cast<const uint4 *>(act + nt * 2048 + off);
-                mma16816(tq[pp][nt], at, xv.x, xv.y, tq[pp][nt]);
-                mma16816(t16[pp][nt], at16, xv.z, xv.w, t16[pp][nt]);
+                mma16816(tq[k][nt], at, xv.x, xv.y, tq[k][nt]);
+                if (S16) mma16816(t16[k][nt], at16, xv.z, xv.w, t16[k][nt]);
+                else mma16816(tq[k][nt], at16, xv.z, xv.w, tq[k][nt]);
             }
         }
     }
@@ -132,7 +145,11 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
         mma16816(tmin[nt], am, s.x, s.y, zero4);
         float sq[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) sq[i] = (tq[0][nt][i] + t16[0][nt][i]) + (tq[1][nt][i] + t16[1][nt][i]);
+        for (int i = 0; i < 4; i++) {
+            sq[i] = tq[0][nt][i];
+            if (PP == 2) sq[i] += tq[PP - 1][nt][i];
+            if (S16) sq[i] += t16[0][nt][i] + t16[S16 ? PP - 1 : 0][nt][i];
+        }
         acc[nt][0] += tm.dg * sq[0] - tm.dming * tmin[nt][0];
         acc[nt][1] += tm.dg * sq[1] - tm.dming * tmin[nt][1];
         acc[nt][2] += tm.d8 * sq[2] - tm.dmin8 * tmin[nt][2];

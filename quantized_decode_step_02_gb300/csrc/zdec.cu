@@ -30,6 +30,14 @@ size_t tile_bytes(int rows16, int nsb) { return (size_t)n_groups(rows16) * nsb *
 
 // K split (cluster size) for a projection: grow it until the grid covers the
 // GPU, keeping at least two super-blocks per CTA.
+// Projection pipeline mode (GemmParams::pipe): 0 (stage pairs) unless
+// ZDEC_GEMM_PIPE=1; pairs measured faster, their two independent stages
+// giving each warp more instruction-level parallelism.
+int gemm_pipe_mode() {
+    static const int mode = getenv("ZDEC_GEMM_PIPE") ? (atoi(getenv("ZDEC_GEMM_PIPE")) ? 1 : 0) : 0;
+    return mode;
+}
+
 int pick_cs(int groups, int nsb, int target_ctas, int max_cs = 8) {
     int cs = 1;
     while (cs < max_cs && groups * cs * 2 <= target_ctas && nsb / (cs * 2) >= 2) cs *= 2;
@@ -562,10 +570,25 @@ extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
 // --------------------------------------------------------------- step ---
 // CTAs per (sequence, kv head) for the attention cluster: a power of two that
 // gives about two CTAs per SM, at most 16.
+// Attention split (cluster size): the largest power of two up to 16 keeping
+// the grid within ZDEC_ATT_CTAS (default 2) CTAs per SM.
 static int attn_cluster(const zdec_ctx *ctx, int B) {
-    int per = B * ctx->d.n_kv_heads, cs = 1;   // largest power of two keeping one wave of 2 CTAs/SM
-    while (cs < 16 && per * cs * 2 <= 2 * ctx->num_sms) cs *= 2;
+    static const int per_sm = getenv("ZDEC_ATT_CTAS") ? std::max(1, atoi(getenv("ZDEC_ATT_CTAS"))) : 2;
+    int per = B * ctx->d.n_kv_heads, cs = 1;
+    while (cs < 16 && per * cs * 2 <= per_sm * ctx->num_sms) cs *= 2;
     return cs;
+}
+
+// Attention chunks in flight per CTA (ZDEC_ATT_STAGES overrides).  A deeper
+// ring pays off only where the attention dominates the step; elsewhere its
+// shared memory keeps the neighbouring projections' CTAs (which prefetch
+// their weights) off the SMs.  Measured: batch of one, two stages; batch of
+// eight, two for an fp16 cache (a third would drop to one CTA per SM) and
+// four for Q8_0 (still two CTAs per SM).
+static int attn_stages(const zdec_ctx *ctx, int B) {
+    static const int env = getenv("ZDEC_ATT_STAGES") ? atoi(getenv("ZDEC_ATT_STAGES")) : 0;
+    if (env >= 2) return std::min(env, ctx->kv_dtype ? 8 : 5);
+    return (B > 4 && ctx->kv_dtype) ? 4 : 2;
 }
 
 static int pick_impl(const zdec_ctx *ctx, int B) {
@@ -632,6 +655,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     gp.Bp = Bp;
     gp.out_Bp = Bp;
     gp.status = ctx->status;
+    gp.pipe = gemm_pipe_mode();
     // Every projection takes its activation as fp16 hi + lo planes (~22 bits):
     // the new K/V rows are rounded and quantized, and over dozens of layers a
     // single fp16 operand would drift past the parity tolerance.
@@ -655,6 +679,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     ap.rope = ctx->rope;
     ap.append = 1;
     ap.cs = attn_cluster(ctx, B);
+    ap.stages = attn_stages(ctx, B);
     ap.o = ctx->o;
     ap.o16 = ctx->o16;
     ap.o16lo = ctx->o16lo;
@@ -1215,6 +1240,7 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     gp.out = y_dev;
     gp.ldo = N;
     gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm * gemm_ctas_per_sm(B, impl));
+    gp.pipe = gemm_pipe_mode();
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
 }
@@ -1283,6 +1309,7 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
     gp.out = y_dev;
     gp.ldo = N;
     gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm * gemm_ctas_per_sm(B, impl));
+    gp.pipe = gemm_pipe_mode();
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
 }

@@ -64,12 +64,16 @@ struct GemmParams {
     int *amax_idx;
     int cs;                // K split over a cluster of cs CTAs (1, 2, 4, 8, 16)
     int stages;            // pipeline depth (set by the launcher)
+    int pipe;              // 0: stages consumed in pairs, refilled after a block barrier;
+                           // 1: each stage refilled by the last warp done with it
+    uint32_t red_off;      // cluster rank 0's area for the peers' partial tiles (set by the launcher)
+    int red_alias;         // 1: that area is rank 0's stage ring, written once its K loop is done
     const uint8_t *pf_ptr; // read-only bytes the next kernel streams (L2 prefetch), or null
     size_t pf_bytes;       // multiple of 16, pf_ptr 16-byte aligned
     uint32_t *status;      // device status word (bounded-wait timeouts)
     unsigned long long *tl;   // launch timeline slot (zdec_internal.cuh) or null
     // STORE of a QKV projection: the query heads (groups < q_heads, one 128-row
-    // group each) also go out rotated (RoPE at q_pos[b]), scaled by 1/sqrt(128)
+    // group each) also go out rotated (RoPE at q_pos[b]), scaled by log2(e)/sqrt(128)
     // and split into fp16 hi + lo, in the attention's mma A-fragment order:
     // q_frag[((b * q_heads + head) * 8 + st) * 4 + tig] = (hi, lo) of dims
     // 16 st + 4 tig + {0,1} and (hi, lo) of dims + {2,3} (null: off)
@@ -126,11 +130,14 @@ struct AttnParams {
     uint32_t *status;      // device status word (bounded-wait timeouts)
     unsigned long long *tl;   // launch timeline slot (zdec_internal.cuh) or null
     const uint4 *q_frag;   // query fragments prepared by the QKV projection (GemmParams), or null
+    int stages;            // 64-token chunks in flight per CTA (2..8; 0: the KV type's default)
 };
 cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream);
 // Raise the attention kernel's dynamic shared-memory limit (once, before capture).
 cudaError_t attention_setup(int kv_dtype);
-size_t attention_smem_bytes(int kv_dtype);
+// Dynamic shared memory of a launch with `stages` chunks in flight (0: default).
+size_t attention_smem_bytes(int kv_dtype, int stages = 0);
+int attention_default_stages(int kv_dtype);
 // Bulk append of fp16 K/V [n_layers][n][n_kv][128] (device) at tokens t0.. of slot.
 cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const uint16_t *k16,
                              const uint16_t *v16, cudaStream_t stream);
