@@ -672,8 +672,10 @@ int gemm_ctas_per_sm(int B, int impl) {
     return B <= 8 ? 3 : 1;
 }
 
-template <int NT, int EPI, int IMPL>
-static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
+// Shared-memory plan of a launch: ring depth, the reduction area and its
+// place; may halve p.cs.  Returns the dynamic shared-memory bytes.
+template <int NT, int IMPL>
+static size_t plan_smem(GemmParams &p) {
     const StageLayout lay(GemmBR<NT, IMPL>::v);
     // rank 0 of a cluster holds the cs - 1 peers' partial tiles; a split whose
     // tiles do not fit next to two stages is halved
@@ -695,17 +697,85 @@ static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
     }
     p.stages = p.red_alias ? d_plain : stages_for(lay.bytes, OCC, red_bytes);
     p.red_off = p.red_alias ? 0u : (uint32_t)p.stages * lay.bytes + 64u;
-    const size_t smem = (size_t)p.stages * lay.bytes + 64 + red_bytes;
-    static bool configured = false;   // raise the dynamic shared-memory limit once per instance
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    return (size_t)p.stages * lay.bytes + 64 + red_bytes;
+}
+
+// Raise the dynamic shared-memory limit and allow clusters up to 16, once per instance.
+template <int NT, int EPI, int IMPL>
+static cudaError_t configure_one() {
+    static bool configured = false;
+    if (configured) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         210 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<NT, EPI, IMPL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) configured = true;
+    return e;
+}
+
+template <int NT, int EPI, int IMPL>
+static cudaError_t launch_one(GemmParams p, bool pdl, cudaStream_t s) {
+    const size_t smem = plan_smem<NT, IMPL>(p);
+    cudaError_t e = configure_one<NT, EPI, IMPL>();
+    if (e != cudaSuccess) return e;
     return launch_k(gemm_kernel<NT, EPI, IMPL>, dim3(gemm_grid(p)), dim3(256), smem, pdl, p.cs, s, p);
+}
+
+// CTAs of a split-cs launch that the GPU holds at once: the occupancy API's
+// count of co-resident clusters (clusters must fit inside one GPC) times cs;
+// 0 when the split cannot be launched as asked.
+template <int NT, int EPI, int IMPL>
+static int slots_one(int cs) {
+    GemmParams p{};
+    p.cs = cs;
+    const size_t smem = plan_smem<NT, IMPL>(p);
+    if (p.cs != cs || configure_one<NT, EPI, IMPL>() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16 * cs);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<NT, EPI, IMPL>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n * cs;
+}
+
+template <int EPI>
+static int slots_epi(int B, int impl, int cs) {
+    if (impl == 3) return B == 1 ? slots_one<1, EPI, 3>(cs) : 0;
+    if (impl == 1) {
+        switch (B) {
+            case 1: return slots_one<1, EPI, 1>(cs);
+            case 2: return slots_one<2, EPI, 1>(cs);
+            case 3: return slots_one<3, EPI, 1>(cs);
+            case 4: return slots_one<4, EPI, 1>(cs);
+            default: return 0;
+        }
+    }
+    if (B <= 4) return slots_one<1, EPI, 2>(cs);
+    if (B <= 8) return slots_one<2, EPI, 2>(cs);
+    if (B <= 16) return slots_one<4, EPI, 2>(cs);
+    return slots_one<8, EPI, 2>(cs);
+}
+
+int gemm_cluster_slots(int B, int impl, int epi, int cs) {
+    if (cs < 1 || cs > 16 || B < 1 || B > MAX_B) return 0;
+    switch (epi) {
+        case EPI_STORE: return slots_epi<EPI_STORE>(B, impl, cs);
+        case EPI_RESID: return slots_epi<EPI_RESID>(B, impl, cs);
+        case EPI_SWIGLU: return slots_epi<EPI_SWIGLU>(B, impl, cs);
+        case EPI_LMHEAD: return slots_epi<EPI_LMHEAD>(B, impl, cs);
+    }
+    return 0;
 }
 
 template <int EPI>
@@ -730,7 +800,7 @@ static cudaError_t launch_epi(const GemmParams &p, int impl, bool pdl, cudaStrea
 }
 
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream) {
-    if (p.cs != 1 && p.cs != 2 && p.cs != 4 && p.cs != 8 && p.cs != 16) return cudaErrorInvalidValue;
+    if (p.cs < 1 || p.cs > 16) return cudaErrorInvalidValue;
     if (p.B < 1 || p.B > MAX_B || p.B > p.Bp || !p.x16 || !p.x16lo || !p.sx) return cudaErrorInvalidValue;
     switch (epi) {
         case EPI_STORE: return launch_epi<EPI_STORE>(p, impl, pdl, stream);

@@ -28,8 +28,6 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Bytes of a matrix of rows16 row tiles in the grouped layout (padded to whole groups).
 size_t tile_bytes(int rows16, int nsb) { return (size_t)n_groups(rows16) * nsb * GROUP_BYTES; }
 
-// K split (cluster size) for a projection: grow it until the grid covers the
-// GPU, keeping at least two super-blocks per CTA.
 // Projection pipeline mode (GemmParams::pipe): 0 (stage pairs) unless
 // ZDEC_GEMM_PIPE=1; pairs measured faster, their two independent stages
 // giving each warp more instruction-level parallelism.
@@ -38,11 +36,29 @@ int gemm_pipe_mode() {
     return mode;
 }
 
-int pick_cs(int groups, int nsb, int target_ctas, int max_cs = 8) {
-    int cs = 1;
-    while (cs < max_cs && groups * cs * 2 <= target_ctas && nsb / (cs * 2) >= 2) cs *= 2;
-    return cs;
+// K split (cluster size, any 1..16, at least two super-blocks per CTA) for a
+// projection whose kernel holds `slots` CTAs on the GPU at once: the split of
+// least modelled time, waves x (super-blocks per CTA + 2 for a CTA's fixed
+// ramp, reduction and epilogue).  32 row groups of 56 super-blocks split 14
+// ways fill 448 of 456 slots in one wave of 4 super-blocks per CTA.
+template <typename Slots>
+int pick_cs(int groups, int nsb, Slots slots_of, int max_cs = 16) {
+    if (groups <= 0) return 1;
+    int best = 1;
+    double best_t = 1e30;
+    for (int cs = 1; cs <= std::min(max_cs, std::max(1, nsb / 2)); cs++) {
+        const int slots = slots_of(cs);
+        if (slots <= 0) continue;   // the split cannot be launched
+        const long waves = ((long)groups * cs + slots - 1) / slots;
+        const double t = (double)waves * ((double)nsb / cs + 2.0);
+        if (t < best_t - 1e-9) { best_t = t; best = cs; }
+    }
+    return best;
 }
+// Batch classes of the split tables: B = 1, <= 4, <= 8, <= 16, <= 32.
+int batch_class(int B) { return B == 1 ? 0 : (B <= 4 ? 1 : (B <= 8 ? 2 : (B <= 16 ? 3 : 4))); }
+constexpr int CLASS_B[5] = {1, 4, 8, 16, 32};
+enum { MAT_QKV, MAT_O, MAT_GU, MAT_DOWN, MAT_LM, N_MAT };
 
 struct LayerW {
     uint8_t *qkv, *o, *gu, *down;
@@ -84,7 +100,7 @@ struct zdec_ctx {
     __half *x16 = nullptr, *x16lo = nullptr, *sx = nullptr;
     __half *o16 = nullptr, *o16lo = nullptr, *osx = nullptr;
     __half *a16 = nullptr, *a16lo = nullptr, *asx = nullptr;
-    int cs_qkv[2] = {1, 1}, cs_o[2] = {1, 1}, cs_gu[2] = {1, 1}, cs_down[2] = {1, 1}, cs_lm[2] = {1, 1};  // B<=4, B>4
+    int cs_tab[4][5][N_MAT] = {};   // K split per (projection kernel, batch class, matrix); 0: unset
     int32_t *tok_dev = nullptr, *pos_dev = nullptr, *ids_dev = nullptr, *len_dev = nullptr;
     uint32_t *status = nullptr;
     uint4 *qfrag = nullptr;            // [max_B][n_q][32] query fragments (QKV epilogue -> attention)
@@ -467,20 +483,30 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
             return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate pinned staging"));
     }
     {
-        const int nsm = ctx->num_sms > 0 ? ctx->num_sms : 148;
-        // ZDEC_CS_TARGET: CTAs per SM x 10 that the split factors aim at (default:
-        // the kernel's residency); ZDEC_CS_MAX: largest split (8, or 16 with
-        // non-portable clusters)
-        const int tgt10 = getenv("ZDEC_CS_TARGET") ? atoi(getenv("ZDEC_CS_TARGET")) : 0;
-        const int csmax = getenv("ZDEC_CS_MAX") ? atoi(getenv("ZDEC_CS_MAX")) : 8;
-        for (int v = 0; v < 2; v++) {   // split factors filling the kernel's CTAs per SM
-            const int target = tgt10 > 0 ? nsm * tgt10 / 10 : nsm * gemm_ctas_per_sm(v ? 8 : 4, 2);
-            ctx->cs_qkv[v] = pick_cs(n_groups(ctx->qkv_ld / 16), ctx->nsb_h, target, csmax);
-            ctx->cs_o[v] = pick_cs(n_groups(H / 16), ctx->nsb_q, target, csmax);
-            ctx->cs_gu[v] = pick_cs(n_groups(F / 8), ctx->nsb_h, target, csmax);
-            ctx->cs_down[v] = pick_cs(n_groups(H / 16), ctx->nsb_f, target, csmax);
-            ctx->cs_lm[v] = pick_cs(n_groups(ctx->nrt_vocab), ctx->nsb_h, target, csmax);
-        }
+        // K splits of every projection for every kernel and batch class, from
+        // the occupancy API (ZDEC_CS_MAX: largest split, default 16, a
+        // non-portable cluster size)
+        const int csmax = getenv("ZDEC_CS_MAX") ? std::max(1, std::min(16, atoi(getenv("ZDEC_CS_MAX")))) : 16;
+        const int groups[N_MAT] = {n_groups(ctx->qkv_ld / 16), n_groups(H / 16), n_groups(F / 8), n_groups(H / 16),
+                                   n_groups(ctx->nrt_vocab)};
+        const int nsb[N_MAT] = {ctx->nsb_h, ctx->nsb_q, ctx->nsb_h, ctx->nsb_f, ctx->nsb_h};
+        const int epi[N_MAT] = {EPI_STORE, EPI_RESID, EPI_SWIGLU, EPI_RESID, EPI_LMHEAD};
+        for (int impl = 1; impl <= 3; impl++)
+            for (int c = 0; c < 5; c++) {
+                const int Bc = CLASS_B[c];
+                if ((impl == 3 && Bc != 1) || (impl == 1 && Bc > 4)) continue;
+                for (int m = 0; m < N_MAT; m++)
+                    ctx->cs_tab[impl][c][m] = pick_cs(
+                        groups[m], nsb[m], [&](int cs) { return gemm_cluster_slots(Bc, impl, epi[m], cs); }, csmax);
+            }
+        cudaGetLastError();
+        if (getenv("ZDEC_PRINT_SPLITS"))   // impl, batch class: splits of qkv, o, gate/up, down, lm head
+            for (int impl = 1; impl <= 3; impl++)
+                for (int c = 0; c < 5; c++)
+                    if (ctx->cs_tab[impl][c][0])
+                        fprintf(stderr, "zdec splits impl %d B<=%d: %d %d %d %d %d\n", impl, CLASS_B[c],
+                                ctx->cs_tab[impl][c][0], ctx->cs_tab[impl][c][1], ctx->cs_tab[impl][c][2],
+                                ctx->cs_tab[impl][c][3], ctx->cs_tab[impl][c][4]);
     }
     if (attention_setup(kv_dtype) != cudaSuccess)
         return bail(fail(nullptr, ZDEC_ERR_CUDA, "attention smem attribute failed"));
@@ -644,7 +670,8 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     } while (0)
 
     const int Bp0 = ctx->Bp_max;
-    const int cv = B <= 4 ? 0 : 1;   // split-factor set
+    const int bc = batch_class(B);   // split-table row
+    auto split = [&](int m) { const int c = ctx->cs_tab[impl][bc][m]; return c > 0 ? c : 1; };
     STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev,
                                          ctx->len_dev, ctx->status, B, ctx->x, H, ctx->L[0].attn_norm,
                                          ctx->x16, ctx->x16lo, ctx->sx, Bp0, ctx->rms_part, pdl, s, tlk));
@@ -705,7 +732,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     for (int l = 0; l < d.n_layers; l++) {
         const LayerW &lw = ctx->L[l];
         normed_input(l == 0 ? 1 : resid_groups);
-        matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, ctx->cs_qkv[cv]);
+        matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, split(MAT_QKV));
         prefetch(lw.o, H / 16, ctx->nsb_q);
         gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld;
         gp.q_frag = ctx->qfrag; gp.q_pos = ctx->pos_dev; gp.q_rope = ctx->rope; gp.q_heads = d.n_q_heads;
@@ -714,20 +741,20 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         ap.layer = l;
         STEP(ZDEC_KERNEL_ATTENTION, (ap.tl = tlk, launch_attention(ap, pdl, s)));
         plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention combine
-        matrix(lw.o, H, H / 16, ctx->nsb_q, ctx->cs_o[cv]);
+        matrix(lw.o, H, H / 16, ctx->nsb_q, split(MAT_O));
         prefetch(lw.gu, F / 8, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
         gp.next_gain = lw.ffn_norm; gp.part_out = ctx->rms_part;
         gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
         STEP(ZDEC_KERNEL_GEMM_O, (gp.tl = tlk, launch_gemm(gp, EPI_RESID, impl, pdl, s)));
         normed_input(resid_groups);
-        matrix(lw.gu, F, F / 8, ctx->nsb_h, ctx->cs_gu[cv]);
+        matrix(lw.gu, F, F / 8, ctx->nsb_h, split(MAT_GU));
         prefetch(lw.down, H / 16, ctx->nsb_f);
         gp.out = nullptr; gp.ldo = F;
         gp.out16 = ctx->a16; gp.out16lo = ctx->a16lo; gp.out_sx = ctx->asx;
         STEP(ZDEC_KERNEL_GEMM_GATEUP, (gp.tl = tlk, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s)));
         plain_input(ctx->a16, ctx->a16lo, ctx->asx);   // written by the gate/up epilogue
-        matrix(lw.down, H, H / 16, ctx->nsb_f, ctx->cs_down[cv]);
+        matrix(lw.down, H, H / 16, ctx->nsb_f, split(MAT_DOWN));
         if (l + 1 < d.n_layers) prefetch(ctx->L[l + 1].qkv, ctx->qkv_ld / 16, ctx->nsb_h);
         else prefetch(ctx->embed, ctx->nrt_vocab, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
@@ -738,7 +765,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         if ((e = capture_x(l + 1)) != cudaSuccess) return e;
     }
     normed_input(resid_groups);
-    matrix(ctx->embed, d.vocab, ctx->nrt_vocab, ctx->nsb_h, ctx->cs_lm[cv]);
+    matrix(ctx->embed, d.vocab, ctx->nrt_vocab, ctx->nsb_h, split(MAT_LM));
     gp.out = logits_out; gp.ldo = d.vocab;
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
     STEP(ZDEC_KERNEL_GEMM_LMHEAD, (gp.tl = tlk, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s)));
@@ -1224,9 +1251,6 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     __half *sums = (__half *)((uint8_t *)workspace_dev + 2 * plane);
     cudaStream_t s = (cudaStream_t)stream;
     CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, B, hi, lo, sums, false, s));
-    int dev = 0, nsm = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     GemmParams gp{};
     gp.W = (const uint8_t *)repacked_dev;
     gp.N = N;
@@ -1239,7 +1263,7 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     gp.Bp = B;
     gp.out = y_dev;
     gp.ldo = N;
-    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm * gemm_ctas_per_sm(B, impl));
+    gp.cs = pick_cs(n_groups(N / 16), K / QK, [&](int cs) { return gemm_cluster_slots(B, impl, EPI_STORE, cs); });
     gp.pipe = gemm_pipe_mode();
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
@@ -1280,7 +1304,7 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
                     "use zdec_q4k_gemm with a caller workspace",
                     (long long)K * B, ZDEC_Q4K_GEMM_STATIC_MAX_KB);
     if ((uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "x_dev must be 16-byte aligned");
-    int dev = 0, nsm = 148;
+    int dev = 0;
     CK(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kStaticMaxDevices) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
     void *base = nullptr;
@@ -1289,7 +1313,6 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
         if (!g_static_addr[dev]) CK(cudaGetSymbolAddress(&g_static_addr[dev], g_static_scratch));
         base = g_static_addr[dev];
     }
-    CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
     const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
     __half *hi = (__half *)base;
     __half *lo = (__half *)((uint8_t *)base + plane);
@@ -1308,7 +1331,7 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
     gp.Bp = B;
     gp.out = y_dev;
     gp.ldo = N;
-    gp.cs = pick_cs(n_groups(N / 16), K / QK, nsm * gemm_ctas_per_sm(B, impl));
+    gp.cs = pick_cs(n_groups(N / 16), K / QK, [&](int cs) { return gemm_cluster_slots(B, impl, EPI_STORE, cs); });
     gp.pipe = gemm_pipe_mode();
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;

@@ -62,7 +62,7 @@ struct GemmParams {
     float rms_eps;
     float *amax_val;       // LMHEAD: per-CTA argmax partials [grid][MAX_B]
     int *amax_idx;
-    int cs;                // K split over a cluster of cs CTAs (1, 2, 4, 8, 16)
+    int cs;                // K split over a cluster of cs CTAs (1..16)
     int stages;            // pipeline depth (set by the launcher)
     int pipe;              // 0: stages consumed in pairs, refilled after a block barrier;
                            // 1: each stage refilled by the last warp done with it
@@ -88,6 +88,9 @@ int gemm_grid(const GemmParams &p);
 // CTAs per SM the projection kernel is built for at batch B (its split
 // factor targets that many CTAs per SM).
 int gemm_ctas_per_sm(int B, int impl);
+// CTAs of the (B, impl, epi) projection kernel split cs ways that the GPU holds
+// at once (the occupancy API's co-resident clusters times cs); 0: not launchable.
+int gemm_cluster_slots(int B, int impl, int epi, int cs);
 
 // prep: fp32 rows -> fp16 operand + sub-block sums.  gain != nullptr applies
 // RMSNorm (x * rsqrt(mean x^2 + eps) * gain).  Rows B..Bp-1 are zeroed.
