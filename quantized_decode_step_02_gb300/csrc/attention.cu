@@ -676,6 +676,29 @@ cudaError_t attention_setup(int kv_dtype) {
     return e;
 }
 
+int attention_max_clusters(int kv_dtype, int stages, int cs) {
+    if (cs < 1 || cs > 16 || stages < 2 || stages > att_max_stages(kv_dtype)) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 8, 1);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = attention_smem_bytes(kv_dtype, stages);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = kv_dtype ? cudaOccupancyMaxActiveClusters(&n, attention_kernel<1>, &cfg)
+                             : cudaOccupancyMaxActiveClusters(&n, attention_kernel<0>, &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 cudaError_t launch_attention(const AttnParams &p0, bool pdl, cudaStream_t stream) {
     AttnParams p = p0;
     if (p.cs < 1 || p.cs > 16) return cudaErrorInvalidValue;

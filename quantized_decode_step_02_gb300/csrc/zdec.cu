@@ -596,13 +596,26 @@ extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
 // --------------------------------------------------------------- step ---
 // CTAs per (sequence, kv head) for the attention cluster: a power of two that
 // gives about two CTAs per SM, at most 16.
-// Attention split (cluster size): the largest power of two up to 16 keeping
-// the grid within ZDEC_ATT_CTAS (default 2) CTAs per SM.
+// Attention split (cluster size, 1..16; ZDEC_ATT_CS forces one): the split
+// of least modelled time over the B x n_kv clusters, waves x (chunks per CTA
+// + 1 for the CTA's query load and merge) for a nominal 64 chunks per
+// sequence, the waves from the occupancy API's co-resident clusters (which
+// must each fit one GPC: 64 clusters of 6 Q8_0 CTAs fit at once, of 7 not).
+static int attn_stages(const zdec_ctx *ctx, int B);
 static int attn_cluster(const zdec_ctx *ctx, int B) {
-    static const int per_sm = getenv("ZDEC_ATT_CTAS") ? std::max(1, atoi(getenv("ZDEC_ATT_CTAS"))) : 2;
-    int per = B * ctx->d.n_kv_heads, cs = 1;
-    while (cs < 16 && per * cs * 2 <= per_sm * ctx->num_sms) cs *= 2;
-    return cs;
+    static const int forced = getenv("ZDEC_ATT_CS") ? atoi(getenv("ZDEC_ATT_CS")) : 0;
+    if (forced >= 1 && forced <= 16) return forced;
+    const int clusters = B * ctx->d.n_kv_heads, stages = attn_stages(ctx, B);
+    int best = 1;
+    double best_t = 1e30;
+    for (int cs = 1; cs <= 16; cs++) {
+        const int maxc = attention_max_clusters(ctx->kv_dtype, stages, cs);
+        if (maxc <= 0) continue;
+        const double t = (double)((clusters + maxc - 1) / maxc) * (64.0 / cs + 1.0);
+        if (t < best_t - 1e-9) { best_t = t; best = cs; }
+    }
+    if (getenv("ZDEC_PRINT_SPLITS")) fprintf(stderr, "zdec attention B=%d: %d stages, split %d\n", B, stages, best);
+    return best;
 }
 
 // Attention chunks in flight per CTA (ZDEC_ATT_STAGES overrides).  A deeper
@@ -610,11 +623,11 @@ static int attn_cluster(const zdec_ctx *ctx, int B) {
 // shared memory keeps the neighbouring projections' CTAs (which prefetch
 // their weights) off the SMs.  Measured: batch of one, two stages; batch of
 // eight, two for an fp16 cache (a third would drop to one CTA per SM) and
-// four for Q8_0 (still two CTAs per SM).
+// three for Q8_0 (still three CTAs per SM).
 static int attn_stages(const zdec_ctx *ctx, int B) {
     static const int env = getenv("ZDEC_ATT_STAGES") ? atoi(getenv("ZDEC_ATT_STAGES")) : 0;
     if (env >= 2) return std::min(env, ctx->kv_dtype ? 8 : 5);
-    return (B > 4 && ctx->kv_dtype) ? 4 : 2;
+    return (B > 4 && ctx->kv_dtype) ? 3 : 2;
 }
 
 static int pick_impl(const zdec_ctx *ctx, int B) {

@@ -141,6 +141,9 @@ cudaError_t attention_setup(int kv_dtype);
 // Dynamic shared memory of a launch with `stages` chunks in flight (0: default).
 size_t attention_smem_bytes(int kv_dtype, int stages = 0);
 int attention_default_stages(int kv_dtype);
+// Clusters of cs attention CTAs (with `stages` chunks in flight) the GPU holds
+// at once, from the occupancy API (0: not launchable).  Needs attention_setup.
+int attention_max_clusters(int kv_dtype, int stages, int cs);
 // Bulk append of fp16 K/V [n_layers][n][n_kv][128] (device) at tokens t0.. of slot.
 cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const uint16_t *k16,
                              const uint16_t *v16, cudaStream_t stream);
