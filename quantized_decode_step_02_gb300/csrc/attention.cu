@@ -253,7 +253,10 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     if (pos < 0 || pos >= p.max_L) return;   // bad device input (whole cluster); flagged by the embedding kernel
     const int ntok = pos + 1;
     const int nch = (ntok + ATT_CHUNK - 1) / ATT_CHUNK;
-    const int c_lo = rank * nch / CS, c_hi = (rank + 1) * nch / CS;
+    // the rank holding the new token also appends it and patches its chunk:
+    // one virtual chunk of extra work, so its range is one chunk shorter
+    const int nw = nch + (p.append ? 1 : 0);
+    const int c_lo = min(nch, rank * nw / CS), c_hi = min(nch, (rank + 1) * nw / CS);
     const int T0 = c_lo * ATT_CHUNK;
     const int T1 = min(c_hi * ATT_CHUNK, ntok);
     const bool empty = c_lo >= c_hi;       // still takes part in the cluster merge
@@ -403,17 +406,26 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         if (zfrom < ATT_CHUNK) {
             uint8_t *sV = st + Lay::K_BYTES;
             {   // thread d clears row d of V^T from column zfrom on (128 threads, 128 rows)
+                // element stores up to a 16-byte boundary, then whole 16-byte stores
+                // (rows start 16-byte aligned: strides 160 / 80 / 128 bytes)
                 const int d = threadIdx.x;
+                const uint4 z4 = make_uint4(0, 0, 0, 0);
                 if (KVT == 0) {
                     __half *row = reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE);
-                    for (int t = zfrom; t < ATT_CHUNK; t++) row[t] = __ushort_as_half(0);
+                    int t = zfrom;
+                    for (; t < ATT_CHUNK && (t & 7); t++) row[t] = __ushort_as_half(0);
+                    for (; t < ATT_CHUNK; t += 8) *reinterpret_cast<uint4 *>(row + t) = z4;
                 } else {
                     uint8_t *row = sV + d * Lay::V_STRIDE;
-                    for (int t = zfrom; t < ATT_CHUNK; t++) row[t] = 0;
+                    int t = zfrom;
+                    for (; t < ATT_CHUNK && (t & 15); t++) row[t] = 0;
+                    for (; t < ATT_CHUNK; t += 16) *reinterpret_cast<uint4 *>(row + t) = z4;
                     if (d < 4) {
                         uint16_t *srow = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES) +
                                          d * ATT_CHUNK;
-                        for (int t = zfrom; t < ATT_CHUNK; t++) srow[t] = 0;
+                        int u = zfrom;
+                        for (; u < ATT_CHUNK && (u & 7); u++) srow[u] = 0;
+                        for (; u < ATT_CHUNK; u += 8) *reinterpret_cast<uint4 *>(srow + u) = z4;
                     }
                 }
             }
