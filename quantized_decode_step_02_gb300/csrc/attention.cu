@@ -282,6 +282,14 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         cp_async_commit();
     }
 
+    // the rotary row of the new token: a constant table, read before the wait
+    float2 rope_new[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    if (has_new && warp == 0 && p.append) {
+        const float2 *cs = p.rope + (size_t)pos * (HD / 2);
+        rope_new[0] = cs[lane];
+        rope_new[1] = cs[lane + 32];
+    }
+
     pdl_launch_dependents();
     pdl_wait();
     tl_min(p.tl, 1);
@@ -331,20 +339,22 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     }
 
     tl_max(p.tl, 5);
-    // ---- the new token: rotate k, round to fp16, quantize (Q8_0), append
+    // ---- the new token (warp 0 of the CTA that holds it): its k and v rows
+    // are loaded now, but rotated, rounded, quantized (Q8_0) and appended only
+    // at the chunk that holds it, so that the load latency hides behind the
+    // earlier chunks
+    float kx[4], vx[4];
     if (has_new && warp == 0) {
         const float *krow = p.qkv + (size_t)b * p.qkv_ld + (size_t)(p.nq + g) * HD;
         const float *vrow = p.qkv + (size_t)b * p.qkv_ld + (size_t)(p.nq + p.kv.n_kv + g) * HD;
-        const float2 *cs = p.rope + (size_t)pos * (HD / 2);
-        size_t pi = plane_index(p.kv, b, p.layer, g);
-        const int Lp = p.kv.Lp;
-        float kx[4], vx[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) { kx[i] = krow[lane + 32 * i]; vx[i] = vrow[lane + 32 * i]; }
+    }
+    auto append_new = [&]() {
         float kr[4];
 #pragma unroll
         for (int i = 0; i < 2; i++) {   // pairs (d, d+64): d = lane + 32 i
-            float2 c = cs[lane + 32 * i];
+            const float2 c = rope_new[i];
             kr[i] = kx[i] * c.x - kx[i + 2] * c.y;
             kr[i + 2] = kx[i + 2] * c.x + kx[i] * c.y;
         }
@@ -353,26 +363,46 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             int d = lane + 32 * i;
             __half kh = __float2half_rn(kr[i]), vh = __float2half_rn(vx[i]);
             if (KVT == 0) {
-                *reinterpret_cast<__half *>(p.kv.k + pi * Lp * (HD * 2) + kv_k16_off(pos, d)) = kh;
-                *reinterpret_cast<__half *>(p.kv.v + pi * Lp * (HD * 2) + kv_v16_off(d, pos)) = vh;
                 reinterpret_cast<__half *>(s_newk)[d] = kh;
                 reinterpret_cast<__half *>(s_newv)[d] = vh;
             } else {
                 uint16_t ksb, vsb;
                 int8_t kc = q8_0_lane(kh, ksb), vc = q8_0_lane(vh, vsb);
-                *reinterpret_cast<int8_t *>(p.kv.k + pi * Lp * HD + kv_k8_off(pos, d)) = kc;
-                *reinterpret_cast<int8_t *>(p.kv.v + pi * Lp * HD + kv_v8_off(d, pos)) = vc;
                 reinterpret_cast<int8_t *>(s_newk)[d] = kc;
                 reinterpret_cast<int8_t *>(s_newv)[d] = vc;
                 if (lane == 0) {
-                    *reinterpret_cast<uint16_t *>(p.kv.ks + pi * Lp * 8 + kv_ks_off(pos, i)) = ksb;
-                    *reinterpret_cast<uint16_t *>(p.kv.vs + pi * Lp * 8 + kv_vs_off(i, pos)) = vsb;
                     s_newks[i] = ksb;
                     s_newvs[i] = vsb;
                 }
             }
         }
-    }
+    };
+    // the appended token into the arena, from shared memory, once the cluster
+    // no longer waits on this CTA (no global store is then outstanding at the
+    // cluster barriers' release)
+    auto store_new = [&]() {
+        const size_t pi = plane_index(p.kv, b, p.layer, g);
+        const int Lp = p.kv.Lp;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int d = lane + 32 * i;
+            if (KVT == 0) {
+                *reinterpret_cast<__half *>(p.kv.k + pi * Lp * (HD * 2) + kv_k16_off(pos, d)) =
+                    reinterpret_cast<const __half *>(s_newk)[d];
+                *reinterpret_cast<__half *>(p.kv.v + pi * Lp * (HD * 2) + kv_v16_off(d, pos)) =
+                    reinterpret_cast<const __half *>(s_newv)[d];
+            } else {
+                *reinterpret_cast<int8_t *>(p.kv.k + pi * Lp * HD + kv_k8_off(pos, d)) =
+                    reinterpret_cast<const int8_t *>(s_newk)[d];
+                *reinterpret_cast<int8_t *>(p.kv.v + pi * Lp * HD + kv_v8_off(d, pos)) =
+                    reinterpret_cast<const int8_t *>(s_newv)[d];
+                if (lane == 0) {
+                    *reinterpret_cast<uint16_t *>(p.kv.ks + pi * Lp * 8 + kv_ks_off(pos, i)) = s_newks[i];
+                    *reinterpret_cast<uint16_t *>(p.kv.vs + pi * Lp * 8 + kv_vs_off(i, pos)) = s_newvs[i];
+                }
+            }
+        }
+    };
 
     // ---- online softmax state (meaningful on lanes gid < 4: head 4g+gid)
     float m_run = -INFINITY, l_run = 0.0f;
@@ -404,6 +434,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         // past it and insert the new token; whole-history chunks skip both barriers
         const int zfrom = max(H, c0) - c0;
         if (zfrom < ATT_CHUNK) {
+            if (has_new && warp == 0) append_new();   // before the barrier that publishes s_new*
             uint8_t *sV = st + Lay::K_BYTES;
             {   // thread d clears row d of V^T from column zfrom on (128 threads, 128 rows)
                 // element stores up to a 16-byte boundary, then whole 16-byte stores
@@ -609,7 +640,8 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     }
     // ---- rank 0 merges the cluster's partials through distributed shared memory
     cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
+    cluster_arrive_release();   // the partials in s_part (shared memory only)
+    cluster_wait_acquire();
     if (rank == 0) {
         // issue every peer's loads before using any (distributed shared memory
         // latency is paid once, not once per rank)
@@ -669,7 +701,11 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         if ((lane & 7) == 0) store_sum(p.osx, kcol >> 8, b, (kcol >> 5) & 7, p.oBp, part);
     }
     tl_max(p.tl, 7);
-    cluster.sync();   // peers keep their partials alive until rank 0 has read them
+    // peers keep their partials alive until rank 0 has read them (its reads
+    // have returned by the time it arrives; nothing needs ordering)
+    cluster_arrive_relaxed();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (has_new && warp == 0) store_new();
     tl_end(p.tl);
 }
 

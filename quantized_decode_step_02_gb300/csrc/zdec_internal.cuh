@@ -203,6 +203,11 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive without ordering this thread's earlier memory operations (a pure
+// execution barrier: nothing written before it needs to be seen after it).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 // Shared-memory address `a` of this CTA -> the same address in cluster rank r.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t r) {
     uint32_t out;
