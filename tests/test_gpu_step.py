@@ -82,6 +82,36 @@ def test_small_model_multi_step_ragged(kv_dtype):
     dec.close()
 
 
+@pytest.mark.parametrize("kv_dtype", [0, 1])
+def test_batch_of_eight_across_chunk_boundaries(kv_dtype):
+    """Eight sequences whose new tokens fall on and next to 64-token chunk
+    boundaries, over two steps: the attention's split over a cluster gives
+    the rank that appends the new token one chunk less, and that token is
+    rotated, quantized and inserted at its own chunk; the appended tokens
+    must land in the arena."""
+    d = SMALL
+    w = cached_model(d, 103)
+    lengths = [1, 63, 64, 127, 128, 191, 256, 319]
+    dec, om, kvs = setup_pair(d, w, 103, lengths, kv_dtype, 330)
+    pos = np.array(lengths, np.int32)
+    for step in range(2):
+        toks = make_tokens(d, 300 + step, len(lengths))
+        check_step(dec, om, kvs, toks, pos, f"kv{kv_dtype} step {step}")
+        pos += 1
+    for b in (2, 4, 7):
+        n = int(pos[b])
+        got = dec.read_kv(b, 2, 0, n)
+        if kv_dtype == 0:
+            gk = got[0].view(np.float16).astype(np.float64)
+            rk = kvs[b].k16[2, :n].view(np.float16).astype(np.float64)
+            assert np.allclose(gk, rk, rtol=2e-3, atol=2e-3)
+        else:
+            assert np.abs(got[0].astype(int) - kvs[b].kq[2, :n].astype(int)).max() <= 1
+            assert np.abs(got[1].astype(int) - kvs[b].vq[2, :n].astype(int)).max() <= 1
+    assert [dec.seq_len(b) for b in range(8)] == [L + 2 for L in lengths]
+    dec.close()
+
+
 @pytest.mark.parametrize("impl", [1, 2, 3])
 def test_matvec_and_mma_paths_both_match(impl):
     d = SMALL
