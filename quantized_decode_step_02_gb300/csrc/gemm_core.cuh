@@ -91,9 +91,6 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
     const int tig = lane & 3;
     const uint8_t *tile = st + warp * TILE_BYTES;
     const uint8_t *act = st + act_off;   // this lane's B column of n-tile 0 (see gemm_kernel)
-    uint4 q[4];
-#pragma unroll
-    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
     TileMeta tm;
     decode_meta(*reinterpret_cast<const uint2 *>(tile + TILE_CODE_BYTES + 8 * lane), tig, tm);
     // independent accumulator chains per n-tile, so a warp always has MMAs
@@ -119,10 +116,11 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
         const int h = c >> 1;
         const __half2 cg = h ? tm.cg1 : tm.cg0, og = h ? tm.og1 : tm.og0;
         const __half2 c8 = h ? tm.c81 : tm.c80, o8 = h ? tm.o81 : tm.o80;
+        const uint4 qc = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);   // codes of chunk c
 #pragma unroll
         for (int pp = 0; pp < 2; pp++) {
             const int pidx = (c & 1) * 2 + pp;
-            uint32_t w0 = pp ? q[c].z : q[c].x, w1 = pp ? q[c].w : q[c].y;
+            uint32_t w0 = pp ? qc.z : qc.x, w1 = pp ? qc.w : qc.y;
             uint32_t at[4], at16[4];
             decode_word(w0, cg, og, at[0], at16[0], at[2], at16[2]);
             decode_word(w1, c8, o8, at[1], at16[1], at[3], at16[3]);
