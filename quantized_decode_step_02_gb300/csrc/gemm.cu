@@ -665,13 +665,6 @@ static int stages_for(uint32_t stage_bytes, int occ, uint32_t reserved) {
     return d < 2 ? 2 : (d > 6 ? 6 : d);
 }
 
-// CTAs per SM of the kernel launch_epi picks for (B, impl): GemmOcc of its NT
-int gemm_ctas_per_sm(int B, int impl) {
-    if (impl == 1) return B <= 2 ? 2 : 1;
-    if (impl == 3) return 3;
-    return B <= 8 ? 3 : 1;
-}
-
 // Shared-memory plan of a launch: ring depth, the reduction area and its
 // place; may halve p.cs.  Returns the dynamic shared-memory bytes.
 template <int NT, int IMPL>

@@ -85,9 +85,6 @@ struct GemmParams {
 // impl 1: CUDA-core dequant-matvec (B <= 4); impl 2: mma.sync swap-AB GEMM.
 cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaStream_t stream);
 int gemm_grid(const GemmParams &p);
-// CTAs per SM the projection kernel is built for at batch B (its split
-// factor targets that many CTAs per SM).
-int gemm_ctas_per_sm(int B, int impl);
 // CTAs of the (B, impl, epi) projection kernel split cs ways that the GPU holds
 // at once (the occupancy API's co-resident clusters times cs); 0: not launchable.
 int gemm_cluster_slots(int B, int impl, int epi, int cs);
