@@ -11,8 +11,9 @@
 // Grid: (cluster rank r, kv head g, sequence b); 128 threads; the CS CTAs of
 // one (b, g) form a thread-block cluster.  The 4 query heads of a kv head
 // share one read of its K/V tiles.  The pos+1 tokens are cut into 64-token
-// chunks; rank r takes chunks [r*nch/CS, (r+1)*nch/CS), streamed through two
-// shared-memory stages with cp.async.  Both products run on
+// chunks; rank r takes a contiguous range of them (the rank that appends the
+// new token one chunk fewer), streamed through a ring of 2-8 shared-memory
+// stages with cp.async.  Both products run on
 // mma.sync.m16n8k16 with fp32 accumulation:
 //   scores: A = q (rows 0-3 the fp16 high parts of the 4 heads, rows 8-11 the
 //           low parts, so q keeps ~22 bits), B = K^T (8 tokens per MMA);
@@ -20,9 +21,10 @@
 //           V^T tile, whose layout makes each thread's four tokens adjacent.
 // Q8_0: codes become exact fp16 integers in registers; K scales multiply the
 // per-32-dim partial scores, V scales are folded into p per 32-dim block.
-// Each CTA reduces its warps to one (max, sum, unnormalised output) partial in
-// shared memory; rank 0 of the cluster merges the ranks' partials through
-// distributed shared memory (fixed rank order) and writes the output.
+// Softmax runs in log2 units (q carries log2(e)/sqrt(128)).  Each CTA reduces
+// its warps to one (max, sum, unnormalised output) partial in shared memory;
+// rank 0 of the cluster merges the ranks' partials through distributed shared
+// memory (fixed rank order) and writes the output.
 #include <cooperative_groups.h>
 
 #include "zdec_kernels.cuh"

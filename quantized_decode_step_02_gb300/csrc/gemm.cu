@@ -670,8 +670,7 @@ static int stages_for(uint32_t stage_bytes, int occ, uint32_t reserved) {
 template <int NT, int IMPL>
 static size_t plan_smem(GemmParams &p) {
     const StageLayout lay(GemmBR<NT, IMPL>::v);
-    // rank 0 of a cluster holds the cs - 1 peers' partial tiles; a split whose
-    // tiles do not fit next to two stages is halved
+    // rank 0 of a cluster holds the cs - 1 peers' partial tiles
     constexpr uint32_t NYB = GemmRed<NT, IMPL>::v;
     constexpr int OCC = GemmOcc<NT, IMPL>::v;
     // the peers' tiles go behind the ring when ring and tiles fit the CTA's

@@ -594,8 +594,6 @@ extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
 }
 
 // --------------------------------------------------------------- step ---
-// CTAs per (sequence, kv head) for the attention cluster: a power of two that
-// gives about two CTAs per SM, at most 16.
 // Attention split (cluster size, 1..16; ZDEC_ATT_CS forces one): the split
 // of least modelled time over the B x n_kv clusters, waves x (chunks per CTA
 // + 1 for the CTA's query load and merge) for a nominal 64 chunks per
