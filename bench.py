@@ -81,6 +81,20 @@ def aggregate_tok_s(B: int, world: int, ms_per_step: float) -> float:
     return B * world * 1000.0 / ms_per_step
 
 
+def fit_time_model(points):
+    """Least-squares fit of the pages' decode time model t(B, L) = a + B (b + k L)
+    to measured (B, L, ms) points: features 1, B and B L.  Returns a, b and k in
+    ms, ms and ms per token, and the largest relative residual."""
+    import numpy as np
+    P = np.asarray(points, dtype=np.float64)
+    B, L, t = P[:, 0], P[:, 1], P[:, 2]
+    A = np.stack([np.ones_like(B), B, B * L], axis=1)
+    coef, *_ = np.linalg.lstsq(A, t, rcond=None)
+    resid = np.abs(A @ coef - t) / t
+    return {"a_ms": float(coef[0]), "b_ms": float(coef[1]), "k_ms_per_token": float(coef[2]),
+            "max_rel_residual": float(resid.max()), "points": int(len(t))}
+
+
 def ncu_traffic(engine: str, kind: str, B: int, kv: str, impl: int):
     """DRAM bytes per launch of a kernel kind from a committed ncu capture
     (profiles/ncu_traffic.json), or None when no capture matches."""
@@ -354,12 +368,16 @@ def main():
         # shared by the sequences), then the projection-kernel switch point
         hist = device_history(32768)
         for kv in ("f16", "q8_0"):
+            pts = []
             for B in (1, 4, 8, 16, 32):
                 for L in (2048, 8192, 16384, 32768):
                     r = bench_point(a, desc, w, B, L, kv, rank, world, dev_hist=hist)
+                    pts.append((B, L, r["ms_per_step"]))
                     if rank == 0:
                         print(json.dumps({"sweep": True, **{k: v for k, v in r.items() if k != "profile_ms"},
                                           "profile_ms": r["profile_ms"]}), flush=True)
+            if rank == 0:   # the pages' time model t(B, L) = a + B (b + k L), fitted to this kv type's grid
+                print(json.dumps({"time_model": True, "kv": kv, **fit_time_model(pts)}), flush=True)
         for B in (1, 2, 3, 4):
             for impl in ((1, 2, 3) if B == 1 else (1, 2)):
                 a.gemm_impl = impl

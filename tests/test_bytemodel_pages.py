@@ -76,3 +76,19 @@ def test_weight_bytes_of_synthetic_model():
     k = 147456
     assert bm.step_bytes(W, 8, 2048, k) - bm.step_bytes(W, 4, 2048, k) == 4 * 2048 * k
     assert bm.step_bytes(W, 1, 0, k) == W
+
+
+def test_time_model_fit_recovers_its_coefficients():
+    """bench.py fits the pages' time model t(B, L) = a + B (b + k L) to a sweep;
+    on points generated from known coefficients (the pages' 16.9 ms and 1.1 ms,
+    with a per-token k) the fit returns them, and a perturbed point shows up
+    as the largest relative residual."""
+    import bench
+    a, b, k = 16.9, 1.1, 2.0e-4
+    pts = [(B, L, a + B * (b + k * L)) for B in (1, 4, 8, 16, 32) for L in (2048, 8192, 16384, 32768)]
+    fit = bench.fit_time_model(pts)
+    assert abs(fit["a_ms"] - a) < 1e-9 * a and abs(fit["b_ms"] - b) < 1e-9 and abs(fit["k_ms_per_token"] - k) < 1e-13
+    assert fit["max_rel_residual"] < 1e-12 and fit["points"] == 20
+    B0, L0, t0 = pts[7]
+    pts[7] = (B0, L0, t0 * 1.1)
+    assert bench.fit_time_model(pts)["max_rel_residual"] > 0.05
