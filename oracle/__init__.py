@@ -61,7 +61,11 @@ class _KV(ctypes.Structure):
     _fields_ = [("kv_dtype", ctypes.c_int), ("max_L", ctypes.c_int64),
                 ("k16", ctypes.c_void_p), ("v16", ctypes.c_void_p),
                 ("kq", ctypes.c_void_p), ("vq", ctypes.c_void_p),
-                ("ks", ctypes.c_void_p), ("vs", ctypes.c_void_p)]
+                ("ks", ctypes.c_void_p), ("vs", ctypes.c_void_p),
+                ("k8", ctypes.c_void_p), ("v8", ctypes.c_void_p),
+                ("k_type", ctypes.c_int), ("v_type", ctypes.c_int)]
+
+KV_F16, KV_Q8_0, KV_FP8 = 0, 1, 2   # per-tensor cache types
 
 
 def _load():
@@ -79,6 +83,8 @@ def _load():
         "orc_q4k_matvec": (None, [vp, i64, i64, vp, vp]),
         "orc_q8_0_quantize": (None, [vp, vp, vp]),
         "orc_q8_0_value": (f64, [ctypes.c_uint16, ctypes.c_int8]),
+        "orc_e4m3_from_half": (ctypes.c_uint8, [ctypes.c_uint16]),
+        "orc_e4m3_value": (f64, [ctypes.c_uint8]),
         "orc_rmsnorm": (None, [vp, vp, i64, f64, vp]),
         "orc_rope": (None, [vp, ctypes.c_int, i64, f64]),
         "orc_silu": (f64, [f64]),
@@ -164,6 +170,16 @@ def q8_0_value(scale_bits: int, code: int) -> float:
     return float(_load().orc_q8_0_value(int(scale_bits), int(code)))
 
 
+# ------------------------------------------------------------ FP8 e4m3
+def e4m3_from_half(bits: int) -> int:
+    """e4m3 code of one fp16 value (nearest, ties to even, saturating to +-448)."""
+    return int(_load().orc_e4m3_from_half(int(bits)))
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().orc_e4m3_value(int(code)))
+
+
 # ------------------------------------------------------------ layer math
 def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
@@ -232,22 +248,26 @@ class Model:
 class KV:
     """One sequence's cache in canonical token-major layout (see oracle.c)."""
 
-    def __init__(self, desc: Desc, max_L: int, kv_dtype: int):
+    def __init__(self, desc: Desc, max_L: int, kv_dtype):
+        """kv_dtype: one type for both tensors (KV_F16, KV_Q8_0, KV_FP8) or a
+        (k_type, v_type) pair."""
         self.desc, self.max_L, self.kv_dtype = desc, max_L, kv_dtype
+        kt, vt = (kv_dtype, kv_dtype) if isinstance(kv_dtype, int) else tuple(kv_dtype)
+        assert kt in (KV_F16, KV_Q8_0, KV_FP8) and vt in (KV_F16, KV_Q8_0, KV_FP8)
+        self.k_type, self.v_type = kt, vt
         shape = (desc.n_layers, max_L, desc.n_kv_heads, desc.head_dim)
         sshape = (desc.n_layers, max_L, desc.n_kv_heads, desc.head_dim // 32)
         z = lambda s, t: np.zeros(s, dtype=t)
-        if kv_dtype == 0:
-            self.k16, self.v16 = z(shape, np.uint16), z(shape, np.uint16)
-            self.kq = self.vq = self.ks = self.vs = None
-        else:
-            self.k16 = self.v16 = None
-            self.kq, self.vq = z(shape, np.int8), z(shape, np.int8)
-            self.ks, self.vs = z(sshape, np.uint16), z(sshape, np.uint16)
+        self.k16 = z(shape, np.uint16) if kt == KV_F16 else None
+        self.v16 = z(shape, np.uint16) if vt == KV_F16 else None
+        self.kq, self.ks = (z(shape, np.int8), z(sshape, np.uint16)) if kt == KV_Q8_0 else (None, None)
+        self.vq, self.vs = (z(shape, np.int8), z(sshape, np.uint16)) if vt == KV_Q8_0 else (None, None)
+        self.k8 = z(shape, np.uint8) if kt == KV_FP8 else None
+        self.v8 = z(shape, np.uint8) if vt == KV_FP8 else None
         self.len = 0
         ptr = lambda a: _p(a) if a is not None else None
-        self.c = _KV(kv_dtype, max_L, ptr(self.k16), ptr(self.v16), ptr(self.kq),
-                     ptr(self.vq), ptr(self.ks), ptr(self.vs))
+        self.c = _KV(kt if kt == vt else -1, max_L, ptr(self.k16), ptr(self.v16), ptr(self.kq),
+                     ptr(self.vq), ptr(self.ks), ptr(self.vs), ptr(self.k8), ptr(self.v8), kt, vt)
 
     def append(self, k16: np.ndarray, v16: np.ndarray):
         """Append n tokens of rotated fp16 K/V, arrays [n_layers][n][n_kv][hd] uint16."""

@@ -17,13 +17,20 @@ def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int, kv: str = 
     """KV bytes one token adds to one sequence's cache, K and V over all layers.
 
     f16: 2 bytes per element.  q8_0: 32-element blocks of int8 codes plus one
-    fp16 scale, i.e. 34 bytes per 32 elements."""
+    fp16 scale, i.e. 34 bytes per 32 elements.  fp8: one e4m3 byte per element,
+    no scale.  A (k, v) pair of kinds gives each tensor its own type."""
+    if isinstance(kv, tuple):
+        k, v = kv
+        return (kv_bytes_per_token(n_layers, n_kv_heads, head_dim, k) +
+                kv_bytes_per_token(n_layers, n_kv_heads, head_dim, v)) // 2
     elems = 2 * n_layers * n_kv_heads * head_dim
     if kv == "f16":
         return 2 * elems
     if kv == "q8_0":
         assert head_dim % 32 == 0
         return elems // 32 * 34
+    if kv == "fp8":
+        return elems
     raise ValueError(kv)
 
 

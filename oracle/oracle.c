@@ -12,8 +12,9 @@
  *     of them and each sequence reads its own KV cache ("The weight read is
  *     the only term that does not scale", "The two halves of a decode-step
  *     memory bill");
- *   - the KV cache is fp16 or 8-bit (Q8), dequantized where it is read
- *     ("Why Q8 is close to free and where the sharp edges are");
+ *   - the KV cache is fp16 or 8-bit (Q8_0, or FP8 e4m3 as the pages' scale-free
+ *     alternative), per tensor, dequantized where it is read ("Why Q8 is
+ *     close to free and where the sharp edges are");
  *   - greedy sampling of the LM head output.
  * The pages leave the model's layer arithmetic open; the plain readings used
  * here are: RMSNorm (eps 1e-6 unless given), rotate-half RoPE on pairs
@@ -155,6 +156,42 @@ double orc_q8_0_value(uint16_t scale, int8_t q) {
     return (double)orc_half_to_float(scale) * (double)q;
 }
 
+/* ------------------------------------------------------------ FP8 ----- */
+
+/* FP8 e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities, S.1111.111 is NaN, largest finite 448).  The cache type the
+ * pages name as the scale-free alternative to Q8 ("FP8 (e4m3) KV ... native
+ * Blackwell conversion, same bytes as Q8, no scale"): each fp16 value maps to
+ * the nearest e4m3 value, ties to the even code, magnitudes at or beyond 448
+ * to +-448 (saturating, as the hardware's satfinite conversion), NaN to NaN. */
+uint8_t orc_e4m3_from_half(uint16_t h) {
+    double x = (double)orc_half_to_float(h);
+    uint8_t sign = (h & 0x8000u) ? 0x80u : 0x00u;
+    if (x != x) return (uint8_t)(sign | 0x7Fu);
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (a >= 448.0) return (uint8_t)(sign | 0x7Eu);
+    int e;
+    frexp(a, &e);                   /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                         /* a = (1 + m) * 2^e, m in [0, 1) */
+    if (e < -6) {                   /* subnormal: a = M * 2^-9, M in 0..7 */
+        double M = rint(ldexp(a, 9));   /* exact scaling; rint ties to even */
+        return (uint8_t)(sign | (uint8_t)M);   /* M = 8 is the smallest normal's code */
+    }
+    double M = rint((ldexp(a, -e) - 1.0) * 8.0);
+    if (M == 8.0) { M = 0.0; e += 1; }
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)M);
+}
+
+/* Value of an e4m3 code (NaN for S.1111.111). */
+double orc_e4m3_value(uint8_t c) {
+    int E = (c >> 3) & 15, M = c & 7;
+    double sign = (c & 0x80u) ? -1.0 : 1.0;
+    if (E == 15 && M == 7) return NAN;
+    if (E == 0) return sign * ldexp((double)M, -9);
+    return sign * ldexp(1.0 + M / 8.0, E - 7);
+}
+
 /* ------------------------------------------------------- layer math ---- */
 
 /* y = x / sqrt(mean(x^2) + eps) * g, in double. */
@@ -194,14 +231,40 @@ int64_t orc_argmax(const float *x, int64_t n) {
 /* One sequence's cache in canonical layout, tokens major:
  *   fp16:  k16/v16  [n_layers][max_L][n_kv][hd]          binary16 bits
  *   Q8_0:  kq/vq    [n_layers][max_L][n_kv][hd]          int8 codes
- *          ks/vs    [n_layers][max_L][n_kv][hd/32]       fp16 scales  */
+ *          ks/vs    [n_layers][max_L][n_kv][hd/32]       fp16 scales
+ *   FP8:   k8/v8    [n_layers][max_L][n_kv][hd]          e4m3 codes
+ * K and V may have different types (llama.cpp-style separate cache types). */
 typedef struct {
-    int kv_dtype;          /* 0 = fp16, 1 = Q8_0 */
+    int kv_dtype;          /* 0 = fp16, 1 = Q8_0, 2 = FP8 e4m3 for both tensors; -1: k_type / v_type */
     int64_t max_L;
     uint16_t *k16, *v16;
     int8_t *kq, *vq;
     uint16_t *ks, *vs;
+    uint8_t *k8, *v8;      /* e4m3 codes [n_layers][max_L][n_kv][hd] */
+    int k_type, v_type;    /* per-tensor types when kv_dtype = -1 */
 } orc_kv;
+
+/* Storage type of K (which = 0) or V (which = 1). */
+static inline int orc_kv_type(const orc_kv *kv, int which) {
+    return kv->kv_dtype >= 0 ? kv->kv_dtype : (which ? kv->v_type : kv->k_type);
+}
+
+/* Store one head row of hd fp16 values of K (which = 0) or V at `row`. */
+static void orc_kv_put_row(orc_kv *kv, int which, int hd, int64_t row, const uint16_t *x16) {
+    switch (orc_kv_type(kv, which)) {
+        case 0:
+            memcpy((which ? kv->v16 : kv->k16) + row * hd, x16, (size_t)hd * 2);
+            break;
+        case 1:
+            for (int b = 0; b < hd / 32; b++)
+                orc_q8_0_quantize(x16 + 32 * b, (which ? kv->vs : kv->ks) + row * (hd / 32) + b,
+                                  (which ? kv->vq : kv->kq) + row * hd + 32 * b);
+            break;
+        default:
+            for (int i = 0; i < hd; i++) (which ? kv->v8 : kv->k8)[row * hd + i] = orc_e4m3_from_half(x16[i]);
+            break;
+    }
+}
 
 typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
@@ -227,15 +290,8 @@ static void orc_kv_store(const orc_desc *m, orc_kv *kv, int layer, int64_t t, in
         k16[i] = orc_double_to_half(kr[i]);
         v16[i] = orc_double_to_half(vr[i]);
     }
-    if (kv->kv_dtype == 0) {
-        memcpy(kv->k16 + row * hd, k16, (size_t)hd * 2);
-        memcpy(kv->v16 + row * hd, v16, (size_t)hd * 2);
-    } else {
-        for (int b = 0; b < hd / 32; b++) {
-            orc_q8_0_quantize(k16 + 32 * b, kv->ks + row * (hd / 32) + b, kv->kq + row * hd + 32 * b);
-            orc_q8_0_quantize(v16 + 32 * b, kv->vs + row * (hd / 32) + b, kv->vq + row * hd + 32 * b);
-        }
-    }
+    orc_kv_put_row(kv, 0, hd, row, k16);
+    orc_kv_put_row(kv, 1, hd, row, v16);
 }
 
 /* Element i of the stored K (which=0) or V (which=1) row at (layer, t, kvh). */
@@ -243,11 +299,15 @@ static inline double orc_kv_get(const orc_desc *m, const orc_kv *kv, int layer, 
                                 int kvh, int which, int i) {
     int hd = m->head_dim;
     int64_t row = (((int64_t)layer * kv->max_L + t) * m->n_kv_heads + kvh);
-    if (kv->kv_dtype == 0)
-        return (double)orc_half_to_float((which ? kv->v16 : kv->k16)[row * hd + i]);
-    const int8_t *q = which ? kv->vq : kv->kq;
-    const uint16_t *s = which ? kv->vs : kv->ks;
-    return orc_q8_0_value(s[row * (hd / 32) + i / 32], q[row * hd + i]);
+    switch (orc_kv_type(kv, which)) {
+        case 0: return (double)orc_half_to_float((which ? kv->v16 : kv->k16)[row * hd + i]);
+        case 1: {
+            const int8_t *q = which ? kv->vq : kv->kq;
+            const uint16_t *s = which ? kv->vs : kv->ks;
+            return orc_q8_0_value(s[row * (hd / 32) + i / 32], q[row * hd + i]);
+        }
+        default: return orc_e4m3_value((which ? kv->v8 : kv->k8)[row * hd + i]);
+    }
 }
 
 /* Grouped-query attention for one sequence at position pos over the stored
@@ -358,7 +418,8 @@ void orc_decode_step(const orc_desc *m, const orc_weights *w, orc_kv *kv, int B,
 }
 
 /* Bulk append of already-rotated fp16 K/V rows ([n_layers][n][n_kv][hd]) at
- * tokens t0..t0+n-1 of one sequence; Q8_0 caches quantize each 32-block. */
+ * tokens t0..t0+n-1 of one sequence; Q8_0 tensors quantize each 32-block,
+ * FP8 tensors convert each value. */
 void orc_kv_append(const orc_desc *m, orc_kv *kv, int64_t t0, int64_t n,
                    const uint16_t *k16, const uint16_t *v16) {
     int hd = m->head_dim, nkv = m->n_kv_heads;
@@ -367,16 +428,7 @@ void orc_kv_append(const orc_desc *m, orc_kv *kv, int64_t t0, int64_t n,
             for (int g = 0; g < nkv; g++) {
                 int64_t src = (((int64_t)l * n + t) * nkv + g) * hd;
                 int64_t row = (((int64_t)l * kv->max_L + t0 + t) * nkv + g);
-                if (kv->kv_dtype == 0) {
-                    memcpy(kv->k16 + row * hd, k16 + src, (size_t)hd * 2);
-                    memcpy(kv->v16 + row * hd, v16 + src, (size_t)hd * 2);
-                } else {
-                    for (int b = 0; b < hd / 32; b++) {
-                        orc_q8_0_quantize(k16 + src + 32 * b, kv->ks + row * (hd / 32) + b,
-                                          kv->kq + row * hd + 32 * b);
-                        orc_q8_0_quantize(v16 + src + 32 * b, kv->vs + row * (hd / 32) + b,
-                                          kv->vq + row * hd + 32 * b);
-                    }
-                }
+                orc_kv_put_row(kv, 0, hd, row, k16 + src);
+                orc_kv_put_row(kv, 1, hd, row, v16 + src);
             }
 }

@@ -28,16 +28,22 @@ def _kv_with_history(d, seed, seq, L, max_L, kv_dtype):
     return kv
 
 
+def _stored_tensor(kind, x16, xq, xs, x8, layer, n):
+    """One stored tensor of one layer, dequantized by library routines and
+    numpy: fp16 bits through numpy, Q8_0 codes times their fp16 scales, e4m3
+    codes through torch's float8_e4m3fn."""
+    if kind == oracle.KV_F16:
+        return x16[layer, :n].view(np.float16).astype(np.float64)
+    if kind == oracle.KV_Q8_0:
+        s = xs[layer, :n].view(np.float16).astype(np.float64)
+        return xq[layer, :n].astype(np.float64) * np.repeat(s, 32, axis=-1)
+    return torch.from_numpy(np.ascontiguousarray(x8[layer, :n])).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
 def _stored_kv(kv, layer, n):
     """Dequantized stored K, V of one layer: [n_kv, n, hd] float64."""
-    if kv.kv_dtype == 0:
-        k = kv.k16[layer, :n].view(np.float16).astype(np.float64)
-        v = kv.v16[layer, :n].view(np.float16).astype(np.float64)
-    else:
-        ks = kv.ks[layer, :n].view(np.float16).astype(np.float64)
-        vs = kv.vs[layer, :n].view(np.float16).astype(np.float64)
-        k = kv.kq[layer, :n].astype(np.float64) * np.repeat(ks, 32, axis=-1)
-        v = kv.vq[layer, :n].astype(np.float64) * np.repeat(vs, 32, axis=-1)
+    k = _stored_tensor(kv.k_type, kv.k16, kv.kq, kv.ks, kv.k8, layer, n)
+    v = _stored_tensor(kv.v_type, kv.v16, kv.vq, kv.vs, kv.v8, layer, n)
     return np.transpose(k, (1, 0, 2)), np.transpose(v, (1, 0, 2))
 
 
@@ -54,6 +60,52 @@ def test_attention_matches_torch_sdpa_gqa(kv_dtype):
         torch.from_numpy(q.reshape(1, d.n_q_heads, 1, d.head_dim)),
         torch.from_numpy(k[None]), torch.from_numpy(v[None]), enable_gqa=True)
     assert np.allclose(o, ref.numpy().reshape(-1), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("k_type", [0, 1, 2])
+@pytest.mark.parametrize("v_type", [0, 1, 2])
+def test_attention_with_separate_k_and_v_types(k_type, v_type):
+    """Separate K and V cache types (fp16, Q8_0, FP8 e4m3 each): the oracle's
+    attention equals torch's grouped-query SDPA over the stored tensors, each
+    dequantized by its own type; a tensor read with the other's type, or an
+    e4m3 code read as anything else, fails."""
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    d = TINY
+    L = 45
+    kv = _kv_with_history(d, 8, 0, L, 64, (k_type, v_type))
+    q = np.random.default_rng(4).standard_normal(d.n_q_heads * d.head_dim) * 1.3
+    o = oracle.attention(odesc(d), kv, 0, L - 1, q)
+    k, v = _stored_kv(kv, 0, L)
+    ref = F.scaled_dot_product_attention(
+        torch.from_numpy(q.reshape(1, d.n_q_heads, 1, d.head_dim)),
+        torch.from_numpy(k[None]), torch.from_numpy(v[None]), enable_gqa=True)
+    assert np.allclose(o, ref.numpy().reshape(-1), rtol=1e-10, atol=1e-12)
+    # the types really differ: an fp16 K read back as stored equals the history
+    # only for the fp16 type
+    kh, _ = make_kv_history(d, 8, 0, L)
+    exact = np.array_equal(k, np.transpose(kh[0].view(np.float16).astype(np.float64), (1, 0, 2)))
+    assert exact == (k_type == oracle.KV_F16)
+
+
+def test_fp8_cache_in_a_full_decode_step():
+    """A decode step over an FP8 cache: a batch of two equals two single
+    steps, bit for bit in the logits and in the e4m3 codes appended."""
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    d = TINY
+    w = make_model(d, 31)
+    m = oracle.Model(odesc(d), w)
+    toks = make_tokens(d, 32, 2)
+    kvs = [_kv_with_history(d, 9, b, L, 48, oracle.KV_FP8) for b, L in enumerate((5, 20))]
+    pos = np.array([5, 20], np.int32)
+    logits, ids, _ = oracle.decode_step(m, kvs, toks, pos)
+    one = [_kv_with_history(d, 9, b, L, 48, oracle.KV_FP8) for b, L in enumerate((5, 20))]
+    for b in range(2):
+        lb, ib, _ = oracle.decode_step(m, [one[b]], toks[b:b + 1], pos[b:b + 1])
+        assert np.array_equal(lb[0], logits[b]) and ib[0] == ids[b]
+        assert np.array_equal(one[b].k8, kvs[b].k8) and np.array_equal(one[b].v8, kvs[b].v8)
+    assert np.isfinite(logits).all()
 
 
 def test_attention_single_token_returns_v():

@@ -256,3 +256,48 @@ def test_argmax_ties_lowest_index():
     assert oracle.argmax(x) == 17
     x[3] = 5.0000005
     assert oracle.argmax(x) == 3
+
+
+# ------------------------------------------------------------------ FP8 e4m3
+def test_e4m3_worked_values():
+    """The e4m3 format: bias 7, 3 mantissa bits, largest finite 448 (code 0x7E),
+    smallest normal 2^-6 (0x08), smallest subnormal 2^-9 (0x01); nearest value,
+    ties to the even code; magnitudes beyond 448 saturate (the hardware's
+    satfinite conversion, the reading taken for an FP8 cache)."""
+    h = oracle.double_to_half
+    cases = {1.0: 0x38, -1.0: 0xB8, 448.0: 0x7E, 1000.0: 0x7E, -60000.0: 0xFE, 2.0 ** -6: 0x08,
+             2.0 ** -9: 0x01, 2.0 ** -10: 0x00, 3 * 2.0 ** -10: 0x02, 1.0625: 0x38, 1.1875: 0x3A,
+             0.0: 0x00, 240.0: 0x77, 0.5: 0x30}
+    for v, code in cases.items():
+        assert oracle.e4m3_from_half(h(v)) == code, (v, hex(code))
+    assert oracle.e4m3_from_half(0x8000) == 0x80            # -0
+    assert oracle.e4m3_from_half(0x7C00) == 0x7E            # +inf saturates
+    assert oracle.e4m3_from_half(0x7E00) & 0x7F == 0x7F     # NaN stays NaN
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+
+
+def test_e4m3_matches_torch_on_every_in_range_half():
+    """Every finite fp16 value below the rounding boundary to 480 (|x| < 464)
+    converts as PyTorch's float8_e4m3fn cast does (nearest, ties to even); the
+    decoded codes equal PyTorch's decode.  (Above it PyTorch returns NaN where
+    the cache saturates.)"""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16).astype(np.float32)
+    keep = np.isfinite(vals) & (np.abs(vals) < 464.0)
+    ref = torch.from_numpy(vals[keep]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_half(int(b)) for b in bits[keep]], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([oracle.e4m3_value(int(c)) for c in codes])
+    assert np.array_equal(mine, dec)
+
+
+def test_fp8_cache_bytes():
+    from oracle.bytemodel import kv_bytes_per_token
+    assert kv_bytes_per_token(36, 8, 128, "fp8") == 73_728 == kv_bytes_per_token(36, 8, 128, "f16") // 2
+    assert kv_bytes_per_token(36, 8, 128, ("q8_0", "f16")) == (78_336 + 147_456) // 2
