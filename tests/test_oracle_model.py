@@ -88,23 +88,31 @@ def test_attention_with_separate_k_and_v_types(k_type, v_type):
     assert exact == (k_type == oracle.KV_F16)
 
 
-def test_fp8_cache_in_a_full_decode_step():
-    """A decode step over an FP8 cache: a batch of two equals two single
-    steps, bit for bit in the logits and in the e4m3 codes appended."""
+@pytest.mark.parametrize("types", [(2, 2), (1, 0), (0, 2)])
+def test_separate_cache_types_in_a_full_decode_step(types):
+    """Decode steps over FP8 and mixed-type caches: a batch of two equals two
+    single steps, bit for bit in the logits and in every stored array; the
+    appended token sits where the step put it (position pos) and nowhere else."""
     if not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("no float8_e4m3fn in this torch")
     d = TINY
     w = make_model(d, 31)
     m = oracle.Model(odesc(d), w)
     toks = make_tokens(d, 32, 2)
-    kvs = [_kv_with_history(d, 9, b, L, 48, oracle.KV_FP8) for b, L in enumerate((5, 20))]
+    kvs = [_kv_with_history(d, 9, b, L, 48, types) for b, L in enumerate((5, 20))]
     pos = np.array([5, 20], np.int32)
+    before = [{k: getattr(kv, k).copy() for k in ("k16", "v16", "kq", "vq", "ks", "vs", "k8", "v8")
+               if getattr(kv, k) is not None} for kv in kvs]
     logits, ids, _ = oracle.decode_step(m, kvs, toks, pos)
-    one = [_kv_with_history(d, 9, b, L, 48, oracle.KV_FP8) for b, L in enumerate((5, 20))]
+    one = [_kv_with_history(d, 9, b, L, 48, types) for b, L in enumerate((5, 20))]
     for b in range(2):
         lb, ib, _ = oracle.decode_step(m, [one[b]], toks[b:b + 1], pos[b:b + 1])
         assert np.array_equal(lb[0], logits[b]) and ib[0] == ids[b]
-        assert np.array_equal(one[b].k8, kvs[b].k8) and np.array_equal(one[b].v8, kvs[b].v8)
+        for name, old in before[b].items():
+            new = getattr(kvs[b], name)
+            assert np.array_equal(new, getattr(one[b], name)), name
+            changed = np.nonzero(np.any((new != old).reshape(new.shape[0], new.shape[1], -1), axis=-1))[1]
+            assert set(changed.tolist()) <= {int(pos[b])}, name
     assert np.isfinite(logits).all()
 
 
