@@ -92,3 +92,29 @@ def test_time_model_fit_recovers_its_coefficients():
     B0, L0, t0 = pts[7]
     pts[7] = (B0, L0, t0 * 1.1)
     assert bench.fit_time_model(pts)["max_rel_residual"] > 0.05
+
+
+def test_bench_byte_accounting_matches_the_byte_model():
+    """The roofline numerators bench.py reports come from the same closed forms
+    the pages state: its weight stream is the byte model's W (4,767,858,688 B
+    for the 36-layer model), its KV bytes per token are 147,456 (fp16) and
+    78,336 (Q8_0), the five projection launches of a step add up to the Q4_K
+    part of W, and a step's bytes are the model's W + B L k plus the token the
+    step appends and reads, the embedding rows and the logits."""
+    import bench
+    from synth.model import FULL as d
+    W = bm.weight_bytes()
+    assert bench.weight_bytes(d) == W == 4_767_858_688
+    for kv, k in (("f16", 147_456), ("q8_0", 78_336)):
+        assert bench.kv_bytes_per_token(d, kv) == k == bm.kv_bytes_per_token(36, 8, 128, kv)
+    per_layer = sum(bench.kernel_bytes(d, kind, 0, 0, "f16")
+                    for kind in ("gemm_qkv", "gemm_o", "gemm_gateup", "gemm_down"))
+    lm = bench.kernel_bytes(d, "gemm_lmhead", 0, 0, "f16")
+    assert d.n_layers * per_layer + lm == bm.weight_bytes(with_norms=False)
+    for B, L in ((1, 2048), (8, 2400), (32, 32768)):
+        k = bm.kv_bytes_per_token(36, 8, 128, "f16")
+        extra = B * k + B * (d.hidden // 256 * 144 + 4 * d.vocab)
+        assert bench.step_bytes(d, B, L, "f16") == bm.step_bytes(W, B, L + 1, k) + extra
+    # per layer, the attention launch moves 1/36 of the step's KV bytes
+    att = bench.kernel_bytes(d, "attention", 8, 2400, "q8_0")
+    assert att - 8 * (2 * 4096 + 2 * 1024) * 4 == pytest.approx(8 * 2402 * 78_336 / 36)
