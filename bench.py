@@ -57,6 +57,8 @@ def args_parse():
                    help="persistent: the whole step as one cooperative kernel; kernels: one per operation")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-targets", action="store_true",
+                   help="skip the B {1,8} x L {2048,8192} x {f16,q8_0} target grid of the default line")
     p.add_argument("--sweep", action="store_true", help="B x L x kv grid, one JSON line per point")
     p.add_argument("--device-history", action="store_true",
                    help="one seeded device-side N(0,1) KV history shared by the sequences (fast setup)")
@@ -204,6 +206,32 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def workload_config(a, desc, world):
+    """The `config` object both arms print (identical keys and values)."""
+    return {"workload": f"decode step B={a.B} L={a.L} {a.kv} KV, {desc.n_layers}-layer GQA Q4_K synthetic model",
+            "B": a.B, "L": a.L, "kv": a.kv, "model_layers": desc.n_layers, "seed": a.seed,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "no flush: every step streams >4.7 GB, far larger than the 129 MB L2"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or ''."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return ""
+
+
 def oracle_step_sample(desc, w, seed, B, L, kv, budget_s=20.0, max_steps=None):
     """Time the CPU oracle on up to B of the workload's sequences for about
     budget_s seconds; returns (tok/s, threads, description)."""
@@ -238,8 +266,9 @@ def run_reference(a, rank, world):
         return
     w = make_model(desc, a.seed)
     import oracle  # noqa: F401
-    # warm-up steps are untimed; each timed step is one oracle step of one sequence
-    oracle_step_sample(desc, w, a.seed, a.B, a.L, a.kv, budget_s=0.0, max_steps=max(1, min(a.warmup, 1)))
+    # a.warmup untimed steps; each timed step is one oracle step of one sequence
+    if a.warmup > 0:
+        oracle_step_sample(desc, w, a.seed, a.B, a.L, a.kv, budget_s=0.0, max_steps=a.warmup)
     per_step = []
     for i in range(a.steps):
         v, threads, _ = oracle_step_sample(desc, w, a.seed, a.B, a.L, a.kv, budget_s=0.0, max_steps=1)
@@ -249,22 +278,50 @@ def run_reference(a, rank, world):
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": a.gpus, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": 1000 * el / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "impl": "reference",
-            "config": {"workload": f"decode step B={a.B} L={a.L} {a.kv} KV, 36-layer GQA Q4_K synthetic model",
-                       "B": a.B, "L": a.L, "kv": a.kv, "sample": "1 sequence per step"},
+            "impl": "reference", "config": workload_config(a, desc, world),
             "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tok/s", "cores": threads,
-                             "sample": f"{a.steps} oracle step(s) of one sequence"},
+                             "cpu": cpu_model(),
+                             "sample": f"{a.steps} timed oracle step(s) of one sequence of the workload "
+                                       f"after {a.warmup} untimed"},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def time_steps(dec, B, L, first, n_warm, n_timed, stream, world, desc, seed, logits):
+    """n_warm untimed then n_timed CUDA-event-timed steps of rows 0..B-1 whose
+    caches hold `first` tokens; returns (ms per step, clock summary)."""
+    import torch
+    n_total = n_warm + n_timed
+    toks = [torch.from_numpy(make_tokens(desc, seed * 1000 + i, B)).cuda() for i in range(n_total)]
+    pos = [torch.full((B,), first + i, dtype=torch.int32, device="cuda") for i in range(n_total)]
+    ids = torch.empty(B, dtype=torch.int32, device="cuda")
+    for i in range(n_warm):
+        dec.step(toks[i], pos[i], logits, ids)
+    dec.sync()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        for i in range(n_warm, n_total):
+            dec.step(toks[i], pos[i], logits, ids)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    dec.sync()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / n_timed, world, "cuda")
+    if world > 1:
+        torch.distributed.barrier()
+    return ms, clk.summary()
 
 
 def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=None):
     """One measured configuration.  dev_hist: (k, v) fp16 CUDA tensors
     [n_layers][>= L][n_kv][hd] appended to every sequence instead of the seeded
-    host history (the sweep's large points; timing does not depend on values)."""
+    host history (the sweep's large points; timing does not depend on values).
+    The timed steps write logits [B][vocab] and ids, as step_bytes counts."""
     import torch
     import quantized_decode_step_02_gb300 as z
-    dev = torch.cuda.current_device()
     stream = torch.cuda.Stream()
     extra = a.warmup + a.steps + 4 + (0 if a.no_e2e else a.warmup + a.steps)
     dec = z.Decoder(desc, w, z.KV_F16 if kv == "f16" else z.KV_Q8_0, max_B=B, max_L=L + extra + 2,
@@ -283,48 +340,34 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=No
         for b in range(B):
             k, v = make_kv_history(desc, a.seed, b, L)
             dec.append_kv(b, k, v)
+    logits = torch.empty((B, desc.vocab), dtype=torch.float32, device="cuda")
+    ms, clocks = time_steps(dec, B, L, L, a.warmup, a.steps, stream, world, desc, a.seed, logits)
     n_total = a.warmup + a.steps
-    toks = [torch.from_numpy(make_tokens(desc, a.seed * 1000 + i, B)).cuda() for i in range(n_total + 4)]
-    pos = [torch.full((B,), L + i, dtype=torch.int32, device="cuda") for i in range(n_total + 4)]
-    ids = torch.empty(B, dtype=torch.int32, device="cuda")
-    for i in range(a.warmup):
-        dec.step(toks[i], pos[i], None, ids)
-    dec.sync()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with Clocks(dev) as clk:
-        ev0.record(stream)
-        for i in range(a.warmup, n_total):
-            dec.step(toks[i], pos[i], None, ids)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    dec.sync()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / a.steps, world, "cuda")
-    if world > 1:
-        torch.distributed.barrier()
     Lmid = L + a.warmup + a.steps / 2
     res = {"B": B, "L": L, "kv": kv, "ms_per_step": ms, "tok_s": aggregate_tok_s(B, world, ms),
            "step_bytes": step_bytes(desc, B, Lmid, kv), "kernels_per_step": dec.info()["kernels_per_step"],
            "engine": ["auto", "kernels", "persistent"][dec.info()["engine"]],
-           "clocks": clk.summary()}
+           "clocks": clocks}
     res["step_gbs"] = res["step_bytes"] / (ms * 1e-3) / 1e9
     i = n_total
+    toks = [torch.from_numpy(make_tokens(desc, a.seed * 1000 + 400 + j, B)).cuda() for j in range(2)]
+    ids = torch.empty(B, dtype=torch.int32, device="cuda")
     if a.trace:   # one traced step (not timed)
         dec.set_trace(True)
-        dec.step(toks[i], pos[i], None, ids)
+        dec.step(toks[0], torch.full((B,), L + i, dtype=torch.int32, device="cuda"), logits, ids)
         np.save(a.trace, dec.step_trace())
         dec.set_trace(False)
         i += 1
     # ---- per-launch profile of one eager step (CUDA events on the library stream)
-    prof = dec.profile_step(toks[i], pos[i], None, ids)
+    prof = dec.profile_step(toks[1], torch.full((B,), L + i, dtype=torch.int32, device="cuda"), logits, ids)
     by_kind = {}
     for kind, t in prof:
         by_kind.setdefault(kind, []).append(t)
     res["profile_ms"] = {k: {"launches": len(v), "total_ms": sum(v), "avg_ms": sum(v) / len(v)}
                          for k, v in by_kind.items()}
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: token ids and
+    # positions in, argmax ids out, every step (the LM head writes no logits
+    # buffer on this path: the ids are the step's result)
     if not a.no_e2e:
         base = i + 1
         ht = [make_tokens(desc, a.seed * 1000 + 700 + j, B) for j in range(n_total)]
@@ -339,6 +382,48 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=No
                       "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B}
     dec.close()
     return res
+
+
+def target_grid(a, desc, w, world, hbm_peak):
+    """The target cells B in {1, 8} x L in {2048, 8192} x {f16, q8_0}: one
+    decoder per KV type (max_B = 8), a seeded device-side N(0,1) history
+    appended to every sequence of a cell, then the same warm-up and timed
+    steps as the headline.  Each cell: ms/step, tok/s, the bytes-moved
+    fraction of the measured HBM bandwidth, and the clocks of its timed region."""
+    import torch
+    import quantized_decode_step_02_gb300 as z
+    Lmax = 8192
+    gen = torch.Generator(device="cuda").manual_seed(10)
+    shape = (desc.n_layers, Lmax, desc.n_kv_heads, desc.head_dim)
+    hist = (torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16),
+            torch.randn(shape, generator=gen, device="cuda", dtype=torch.float16))
+    cells = []
+    n = a.warmup + a.steps
+    for kv in ("f16", "q8_0"):
+        stream = torch.cuda.Stream()
+        dec = z.Decoder(desc, w, z.KV_F16 if kv == "f16" else z.KV_Q8_0, max_B=8, max_L=Lmax + n + 2,
+                        stream=stream.cuda_stream)
+        for L in (2048, 8192):
+            k, v = hist[0][:, :L].contiguous(), hist[1][:, :L].contiguous()
+            for B in (1, 8):
+                for b in range(8):
+                    dec.reset_seq(b)
+                torch.cuda.synchronize()
+                for b in range(B):
+                    dec.append_kv(b, k, v)
+                dec.sync()
+                logits = torch.empty((B, desc.vocab), dtype=torch.float32, device="cuda")
+                ms, clk = time_steps(dec, B, L, L, a.warmup, a.steps, stream, world, desc, a.seed, logits)
+                sb = step_bytes(desc, B, L + a.warmup + a.steps / 2, kv)
+                gbs = sb / (ms * 1e-3) / 1e9
+                cells.append({"B": B, "L": L, "kv": kv, "ms_per_step": round(ms, 4),
+                              "tok_s": round(aggregate_tok_s(B, world, ms), 1),
+                              "step_hbm_gbs": round(gbs, 1), "step_frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+                              "step_frac_of_8tbs": round(gbs / 8000.0, 4), "clocks": clk})
+            del k, v
+        dec.close()
+    del hist
+    return cells
 
 
 def main():
@@ -412,26 +497,33 @@ def main():
             "frac": achieved / hbm_peak, "peak_source": peak_src,
             "traffic": ncu_traffic(r["engine"], dom, a.B, a.kv, impl),
             "bytes_per_launch": kb, "avg_launch_ms": launch_ms, "launches_per_step": launches}
+    targets = None
+    if not a.no_targets and a.layers is None and world == 1:
+        targets = target_grid(a, desc, w, world, hbm_peak)
     cpu = None
     if not a.no_cpu_baseline and world == 1:
+        import oracle
         v, threads, sample = oracle_step_sample(desc, w, a.seed, a.B, a.L, a.kv, budget_s=15.0)
-        cpu = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample,
+               "cpu": cpu_model()}
+        # the same oracle on one core: one step (about cores x the time above)
+        oracle.set_threads(1)
+        v1, _, sample1 = oracle_step_sample(desc, w, a.seed, a.B, a.L, a.kv, budget_s=0.0, max_steps=1)
+        oracle.set_threads(threads)
+        cpu["single_thread"] = {"value": v1, "unit": "tok/s", "cores": 1, "sample": sample1}
     line = {"metric": METRIC, "value": r["tok_s"], "unit": "tok/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "q4_k weights, f16 activations, f32 accumulate",
             "data": "synthetic (seeded N(0,0.02) weights quantized to Q4_K, N(0,1) fp16 KV history)",
-            "config": {"workload": f"decode step B={a.B} L={a.L} {a.kv} KV, 36-layer GQA Q4_K synthetic model",
-                       "B": a.B, "L": a.L, "kv": a.kv, "model_layers": desc.n_layers, "seed": a.seed,
-                       "engine": r["engine"],
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "no flush: every step streams >4.7 GB, far larger than the 129 MB L2",
-                       "step_bytes": r["step_bytes"], "step_hbm_gbs": r["step_gbs"],
-                       "step_frac_of_measured_hbm": r["step_gbs"] / hbm_peak,
-                       "step_frac_of_8tbs": r["step_gbs"] / 8000.0,
-                       "model_gen_s": round(gen_s, 1)},
+            "config": workload_config(a, desc, world),
+            "step": {"engine": r["engine"], "bytes": r["step_bytes"], "hbm_gbs": r["step_gbs"],
+                     "frac_of_measured_hbm": r["step_gbs"] / hbm_peak, "frac_of_8tbs": r["step_gbs"] / 8000.0,
+                     "bytes_counted": "weights once + per sequence (L+2) KV tokens + embedding row + fp32 logits "
+                                      "(the timed steps write logits)",
+                     "model_gen_s": round(gen_s, 1)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": r.get("e2e"),
             "gpu_launches": r["kernels_per_step"] * a.steps, "clocks": r["clocks"],
-            "profile_ms": prof}
+            "targets": targets, "profile_ms": prof}
     print(json.dumps(line), flush=True)
 
 

@@ -84,6 +84,12 @@ typedef struct {
 typedef struct zdec_ctx zdec_ctx;
 
 /* Create a decoder: validate the shape, allocate on the current CUDA device
+ * Defined by: "Eight concurrent agents pull 5.6x more tokens from one RX 9070
+ * XT", sections "The weight read is the only term that does not scale" (one
+ * copy of the weights, shared by every sequence of a step) and "Where it
+ * stops, and the argument I got wrong in May" (the KV budget, not the
+ * arithmetic, bounds how many sequences fit: max_B x max_L tokens).
+ *
  * (repacked weights ~0.5625 B/weight, the KV arena of max_B x max_L tokens,
  * the per-step workspace), repack the weights on the GPU and wait for it.
  * kv_dtype fixes the cache format: F16 (2 B/element) or Q8_0 (32-element
@@ -95,7 +101,12 @@ zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights
                         zdec_ctx **out);
 void zdec_destroy(zdec_ctx *ctx);
 
-/* Append n_tokens already-rotated K/V rows to sequence `seq`, starting at its
+/* Defined by: "Q8 KV cache pushes an RDNA4 swarm crossover from 5k to 10k
+ * tokens", sections "The crossover is just a byte count" (the cache holds K
+ * and V of every cached token, fp16 or one byte per element) and "Why Q8 is
+ * close to free and where the sharp edges are" (the cache is quantized where
+ * it is written).
+ * Append n_tokens already-rotated K/V rows to sequence `seq`, starting at its
  * current length.  k_f16 / v_f16: [n_layers][n_tokens][n_kv_heads][head_dim]
  * fp16, host memory (on_device = 0; the call waits for the copy) or device
  * memory (on_device = 1; asynchronous).  A Q8_0 cache quantizes every
@@ -110,11 +121,17 @@ zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f
                                   copies in, runs, copies out and waits */
 #define ZDEC_STEP_EAGER    2   /* launch kernel by kernel instead of replaying a CUDA graph */
 
-/* One decode step for sequences (slots) 0..B-1, B <= max_B.
+/* Defined by: "Eight concurrent agents pull 5.6x more tokens from one RX 9070
+ * XT", section "The workload stopped being one person typing" (advance B
+ * in-flight sequences by one token each per step, reading the weights once)
+ * and "Batched swarm: the KV read does not amortize", section "The two halves
+ * of a decode-step memory bill" (each sequence reads its own KV cache).
+ * One decode step for sequences (slots) 0..B-1, B <= max_B.
  *   tokens [B] int32 token ids, positions [B] int32: position b must equal the
  *   number of tokens cached for slot b.  With host I/O the check happens
  *   before anything is enqueued (ZDEC_ERR_POSITION); with device inputs the
- *   first kernel checks it and zdec_sync reports ZDEC_ERR_DEVICE.
+ *   first kernel checks it (and the token ids), the step then writes no KV
+ *   row and advances no length, and zdec_sync reports ZDEC_ERR_DEVICE.
  *   logits [B][vocab] fp32 (may be NULL), ids [B] int32 greedy argmax (lowest
  *   index on ties).
  * The step embeds each token, runs every layer (RMSNorm, QKV, RoPE, KV append,
@@ -127,15 +144,27 @@ zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tokens,
                              const int32_t *positions, float *logits, int32_t *ids, int flags);
 
 /* Wait for the context's stream and report any device-side status
- * (ZDEC_ERR_DEVICE / ZDEC_ERR_TIMEOUT), clearing it. */
+ * (ZDEC_ERR_DEVICE / ZDEC_ERR_TIMEOUT), clearing it.  A step whose device
+ * check failed, and every step enqueued after it until this call, wrote no
+ * KV row and advanced no length; on either error this call also resets the
+ * host's lengths (zdec_seq_len) to the device's.  The pages define no such
+ * call: it is the asynchronous ABI's error channel. */
 zdec_status zdec_sync(zdec_ctx *ctx);
 
+/* Sequence slots, per "Eight concurrent agents pull 5.6x more tokens from one
+ * RX 9070 XT", section "The workload stopped being one person typing" (server
+ * slots that admit and retire agents between steps): reset_seq empties slot
+ * `seq` (length := 0; waits for the stream); seq_len reads the host's copy of
+ * its length.  ZDEC_ERR_ARG for a slot outside [0, max_B). */
 zdec_status zdec_reset_seq(zdec_ctx *ctx, int seq);            /* length := 0 */
 zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len);
 const char *zdec_last_error(const zdec_ctx *ctx);
 const char *zdec_last_global_error(void);
 
-/* Which dense kernel runs the Q4_K projections of the kernel engine:
+/* Defined by: "Eight concurrent agents pull 5.6x more tokens from one RX 9070
+ * XT", section "RDNA4 pads the batch dimension to 16" (a dequant-matvec for
+ * one sequence, a tensor-core GEMM past a few sequences).
+ * Which dense kernel runs the Q4_K projections of the kernel engine:
  * 0 = default (B = 1: the sub-block-column mma matvec, impl 3; 2 <= B <= 4 by
  * the measured switch point between the CUDA-core matvec and the GEMM),
  * 1 = always the CUDA-core dequant-matvec (B <= 4 only), 2 = always the
@@ -227,6 +256,15 @@ zdec_status zdec_debug_read_kv(zdec_ctx *ctx, int seq, int layer, int t0, int n,
  * (after the embedding and after each layer) before it returns.  out must
  * hold B*(n_layers+1)*hidden floats for the B of that step; host memory. */
 zdec_status zdec_debug_capture_hidden(zdec_ctx *ctx, float *out_host);
+/* Bound of the projection kernels' stage waits, in GPU clock cycles (0: the
+ * default, about 2 s; -1: every projection's first stage wait counts as run
+ * out at once, which tests use to take the give-up path deterministically).
+ * A wait that runs out sets the device status that zdec_sync reports as
+ * ZDEC_ERR_TIMEOUT; the kernel first waits (with the full bound) for its own
+ * copies still in flight, then returns, and the step writes no KV row and
+ * advances no length.  Waits for the stream; cached CUDA graphs are rebuilt
+ * at the next step.  ZDEC_ERR_ARG for cycles < -1. */
+zdec_status zdec_debug_set_wait_limit(zdec_ctx *ctx, long long cycles);
 /* Attention alone on the cached tokens 0..positions[b] of layer `layer`
  * (nothing appended): q [B][n_q_heads][head_dim] fp32 already rotated,
  * o [B][n_q_heads][head_dim] fp32.  Host memory. */
@@ -245,10 +283,13 @@ size_t zdec_q4k_repacked_bytes(int N, int K);
 zdec_status zdec_q4k_repack(const void *canonical_dev, int N, int K, void *repacked_dev,
                             void *stream);
 /* Scratch bytes zdec_q4k_gemm needs for B rows of length K: fp16 high and
- * low parts of the activations (padded to a multiple of 8 rows) and their
- * per-32 sub-block sums. */
+ * low parts of the activations (exactly B rows, no padding) and their per-32
+ * sub-block sums. */
 size_t zdec_q4k_gemm_workspace_bytes(int K, int B);
-/* y[b][n] = sum_k W[n][k] x[b][k] for b < B.  x_dev fp32 [B][K], y_dev fp32
+/* Defined by: "Eight concurrent agents pull 5.6x more tokens from one RX 9070
+ * XT", section "The weight read is the only term that does not scale" (one
+ * read of each weight tile multiplied against every row of the batch).
+ * y[b][n] = sum_k W[n][k] x[b][k] for b < B.  x_dev fp32 [B][K], y_dev fp32
  * [B][N], workspace_dev >= zdec_q4k_gemm_workspace_bytes(K, B) bytes, 16-byte
  * aligned, owned by the caller.  impl: 1 = dequant-matvec (B <= 4),
  * 2 = mma.sync GEMM, 3 = sub-block-column mma matvec (B = 1).  Activations enter as fp16 high + low parts (about 22
@@ -270,7 +311,10 @@ zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x
  * any CUDA call; the other checks are zdec_q4k_gemm's.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, which may load the module); make that first call
- *   before any stream capture begins on that device.
+ *   before any stream capture begins on that device.  The address is kept
+ *   per device ordinal for the life of the process: after cudaDeviceReset
+ *   (or anything else that destroys the device's primary context) it no
+ *   longer names the array, so do not call this entry point after that.
  * - Calls whose kernels may overlap in time (different streams with no
  *   ordering between them, or different host threads) share the array and
  *   race on it: order them, e.g. on one stream or with events.  Consecutive

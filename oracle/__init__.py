@@ -103,6 +103,15 @@ def _load():
     return lib
 
 
+def set_threads(n: int) -> None:
+    """OpenMP threads the oracle's parallel loops use from now on."""
+    lib = _load()
+    f = lib.omp_set_num_threads   # libgomp, a dependency of the oracle library
+    f.restype = None
+    f.argtypes = [ctypes.c_int]
+    f(int(n))
+
+
 def _p(a: np.ndarray) -> int:
     assert a.flags["C_CONTIGUOUS"], "oracle wants C-contiguous arrays"
     return a.ctypes.data

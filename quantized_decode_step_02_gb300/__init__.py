@@ -35,7 +35,7 @@ EXPORTS = ["zdec_create", "zdec_destroy", "zdec_append_kv", "zdec_decode_step", 
            "zdec_reset_seq", "zdec_seq_len", "zdec_last_error", "zdec_last_global_error",
            "zdec_set_gemm_impl", "zdec_set_engine", "zdec_set_trace", "zdec_debug_step_trace", "zdec_get_info", "zdec_profile_step", "zdec_debug_export_q4k",
            "zdec_debug_dequant", "zdec_debug_read_kv", "zdec_debug_capture_hidden",
-           "zdec_debug_attention", "zdec_q4k_repacked_bytes", "zdec_q4k_repack",
+           "zdec_debug_attention", "zdec_debug_set_wait_limit", "zdec_q4k_repacked_bytes", "zdec_q4k_repack",
            "zdec_q4k_gemm_workspace_bytes", "zdec_q4k_gemm", "zdec_q4k_gemm_static"]
 
 
@@ -110,6 +110,7 @@ def load_library(build_if_missing: bool = True):
         "zdec_debug_read_kv": (i, [vp, i, i, i, i, vp, vp, vp, vp]),
         "zdec_debug_capture_hidden": (i, [vp, vp]),
         "zdec_debug_attention": (i, [vp, i, i, vp, vp, vp]),
+        "zdec_debug_set_wait_limit": (i, [vp, ctypes.c_longlong]),
         "zdec_q4k_repacked_bytes": (sz, [i, i]),
         "zdec_q4k_repack": (i, [vp, i, i, vp, vp]),
         "zdec_q4k_gemm_workspace_bytes": (sz, [i, i]),
@@ -273,8 +274,8 @@ class Decoder:
         self._check(self.lib.zdec_set_gemm_impl(self.h, impl))
 
     def set_engine(self, engine: int):
-        """ENGINE_AUTO (persistent step kernel where available), ENGINE_KERNELS or
-        ENGINE_PERSISTENT."""
+        """ENGINE_AUTO (the default: the kernel engine, one kernel per operation),
+        ENGINE_KERNELS or ENGINE_PERSISTENT (opt-in single-kernel step)."""
         self._check(self.lib.zdec_set_engine(self.h, engine))
 
     def set_trace(self, on: bool):
@@ -311,6 +312,11 @@ class Decoder:
         return [(KERNEL_KINDS[kind[i]], float(ms[i])) for i in range(min(n.value, cap))]
 
     # ---------------------------------------------------------------- debug
+    def set_wait_limit(self, cycles: int):
+        """Bound of the projection kernels' stage waits in clock cycles (0: the
+        default ~2 s); a wait that runs out makes sync() raise a timeout."""
+        self._check(self.lib.zdec_debug_set_wait_limit(self.h, int(cycles)))
+
     def _cols(self, which: int) -> int:
         d = self.desc
         return {T_WO: d.n_q_heads * d.head_dim, T_DOWN: d.ffn}.get(which, d.hidden)

@@ -707,7 +707,10 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     // have returned by the time it arrives; nothing needs ordering)
     cluster_arrive_relaxed();
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    if (has_new && warp == 0) store_new();
+    // a step whose inputs a device check flagged (or that follows one before
+    // zdec_sync) changes no cache state: the status word is final by now,
+    // every kernel that sets it having completed before this kernel's wait
+    if (has_new && warp == 0 && (*(volatile uint32_t *)p.status & STATUS_STATE_ERRORS) == 0) store_new();
     tl_end(p.tl);
 }
 

@@ -318,11 +318,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, float (&y)[NT
 }
 
 // Bounded wait on a stage's mbarrier; on timeout the status word records it.
-__device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, uint32_t *status) {
+// limit: clock cycles (GEMM_WAIT_LIMIT, ~2 s: a copy that never lands).
+constexpr long long GEMM_WAIT_LIMIT = 1LL << 32;
+__device__ __forceinline__ bool wait_stage(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                           long long limit = GEMM_WAIT_LIMIT) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > (1LL << 32)) {   // ~2 s: a copy that never lands
+        if (clock64() - t0 > limit) {
             if (status) atomicOr(status, STATUS_TIMEOUT);
             return false;
         }
@@ -494,11 +497,22 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     // gives each warp two dependency chains to interleave, and halves the
     // block-wide syncs that release stages for refilling
     bool ok = true;
+    const long long wlim = p.wait_limit > 0 ? p.wait_limit : GEMM_WAIT_LIMIT;
+    // wait_limit < 0 (tests): the first stage wait counts as run out at once,
+    // so the give-up path (status, drain of the copies in flight, return)
+    // runs deterministically, without racing the copies
+    auto expired = [&](int i, int parity_i) {
+        if (p.wait_limit < 0 && i == 0) {
+            if (p.status) atomicOr(p.status, STATUS_TIMEOUT);
+            return true;
+        }
+        return !wait_stage(&full[parity_i % D], (uint32_t)(parity_i / D) & 1u, p.status, wlim);
+    };
     if (p.pipe == 1) {
         // each warp takes the stages in order; the last warp done with a stage
         // refills its slot, so no block-wide barrier stalls the ring
         for (int i = 0; i < n; i++) {
-            if (ok && !wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, p.status)) { ok = false; s_bad = 1; }
+            if (ok && expired(i, i)) { ok = false; s_bad = 1; }
             if (i == 0) tl_max(p.tl, 5);
             if (ok && rt < p.nrt) {
                 if (IMPL == 2) stage_mma<NA, GemmChains<NT>::v>(stage(i), warp, lane, act_off, sum_off, swz, acc);
@@ -521,9 +535,9 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     } else
     for (int i = 0; i < n; i += 2) {
         const bool two = i + 1 < n;
-        if (ok && !wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, p.status)) { ok = false; s_bad = 1; }
+        if (ok && expired(i, i)) { ok = false; s_bad = 1; }
         if (i == 0) tl_max(p.tl, 5);
-        if (two && ok && !wait_stage(&full[(i + 1) % D], (uint32_t)((i + 1) / D) & 1u, p.status)) {
+        if (two && ok && expired(i + 1, i + 1)) {
             ok = false;
             s_bad = 1;
         }
@@ -547,7 +561,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     }
     tl_max(p.tl, 6);
     const bool bad = s_bad != 0;
-    if (bad) {   // drain the last D issued stages, which may still be in flight (bounded); the result is abandoned
+    if (bad) {   // drain the last D issued stages, which may still be in flight (full bound); the result is abandoned
         if (threadIdx.x == 0)
             for (int i = max(0, s_issued - D); i < s_issued; i++) wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, nullptr);
         __syncthreads();
@@ -806,7 +820,7 @@ cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaSt
 // --------------------------------------------------------- argmax final ---
 __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *__restrict__ idxs,
                                     int nparts, int B, int32_t *ids, const int32_t *positions,
-                                    int32_t *len_dev, unsigned long long *tl) {
+                                    int32_t *len_dev, const uint32_t *status, unsigned long long *tl) {
     tl_min(tl, 0);
     pdl_launch_dependents();
     pdl_wait();
@@ -833,16 +847,17 @@ __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *_
         for (int w = 1; w < (int)(blockDim.x >> 5); w++)
             if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
         ids[b] = bi == 0x7FFFFFFF ? 0 : bi;
-        len_dev[b] = positions[b] + 1;
+        // the length advances only for a step no device check has flagged
+        if ((*(volatile const uint32_t *)status & STATUS_STATE_ERRORS) == 0) len_dev[b] = positions[b] + 1;
         tl_end(tl);
     }
 }
 
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
                                 int32_t *ids, const int32_t *positions, int32_t *len_dev,
-                                bool pdl, cudaStream_t stream, unsigned long long *tl) {
+                                const uint32_t *status, bool pdl, cudaStream_t stream, unsigned long long *tl) {
     return launch_k(argmax_final_kernel, dim3(B), dim3(256), 0, pdl, 1, stream, amax_val, amax_idx,
-                    nparts, B, ids, positions, len_dev, tl);
+                    nparts, B, ids, positions, len_dev, status, tl);
 }
 
 }  // namespace zdec

@@ -110,6 +110,7 @@ struct zdec_ctx {
     int gemm_impl = 0, matvec_max_B = 0;
     int b1_impl = 3;                   // projection kernel at B = 1 (ZDEC_B1_IMPL)
     size_t prefetch_cap = 0;   // bytes of the next matrix a GEMM warms in L2 (0: off; ZDEC_L2_PREFETCH_MB)
+    long long wait_limit = 0;  // projection stage-wait bound in clock cycles (0: the kernels' ~2 s)
     std::map<std::tuple<int, const void *, int>, cudaGraphExec_t> graphs;
     std::string err;
     int last_kernels = 0, last_splits = 0;
@@ -693,6 +694,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     gp.Bp = Bp;
     gp.out_Bp = Bp;
     gp.status = ctx->status;
+    gp.wait_limit = ctx->wait_limit;
     gp.pipe = gemm_pipe_mode();
     // Every projection takes its activation as fp16 hi + lo planes (~22 bits):
     // the new K/V rows are rounded and quantized, and over dozens of layers a
@@ -781,7 +783,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
     STEP(ZDEC_KERNEL_GEMM_LMHEAD, (gp.tl = tlk, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s)));
     STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, n_groups(ctx->nrt_vocab), B, ctx->ids_dev,
-                                                 ctx->pos_dev, ctx->len_dev, pdl, s, tlk));
+                                                 ctx->pos_dev, ctx->len_dev, ctx->status, pdl, s, tlk));
 #undef STEP
     ctx->last_kernels = nk;
     ctx->last_splits = ap.cs;
@@ -979,11 +981,26 @@ extern "C" zdec_status zdec_sync(zdec_ctx *ctx) {
     if (st) {
         uint32_t zero = 0;
         CK(cudaMemcpy(ctx->status, &zero, 4, cudaMemcpyHostToDevice));
+        // the flagged steps advanced no device length, while the host mirror
+        // counted every step it enqueued: take the device's lengths back
+        std::vector<int32_t> len(ctx->max_B);
+        CK(cudaMemcpy(len.data(), ctx->len_dev, ctx->max_B * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        for (int b = 0; b < ctx->max_B; b++) ctx->len_host[b] = len[b];
         if (st & STATUS_TIMEOUT) return fail(ctx, ZDEC_ERR_TIMEOUT, "a bounded device wait gave up");
         return fail(ctx, ZDEC_ERR_DEVICE, "device check failed (status 0x%x:%s%s)", st,
                     (st & STATUS_POSITION) ? " position != cached length" : "",
                     (st & STATUS_TOKEN) ? " token outside the vocabulary" : "");
     }
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_debug_set_wait_limit(zdec_ctx *ctx, long long cycles) {
+    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
+    if (cycles < -1) return fail(ctx, ZDEC_ERR_ARG, "cycles must be >= -1");
+    CK(cudaStreamSynchronize(ctx->stream));
+    for (auto &kv : ctx->graphs) cudaGraphExecDestroy(kv.second);   // they captured the old bound
+    ctx->graphs.clear();
+    ctx->wait_limit = cycles;
     return ZDEC_OK;
 }
 
@@ -1245,22 +1262,29 @@ extern "C" size_t zdec_q4k_gemm_workspace_bytes(int K, int B) {
     return 2 * plane + (size_t)(K / QK) * B * 16 * 2 + 256;
 }
 
-extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B, float *y_dev,
-                                     int impl, void *workspace_dev, size_t workspace_bytes, void *stream) {
+// Argument checks shared by the two stateless projection entry points.
+static zdec_status check_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B,
+                                  const float *y_dev, int impl) {
     zdec_ctx *ctx = nullptr;
-    if (!repacked_dev || !x_dev || !y_dev || !workspace_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
+    if (!repacked_dev || !x_dev || !y_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
     if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
     if (B < 1 || B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "B must be in [1, %d]", MAX_B);
     if (impl < 1 || impl > 3) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1, 2 or 3");
     if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
     if (impl == 3 && B != 1) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "impl 3 handles B = 1");
-    if (workspace_bytes < zdec_q4k_gemm_workspace_bytes(K, B)) return fail(ctx, ZDEC_ERR_ARG, "workspace too small");
-    if ((uintptr_t)workspace_dev % 16 || (uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "pointers must be 16-byte aligned");
+    if ((uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "x_dev must be 16-byte aligned");
+    return ZDEC_OK;
+}
+
+// The projection itself on checked arguments, with its scratch (hi plane, lo
+// plane, sub-block sums; zdec_q4k_gemm_workspace_bytes(K, B) bytes) at `scratch`.
+static zdec_status run_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B, float *y_dev,
+                                int impl, void *scratch, cudaStream_t s) {
+    zdec_ctx *ctx = nullptr;
     const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
-    __half *hi = (__half *)workspace_dev;
-    __half *lo = (__half *)((uint8_t *)workspace_dev + plane);
-    __half *sums = (__half *)((uint8_t *)workspace_dev + 2 * plane);
-    cudaStream_t s = (cudaStream_t)stream;
+    __half *hi = (__half *)scratch;
+    __half *lo = (__half *)((uint8_t *)scratch + plane);
+    __half *sums = (__half *)((uint8_t *)scratch + 2 * plane);
     CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, B, hi, lo, sums, false, s));
     GemmParams gp{};
     gp.W = (const uint8_t *)repacked_dev;
@@ -1278,6 +1302,17 @@ extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, con
     gp.pipe = gemm_pipe_mode();
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B, float *y_dev,
+                                     int impl, void *workspace_dev, size_t workspace_bytes, void *stream) {
+    zdec_ctx *ctx = nullptr;
+    zdec_status st = check_q4k_gemm(repacked_dev, N, K, x_dev, B, y_dev, impl);
+    if (st != ZDEC_OK) return st;
+    if (!workspace_dev) return fail(ctx, ZDEC_ERR_ARG, "null workspace");
+    if (workspace_bytes < zdec_q4k_gemm_workspace_bytes(K, B)) return fail(ctx, ZDEC_ERR_ARG, "workspace too small");
+    if ((uintptr_t)workspace_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "pointers must be 16-byte aligned");
+    return run_q4k_gemm(repacked_dev, N, K, x_dev, B, y_dev, impl, workspace_dev, (cudaStream_t)stream);
 }
 
 // ------------------------------------------------- allocation-free GEMM ---
@@ -1303,18 +1338,13 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int K, const float *x_dev, int B,
                                             float *y_dev, int impl, void *stream) {
     zdec_ctx *ctx = nullptr;
-    if (!repacked_dev || !x_dev || !y_dev) return fail(ctx, ZDEC_ERR_ARG, "null pointer");
-    if (N <= 0 || N % 16 || K <= 0 || K % 512) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "N must be a multiple of 16 and K of 512");
-    if (B < 1 || B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "B must be in [1, %d]", MAX_B);
-    if (impl < 1 || impl > 3) return fail(ctx, ZDEC_ERR_ARG, "impl must be 1, 2 or 3");
-    if (impl == 1 && B > 4) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the matvec handles B <= 4");
-    if (impl == 3 && B != 1) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "impl 3 handles B = 1");
+    zdec_status st = check_q4k_gemm(repacked_dev, N, K, x_dev, B, y_dev, impl);
+    if (st != ZDEC_OK) return st;
     if ((long long)K * B > ZDEC_Q4K_GEMM_STATIC_MAX_KB)
         return fail(ctx, ZDEC_ERR_ARG,
                     "K*B = %lld exceeds the static scratch of zdec_q4k_gemm_static (K*B <= %d); "
                     "use zdec_q4k_gemm with a caller workspace",
                     (long long)K * B, ZDEC_Q4K_GEMM_STATIC_MAX_KB);
-    if ((uintptr_t)x_dev % 16) return fail(ctx, ZDEC_ERR_ARG, "x_dev must be 16-byte aligned");
     int dev = 0;
     CK(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kStaticMaxDevices) return fail(ctx, ZDEC_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
@@ -1324,26 +1354,5 @@ extern "C" zdec_status zdec_q4k_gemm_static(const void *repacked_dev, int N, int
         if (!g_static_addr[dev]) CK(cudaGetSymbolAddress(&g_static_addr[dev], g_static_scratch));
         base = g_static_addr[dev];
     }
-    const size_t plane = align_up((size_t)(K / QK) * B * 256 * 2, 256);
-    __half *hi = (__half *)base;
-    __half *lo = (__half *)((uint8_t *)base + plane);
-    __half *sums = (__half *)((uint8_t *)base + 2 * plane);
-    cudaStream_t s = (cudaStream_t)stream;
-    CK(launch_prep(x_dev, K, K, nullptr, 0.0f, B, B, hi, lo, sums, false, s));
-    GemmParams gp{};
-    gp.W = (const uint8_t *)repacked_dev;
-    gp.N = N;
-    gp.nrt = N / 16;
-    gp.nsb = K / QK;
-    gp.x16 = hi;
-    gp.x16lo = lo;
-    gp.sx = sums;
-    gp.B = B;
-    gp.Bp = B;
-    gp.out = y_dev;
-    gp.ldo = N;
-    gp.cs = pick_cs(n_groups(N / 16), K / QK, [&](int cs) { return gemm_cluster_slots(B, impl, EPI_STORE, cs); });
-    gp.pipe = gemm_pipe_mode();
-    CK(launch_gemm(gp, EPI_STORE, impl, false, s));
-    return ZDEC_OK;
+    return run_q4k_gemm(repacked_dev, N, K, x_dev, B, y_dev, impl, base, (cudaStream_t)stream);
 }

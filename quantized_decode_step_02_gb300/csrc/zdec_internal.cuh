@@ -302,6 +302,9 @@ __device__ __forceinline__ void tl_max(unsigned long long *tl, int k) {
 
 // ------------------------------------------------------- device status ---
 enum : uint32_t { STATUS_POSITION = 1u, STATUS_CAPACITY = 2u, STATUS_TIMEOUT = 4u, STATUS_TOKEN = 8u };
+// Any of these makes the step (and every later step until the host clears the
+// word) leave the KV cache and the device lengths untouched.
+constexpr uint32_t STATUS_STATE_ERRORS = STATUS_POSITION | STATUS_CAPACITY | STATUS_TIMEOUT | STATUS_TOKEN;
 
 
 }  // namespace zdec

@@ -71,6 +71,9 @@ struct GemmParams {
     const uint8_t *pf_ptr; // read-only bytes the next kernel streams (L2 prefetch), or null
     size_t pf_bytes;       // multiple of 16, pf_ptr 16-byte aligned
     uint32_t *status;      // device status word (bounded-wait timeouts)
+    long long wait_limit;  // clock cycles a stage wait may take before it gives up (0: ~2 s;
+                           // < 0: the first stage wait gives up at once, for tests); the drain
+                           // of copies in flight after a give-up always takes the full bound
     unsigned long long *tl;   // launch timeline slot (zdec_internal.cuh) or null
     // STORE of a QKV projection: the query heads (groups < q_heads, one 128-row
     // group each) also go out rotated (RoPE at q_pos[b]), scaled by log2(e)/sqrt(128)
@@ -94,10 +97,12 @@ int gemm_cluster_slots(int B, int impl, int epi, int cs);
 cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B, int Bp,
                         __half *hi, __half *lo, __half *sums, bool pdl, cudaStream_t stream);
 // ids[b] = argmax over the per-CTA partials (lowest index on ties); also
-// advances the device lengths: len_dev[b] = positions[b] + 1.
+// advances the device lengths, len_dev[b] = positions[b] + 1, unless the
+// status word holds an error (then the step changes no length).
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
                                 int32_t *ids, const int32_t *positions, int32_t *len_dev,
-                                bool pdl, cudaStream_t stream, unsigned long long *tl = nullptr);
+                                const uint32_t *status, bool pdl, cudaStream_t stream,
+                                unsigned long long *tl = nullptr);
 
 // ---------------------------------------------------------- attention.cu
 struct KvArena {

@@ -2,6 +2,8 @@
 from __future__ import annotations
 
 import functools
+import json
+import os
 
 import numpy as np
 import pytest
@@ -39,3 +41,16 @@ needs_cuda = pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")
 def cached_model(desc, seed):
     from synth.model import make_model
     return make_model(desc, seed)
+
+
+def record_margin(tag: str, hidden_err: float, logits_err: float, ids_checked: int, rows: int):
+    """Print a parity check's worst normwise errors (and append them as a JSON
+    line to $ZDEC_MARGINS_FILE when that is set)."""
+    rec = {"case": tag, "worst_hidden": hidden_err, "worst_logits": logits_err, "tol": TOL,
+           "ids_checked": ids_checked, "rows": rows}
+    print(f"[margin] {tag}: hidden {hidden_err:.3g} logits {logits_err:.3g} (tol {TOL:g}), "
+          f"ids checked {ids_checked}/{rows}")
+    path = os.environ.get("ZDEC_MARGINS_FILE")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from synth.model import ModelDesc, make_kv_history, make_tokens
-from tests.helpers import GAP, TOL, cached_model, gpu, needs_cuda, normwise, top2_gap
+from tests.helpers import GAP, TOL, cached_model, gpu, needs_cuda, normwise, record_margin, top2_gap
 
 pytestmark = [gpu, needs_cuda]
 
@@ -39,19 +39,30 @@ def setup_pair(d, w, seed, lengths, kv_dtype, max_L):
 
 
 def check_step(dec, om, kvs, tokens, positions, tag=""):
+    """One host-I/O step through the C ABI against the oracle's step: every
+    row's residual after the embedding and after each layer and its logits
+    within TOL (normwise), ids equal where the oracle's top-2 gap exceeds GAP.
+    The worst errors go to record_margin (printed, and kept in a file when
+    ZDEC_MARGINS_FILE is set)."""
     B = len(tokens)
     logits = np.empty((B, dec.desc.vocab), np.float32)
     _, ids, hid = dec.step_capture_hidden(tokens, positions, logits)
     rl, rid, rhid = oracle.decode_step(om, kvs, tokens, positions, capture_hidden=True)
     gaps = top2_gap(rl)
+    worst_h = worst_l = 0.0
+    n_ids = 0
     for b in range(B):
         for l in range(hid.shape[1]):
             err = normwise(hid[b, l], rhid[b, l])
+            worst_h = max(worst_h, err)
             assert err <= TOL, f"{tag} row {b} layer {l}: hidden error {err:.3g}"
         err = normwise(logits[b], rl[b])
+        worst_l = max(worst_l, err)
         assert err <= TOL, f"{tag} row {b}: logits error {err:.3g}"
         if gaps[b] > GAP:
+            n_ids += 1
             assert ids[b] == rid[b], f"{tag} row {b}: id {ids[b]} != oracle {rid[b]} (gap {gaps[b]:.3g})"
+    record_margin(tag, worst_h, worst_l, n_ids, B)
     return logits, ids, rl, rid
 
 
@@ -190,16 +201,51 @@ def test_device_io_step_and_position_checks():
         dec.step_host(np.array([1, 2], np.int32), np.array([13, 5], np.int32))
     assert e.value.status == -4
     assert dec.seq_len(0) == 13 and dec.seq_len(1) == 4
-    # device inputs: the first kernel checks positions, zdec_sync reports it
+    # device inputs: the first kernel checks positions (row 1 is wrong but in
+    # range), the step writes no KV row and advances no length, and
+    # zdec_sync reports it
+    before = [dec.read_kv(b, l, 0, 32) for b in range(2) for l in range(d.n_layers)]
     bad = torch.tensor([13, 9], dtype=torch.int32, device=dev)
     dec.step(toks, bad, logits, ids)
     with pytest.raises(z.ZdecError) as e:
         dec.sync()
     assert e.value.status == -8
     dec.sync()   # the status was cleared
+    assert dec.seq_len(0) == 13 and dec.seq_len(1) == 4
+    after = [dec.read_kv(b, l, 0, 32) for b in range(2) for l in range(d.n_layers)]
+    for x, y in zip(before, after):
+        assert all(np.array_equal(u, v) for u, v in zip(x, y))
+    # the next correct step is the oracle's step at the unchanged lengths
+    check_step(dec, om, kvs, make_tokens(d, 1051, 2), np.array([13, 4], np.int32), "after a flagged step")
     with pytest.raises(z.ZdecError) as e:
-        dec.step_host(np.array([d.vocab], np.int32), np.array([14, 5], np.int32))
+        dec.step_host(np.array([d.vocab], np.int32), np.array([14], np.int32))
     assert e.value.status == -1
+    dec.close()
+
+
+def test_wait_that_runs_out_reports_timeout_and_changes_nothing():
+    """Every projection's first stage wait gives up at once (the debug bound
+    -1): the kernels record the timeout, wait for their own copies in flight
+    and return; the step writes no KV row and advances no length; sync
+    reports ZDEC_ERR_TIMEOUT; with the default bound back, the next step
+    matches the oracle."""
+    d = SMALL
+    w = cached_model(d, 111)
+    lengths = [40, 7]
+    dec, om, kvs = setup_pair(d, w, 111, lengths, 1, 64)
+    dec.set_engine(z.ENGINE_KERNELS)
+    before = [dec.read_kv(b, l, 0, 64) for b in range(2) for l in range(d.n_layers)]
+    dec.set_wait_limit(-1)
+    for eager in (True, False):   # launched directly and from a captured graph
+        with pytest.raises(z.ZdecError) as e:
+            dec.step_host(make_tokens(d, 1110, 2), np.array(lengths, np.int32), eager=eager)
+        assert e.value.status == -7
+        assert [dec.seq_len(b) for b in range(2)] == lengths
+    after = [dec.read_kv(b, l, 0, 64) for b in range(2) for l in range(d.n_layers)]
+    for x, y in zip(before, after):
+        assert all(np.array_equal(u, v) for u, v in zip(x, y))
+    dec.set_wait_limit(0)
+    check_step(dec, om, kvs, make_tokens(d, 1111, 2), np.array(lengths, np.int32), "after a timeout")
     dec.close()
 
 
@@ -333,6 +379,13 @@ def test_full_step_b8_l2400_fp16_and_batch_invariance():
         _, id1 = d1.step_host(toks[b:b + 1], np.array([2400], np.int32))
         assert id1[0] == ids8[b]
         d1.close()
+
+
+@pytest.mark.slow
+def test_full_step_b1_l8192_q8_0():
+    """The 36-layer model at B = 1 over an 8k Q8_0 cache (the sub-block-column
+    projection kernel and the batch-of-one attention split)."""
+    _full_config(4, 1, [8192], 1, n_steps=2)
 
 
 @pytest.mark.slow
