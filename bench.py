@@ -11,11 +11,9 @@ resident in HBM.  Every step streams ~5 GB (weights + KV), far more than the
 129 MB L2, so no explicit flush is needed.
 e2e: the same metric through the C ABI with host buffers (token ids and
 positions copied in, argmax ids copied out, every step).
-roofline: the persistent engine runs the step as one kernel, whose
-algorithmic bytes (weights once, every KV byte, embedding rows, logits) are
-divided by the per-step time of the timed region; the kernel engine reports
-its dominant kernel kind (largest total time in one profiled eager step).
-Both against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
+roofline: the dominant kernel kind (largest total time in one profiled
+eager step): its algorithmic bytes per launch over its mean CUDA-event
+launch time, against the measured HBM copy bandwidth in MEASURED_PEAKS.json.
 cpu_baseline: the CPU oracle (plain C, fp64, OpenMP) on a bounded sample.
 
 --impl reference times that oracle, as it stands, on the same workload.
@@ -39,7 +37,22 @@ import numpy as np  # noqa: E402
 from synth.model import FULL, ModelDesc, make_kv_history, make_model, make_tokens  # noqa: E402
 
 METRIC = "aggregate decode tok/s"
-KV_BYTES_PER_ELEM = {"f16": 2.0, "q8_0": 34.0 / 32.0}
+KV_BYTES_PER_ELEM = {"f16": 2.0, "q8_0": 34.0 / 32.0, "fp8": 1.0}
+KV_CODE = {"f16": 0, "q8_0": 1, "fp8": 2}
+
+
+def kv_types(kv: str):
+    """'t' (both tensors) or 'k_type:v_type' -> (k, v) type names."""
+    parts = kv.split(":")
+    k, v = (parts[0], parts[0]) if len(parts) == 1 else (parts[0], parts[1])
+    if k not in KV_CODE or v not in KV_CODE:
+        raise ValueError(f"bad KV type {kv!r}: use f16, q8_0, fp8 or K:V")
+    return k, v
+
+
+def kv_codes(kv: str):
+    k, v = kv_types(kv)
+    return KV_CODE[k], KV_CODE[v]
 
 
 def args_parse():
@@ -50,11 +63,11 @@ def args_parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--B", type=int, default=1)
     p.add_argument("--L", type=int, default=2048)
-    p.add_argument("--kv", default="f16", choices=["f16", "q8_0"])
+    p.add_argument("--kv", default="f16", help="cache type of K and V (f16, q8_0, fp8) or K:V, e.g. q8_0:f16")
+    p.add_argument("--lengths", default=None,
+                   help="comma-separated cached tokens per row (a ragged batch; overrides --B and --L)")
     p.add_argument("--seed", type=int, default=1)
     p.add_argument("--gemm-impl", type=int, default=0, help="0 auto, 1 matvec, 2 mma")
-    p.add_argument("--engine", default="auto", choices=["auto", "kernels", "persistent"],
-                   help="persistent: the whole step as one cooperative kernel; kernels: one per operation")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-targets", action="store_true",
@@ -63,7 +76,7 @@ def args_parse():
     p.add_argument("--device-history", action="store_true",
                    help="one seeded device-side N(0,1) KV history shared by the sequences (fast setup)")
     p.add_argument("--layers", type=int, default=None, help="smaller model (profiling runs only)")
-    p.add_argument("--trace", default=None, help="save the phase timeline of one persistent step (.npy)")
+    p.add_argument("--trace", default=None, help="save the launch timeline of one step (.npy)")
     return p.parse_args()
 
 
@@ -97,14 +110,14 @@ def fit_time_model(points):
             "max_rel_residual": float(resid.max()), "points": int(len(t))}
 
 
-def ncu_traffic(engine: str, kind: str, B: int, kv: str, impl: int):
+def ncu_traffic(kind: str, B: int, kv: str, impl: int):
     """DRAM bytes per launch of a kernel kind from a committed ncu capture
     (profiles/ncu_traffic.json), or None when no capture matches."""
     try:
         tab = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))["kernels"]
     except Exception:
         return None
-    key = f"{engine}/{kind}/B{B}/" + (kv if kind == "attention" else f"impl{impl}")
+    key = f"{kind}/B{B}/" + (kv if kind == "attention" else f"impl{impl}")
     return tab.get(key, {}).get("bytes")
 
 
@@ -116,7 +129,8 @@ def peaks():
 
 
 def kv_bytes_per_token(d: ModelDesc, kv: str) -> float:
-    return 2 * d.n_layers * d.n_kv_heads * d.head_dim * KV_BYTES_PER_ELEM[kv]
+    k, v = kv_types(kv)
+    return d.n_layers * d.n_kv_heads * d.head_dim * (KV_BYTES_PER_ELEM[k] + KV_BYTES_PER_ELEM[v])
 
 
 def q4k_bytes(rows, cols):
@@ -132,7 +146,8 @@ def weight_bytes(d: ModelDesc) -> int:
 
 def step_bytes(d: ModelDesc, B: int, L: float, kv: str) -> float:
     """Algorithmic HBM bytes of one step: weights once, each sequence's KV read
-    over L+1 tokens and one token written, embedding rows and logits."""
+    over L+1 tokens and one token written, embedding rows and logits.  L is
+    the mean cached length of the B rows."""
     k = kv_bytes_per_token(d, kv)
     return weight_bytes(d) + B * (L + 2) * k + B * (d.hidden // 256 * 144 + 4 * d.vocab)
 
@@ -152,8 +167,6 @@ def kernel_bytes(d: ModelDesc, kind: str, B: int, L: float, kv: str) -> float:
         return q4k_bytes(H, F) + act(F, 2 * H)
     if kind == "gemm_lmhead":
         return q4k_bytes(d.vocab, H) + act(H, d.vocab)
-    if kind == "step":
-        return step_bytes(d, B, L, kv)
     if kind == "attention":
         per_tok_layer = kv_bytes_per_token(d, kv) / d.n_layers
         return B * (L + 2) * per_tok_layer + B * (qd + 2 * kvd + qd) * 4
@@ -208,8 +221,10 @@ class Clocks:
 
 def workload_config(a, desc, world):
     """The `config` object both arms print (identical keys and values)."""
-    return {"workload": f"decode step B={a.B} L={a.L} {a.kv} KV, {desc.n_layers}-layer GQA Q4_K synthetic model",
+    shape = f"lengths {a.lengths}" if a.lengths else f"L={a.L}"
+    return {"workload": f"decode step B={a.B} {shape} {a.kv} KV, {desc.n_layers}-layer GQA Q4_K synthetic model",
             "B": a.B, "L": a.L, "kv": a.kv, "model_layers": desc.n_layers, "seed": a.seed,
+            "lengths": a.lengths,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "no flush: every step streams >4.7 GB, far larger than the 129 MB L2"}
 
@@ -238,7 +253,7 @@ def oracle_step_sample(desc, w, seed, B, L, kv, budget_s=20.0, max_steps=None):
     import oracle
     od = oracle.Desc(*desc.astuple())
     om = oracle.Model(od, w)
-    kvd = 0 if kv == "f16" else 1
+    kvd = kv_codes(kv)
     nb = 1   # one sequence per sampled step: the oracle computes rows independently
     kvs = []
     steps_possible = max_steps or 64
@@ -287,13 +302,13 @@ def run_reference(a, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def time_steps(dec, B, L, first, n_warm, n_timed, stream, world, desc, seed, logits):
+def time_steps(dec, B, lengths, n_warm, n_timed, stream, world, desc, seed, logits):
     """n_warm untimed then n_timed CUDA-event-timed steps of rows 0..B-1 whose
-    caches hold `first` tokens; returns (ms per step, clock summary)."""
+    caches hold lengths[b] tokens; returns (ms per step, clock summary)."""
     import torch
     n_total = n_warm + n_timed
     toks = [torch.from_numpy(make_tokens(desc, seed * 1000 + i, B)).cuda() for i in range(n_total)]
-    pos = [torch.full((B,), first + i, dtype=torch.int32, device="cuda") for i in range(n_total)]
+    pos = [torch.tensor([n + i for n in lengths], dtype=torch.int32, device="cuda") for i in range(n_total)]
     ids = torch.empty(B, dtype=torch.int32, device="cuda")
     for i in range(n_warm):
         dec.step(toks[i], pos[i], logits, ids)
@@ -315,51 +330,53 @@ def time_steps(dec, B, L, first, n_warm, n_timed, stream, world, desc, seed, log
     return ms, clk.summary()
 
 
-def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=None):
-    """One measured configuration.  dev_hist: (k, v) fp16 CUDA tensors
-    [n_layers][>= L][n_kv][hd] appended to every sequence instead of the seeded
-    host history (the sweep's large points; timing does not depend on values).
-    The timed steps write logits [B][vocab] and ids, as step_bytes counts."""
+def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=None, lengths=None):
+    """One measured configuration: B rows of L cached tokens each (or of
+    `lengths` tokens: a ragged batch).  dev_hist: (k, v) fp16 CUDA tensors
+    [n_layers][>= max L][n_kv][hd] appended to every sequence instead of the
+    seeded host history (timing does not depend on values).  The timed steps
+    write logits [B][vocab] and ids, as step_bytes counts."""
     import torch
     import quantized_decode_step_02_gb300 as z
     stream = torch.cuda.Stream()
+    lengths = list(lengths) if lengths is not None else [L] * B
+    Lmax, Lmean = max(lengths), sum(lengths) / len(lengths)
     extra = a.warmup + a.steps + 4 + (0 if a.no_e2e else a.warmup + a.steps)
-    dec = z.Decoder(desc, w, z.KV_F16 if kv == "f16" else z.KV_Q8_0, max_B=B, max_L=L + extra + 2,
-                    stream=stream.cuda_stream)
+    dec = z.Decoder(desc, w, kv_codes(kv), max_B=B, max_L=Lmax + extra + 2, stream=stream.cuda_stream)
     if a.gemm_impl:
         dec.set_gemm_impl(a.gemm_impl)
-    dec.set_engine({"auto": z.ENGINE_AUTO, "kernels": z.ENGINE_KERNELS, "persistent": z.ENGINE_PERSISTENT}[a.engine])
-    if dev_hist is not None:   # one contiguous copy, alive until the appends have run
-        k, v = dev_hist[0][:, :L].contiguous(), dev_hist[1][:, :L].contiguous()
+    if dev_hist is not None:
         torch.cuda.synchronize()
-        for b in range(B):
+        for b in range(B):   # one contiguous copy each, alive until its append has run
+            k, v = dev_hist[0][:, :lengths[b]].contiguous(), dev_hist[1][:, :lengths[b]].contiguous()
             dec.append_kv(b, k, v)
+            del k, v
         dec.sync()
-        del k, v
     else:
         for b in range(B):
-            k, v = make_kv_history(desc, a.seed, b, L)
+            k, v = make_kv_history(desc, a.seed, b, lengths[b])
             dec.append_kv(b, k, v)
     logits = torch.empty((B, desc.vocab), dtype=torch.float32, device="cuda")
-    ms, clocks = time_steps(dec, B, L, L, a.warmup, a.steps, stream, world, desc, a.seed, logits)
+    ms, clocks = time_steps(dec, B, lengths, a.warmup, a.steps, stream, world, desc, a.seed, logits)
     n_total = a.warmup + a.steps
-    Lmid = L + a.warmup + a.steps / 2
-    res = {"B": B, "L": L, "kv": kv, "ms_per_step": ms, "tok_s": aggregate_tok_s(B, world, ms),
-           "step_bytes": step_bytes(desc, B, Lmid, kv), "kernels_per_step": dec.info()["kernels_per_step"],
-           "engine": ["auto", "kernels", "persistent"][dec.info()["engine"]],
-           "clocks": clocks}
+    Lmid = Lmean + a.warmup + a.steps / 2
+    res = {"B": B, "L": L if len(set(lengths)) == 1 else lengths, "kv": kv, "ms_per_step": ms,
+           "tok_s": aggregate_tok_s(B, world, ms), "step_bytes": step_bytes(desc, B, Lmid, kv),
+           "kernels_per_step": dec.info()["kernels_per_step"], "clocks": clocks,
+           "attn_cluster": dec.info()["attn_splits"], "attn_segments": dec.info()["attn_segments"]}
     res["step_gbs"] = res["step_bytes"] / (ms * 1e-3) / 1e9
     i = n_total
     toks = [torch.from_numpy(make_tokens(desc, a.seed * 1000 + 400 + j, B)).cuda() for j in range(2)]
     ids = torch.empty(B, dtype=torch.int32, device="cuda")
+    at = lambda j: torch.tensor([n + j for n in lengths], dtype=torch.int32, device="cuda")
     if a.trace:   # one traced step (not timed)
         dec.set_trace(True)
-        dec.step(toks[0], torch.full((B,), L + i, dtype=torch.int32, device="cuda"), logits, ids)
+        dec.step(toks[0], at(i), logits, ids)
         np.save(a.trace, dec.step_trace())
         dec.set_trace(False)
         i += 1
     # ---- per-launch profile of one eager step (CUDA events on the library stream)
-    prof = dec.profile_step(toks[1], torch.full((B,), L + i, dtype=torch.int32, device="cuda"), logits, ids)
+    prof = dec.profile_step(toks[1], at(i), logits, ids)
     by_kind = {}
     for kind, t in prof:
         by_kind.setdefault(kind, []).append(t)
@@ -371,7 +388,7 @@ def bench_point(a, desc, w, B, L, kv, rank, world, full_report=True, dev_hist=No
     if not a.no_e2e:
         base = i + 1
         ht = [make_tokens(desc, a.seed * 1000 + 700 + j, B) for j in range(n_total)]
-        hp = [np.full(B, L + base + j, np.int32) for j in range(n_total)]
+        hp = [np.array([n + base + j for n in lengths], np.int32) for j in range(n_total)]
         for j in range(a.warmup):
             dec.step_host(ht[j], hp[j])
         t0 = time.perf_counter()
@@ -401,8 +418,7 @@ def target_grid(a, desc, w, world, hbm_peak):
     n = a.warmup + a.steps
     for kv in ("f16", "q8_0"):
         stream = torch.cuda.Stream()
-        dec = z.Decoder(desc, w, z.KV_F16 if kv == "f16" else z.KV_Q8_0, max_B=8, max_L=Lmax + n + 2,
-                        stream=stream.cuda_stream)
+        dec = z.Decoder(desc, w, kv_codes(kv), max_B=8, max_L=Lmax + n + 2, stream=stream.cuda_stream)
         for L in (2048, 8192):
             k, v = hist[0][:, :L].contiguous(), hist[1][:, :L].contiguous()
             for B in (1, 8):
@@ -413,7 +429,7 @@ def target_grid(a, desc, w, world, hbm_peak):
                     dec.append_kv(b, k, v)
                 dec.sync()
                 logits = torch.empty((B, desc.vocab), dtype=torch.float32, device="cuda")
-                ms, clk = time_steps(dec, B, L, L, a.warmup, a.steps, stream, world, desc, a.seed, logits)
+                ms, clk = time_steps(dec, B, [L] * B, a.warmup, a.steps, stream, world, desc, a.seed, logits)
                 sb = step_bytes(desc, B, L + a.warmup + a.steps / 2, kv)
                 gbs = sb / (ms * 1e-3) / 1e9
                 cells.append({"B": B, "L": L, "kv": kv, "ms_per_step": round(ms, 4),
@@ -452,7 +468,7 @@ def main():
         # B x L x kv grid on a seeded device-side N(0,1) history (one per L,
         # shared by the sequences), then the projection-kernel switch point
         hist = device_history(32768)
-        for kv in ("f16", "q8_0"):
+        for kv in ("f16", "q8_0", "fp8"):
             pts = []
             for B in (1, 4, 8, 16, 32):
                 for L in (2048, 8192, 16384, 32768):
@@ -472,30 +488,26 @@ def main():
                                       "profile_ms": r["profile_ms"]}), flush=True)
         a.gemm_impl = 0
         return
-    r = bench_point(a, desc, w, a.B, a.L, a.kv, rank, world,
-                    dev_hist=device_history(a.L) if a.device_history else None)
+    lengths = [int(x) for x in a.lengths.split(",")] if a.lengths else None
+    if lengths:
+        a.B, a.L = len(lengths), int(round(sum(lengths) / len(lengths)))
+    r = bench_point(a, desc, w, a.B, a.L, a.kv, rank, world, lengths=lengths,
+                    dev_hist=device_history(max(lengths) if lengths else a.L) if a.device_history else None)
     if rank != 0:
         return
     pk = peaks() or {}
     hbm_peak = pk.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in pk else "fallback"
     prof = r["profile_ms"]
-    if "step" in prof:
-        # persistent engine: the step kernel is the step; its duration is taken
-        # from the timed region itself (K graph replays of input check + step
-        # kernel), which charges the small check kernel and launch gaps to it
-        dom, launch_ms, launches = "step", r["ms_per_step"], 1
-        Lmid = a.L + (a.warmup + a.steps) / 2.0
-    else:
-        dom = max((k for k in prof if k.startswith("gemm") or k == "attention"), key=lambda k: prof[k]["total_ms"])
-        launch_ms, launches = prof[dom]["avg_ms"], prof[dom]["launches"]
-        Lmid = a.L + a.warmup + a.steps + 0.5
+    dom = max((k for k in prof if k.startswith("gemm") or k == "attention"), key=lambda k: prof[k]["total_ms"])
+    launch_ms, launches = prof[dom]["avg_ms"], prof[dom]["launches"]
+    Lmid = a.L + a.warmup + a.steps + 0.5
     kb = kernel_bytes(desc, dom, a.B, Lmid, a.kv)
     achieved = kb / (launch_ms * 1e-3) / 1e9
     impl = a.gemm_impl or (3 if a.B == 1 else 2)
     roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved / hbm_peak, "peak_source": peak_src,
-            "traffic": ncu_traffic(r["engine"], dom, a.B, a.kv, impl),
+            "traffic": ncu_traffic(dom, a.B, a.kv, impl),
             "bytes_per_launch": kb, "avg_launch_ms": launch_ms, "launches_per_step": launches}
     targets = None
     if not a.no_targets and a.layers is None and world == 1:
@@ -516,7 +528,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "q4_k weights, f16 activations, f32 accumulate",
             "data": "synthetic (seeded N(0,0.02) weights quantized to Q4_K, N(0,1) fp16 KV history)",
             "config": workload_config(a, desc, world),
-            "step": {"engine": r["engine"], "bytes": r["step_bytes"], "hbm_gbs": r["step_gbs"],
+            "step": {"bytes": r["step_bytes"], "hbm_gbs": r["step_gbs"],
+                     "lengths": lengths, "attn_cluster": r["attn_cluster"], "attn_segments": r["attn_segments"],
                      "frac_of_measured_hbm": r["step_gbs"] / hbm_peak, "frac_of_8tbs": r["step_gbs"] / 8000.0,
                      "bytes_counted": "weights once + per sequence (L+2) KV tokens + embedding row + fp32 logits "
                                       "(the timed steps write logits)",

@@ -3,7 +3,8 @@
  *
  * The operation: one decode step of a grouped-query-attention decoder for B
  * sequences at once.  The Q4_K weight stream is read once per step and shared
- * by all B sequences; each sequence reads its own KV cache (fp16 or Q8_0).
+ * by all B sequences; each sequence reads its own KV cache (fp16, Q8_0 or FP8
+ * e4m3, chosen separately for K and V) from a paged pool.
  * Source: the blog pages "Eight concurrent agents pull 5.6x more tokens from
  * one RX 9070 XT" (sections "The weight read is the only term that does not
  * scale", "RDNA4 pads the batch dimension to 16"), "Batched swarm: the KV read
@@ -17,13 +18,13 @@
  *     failure zdec_last_error(ctx) holds a message (per context; calls that
  *     take no context report through zdec_last_global_error()).
  *   - A failed call changes no state unless its comment says otherwise.
- *   - All GPU work is enqueued on the CUDA stream given to zdec_create (or,
- *     for the stateless op entry points, on the stream argument; NULL means
- *     the legacy default stream).  Calls are asynchronous unless noted.
+ *   - All GPU work is enqueued on the CUDA stream given at create (or, for
+ *     the stateless op entry points, on the stream argument; NULL means the
+ *     legacy default stream).  Calls are asynchronous unless noted.
  *   - "dev" pointers are CUDA device pointers; "host" pointers are ordinary
  *     (pageable or pinned) host memory.  The library never frees caller
  *     memory and never keeps caller pointers past the call, except the
- *     output pointers of zdec_decode_step, which it writes asynchronously.
+ *     output pointers of a decode step, which it writes asynchronously.
  *   - fp16 means IEEE binary16 bit patterns (uint16_t).
  */
 #ifndef ZDEC_H
@@ -40,15 +41,27 @@ typedef enum {
     ZDEC_OK = 0,
     ZDEC_ERR_ARG = -1,          /* bad argument: null pointer, out-of-range index, bad shape  */
     ZDEC_ERR_OOM = -2,          /* device or host allocation failed; nothing was created        */
-    ZDEC_ERR_CAPACITY = -3,     /* the sequence would exceed max_L tokens                      */
-    ZDEC_ERR_POSITION = -4,     /* positions[b] != number of tokens cached for sequence b      */
+    ZDEC_ERR_CAPACITY = -3,     /* a sequence would exceed max_L, or the KV pool has no page   */
+    ZDEC_ERR_POSITION = -4,     /* positions[b] != number of tokens cached for row b's slot    */
     ZDEC_ERR_UNSUPPORTED = -5,  /* shape outside what the kernels implement (see zdec_create)  */
     ZDEC_ERR_CUDA = -6,         /* a CUDA runtime call failed; message has cudaGetErrorString  */
     ZDEC_ERR_TIMEOUT = -7,      /* a bounded device wait gave up (reported by zdec_sync)       */
     ZDEC_ERR_DEVICE = -8        /* a device-side check flagged an error (reported by zdec_sync) */
 } zdec_status;
 
-typedef enum { ZDEC_KV_F16 = 0, ZDEC_KV_Q8_0 = 1 } zdec_kv_dtype;
+/* Storage type of a cached tensor (K or V), per "Q8 KV cache pushes an RDNA4
+ * swarm crossover from 5k to 10k tokens", section "Why Q8 is close to free
+ * and where the sharp edges are" (independent K and V cache types) and
+ * "Batched swarm: the KV read does not amortize", section "What a
+ * long-running swarm should actually tune" (fp8 or int8 KV):
+ *   F16   2 bytes per element.
+ *   Q8_0  32-element blocks: one fp16 scale d = fp16(amax/127) (IEEE fp32
+ *         division) and 32 int8 codes clamp(rint(x/d), -127, 127), ties to
+ *         even, dividing by the fp32 d; an all-zero block stores 0 and 0.
+ *         34 bytes per 32 elements.
+ *   FP8   e4m3 (4 exponent bits, bias 7, 3 mantissa bits), nearest value,
+ *         ties to the even code, saturating at +-448; 1 byte per element. */
+typedef enum { ZDEC_KV_F16 = 0, ZDEC_KV_Q8_0 = 1, ZDEC_KV_FP8 = 2 } zdec_kv_dtype;
 
 /* Model shape.  Supported: hidden and ffn multiples of 512, n_q_heads*head_dim
  * a multiple of 512, head_dim == 128, n_q_heads/n_kv_heads == 4 (the grouped
@@ -81,21 +94,39 @@ typedef struct {
     const void *const *w_gate, *const *w_up, *const *w_down;
 } zdec_weights;
 
+/* The KV cache of a context.  Its memory is a pool of pages of 64 tokens
+ * (every layer and kv head, K and V); each sequence slot owns a block table
+ * of pages, taken from the pool as the slot grows and returned by
+ * zdec_reset_seq, so slots of very different lengths share one budget
+ * ("Eight concurrent agents pull 5.6x more tokens from one RX 9070 XT",
+ * section "Where it stops, and the argument I got wrong in May": agents hold
+ * 800 to 30,000 tokens and VRAM, not arithmetic, bounds the swarm). */
+typedef struct {
+    int k_type;              /* zdec_kv_dtype of K                                     */
+    int v_type;              /* zdec_kv_dtype of V                                     */
+    int max_B;               /* sequence slots, also the largest batch of a step (<= 32) */
+    int max_L;               /* tokens one slot may hold                               */
+    long long pool_tokens;   /* pool capacity in tokens, rounded up to whole pages
+                                (0: max_B slots of max_L tokens each)                  */
+} zdec_cache_desc;
+
 typedef struct zdec_ctx zdec_ctx;
 
 /* Create a decoder: validate the shape, allocate on the current CUDA device
+ * (repacked weights ~0.5625 B/weight, the KV pool, the block tables, the
+ * per-step workspace), repack the weights on the GPU and wait for it.
  * Defined by: "Eight concurrent agents pull 5.6x more tokens from one RX 9070
  * XT", sections "The weight read is the only term that does not scale" (one
  * copy of the weights, shared by every sequence of a step) and "Where it
  * stops, and the argument I got wrong in May" (the KV budget, not the
- * arithmetic, bounds how many sequences fit: max_B x max_L tokens).
- *
- * (repacked weights ~0.5625 B/weight, the KV arena of max_B x max_L tokens,
- * the per-step workspace), repack the weights on the GPU and wait for it.
- * kv_dtype fixes the cache format: F16 (2 B/element) or Q8_0 (32-element
- * blocks: 32 int8 codes + one fp16 scale).  max_B <= 32.  cuda_stream is a
- * cudaStream_t (NULL: a new non-blocking stream owned by the context).
- * Returns ZDEC_ERR_OOM (nothing allocated is kept) if the arena does not fit. */
+ * arithmetic, bounds how many sequences fit).
+ * cuda_stream is a cudaStream_t (NULL: a new non-blocking stream owned by the
+ * context).  Returns ZDEC_ERR_OOM (nothing allocated is kept) if the pool does
+ * not fit; ZDEC_ERR_ARG for a bad type, max_B outside [1, 32], max_L < 1 or
+ * pool_tokens < 0. */
+zdec_status zdec_create_cache(const zdec_model_desc *desc, const zdec_weights *weights,
+                              const zdec_cache_desc *cache, void *cuda_stream, zdec_ctx **out);
+/* Shorthand: one type for K and V, a pool of max_B x max_L tokens. */
 zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights,
                         zdec_kv_dtype kv_dtype, int max_B, int max_L, void *cuda_stream,
                         zdec_ctx **out);
@@ -103,16 +134,15 @@ void zdec_destroy(zdec_ctx *ctx);
 
 /* Defined by: "Q8 KV cache pushes an RDNA4 swarm crossover from 5k to 10k
  * tokens", sections "The crossover is just a byte count" (the cache holds K
- * and V of every cached token, fp16 or one byte per element) and "Why Q8 is
- * close to free and where the sharp edges are" (the cache is quantized where
- * it is written).
- * Append n_tokens already-rotated K/V rows to sequence `seq`, starting at its
- * current length.  k_f16 / v_f16: [n_layers][n_tokens][n_kv_heads][head_dim]
- * fp16, host memory (on_device = 0; the call waits for the copy) or device
- * memory (on_device = 1; asynchronous).  A Q8_0 cache quantizes every
- * 32-element block on write: amax = max|x|, d = amax/127 (fp32 division),
- * scale = fp16(d), code = clamp(rint(x/d), -127, 127) (ties to even), all-zero
- * blocks store scale 0.  ZDEC_ERR_CAPACITY if len + n_tokens > max_L. */
+ * and V of every cached token) and "Why Q8 is close to free and where the
+ * sharp edges are" (the cache is quantized where it is written).
+ * Append n_tokens already-rotated K/V rows to sequence slot `seq`, starting at
+ * its current length, taking pool pages as needed.  k_f16 / v_f16:
+ * [n_layers][n_tokens][n_kv_heads][head_dim] fp16, host memory (on_device = 0)
+ * or device memory (on_device = 1); the call waits for the copy either way.
+ * Each tensor is encoded on write by its type (zdec_kv_dtype).
+ * ZDEC_ERR_CAPACITY if len + n_tokens > max_L or the pool lacks pages (nothing
+ * is appended and no page is taken). */
 zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f16,
                            const void *v_f16, int on_device);
 
@@ -126,7 +156,7 @@ zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f
  * in-flight sequences by one token each per step, reading the weights once)
  * and "Batched swarm: the KV read does not amortize", section "The two halves
  * of a decode-step memory bill" (each sequence reads its own KV cache).
- * One decode step for sequences (slots) 0..B-1, B <= max_B.
+ * One decode step for rows b = 0..B-1, row b being sequence slot b, B <= max_B.
  *   tokens [B] int32 token ids, positions [B] int32: position b must equal the
  *   number of tokens cached for slot b.  With host I/O the check happens
  *   before anything is enqueued (ZDEC_ERR_POSITION); with device inputs the
@@ -136,12 +166,22 @@ zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f
  *   index on ties).
  * The step embeds each token, runs every layer (RMSNorm, QKV, RoPE, KV append,
  * split-K attention, O projection + residual, RMSNorm, SwiGLU FFN + residual),
- * the final RMSNorm and the tied LM head, appends each sequence's new K/V at
- * its position and advances its length by one.  ZDEC_ERR_CAPACITY (nothing
- * enqueued) if a sequence is full.  Without ZDEC_STEP_HOST_IO the call is
- * asynchronous; outputs are valid after zdec_sync or a stream sync. */
+ * the final RMSNorm and the tied LM head, appends each row's new K/V at its
+ * position (taking a pool page when the position starts one) and advances
+ * its slot's length by one.  ZDEC_ERR_CAPACITY (nothing enqueued) if a slot
+ * is full or the pool has no page for a new token.  Without ZDEC_STEP_HOST_IO
+ * the call is asynchronous; outputs are valid after zdec_sync or a stream
+ * sync. */
 zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tokens,
                              const int32_t *positions, float *logits, int32_t *ids, int flags);
+/* The same step with row b reading and extending slot slots[b] (host array of
+ * B distinct slots in [0, max_B)), so that sequences are admitted and retired
+ * between steps in any slot ("Eight concurrent agents...", section "What I am
+ * building next": continuous batching over server slots).  A map different
+ * from the previous step's waits for the steps in flight first.  ZDEC_ERR_ARG
+ * for a repeated or out-of-range slot. */
+zdec_status zdec_decode_step_slots(zdec_ctx *ctx, int B, const int32_t *slots, const int32_t *tokens,
+                                   const int32_t *positions, float *logits, int32_t *ids, int flags);
 
 /* Wait for the context's stream and report any device-side status
  * (ZDEC_ERR_DEVICE / ZDEC_ERR_TIMEOUT), clearing it.  A step whose device
@@ -154,9 +194,10 @@ zdec_status zdec_sync(zdec_ctx *ctx);
 /* Sequence slots, per "Eight concurrent agents pull 5.6x more tokens from one
  * RX 9070 XT", section "The workload stopped being one person typing" (server
  * slots that admit and retire agents between steps): reset_seq empties slot
- * `seq` (length := 0; waits for the stream); seq_len reads the host's copy of
- * its length.  ZDEC_ERR_ARG for a slot outside [0, max_B). */
-zdec_status zdec_reset_seq(zdec_ctx *ctx, int seq);            /* length := 0 */
+ * `seq` and returns its pages to the pool (length := 0; waits for the
+ * stream); seq_len reads the host's copy of its length.  ZDEC_ERR_ARG for a
+ * slot outside [0, max_B). */
+zdec_status zdec_reset_seq(zdec_ctx *ctx, int seq);
 zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len);
 const char *zdec_last_error(const zdec_ctx *ctx);
 const char *zdec_last_global_error(void);
@@ -164,7 +205,7 @@ const char *zdec_last_global_error(void);
 /* Defined by: "Eight concurrent agents pull 5.6x more tokens from one RX 9070
  * XT", section "RDNA4 pads the batch dimension to 16" (a dequant-matvec for
  * one sequence, a tensor-core GEMM past a few sequences).
- * Which dense kernel runs the Q4_K projections of the kernel engine:
+ * Which dense kernel runs the Q4_K projections:
  * 0 = default (B = 1: the sub-block-column mma matvec, impl 3; 2 <= B <= 4 by
  * the measured switch point between the CUDA-core matvec and the GEMM),
  * 1 = always the CUDA-core dequant-matvec (B <= 4 only), 2 = always the
@@ -174,61 +215,43 @@ const char *zdec_last_global_error(void);
  * effect at the next step (cached CUDA graphs are rebuilt). */
 zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl);
 
-/* Which engine runs a step.  ZDEC_ENGINE_PERSISTENT: the whole step is one
- * persistent cooperative kernel (two CTAs per SM, each streaming weight tiles
- * and KV units through a shared-memory ring while counters in global memory
- * order the phases); available for B <= 8 when the device supports
- * cooperative launch and n_q_heads*head_dim == hidden.  ZDEC_ENGINE_KERNELS:
- * one kernel per operation (embedding, per layer QKV, attention, O, gate/up,
- * down; LM head, argmax).  ZDEC_ENGINE_AUTO (the default) runs the kernel
- * engine, the faster of the two in every configuration measured so far.
- * Forcing PERSISTENT where it is unavailable fails with ZDEC_ERR_UNSUPPORTED
- * (here, or at the step).  Takes effect at the next step. */
-enum { ZDEC_ENGINE_AUTO = 0, ZDEC_ENGINE_KERNELS = 1, ZDEC_ENGINE_PERSISTENT = 2 };
-zdec_status zdec_set_engine(zdec_ctx *ctx, int engine);
-
 /* Tracing.  on = 1 makes every later step run without graph replay and
- * record a timeline of the GPU global timer (ns); on = 0 stops and frees it.
- * Kernel engine: [launches][8] entries per step: the first CTA's start, the
- * first CTA past its dependency wait, the last CTA's end, the launch's kind
- * (ZDEC_KERNEL_*), then the latest CTA to reach the kernel's milestones (for
- * the projections: past the wait, first stage landed, K loop done, cluster
- * reduction done; zero where a kernel records none).  Persistent engine: per CTA c and phase ph
- * (0 embedding; 1 + 5l + {0 QKV, 1 attention, 2 O, 3 gate/up, 4 down} of
- * layer l; 1 + 5*n_layers LM head), at entry (c*phases + ph)*8 + k: k = 0 the
- * consumer warps enter the phase, 1 its inputs are released, 2 the first item
- * has landed, 3 the last item is consumed, 4 the phase's reductions and
- * epilogues are done, 5 the producer issues the phase's first copy, 6 its
- * first activation copy, and 7 = the number of items of the phase on that CTA
- * (zero where a CTA has no work). */
+ * record a timeline of the GPU global timer (ns): [launches][8] entries per
+ * step: the first CTA's start, the first CTA past its dependency wait, the
+ * last CTA's end, the launch's kind (ZDEC_KERNEL_*), then the latest CTA to
+ * reach the kernel's milestones (for the projections: past the wait, first
+ * stage landed, K loop done, cluster reduction done; zero where a kernel
+ * records none).  on = 0 stops and frees it. */
 zdec_status zdec_set_trace(zdec_ctx *ctx, int on);
-/* Copy the trace of the last traced step (waits for the stream), in the
- * layout of the engine that ran it (zdec_get_info().engine).  *n gets the
+/* Copy the trace of the last traced step (waits for the stream).  *n gets the
  * entry count (0 when tracing is off); out_host needs that many uint64
  * (out_host = NULL: only the size query). */
 zdec_status zdec_debug_step_trace(zdec_ctx *ctx, uint64_t *out_host, size_t cap, size_t *n);
 
 typedef struct {
     size_t weight_bytes;      /* repacked weights on the device              */
-    size_t arena_bytes;       /* KV arena                                    */
+    size_t arena_bytes;       /* KV pool                                     */
     size_t workspace_bytes;   /* per-step activations, partials, logits     */
     size_t kv_bytes_per_token;/* per sequence, K+V over all layers           */
     int kernels_per_step;     /* kernel launches of one step (last B used)   */
-    int attn_splits;          /* split-K factor of the attention (last B)    */
+    int attn_splits;          /* attention CTAs per (segment, kv head), last step */
     int matvec_max_B;         /* switch point in use                         */
-    int engine;               /* engine of the last step (ZDEC_ENGINE_*)     */
-    int step_ctas;            /* CTAs of the persistent kernel (0: unavailable) */
+    int attn_segments;        /* attention segment slots per row, last step  */
+    int k_type, v_type;       /* zdec_kv_dtype of K and V                    */
+    int page_tokens;          /* tokens per pool page                        */
+    int pool_pages;           /* pages in the pool                           */
+    int free_pages;           /* pages no slot holds                         */
 } zdec_info;
 zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info);
 
-/* Per-kernel timing: runs one eager step (like ZDEC_STEP_EAGER, device inputs)
- * with a CUDA event pair around every launch on the context stream, waits, and
- * writes up to `cap` records: kind[i] (see ZDEC_KERNEL_*), ms[i].  *n receives
- * the number of launches.  The step is a real step (lengths advance). */
-enum { ZDEC_KERNEL_EMBED = 0, ZDEC_KERNEL_PREP = 1, ZDEC_KERNEL_GEMM_QKV = 2,
-       ZDEC_KERNEL_ATTENTION = 3, ZDEC_KERNEL_GEMM_O = 4, ZDEC_KERNEL_GEMM_GATEUP = 5,
-       ZDEC_KERNEL_GEMM_DOWN = 6, ZDEC_KERNEL_GEMM_LMHEAD = 7, ZDEC_KERNEL_ARGMAX = 8,
-       ZDEC_KERNEL_STEP = 9 /* persistent engine: input check + the step kernel */ };
+/* Per-kernel timing: runs one eager step (like ZDEC_STEP_EAGER, device inputs,
+ * rows 0..B-1 in slots 0..B-1) with a CUDA event pair around every launch on
+ * the context stream, waits, and writes up to `cap` records: kind[i] (see
+ * ZDEC_KERNEL_*), ms[i].  *n receives the number of launches.  The step is a
+ * real step (lengths advance). */
+enum { ZDEC_KERNEL_EMBED = 0, ZDEC_KERNEL_GEMM_QKV = 2, ZDEC_KERNEL_ATTENTION = 3, ZDEC_KERNEL_GEMM_O = 4,
+       ZDEC_KERNEL_GEMM_GATEUP = 5, ZDEC_KERNEL_GEMM_DOWN = 6, ZDEC_KERNEL_GEMM_LMHEAD = 7,
+       ZDEC_KERNEL_ARGMAX = 8 };
 zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *tokens_dev,
                               const int32_t *positions_dev, float *logits_dev, int32_t *ids_dev,
                               int *kind, float *ms, int cap, int *n);
@@ -245,16 +268,21 @@ zdec_status zdec_debug_export_q4k(zdec_ctx *ctx, int which, int layer, int row0,
 /* The same rows dequantized on the device, fp32 (out: nrows * cols floats). */
 zdec_status zdec_debug_dequant(zdec_ctx *ctx, int which, int layer, int row0, int nrows,
                                float *out_host);
-/* Stored KV of sequence `seq`, layer `layer`, tokens [t0, t0+n) in canonical
- * token-major layout [n][n_kv_heads][head_dim]: F16 -> k,v fp16 (ks, vs
- * unused, may be NULL); Q8_0 -> k,v int8 codes and ks,vs fp16 scales
- * [n][n_kv_heads][head_dim/32]. */
+/* Stored KV of slot `seq`, layer `layer`, tokens [t0, t0+n) in canonical
+ * token-major layout [n][n_kv_heads][head_dim], each tensor in its own type:
+ * F16 -> fp16 (uint16); Q8_0 -> int8 codes, and its scales [n][n_kv_heads]
+ * [head_dim/32] fp16 in ks (K) or vs (V); FP8 -> e4m3 codes (uint8).  ks / vs
+ * may be NULL for a tensor that is not Q8_0.  Tokens without a page read 0. */
 zdec_status zdec_debug_read_kv(zdec_ctx *ctx, int seq, int layer, int t0, int n, void *k,
                                void *v, void *ks, void *vs);
-/* Arm a capture of the fp32 residual stream for the next zdec_decode_step,
- * which then runs eagerly, waits, and fills out [B][n_layers+1][hidden]
- * (after the embedding and after each layer) before it returns.  out must
- * hold B*(n_layers+1)*hidden floats for the B of that step; host memory. */
+/* The block table of slot `seq` as the device holds it (waits for the
+ * stream): *n = entries per slot (ceil(max_L / 64)); pages_host (if not NULL,
+ * cap >= *n) receives the page of each 64 tokens, -1 where none. */
+zdec_status zdec_debug_block_table(zdec_ctx *ctx, int seq, int32_t *pages_host, int cap, int *n);
+/* Arm a capture of the fp32 residual stream for the next decode step, which
+ * then runs eagerly, waits, and fills out [B][n_layers+1][hidden] (after the
+ * embedding and after each layer) before it returns.  out must hold
+ * B*(n_layers+1)*hidden floats for the B of that step; host memory. */
 zdec_status zdec_debug_capture_hidden(zdec_ctx *ctx, float *out_host);
 /* Bound of the projection kernels' stage waits, in GPU clock cycles (0: the
  * default, about 2 s; -1: every projection's first stage wait counts as run
@@ -265,9 +293,9 @@ zdec_status zdec_debug_capture_hidden(zdec_ctx *ctx, float *out_host);
  * advances no length.  Waits for the stream; cached CUDA graphs are rebuilt
  * at the next step.  ZDEC_ERR_ARG for cycles < -1. */
 zdec_status zdec_debug_set_wait_limit(zdec_ctx *ctx, long long cycles);
-/* Attention alone on the cached tokens 0..positions[b] of layer `layer`
- * (nothing appended): q [B][n_q_heads][head_dim] fp32 already rotated,
- * o [B][n_q_heads][head_dim] fp32.  Host memory. */
+/* Attention alone on the cached tokens 0..positions[b] of slot b, layer
+ * `layer` (nothing appended): q [B][n_q_heads][head_dim] fp32 already
+ * rotated, o [B][n_q_heads][head_dim] fp32.  Host memory. */
 zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, const float *q_host,
                                  const int32_t *positions_host, float *o_host);
 
@@ -292,8 +320,9 @@ size_t zdec_q4k_gemm_workspace_bytes(int K, int B);
  * y[b][n] = sum_k W[n][k] x[b][k] for b < B.  x_dev fp32 [B][K], y_dev fp32
  * [B][N], workspace_dev >= zdec_q4k_gemm_workspace_bytes(K, B) bytes, 16-byte
  * aligned, owned by the caller.  impl: 1 = dequant-matvec (B <= 4),
- * 2 = mma.sync GEMM, 3 = sub-block-column mma matvec (B = 1).  Activations enter as fp16 high + low parts (about 22
- * significant bits); weights are exact; accumulation is fp32. */
+ * 2 = mma.sync GEMM, 3 = sub-block-column mma matvec (B = 1).  Activations
+ * enter as fp16 high + low parts (about 22 significant bits); weights are
+ * exact; accumulation is fp32. */
 zdec_status zdec_q4k_gemm(const void *repacked_dev, int N, int K, const float *x_dev, int B,
                           float *y_dev, int impl, void *workspace_dev, size_t workspace_bytes,
                           void *stream);

@@ -17,24 +17,25 @@ from . import _build
 
 __all__ = ["ModelDesc", "Decoder", "ZdecError", "load_library", "q4k_repacked_bytes",
            "q4k_repack", "q4k_gemm", "q4k_gemm_workspace_bytes", "q4k_gemm_static",
-           "Q4K_GEMM_STATIC_MAX_KB", "KV_F16", "KV_Q8_0",
-           "KERNEL_KINDS", "ENGINE_AUTO", "ENGINE_KERNELS", "ENGINE_PERSISTENT", "T_EMBED", "T_WQ", "T_WK", "T_WV", "T_WO", "T_GATE", "T_UP", "T_DOWN"]
+           "Q4K_GEMM_STATIC_MAX_KB", "KV_F16", "KV_Q8_0", "KV_FP8", "PAGE_TOKENS",
+           "KERNEL_KINDS", "T_EMBED", "T_WQ", "T_WK", "T_WV", "T_WO", "T_GATE", "T_UP", "T_DOWN"]
 
-KV_F16, KV_Q8_0 = 0, 1
+KV_F16, KV_Q8_0, KV_FP8 = 0, 1, 2   # per-tensor cache types (zdec_kv_dtype)
+PAGE_TOKENS = 64                    # tokens per KV pool page
 Q4K_GEMM_STATIC_MAX_KB = 262144   # K*B limit of q4k_gemm_static (ZDEC_Q4K_GEMM_STATIC_MAX_KB)
 STEP_HOST_IO, STEP_EAGER = 1, 2
 T_EMBED, T_WQ, T_WK, T_WV, T_WO, T_GATE, T_UP, T_DOWN = range(8)
-KERNEL_KINDS = ["embed", "prep", "gemm_qkv", "attention", "gemm_o", "gemm_gateup", "gemm_down",
-                "gemm_lmhead", "argmax", "step"]
-ENGINE_AUTO, ENGINE_KERNELS, ENGINE_PERSISTENT = 0, 1, 2
+KERNEL_KINDS = ["embed", "-", "gemm_qkv", "attention", "gemm_o", "gemm_gateup", "gemm_down",
+                "gemm_lmhead", "argmax"]
 STATUS = {0: "ok", -1: "bad argument", -2: "out of memory", -3: "capacity", -4: "position",
           -5: "unsupported", -6: "cuda error", -7: "timeout", -8: "device check"}
 
 # Every symbol include/zdec.h declares; load_library() checks they are exported.
-EXPORTS = ["zdec_create", "zdec_destroy", "zdec_append_kv", "zdec_decode_step", "zdec_sync",
-           "zdec_reset_seq", "zdec_seq_len", "zdec_last_error", "zdec_last_global_error",
-           "zdec_set_gemm_impl", "zdec_set_engine", "zdec_set_trace", "zdec_debug_step_trace", "zdec_get_info", "zdec_profile_step", "zdec_debug_export_q4k",
-           "zdec_debug_dequant", "zdec_debug_read_kv", "zdec_debug_capture_hidden",
+EXPORTS = ["zdec_create_cache", "zdec_create", "zdec_destroy", "zdec_append_kv", "zdec_decode_step",
+           "zdec_decode_step_slots", "zdec_sync", "zdec_reset_seq", "zdec_seq_len", "zdec_last_error",
+           "zdec_last_global_error", "zdec_set_gemm_impl", "zdec_set_trace", "zdec_debug_step_trace",
+           "zdec_get_info", "zdec_profile_step", "zdec_debug_export_q4k", "zdec_debug_dequant",
+           "zdec_debug_read_kv", "zdec_debug_block_table", "zdec_debug_capture_hidden",
            "zdec_debug_attention", "zdec_debug_set_wait_limit", "zdec_q4k_repacked_bytes", "zdec_q4k_repack",
            "zdec_q4k_gemm_workspace_bytes", "zdec_q4k_gemm", "zdec_q4k_gemm_static"]
 
@@ -60,11 +61,18 @@ class _Weights(ctypes.Structure):
                 ("wo", _PP), ("w_gate", _PP), ("w_up", _PP), ("w_down", _PP)]
 
 
+class _Cache(ctypes.Structure):
+    _fields_ = [("k_type", ctypes.c_int), ("v_type", ctypes.c_int), ("max_B", ctypes.c_int),
+                ("max_L", ctypes.c_int), ("pool_tokens", ctypes.c_longlong)]
+
+
 class _Info(ctypes.Structure):
     _fields_ = [("weight_bytes", ctypes.c_size_t), ("arena_bytes", ctypes.c_size_t),
                 ("workspace_bytes", ctypes.c_size_t), ("kv_bytes_per_token", ctypes.c_size_t),
                 ("kernels_per_step", ctypes.c_int), ("attn_splits", ctypes.c_int),
-                ("matvec_max_B", ctypes.c_int), ("engine", ctypes.c_int), ("step_ctas", ctypes.c_int)]
+                ("matvec_max_B", ctypes.c_int), ("attn_segments", ctypes.c_int),
+                ("k_type", ctypes.c_int), ("v_type", ctypes.c_int), ("page_tokens", ctypes.c_int),
+                ("pool_pages", ctypes.c_int), ("free_pages", ctypes.c_int)]
 
 
 _lib = None
@@ -91,6 +99,10 @@ def load_library(build_if_missing: bool = True):
     sigs = {
         "zdec_create": (i, [ctypes.POINTER(_Desc), ctypes.POINTER(_Weights), i, i, i, vp,
                             ctypes.POINTER(vp)]),
+        "zdec_create_cache": (i, [ctypes.POINTER(_Desc), ctypes.POINTER(_Weights), ctypes.POINTER(_Cache),
+                                  vp, ctypes.POINTER(vp)]),
+        "zdec_decode_step_slots": (i, [vp, i, vp, vp, vp, vp, vp, i]),
+        "zdec_debug_block_table": (i, [vp, i, vp, i, ctypes.POINTER(i)]),
         "zdec_destroy": (None, [vp]),
         "zdec_append_kv": (i, [vp, i, i, vp, vp, i]),
         "zdec_decode_step": (i, [vp, i, vp, vp, vp, vp, i]),
@@ -101,7 +113,6 @@ def load_library(build_if_missing: bool = True):
         "zdec_last_global_error": (ctypes.c_char_p, []),
         "zdec_set_gemm_impl": (i, [vp, i]),
         "zdec_get_info": (i, [vp, ctypes.POINTER(_Info)]),
-        "zdec_set_engine": (i, [vp, i]),
         "zdec_set_trace": (i, [vp, i]),
         "zdec_debug_step_trace": (i, [vp, vp, sz, ctypes.POINTER(sz)]),
         "zdec_profile_step": (i, [vp, i, vp, vp, vp, vp, vp, vp, i, ctypes.POINTER(i)]),
@@ -165,14 +176,16 @@ class ModelDesc:
 
 
 class Decoder:
-    """One decoder context (weights, KV arena, workspace) on the current GPU.
+    """One decoder context (weights, paged KV pool, workspace) on the current GPU.
 
     ``weights`` holds canonical Q4_K matrices as uint8 numpy arrays
     [rows, cols/256*144] (per-layer tensors as lists) and fp32 norm gains;
-    the library copies and repacks them at creation."""
+    the library copies and repacks them at creation.  ``kv_dtype`` is one
+    cache type for K and V (KV_F16, KV_Q8_0, KV_FP8) or a (k_type, v_type)
+    pair; ``pool_tokens`` sizes the shared page pool (0: max_B * max_L)."""
 
     def __init__(self, desc, weights: dict, kv_dtype=KV_F16, max_B: int = 1, max_L: int = 2048,
-                 stream=None):
+                 stream=None, pool_tokens: int = 0):
         self.lib = load_library()
         self.desc = ModelDesc.of(desc)
         d = self.desc
@@ -193,13 +206,16 @@ class Decoder:
         w = _Weights(_ptr(embed), _ptr(fnorm),
                      arr("attn_norm"), arr("ffn_norm"), arr("wq"), arr("wk"), arr("wv"), arr("wo"),
                      arr("w_gate"), arr("w_up"), arr("w_down"))
-        self.kv_dtype = int(kv_dtype)
+        kt, vt = (int(kv_dtype), int(kv_dtype)) if np.isscalar(kv_dtype) else (int(kv_dtype[0]), int(kv_dtype[1]))
+        self.k_type, self.v_type = kt, vt
+        self.kv_dtype = kt if kt == vt else (kt, vt)
         self.max_B, self.max_L = max_B, max_L
         self.stream = stream
         h = ctypes.c_void_p()
         desc_c = d._c()
-        s = self.lib.zdec_create(ctypes.byref(desc_c), ctypes.byref(w), self.kv_dtype, max_B, max_L,
-                                 ctypes.c_void_p(stream) if stream else None, ctypes.byref(h))
+        cache = _Cache(kt, vt, max_B, max_L, int(pool_tokens))
+        s = self.lib.zdec_create_cache(ctypes.byref(desc_c), ctypes.byref(w), ctypes.byref(cache),
+                                       ctypes.c_void_p(stream) if stream else None, ctypes.byref(h))
         if s != 0:
             raise ZdecError(s, self.lib.zdec_last_global_error().decode())
         self.h = h
@@ -237,26 +253,33 @@ class Decoder:
             v16 = np.ascontiguousarray(v16, np.uint16)
         self._check(self.lib.zdec_append_kv(self.h, seq, n, _ptr(k16), _ptr(v16), on_dev))
 
-    def step(self, tokens, positions, logits=None, ids=None, eager: bool = False):
+    def _run(self, B, slots, tokens, positions, logits, ids, flags):
+        if slots is None:
+            self._check(self.lib.zdec_decode_step(self.h, B, _ptr(tokens), _ptr(positions),
+                                                  _ptr(logits), _ptr(ids), flags))
+        else:
+            sl = np.ascontiguousarray(slots, np.int32)
+            assert sl.shape == (B,)
+            self._check(self.lib.zdec_decode_step_slots(self.h, B, _ptr(sl), _ptr(tokens), _ptr(positions),
+                                                        _ptr(logits), _ptr(ids), flags))
+
+    def step(self, tokens, positions, logits=None, ids=None, eager: bool = False, slots=None):
         """Device I/O step: tokens/positions int32 CUDA tensors [B], logits float32
-        CUDA [B, vocab] or None, ids int32 CUDA [B].  Asynchronous."""
+        CUDA [B, vocab] or None, ids int32 CUDA [B]; row b uses cache slot
+        slots[b] (host ints; default b).  Asynchronous."""
         B = tokens.shape[0]
-        flags = STEP_EAGER if eager else 0
-        self._check(self.lib.zdec_decode_step(self.h, B, _ptr(tokens), _ptr(positions),
-                                              _ptr(logits), _ptr(ids), flags))
+        self._run(B, slots, tokens, positions, logits, ids, STEP_EAGER if eager else 0)
 
     def step_host(self, tokens, positions, logits: np.ndarray | None = None,
-                  ids: np.ndarray | None = None, eager: bool = False):
+                  ids: np.ndarray | None = None, eager: bool = False, slots=None):
         """Host I/O step: numpy int32 tokens/positions; returns (logits, ids) numpy.
-        Copies in, runs, copies out and waits."""
+        Copies in, runs, copies out and waits.  Row b uses slot slots[b]."""
         tokens = np.ascontiguousarray(tokens, np.int32)
         positions = np.ascontiguousarray(positions, np.int32)
         B = tokens.shape[0]
         if ids is None:
             ids = np.empty(B, np.int32)
-        flags = STEP_HOST_IO | (STEP_EAGER if eager else 0)
-        self._check(self.lib.zdec_decode_step(self.h, B, _ptr(tokens), _ptr(positions),
-                                              _ptr(logits), _ptr(ids), flags))
+        self._run(B, slots, tokens, positions, logits, ids, STEP_HOST_IO | (STEP_EAGER if eager else 0))
         return logits, ids
 
     def sync(self):
@@ -273,26 +296,18 @@ class Decoder:
     def set_gemm_impl(self, impl: int):
         self._check(self.lib.zdec_set_gemm_impl(self.h, impl))
 
-    def set_engine(self, engine: int):
-        """ENGINE_AUTO (the default: the kernel engine, one kernel per operation),
-        ENGINE_KERNELS or ENGINE_PERSISTENT (opt-in single-kernel step)."""
-        self._check(self.lib.zdec_set_engine(self.h, engine))
-
     def set_trace(self, on: bool):
-        """Record the phase timeline of the following persistent steps."""
+        """Record the launch timeline of the following steps (run eagerly)."""
         self._check(self.lib.zdec_set_trace(self.h, int(bool(on))))
 
     def step_trace(self) -> np.ndarray:
-        """Timeline of the last traced step (see zdec.h): persistent engine
-        [ctas][phases][8], kernel engine [launches][8] uint64."""
+        """Timeline of the last traced step (see zdec.h): [launches][8] uint64."""
         n = ctypes.c_size_t()
         self._check(self.lib.zdec_debug_step_trace(self.h, None, 0, ctypes.byref(n)))
         if n.value == 0:
             return np.zeros((0, 8), np.uint64)
         out = np.empty(n.value, np.uint64)
         self._check(self.lib.zdec_debug_step_trace(self.h, _ptr(out), n.value, ctypes.byref(n)))
-        if self.info()["engine"] == ENGINE_PERSISTENT:
-            return out.reshape(-1, 2 + 5 * self.desc.n_layers, 8)
         return out.reshape(-1, 8)
 
     def info(self) -> dict:
@@ -332,19 +347,30 @@ class Decoder:
         return out
 
     def read_kv(self, seq: int, layer: int, t0: int, n: int):
-        """Stored K/V of one layer, canonical token-major layout.  fp16 cache:
-        (k uint16, v uint16); Q8_0: (k int8, v int8, k_scales uint16, v_scales uint16)."""
+        """Stored K/V of one layer, canonical token-major layout [n][n_kv][hd],
+        each tensor in its type: fp16 uint16, Q8_0 int8 codes, FP8 uint8 e4m3
+        codes.  Returns (k, v) when neither tensor is Q8_0, else (k, v,
+        k_scales, v_scales) with uint16 scales [n][n_kv][hd/32] (None for a
+        tensor that is not Q8_0)."""
         d = self.desc
         shape = (n, d.n_kv_heads, d.head_dim)
-        if self.kv_dtype == KV_F16:
-            k, v = np.empty(shape, np.uint16), np.empty(shape, np.uint16)
-            self._check(self.lib.zdec_debug_read_kv(self.h, seq, layer, t0, n, _ptr(k), _ptr(v), None, None))
-            return k, v
-        k, v = np.empty(shape, np.int8), np.empty(shape, np.int8)
-        ks = np.empty((n, d.n_kv_heads, d.head_dim // 32), np.uint16)
-        vs = np.empty_like(ks)
+        dt = {KV_F16: np.uint16, KV_Q8_0: np.int8, KV_FP8: np.uint8}
+        k, v = np.empty(shape, dt[self.k_type]), np.empty(shape, dt[self.v_type])
+        sshape = (n, d.n_kv_heads, d.head_dim // 32)
+        ks = np.empty(sshape, np.uint16) if self.k_type == KV_Q8_0 else None
+        vs = np.empty(sshape, np.uint16) if self.v_type == KV_Q8_0 else None
         self._check(self.lib.zdec_debug_read_kv(self.h, seq, layer, t0, n, _ptr(k), _ptr(v), _ptr(ks), _ptr(vs)))
+        if ks is None and vs is None:
+            return k, v
         return k, v, ks, vs
+
+    def block_table(self, seq: int) -> np.ndarray:
+        """Page of each 64 tokens of slot `seq` (-1: none), as the device holds it."""
+        n = ctypes.c_int()
+        self._check(self.lib.zdec_debug_block_table(self.h, seq, None, 0, ctypes.byref(n)))
+        out = np.empty(n.value, np.int32)
+        self._check(self.lib.zdec_debug_block_table(self.h, seq, _ptr(out), n.value, ctypes.byref(n)))
+        return out
 
     def step_capture_hidden(self, tokens, positions, logits=None, ids=None):
         """Host I/O step that also returns the fp32 residual after the embedding and

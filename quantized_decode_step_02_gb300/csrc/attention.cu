@@ -1,32 +1,43 @@
-// attention.cu -- per-sequence KV read: split-K flash-decode over an fp16 or
-// Q8_0 cache, dequantized inside the kernel, plus the KV append paths.
+// attention.cu -- per-sequence KV read: split-K flash-decode over a paged
+// cache whose K and V each hold fp16, Q8_0 or FP8 (e4m3), dequantized inside
+// the kernel, plus the KV append and read-back paths.
 //
 // Each sequence reads its own cache every step; nothing here is shared across
 // the batch ("Batched swarm: the KV read does not amortize", "The two halves
 // of a decode-step memory bill").  A quantized cache only saves bytes if the
 // attention kernel reads the compressed format and dequantizes on chip ("Q8
 // KV cache pushes an RDNA4 swarm crossover...", "Why Q8 is close to free and
-// where the sharp edges are"), which is what the Q8_0 instantiation does.
+// where the sharp edges are"); K and V choose their formats independently, and
+// FP8 is the scale-free one-byte format ("Batched swarm...", "What a
+// long-running swarm should actually tune").
 //
-// Grid: (cluster rank r, kv head g, sequence b); 128 threads; the CS CTAs of
-// one (b, g) form a thread-block cluster.  The 4 query heads of a kv head
-// share one read of its K/V tiles.  The pos+1 tokens are cut into 64-token
-// chunks; rank r takes a contiguous range of them (the rank that appends the
-// new token one chunk fewer), streamed through a ring of 2-8 shared-memory
-// stages with cp.async.  Both products run on
-// mma.sync.m16n8k16 with fp32 accumulation:
-//   scores: A = q (rows 0-3 the fp16 high parts of the 4 heads, rows 8-11 the
-//           low parts, so q keeps ~22 bits), B = K^T (8 tokens per MMA);
-//   output: A = p (same hi/lo split), B = V (8 head dims per MMA) read from a
-//           V^T tile, whose layout makes each thread's four tokens adjacent.
-// Q8_0: codes become exact fp16 integers in registers; K scales multiply the
-// per-32-dim partial scores, V scales are folded into p per 32-dim block.
-// Softmax runs in log2 units (q carries log2(e)/sqrt(128)).  Each CTA reduces
-// its warps to one (max, sum, unnormalised output) partial in shared memory;
-// rank 0 of the cluster merges the ranks' partials through distributed shared
-// memory (fixed rank order) and writes the output.
+// Work split.  Grid (cluster rank, kv head, segment slot); 128 threads; the
+// CS CTAs of one (segment, kv head) form a thread-block cluster.  The batch's
+// rows are cut into segments of at most S 64-token chunks, S the smallest
+// that gives every row ceil(chunks / S) segments within the launch's segment
+// slots, so a long row takes several clusters and a short one few ("Where it
+// stops, and the argument I got wrong in May": agents hold 800 to 30,000
+// tokens).  Within a segment the ranks take contiguous chunk ranges (the rank
+// holding the new token one chunk fewer).  A chunk is one page's (layer, kv
+// head) region: one bulk copy (TMA) per tensor lands it in a ring of
+// shared-memory stages exactly as stored.
+//
+// Arithmetic (4 warps, 16 tokens each per chunk; the 4 query heads of the kv
+// head share every K/V tile): scores and P V run on mma.sync.m16n8k16 with
+// fp32 accumulation; q and p enter as fp16 high parts (rows 0-3) and low
+// parts (rows 8-11), ~22 bits.  Q8_0 codes become exact fp16 integers in
+// registers (byte_perm under exponent 1024, minus 1152) with K scales applied
+// to 32-dim partial scores and V scales folded into p per 32-dim block; FP8
+// codes convert exactly with the hardware's e4m3x2 -> f16x2 cvt.  Softmax in
+// log2 units (q carries log2(e)/sqrt(128)).
+//
+// Merge: warps -> CTA (shared memory), ranks -> rank 0 (distributed shared
+// memory, fixed rank order), segments -> the last segment to finish (global
+// partials and a ticket per (row, kv head), merged in segment order), so the
+// result never depends on timing.
 #include <cooperative_groups.h>
 
+#include "kv_pool.cuh"
 #include "zdec_kernels.cuh"
 
 namespace cg = cooperative_groups;
@@ -34,259 +45,298 @@ namespace cg = cooperative_groups;
 namespace zdec {
 
 constexpr uint32_t AFULL = 0xFFFFFFFFu;
-
-template <int KVT> struct AttnLayout;
-template <> struct AttnLayout<0> {          // fp16
-    static constexpr int K_STRIDE = 288;    // bytes per token row (256 + pad)
-    static constexpr int V_STRIDE = 160;    // bytes per head-dim row of V^T (128 + pad)
-    static constexpr int K_BYTES = ATT_CHUNK * K_STRIDE;
-    static constexpr int V_BYTES = HD * V_STRIDE;
-    static constexpr int KS_BYTES = 0, VS_BYTES = 0;
-    static constexpr int STAGE = K_BYTES + V_BYTES;
-};
-template <> struct AttnLayout<1> {          // Q8_0
-    static constexpr int K_STRIDE = 144;    // 128 codes + pad
-    static constexpr int V_STRIDE = 80;     // 64 codes + pad
-    static constexpr int K_BYTES = ATT_CHUNK * K_STRIDE;
-    static constexpr int V_BYTES = HD * V_STRIDE;
-    static constexpr int KS_BYTES = ATT_CHUNK * 4 * 2;   // [token][4] fp16
-    static constexpr int VS_BYTES = 4 * ATT_CHUNK * 2;   // [blk][token] fp16
-    static constexpr int STAGE = K_BYTES + V_BYTES + KS_BYTES + VS_BYTES;
-};
-
-// A CTA keeps `stages` chunks in flight.  With few CTAs per SM the chunk
-// latency, not the SM's arithmetic, bounds a shallow ring: at two stages a
-// Q8_0 cache ran at half the fp16 cache's bandwidth (the same chunks per
-// latency, half the bytes).
 constexpr int ATT_MAX_STAGES = 8;
-static int att_max_stages(int kv_dtype) { return kv_dtype ? ATT_MAX_STAGES : 5; }   // <= 200 KB
-int attention_default_stages(int kv_dtype) { return kv_dtype ? 4 : 2; }
-size_t attention_smem_bytes(int kv_dtype, int ns) {
-    if (ns < 2 || ns > att_max_stages(kv_dtype)) ns = attention_default_stages(kv_dtype);
-    size_t stages = kv_dtype ? (size_t)ns * AttnLayout<1>::STAGE : (size_t)ns * AttnLayout<0>::STAGE;
-    size_t merge = (4 * 4 * 2 + 4 * 4 * HD) * sizeof(float);
+constexpr int SEG_PART = 4 * (HD + 4);          // floats of one segment's partial per kv head
+constexpr long long ATT_WAIT_LIMIT = 1LL << 32;   // clock cycles (~2 s): a copy that never lands
+
+__host__ __device__ constexpr uint32_t att_stage_bytes(int kt, int vt) { return kv_region_bytes(kt) + kv_region_bytes(vt); }
+static int att_max_stages(int kt, int vt) {
+    const int n = (int)((200u * 1024u) / att_stage_bytes(kt, vt));
+    return n < ATT_MAX_STAGES ? n : ATT_MAX_STAGES;
+}
+int attention_default_stages(int kt, int vt) { return (kt == KV_T_F16 && vt == KV_T_F16) ? 2 : 3; }
+size_t attention_smem_bytes(int kt, int vt, int ns) {
+    if (ns < 2 || ns > att_max_stages(kt, vt)) ns = attention_default_stages(kt, vt);
+    const size_t stages = (size_t)ns * att_stage_bytes(kt, vt);
+    const size_t merge = (4 * 4 * 2 + 4 * 4 * HD) * sizeof(float);
     return stages > merge ? stages : merge;
 }
 
-// Base of the (slot, layer, kv head) plane for a tensor of `per_token` bytes
-// per token (K planes) or `per_dim` rows (V^T planes).
-__device__ __forceinline__ size_t plane_index(const KvArena &a, int slot, int layer, int g) {
-    return ((size_t)slot * a.n_layers + layer) * a.n_kv + g;
+__device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool att_wait(uint64_t *bar, uint32_t parity, long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) return false;
+    return true;
+}
+// Q8_0 codes (stored + 128) of four consecutive elements -> two exact fp16 pairs.
+__device__ __forceinline__ void q8x4_to_h2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const __half2 bias = __float2half2_rn(1152.0f);
+    lo = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, 0x64646464u, 0x4140)), bias));
+    hi = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, 0x64646464u, 0x4342)), bias));
+}
+// fp16 hi + lo split of four values into an mma A fragment.
+__device__ __forceinline__ void split_p(const float (&v)[4], uint32_t (&pa)[4]) {
+    const __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
+    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+    pa[0] = h2_as_u32(h01);
+    pa[1] = h2_as_u32(__floats2half2_rn(v[0] - f01.x, v[1] - f01.y));
+    pa[2] = h2_as_u32(h23);
+    pa[3] = h2_as_u32(__floats2half2_rn(v[2] - f23.x, v[3] - f23.y));
 }
 
-// -------------------------------------------------------- chunk staging ---
-// Copy history tokens [c0, min(c0+64, H)) of the plane into a stage.  Partial
-// 16-byte segments of V^T may pull in tokens >= H; those columns are zeroed
-// by the fix-up before use.
-template <int KVT>
-__device__ __forceinline__ void issue_chunk(const AttnParams &p, uint8_t *stage, int b, int g, int c0,
-                                            int H) {
-    using Lay = AttnLayout<KVT>;
-    int nt = min(ATT_CHUNK, H - c0);
-    if (nt <= 0) return;
-    size_t pi = plane_index(p.kv, b, p.layer, g);
-    const int Lp = p.kv.Lp;
-    uint8_t *sK = stage, *sV = stage + Lay::K_BYTES;
-    if (KVT == 0) {
-        // the arena's 16-byte segments are swizzled (kv_*_off); the padded
-        // stage rows hold them in natural order
-        const uint8_t *gK = p.kv.k + pi * Lp * (HD * 2);
-        const uint8_t *gV = p.kv.v + pi * Lp * (HD * 2);
-        for (int i = threadIdx.x; i < nt * 16; i += blockDim.x) {
-            int t = i >> 4, sg = i & 15;
-            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + kv_k16_off(c0 + t, 8 * sg));
-        }
-        if (nt == ATT_CHUNK) {   // whole chunk: 8 segments per head-dim row
-            for (int i = threadIdx.x; i < HD * 8; i += blockDim.x) {
-                const int d = i >> 3, sg = i & 7;
-                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v16_off(d, c0 + 8 * sg));
+// Scores of this warp's 16 tokens of a chunk against the 4 heads:
+// S[nt] = C fragment of the tokens 16 w + 4 (col >> 1) + 2 nt + (col & 1),
+// i.e. lane (gid, tig) ends with tokens 16 w + 4 tig + {0, 1} (nt = 0) and
+// {2, 3} (nt = 1), rows gid (q high part) and gid + 8 (q low part).
+template <int KT>
+__device__ __forceinline__ void qk_tile(const uint8_t *sK, int warp, int gid, int tig, const uint32_t (&qa)[8][4],
+                                        float (&S)[2][4]) {
+    const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++) {
+        const int tr = 16 * warp + 4 * (gid >> 1) + 2 * nt + (gid & 1);   // token of B column gid
+        if (KT == KV_T_Q8) {
+            const int ta = 16 * warp + 4 * tig + 2 * nt;   // tokens of C columns 2 tig, 2 tig + 1
+            const uint2 sa = *reinterpret_cast<const uint2 *>(sK + ks_off(ta, 0));
+            const uint2 sb = *reinterpret_cast<const uint2 *>(sK + ks_off(ta + 1, 0));
+            const float2 a01 = __half22float2(u32_as_h2(sa.x)), a23 = __half22float2(u32_as_h2(sa.y));
+            const float2 b01 = __half22float2(u32_as_h2(sb.x)), b23 = __half22float2(u32_as_h2(sb.y));
+            const float ka[4] = {a01.x, a01.y, a23.x, a23.y}, kb[4] = {b01.x, b01.y, b23.x, b23.y};
+#pragma unroll
+            for (int i = 0; i < 4; i++) S[nt][i] = 0.0f;
+#pragma unroll
+            for (int bl = 0; bl < 4; bl++) {
+                float tmp[4];
+#pragma unroll
+                for (int hs = 0; hs < 2; hs++) {
+                    const int s8 = 2 * bl + hs;
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(
+                        sK + tr * 128 + ((((uint32_t)s8 ^ (uint32_t)(tr & 7)) << 4) | ((uint32_t)tig << 2)));
+                    uint32_t b0, b1;
+                    q8x4_to_h2(w, b0, b1);
+                    if (hs) mma16816(tmp, qa[s8], b0, b1, tmp);
+                    else mma16816(tmp, qa[s8], b0, b1, zero4);
+                }
+                S[nt][0] += ka[bl] * tmp[0];
+                S[nt][1] += kb[bl] * tmp[1];
+                S[nt][2] += ka[bl] * tmp[2];
+                S[nt][3] += kb[bl] * tmp[3];
             }
         } else {
-            const int vseg = (nt + 7) >> 3;   // 8 tokens per 16 bytes
-            for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
-                const int d = i / vseg, sg = i % vseg;
-                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v16_off(d, c0 + 8 * sg));
+            // two independent accumulator chains (even / odd 16-dim steps)
+            float se[4] = {0.0f, 0.0f, 0.0f, 0.0f}, so[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int s8 = 0; s8 < 8; s8++) {
+                uint32_t b0, b1;
+                if (KT == KV_T_F16) {
+                    const uint2 kb = *reinterpret_cast<const uint2 *>(
+                        sK + tr * 256 + ((((uint32_t)(2 * s8 + (tig >> 1)) ^ (uint32_t)(tr & 7)) << 4) |
+                                         ((uint32_t)(tig & 1) << 3)));
+                    b0 = kb.x;
+                    b1 = kb.y;
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(
+                        sK + tr * 128 + ((((uint32_t)s8 ^ (uint32_t)(tr & 7)) << 4) | ((uint32_t)tig << 2)));
+                    b0 = e4m3x2_to_h2((uint16_t)(w & 0xFFFFu));
+                    b1 = e4m3x2_to_h2((uint16_t)(w >> 16));
+                }
+                if (s8 & 1) mma16816(so, qa[s8], b0, b1, so);
+                else mma16816(se, qa[s8], b0, b1, se);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++) S[nt][i] = se[i] + so[i];
+        }
+    }
+}
+
+// out += P V for this warp's 16 tokens (lane tokens t0 .. t0 + 3, t0 = 16 w + 4 tig).
+template <int VT>
+__device__ __forceinline__ void pv_tile(const uint8_t *sV, int warp, int gid, int tig, const float (&pr)[4],
+                                        float (&oacc)[16][4]) {
+    const int t0 = 16 * warp + 4 * tig;
+    if (VT == KV_T_Q8) {
+#pragma unroll
+        for (int bl = 0; bl < 4; bl++) {
+            const uint2 vsc = *reinterpret_cast<const uint2 *>(sV + vs_off(t0, bl));   // tokens t0..t0+3
+            const float2 v01 = __half22float2(u32_as_h2(vsc.x)), v23 = __half22float2(u32_as_h2(vsc.y));
+            const float q4[4] = {pr[0] * v01.x, pr[1] * v01.y, pr[2] * v23.x, pr[3] * v23.y};
+            uint32_t pa[4];
+            split_p(q4, pa);
+#pragma unroll
+            for (int dq = 0; dq < 4; dq++) {
+                const int dd = 32 * bl + 8 * dq + gid;
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, dd));
+                uint32_t b0, b1;
+                q8x4_to_h2(w, b0, b1);
+                mma16816(oacc[4 * bl + dq], pa, b0, b1, oacc[4 * bl + dq]);
             }
         }
     } else {
-        uint8_t *sKs = stage + Lay::K_BYTES + Lay::V_BYTES, *sVs = sKs + Lay::KS_BYTES;
-        const uint8_t *gK = p.kv.k + pi * Lp * HD;
-        const uint8_t *gKs = p.kv.ks + (pi * Lp + c0) * 8;
-        const uint8_t *gV = p.kv.v + pi * Lp * HD;
-        const uint8_t *gVs = p.kv.vs + pi * Lp * 8;
-        for (int i = threadIdx.x; i < nt * 8; i += blockDim.x) {
-            int t = i >> 3, sg = i & 7;
-            cp_async16(sK + t * Lay::K_STRIDE + sg * 16, gK + kv_k8_off(c0 + t, 16 * sg));
-        }
-        for (int i = threadIdx.x; i < (nt + 1) / 2; i += blockDim.x)   // 2 tokens of scales per 16 B
-            cp_async16(sKs + i * 16, gKs + (size_t)i * 16);
-        if (nt == ATT_CHUNK) {   // whole chunk: 4 code segments per head-dim row, 8 per scale row
-            for (int i = threadIdx.x; i < HD * 4; i += blockDim.x) {
-                const int d = i >> 2, sg = i & 3;
-                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v8_off(d, c0 + 16 * sg));
-            }
-            if (threadIdx.x < 32) {
-                const int bl = threadIdx.x >> 3, sg = threadIdx.x & 7;
-                cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + kv_vs_off(bl, c0 + 8 * sg));
-            }
-        } else {
-            const int vseg = (nt + 15) >> 4;   // 16 tokens per 16 bytes
-            for (int i = threadIdx.x; i < HD * vseg; i += blockDim.x) {
-                const int d = i / vseg, sg = i % vseg;
-                cp_async16(sV + d * Lay::V_STRIDE + sg * 16, gV + kv_v8_off(d, c0 + 16 * sg));
-            }
-            const int sseg = (nt + 7) >> 3;    // 8 tokens of one scale row per 16 B
-            for (int i = threadIdx.x; i < 4 * sseg; i += blockDim.x) {
-                const int bl = i / sseg, sg = i % sseg;
-                cp_async16(sVs + bl * ATT_CHUNK * 2 + sg * 16, gVs + kv_vs_off(bl, c0 + 8 * sg));
-            }
-        }
-    }
-}
-
-// Whole-chunk staging with the index arithmetic hoisted out of the chunk loop.
-// A chunk starts at a multiple of 64 tokens, so every swizzle term depends on
-// the thread alone and the arena offset of each 16-byte segment is
-// c0 * (bytes per token) + a per-thread constant + an unrolled-copy constant.
-// Thread tid copies segments i = tid + 128 j of each tensor (see issue_chunk
-// for the segment order); ks / vs: threads 0-31 copy one scale segment each.
-template <int KVT> struct ChunkPlan {
-    const uint8_t *gK, *gV, *gS, *gT;   // plane bases: K, V codes, K scales, V scales
-    uint32_t k_src, k_dst, v_src, v_dst, s_src, s_dst, t_src, t_dst;
-
-    __device__ ChunkPlan(const AttnParams &p, int b, int g) {
-        using Lay = AttnLayout<KVT>;
-        const uint32_t tid = threadIdx.x;
-        const size_t pi = plane_index(p.kv, b, p.layer, g);
-        const int Lp = p.kv.Lp;
-        if (KVT == 0) {
-            gK = p.kv.k + pi * Lp * (HD * 2);
-            gV = p.kv.v + pi * Lp * (HD * 2);
-            gS = gT = nullptr;
-            const uint32_t t = tid >> 4, sg = tid & 15;          // K: 16 segments per token
-            k_src = t * 256 + ((sg ^ (t & 7)) << 4);
-            k_dst = t * Lay::K_STRIDE + sg * 16;
-            const uint32_t d = tid >> 3, vs = tid & 7;           // V^T: 8 segments per dim row
-            v_src = ((vs >> 2) * HD + d) * 64 + (((vs & 3) ^ ((tid >> 4) & 3)) << 4);
-            v_dst = Lay::K_BYTES + d * Lay::V_STRIDE + vs * 16;
-            s_src = s_dst = t_src = t_dst = 0;
-        } else {
-            gK = p.kv.k + pi * Lp * HD;
-            gV = p.kv.v + pi * Lp * HD;
-            gS = p.kv.ks + pi * Lp * 8;
-            gT = p.kv.vs + pi * Lp * 8;
-            const uint32_t t = tid >> 3, sg = tid & 7;           // K: 8 segments per token
-            k_src = t * 128 + ((sg ^ (t & 7)) << 4);
-            k_dst = t * Lay::K_STRIDE + sg * 16;
-            const uint32_t d = tid >> 2, vs = tid & 3;           // V^T: 4 segments per dim row
-            v_src = ((vs >> 1) * HD + d) * 32 + (((vs & 1) ^ ((tid >> 4) & 1)) << 4);
-            v_dst = Lay::K_BYTES + d * Lay::V_STRIDE + vs * 16;
-            s_src = (tid & 31) * 16;                              // K scales: 512 contiguous bytes
-            s_dst = Lay::K_BYTES + Lay::V_BYTES + (tid & 31) * 16;
-            const uint32_t bl = (tid >> 3) & 3, ss = tid & 7;     // V scales: 4 rows of 8 segments
-            t_src = (((ss >> 2) * 4 + bl) * KU + 8 * (ss & 3)) * 2;
-            t_dst = Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES + bl * ATT_CHUNK * 2 + ss * 16;
-        }
-    }
-
-    // tokens [c0, c0 + 64) of the plane into the stage at shared address st
-    __device__ __forceinline__ void issue(uint32_t st, int c0) const {
-        using Lay = AttnLayout<KVT>;
-        if (KVT == 0) {
-            const uint8_t *k = gK + (size_t)c0 * 256 + k_src, *v = gV + (size_t)c0 * 256 + v_src;
+        uint32_t pa[4];
+        split_p(pr, pa);
 #pragma unroll
-            for (int j = 0; j < 8; j++) {   // tokens t + 8 j; dims d + 16 j
-                cp_async16_s(st + k_dst + j * 8 * Lay::K_STRIDE, k + j * 8 * 256);
-                cp_async16_s(st + v_dst + j * 16 * Lay::V_STRIDE, v + j * 16 * 64);
+        for (int dn = 0; dn < 16; dn++) {
+            const int dd = 8 * dn + gid;
+            uint32_t b0, b1;
+            if (VT == KV_T_F16) {
+                const uint2 vb = *reinterpret_cast<const uint2 *>(sV + v16_off(t0, dd));
+                b0 = vb.x;
+                b1 = vb.y;
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, dd));
+                b0 = e4m3x2_to_h2((uint16_t)(w & 0xFFFFu));
+                b1 = e4m3x2_to_h2((uint16_t)(w >> 16));
             }
-        } else {
-            const uint8_t *k = gK + (size_t)c0 * 128 + k_src, *v = gV + (size_t)c0 * 128 + v_src;
-#pragma unroll
-            for (int j = 0; j < 4; j++) {   // tokens t + 16 j; dims d + 32 j
-                cp_async16_s(st + k_dst + j * 16 * Lay::K_STRIDE, k + j * 16 * 128);
-                cp_async16_s(st + v_dst + j * 32 * Lay::V_STRIDE, v + j * 32 * 32);
-            }
-            if (threadIdx.x < 32) {
-                cp_async16_s(st + s_dst, gS + (size_t)c0 * 8 + s_src);
-                cp_async16_s(st + t_dst, gT + (size_t)c0 * 8 + t_src);
-            }
+            mma16816(oacc[dn], pa, b0, b1, oacc[dn]);
         }
     }
-};
-
-__device__ __forceinline__ void codes4_to_h2(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    // bytes b0..b3 (int8) -> (b0, b1), (b2, b3) as exact fp16 integers:
-    // flip the sign bit, place each byte under exponent 0x64 (value 1024 + byte),
-    // subtract 1024 + 128
-    uint32_t u = w ^ 0x80808080u;
-    const __half2 bias = __float2half2_rn(1152.0f);
-    lo = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4140)), bias));
-    hi = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, 0x4342)), bias));
 }
 
-// Q8_0 of 32 fp16 values held one per lane: returns this lane's code, and the
-// fp16 scale bits.  amax/127 by IEEE division, codes by IEEE division by the
-// fp32 scale, round half to even, clamp to +-127; all-zero blocks -> 0, 0.
-__device__ __forceinline__ int8_t q8_0_lane(__half xh, uint16_t &scale_bits) {
-    float x = __half2float(xh);
-    float amax = fabsf(x);
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(AFULL, amax, o));
-    if (amax == 0.0f) { scale_bits = 0; return 0; }
-    float d = __fdiv_rn(amax, 127.0f);
-    scale_bits = __half_as_ushort(__float2half_rn(d));
-    int q = __float2int_rn(__fdiv_rn(x, d));
-    q = max(-127, min(127, q));
-    return (int8_t)q;
+// Store one element d of a row at token t of a K or V region, `x` in storage
+// form (fp16 bits, Q8_0 code + 128, or an e4m3 byte).
+template <int T>
+__device__ __forceinline__ void put_k(uint8_t *reg, int t, int d, uint16_t x) {
+    if (T == KV_T_F16) *reinterpret_cast<uint16_t *>(reg + k16_off(t, d)) = x;
+    else reg[k8_off(t, d)] = (uint8_t)x;
+}
+template <int T>
+__device__ __forceinline__ void put_v(uint8_t *reg, int t, int d, uint16_t x) {
+    if (T == KV_T_F16) *reinterpret_cast<uint16_t *>(reg + v16_off(t, d)) = x;
+    else reg[v8_off(t, d)] = (uint8_t)x;
+}
+// One element of a row of fp16 values held by the 32 lanes of a warp (dims
+// lane + 32 i) in storage form; a Q8_0 block's scale comes from the whole
+// warp (every lane must call this together).
+template <int T>
+__device__ __forceinline__ uint16_t encode_lane(__half h, uint16_t &scale_bits) {
+    if (T == KV_T_F16) return __half_as_ushort(h);
+    if (T == KV_T_Q8) return (uint16_t)(uint8_t)(q8_0_lane(h, scale_bits) ^ 0x80);
+    return e4m3_from_half(h);
 }
 
-// --------------------------------------------------------------- kernel ---
-template <int KVT>
+// ------------------------------------------------------------------ kernel ---
+template <int KT, int VT>
 __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
-    using Lay = AttnLayout<KVT>;
-    extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ __align__(16) uint8_t s_newk[HD * 2], s_newv[HD * 2];   // new token (fp16 or codes)
+    constexpr uint32_t KB = kv_region_bytes(KT), VB = kv_region_bytes(VT), SB = KB + VB;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint16_t s_newk[HD], s_newv[HD];          // the new token in storage form
     __shared__ uint16_t s_newks[4], s_newvs[4];
-    __shared__ float s_part[GROUP][HD + 4];   // this CTA's (max, sum, output) per head
+    // this CTA's (max, sum, output) per head; read as float4 (also through
+    // distributed shared memory), so 16-byte aligned
+    __shared__ __align__(16) float s_part[GROUP][HD + 4];
+    __shared__ __align__(8) uint64_t full[ATT_MAX_STAGES];
+    __shared__ int s_map[4];                             // row, segment, segments of the row, chunks per segment
+    __shared__ int s_bad, s_last;
 
-    const int rank = blockIdx.x, g = blockIdx.y, b = blockIdx.z, CS = p.cs;
+    const int rank = blockIdx.x, g = blockIdx.y, z = blockIdx.z, CS = p.cs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     tl_min(p.tl, 0);
-    const int pos = p.positions[b];       // staged before the step: not a predecessor output
-    if (pos < 0 || pos >= p.max_L) return;   // bad device input (whole cluster); flagged by the embedding kernel
+    // ---- which row and segment this cluster takes.  Positions, slots and
+    // block tables are step inputs written before the step's first kernel,
+    // so this runs before the dependency wait.
+    if (warp == 0) {
+        int nch = 0;
+        if (lane < p.B) {
+            const int pos = p.positions[lane];
+            nch = (pos >= 0 && pos < p.max_L) ? (pos + PAGE_TOKENS) / PAGE_TOKENS : 0;
+        }
+        int tot = nch, mx = nch;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            tot += __shfl_xor_sync(AFULL, tot, o);
+            mx = max(mx, __shfl_xor_sync(AFULL, mx, o));
+        }
+        const int NZ = (int)gridDim.z;
+        int lo = max(1, (tot + NZ - 1) / NZ), hi = max(1, mx);
+        lo = min(hi, max(lo, p.seg_min));
+        while (lo < hi) {   // the smallest S whose segment count fits the launch
+            const int mid = (lo + hi) >> 1;
+            int cnt = nch ? (nch + mid - 1) / mid : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(AFULL, cnt, o);
+            if (cnt <= NZ) hi = mid;
+            else lo = mid + 1;
+        }
+        const int S = lo;
+        const int segs = nch ? (nch + S - 1) / S : 0;
+        int incl = segs;   // inclusive prefix sum over the rows
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(AFULL, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const unsigned hit = __ballot_sync(AFULL, lane < p.B && incl > z);
+        if (lane == 0) {
+            s_map[0] = -1;
+            s_bad = 0;
+        }
+        __syncwarp();
+        if (hit) {
+            const int r = __ffs(hit) - 1;
+            if (lane == r) {
+                s_map[0] = r;
+                s_map[1] = z - (incl - segs);
+                s_map[2] = segs;
+                s_map[3] = S;
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; i++) mbar_init(&full[i], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int b = s_map[0];
+    if (b < 0) {   // an idle segment slot: every CTA of the cluster leaves here
+        pdl_launch_dependents();
+        return;
+    }
+    const int seg = s_map[1], nseg = s_map[2], S = s_map[3];
+    const int pos = p.positions[b];
+    const int slot = p.slots[b];
     const int ntok = pos + 1;
-    const int nch = (ntok + ATT_CHUNK - 1) / ATT_CHUNK;
-    // the rank holding the new token also appends it and patches its chunk:
-    // one virtual chunk of extra work, so its range is one chunk shorter
-    const int nw = nch + (p.append ? 1 : 0);
-    const int c_lo = min(nch, rank * nw / CS), c_hi = min(nch, (rank + 1) * nw / CS);
-    const int T0 = c_lo * ATT_CHUNK;
-    const int T1 = min(c_hi * ATT_CHUNK, ntok);
-    const bool empty = c_lo >= c_hi;       // still takes part in the cluster merge
-    const int H = p.append ? min(T1, pos) : T1;   // tokens read from the arena
+    const int nch = (ntok + PAGE_TOKENS - 1) / PAGE_TOKENS;
+    const int sc0 = seg * S, nseg_ch = min(nch, sc0 + S) - sc0;   // this segment's chunks
+    const bool seg_new = p.append && sc0 + nseg_ch == nch;         // it holds the new token
+    const int nw = nseg_ch + (seg_new ? 1 : 0);   // the appending rank counts one chunk more
+    const int c_lo = sc0 + min(nseg_ch, rank * nw / CS), c_hi = sc0 + min(nseg_ch, (rank + 1) * nw / CS);
+    const int T1 = min(c_hi * PAGE_TOKENS, ntok);
+    const bool empty = c_lo >= c_hi;          // still takes part in the cluster merge
+    const int H = p.append ? min(T1, pos) : T1;   // tokens read from the cache
     const int nchunks = c_hi - c_lo;
     const bool has_new = p.append && !empty && T1 == ntok;
-
-    const int NS = p.stages;   // 2..ATT_MAX_STAGES (checked at launch)
-    const ChunkPlan<KVT> plan(p, b, g);
-    const uint32_t smem_s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    // whole chunks through the plan, the history's ragged end through issue_chunk
-    auto load_chunk = [&](int slot, int c0) {
-        if (H - c0 >= ATT_CHUNK) plan.issue(smem_s + (uint32_t)(slot * Lay::STAGE), c0);
-        else issue_chunk<KVT>(p, smem + slot * Lay::STAGE, b, g, c0, H);
+    const int NS = p.stages;
+    const size_t coff = kv_chunk_off(p.kv, p.layer, g);
+    auto stage = [&](int i) { return smem + (size_t)(i % NS) * SB; };
+    // chunk c (of the row) into ring slot i; a chunk with no cached token
+    // (only the new one) or without a page completes its stage with no copy
+    auto issue = [&](int i, int c) {
+        uint64_t *bar = &full[i % NS];
+        const int page = kv_page(p.kv, slot, c * PAGE_TOKENS);
+        if (c * PAGE_TOKENS < H && kv_page_ok(p.kv, page)) {
+            const uint8_t *src = p.kv.base + (size_t)page * p.kv.page_bytes + coff;
+            mbar_expect_tx(bar, SB);
+            bulk_g2s(stage(i), src, KB, bar);
+            bulk_g2s(stage(i) + KB, src + KB, VB, bar);
+        } else {
+            if (c * PAGE_TOKENS < H) atomicOr(p.status, STATUS_PAGE);
+            mbar_arrive_local(bar);
+        }
     };
-    // ring of NS slots: chunks 0..NS-2 now (the history is no predecessor's
-    // output: loaded before the wait); chunk ci + NS - 1 goes out at the top of
-    // iteration ci, into the slot chunk ci - 1 has just freed, so that one
-    // block barrier per chunk covers both the landing and the reuse
-#pragma unroll 1
-    for (int s = 0; s < NS - 1; s++) {
-        if (s < nchunks) load_chunk(s, T0 + s * ATT_CHUNK);
-        cp_async_commit();
-    }
+    // the cached history does not depend on the previous kernel: the first
+    // NS - 1 chunks go out before the dependency wait
+    if (threadIdx.x == 0)
+        for (int i = 0; i < NS - 1 && i < nchunks; i++) issue(i, c_lo + i);
+    int issued = min(NS - 1, nchunks);   // chunks due in the ring (the same count on every thread)
+    int sent = issued;                   // thread 0: chunks it actually put in flight
 
     // the rotary row of the new token: a constant table, read before the wait
     float2 rope_new[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    if (has_new && warp == 0 && p.append) {
+    if (has_new && warp == 0) {
         const float2 *cs = p.rope + (size_t)pos * (HD / 2);
         rope_new[0] = cs[lane];
         rope_new[1] = cs[lane + 32];
@@ -297,7 +347,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     tl_min(p.tl, 1);
     tl_max(p.tl, 4);
 
-    // ---- query fragments: head 4g+gid (gid < 4), dims 16s' + 4tig + {0..3}
+    // ---- query fragments: head 4g + gid (gid < 4), dims 16 s + 4 tig + {0..3}
     uint32_t qa[8][4];
     if (p.q_frag) {   // prepared by the QKV projection's epilogue (rotated, scaled, hi/lo)
         const uint4 *qf = p.q_frag + ((size_t)b * p.nq + GROUP * g + (gid < GROUP ? gid : 0)) * 32 + tig;
@@ -319,32 +369,25 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             float v[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                int d = 16 * st + 4 * tig + e;
+                const int d = 16 * st + 4 * tig + e;
                 float x = 0.0f;
                 if (gid < GROUP) {
                     x = qrow[d];
                     if (p.append) {
-                        int i = d & 63;
-                        float2 c = cs[i];
+                        const float2 c = cs[d & 63];
                         x = d < 64 ? x * c.x - qrow[d + 64] * c.y : x * c.x + qrow[d - 64] * c.y;
                     }
                 }
                 v[e] = x * qscale;
             }
-            __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
-            float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            qa[st][0] = h2_as_u32(h01);
-            qa[st][1] = h2_as_u32(__floats2half2_rn(v[0] - f01.x, v[1] - f01.y));
-            qa[st][2] = h2_as_u32(h23);
-            qa[st][3] = h2_as_u32(__floats2half2_rn(v[2] - f23.x, v[3] - f23.y));
+            split_p(v, qa[st]);
         }
     }
-
     tl_max(p.tl, 5);
+
     // ---- the new token (warp 0 of the CTA that holds it): its k and v rows
-    // are loaded now, but rotated, rounded, quantized (Q8_0) and appended only
-    // at the chunk that holds it, so that the load latency hides behind the
-    // earlier chunks
+    // are loaded now, and rotated, rounded and encoded at the chunk that holds
+    // it, so that the load latency hides behind the earlier chunks
     float kx[4], vx[4];
     if (has_new && warp == 0) {
         const float *krow = p.qkv + (size_t)b * p.qkv_ld + (size_t)(p.nq + g) * HD;
@@ -352,191 +395,77 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
 #pragma unroll
         for (int i = 0; i < 4; i++) { kx[i] = krow[lane + 32 * i]; vx[i] = vrow[lane + 32 * i]; }
     }
-    auto append_new = [&]() {
+    auto encode_new = [&]() {   // warp 0: rotate-half pairs (d, d + 64), d = lane + 32 i
         float kr[4];
 #pragma unroll
-        for (int i = 0; i < 2; i++) {   // pairs (d, d+64): d = lane + 32 i
+        for (int i = 0; i < 2; i++) {
             const float2 c = rope_new[i];
             kr[i] = kx[i] * c.x - kx[i + 2] * c.y;
             kr[i + 2] = kx[i + 2] * c.x + kx[i] * c.y;
         }
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            int d = lane + 32 * i;
-            __half kh = __float2half_rn(kr[i]), vh = __float2half_rn(vx[i]);
-            if (KVT == 0) {
-                reinterpret_cast<__half *>(s_newk)[d] = kh;
-                reinterpret_cast<__half *>(s_newv)[d] = vh;
-            } else {
-                uint16_t ksb, vsb;
-                int8_t kc = q8_0_lane(kh, ksb), vc = q8_0_lane(vh, vsb);
-                reinterpret_cast<int8_t *>(s_newk)[d] = kc;
-                reinterpret_cast<int8_t *>(s_newv)[d] = vc;
-                if (lane == 0) {
-                    s_newks[i] = ksb;
-                    s_newvs[i] = vsb;
-                }
-            }
-        }
-    };
-    // the appended token into the arena, from shared memory, once the cluster
-    // no longer waits on this CTA (no global store is then outstanding at the
-    // cluster barriers' release)
-    auto store_new = [&]() {
-        const size_t pi = plane_index(p.kv, b, p.layer, g);
-        const int Lp = p.kv.Lp;
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
             const int d = lane + 32 * i;
-            if (KVT == 0) {
-                *reinterpret_cast<__half *>(p.kv.k + pi * Lp * (HD * 2) + kv_k16_off(pos, d)) =
-                    reinterpret_cast<const __half *>(s_newk)[d];
-                *reinterpret_cast<__half *>(p.kv.v + pi * Lp * (HD * 2) + kv_v16_off(d, pos)) =
-                    reinterpret_cast<const __half *>(s_newv)[d];
-            } else {
-                *reinterpret_cast<int8_t *>(p.kv.k + pi * Lp * HD + kv_k8_off(pos, d)) =
-                    reinterpret_cast<const int8_t *>(s_newk)[d];
-                *reinterpret_cast<int8_t *>(p.kv.v + pi * Lp * HD + kv_v8_off(d, pos)) =
-                    reinterpret_cast<const int8_t *>(s_newv)[d];
-                if (lane == 0) {
-                    *reinterpret_cast<uint16_t *>(p.kv.ks + pi * Lp * 8 + kv_ks_off(pos, i)) = s_newks[i];
-                    *reinterpret_cast<uint16_t *>(p.kv.vs + pi * Lp * 8 + kv_vs_off(i, pos)) = s_newvs[i];
-                }
+            uint16_t ksb = 0, vsb = 0;
+            s_newk[d] = encode_lane<KT>(__float2half_rn(kr[i]), ksb);
+            s_newv[d] = encode_lane<VT>(__float2half_rn(vx[i]), vsb);
+            if (lane == 0) {
+                s_newks[i] = ksb;
+                s_newvs[i] = vsb;
             }
         }
     };
 
-    // ---- online softmax state (meaningful on lanes gid < 4: head 4g+gid)
+    // ---- online softmax state (meaningful on lanes gid < 4: head 4g + gid)
     float m_run = -INFINITY, l_run = 0.0f;
     float oacc[16][4];
 #pragma unroll
     for (int dn = 0; dn < 16; dn++)
 #pragma unroll
         for (int i = 0; i < 4; i++) oacc[dn][i] = 0.0f;
-    const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    bool ok = true;
 
-    int slot = 0, rslot = NS - 1;
     for (int ci = 0; ci < nchunks; ci++) {
-        uint8_t *st = smem + slot * Lay::STAGE;
-        const int c0 = T0 + ci * ATT_CHUNK;
-        switch (NS) {   // NS - 1 + ci groups committed; chunk ci's is group ci
-            case 2: cp_async_wait<0>(); break;
-            case 3: cp_async_wait<1>(); break;
-            case 4: cp_async_wait<2>(); break;
-            case 5: cp_async_wait<3>(); break;
-            case 6: cp_async_wait<4>(); break;
-            case 7: cp_async_wait<5>(); break;
-            default: cp_async_wait<6>(); break;
-        }
-        __syncthreads();   // chunk ci has landed; every warp is done with chunk ci - 1
-        if (ci + NS - 1 < nchunks) load_chunk(rslot, T0 + (ci + NS - 1) * ATT_CHUNK);
-        cp_async_commit();
-        rslot = rslot + 1 == NS ? 0 : rslot + 1;
-        // fix-up (only the chunk at the end of the loaded history): zero V columns
-        // past it and insert the new token; whole-history chunks skip both barriers
-        const int zfrom = max(H, c0) - c0;
-        if (zfrom < ATT_CHUNK) {
-            if (has_new && warp == 0) append_new();   // before the barrier that publishes s_new*
-            uint8_t *sV = st + Lay::K_BYTES;
-            {   // thread d clears row d of V^T from column zfrom on (128 threads, 128 rows)
-                // element stores up to a 16-byte boundary, then whole 16-byte stores
-                // (rows start 16-byte aligned: strides 160 / 80 / 128 bytes)
-                const int d = threadIdx.x;
-                const uint4 z4 = make_uint4(0, 0, 0, 0);
-                if (KVT == 0) {
-                    __half *row = reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE);
-                    int t = zfrom;
-                    for (; t < ATT_CHUNK && (t & 7); t++) row[t] = __ushort_as_half(0);
-                    for (; t < ATT_CHUNK; t += 8) *reinterpret_cast<uint4 *>(row + t) = z4;
-                } else {
-                    uint8_t *row = sV + d * Lay::V_STRIDE;
-                    int t = zfrom;
-                    for (; t < ATT_CHUNK && (t & 15); t++) row[t] = 0;
-                    for (; t < ATT_CHUNK; t += 16) *reinterpret_cast<uint4 *>(row + t) = z4;
-                    if (d < 4) {
-                        uint16_t *srow = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES) +
-                                         d * ATT_CHUNK;
-                        int u = zfrom;
-                        for (; u < ATT_CHUNK && (u & 7); u++) srow[u] = 0;
-                        for (; u < ATT_CHUNK; u += 8) *reinterpret_cast<uint4 *>(srow + u) = z4;
-                    }
-                }
+        const int c0 = (c_lo + ci) * PAGE_TOKENS;
+        const int zfrom = max(H, c0) - c0;   // first local token not read from the cache
+        if (zfrom < PAGE_TOKENS && has_new && warp == 0) encode_new();   // published by the barrier below
+        __syncthreads();   // every warp is done with chunk ci - 1: its slot may be refilled
+        if (issued < nchunks) {   // chunk ci + NS - 1 into the slot chunk ci - 1 freed
+            if (threadIdx.x == 0 && !s_bad) {
+                issue(issued, c_lo + issued);
+                sent = issued + 1;
             }
-            __syncthreads();
-            if (has_new && pos >= c0 && pos < c0 + ATT_CHUNK) {
-                int t = pos - c0;
-                uint8_t *sK = st;
-                int d = threadIdx.x;   // 128 threads, one head dim each
-                if (KVT == 0) {
-                    reinterpret_cast<__half *>(sK + t * Lay::K_STRIDE)[d] = reinterpret_cast<__half *>(s_newk)[d];
-                    reinterpret_cast<__half *>(sV + d * Lay::V_STRIDE)[t] = reinterpret_cast<__half *>(s_newv)[d];
-                } else {
-                    sK[t * Lay::K_STRIDE + d] = s_newk[d];
-                    sV[d * Lay::V_STRIDE + t] = s_newv[d];
-                    if (d < 4) {
-                        uint16_t *sKs = reinterpret_cast<uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES);
-                        uint16_t *sVs = sKs + ATT_CHUNK * 4;
-                        sKs[t * 4 + d] = s_newks[d];
-                        sVs[d * ATT_CHUNK + t] = s_newvs[d];
-                    }
-                }
+            issued++;
+        }
+        if (ok && !att_wait(&full[ci % NS], (uint32_t)(ci / NS) & 1u, ATT_WAIT_LIMIT)) {
+            ok = false;
+            s_bad = 1;
+            atomicOr(p.status, STATUS_TIMEOUT);
+        }
+        uint8_t *sK = stage(ci), *sV = stage(ci) + KB;
+        if (zfrom < PAGE_TOKENS) {
+            // the chunk holding the end of the history: clear what lies past
+            // it (stale values of the page's earlier use may be Inf or NaN, and
+            // 0 * NaN would reach the output) and insert the new token
+            const int d = threadIdx.x;   // 128 threads, one head dim each
+            for (int t = zfrom; t < PAGE_TOKENS; t++) put_v<VT>(sV, t, d, VT == KV_T_Q8 ? 0x80 : 0);
+            if (VT == KV_T_Q8 && d < 4)
+                for (int t = zfrom; t < PAGE_TOKENS; t++) *reinterpret_cast<uint16_t *>(sV + vs_off(t, d)) = 0;
+            if (has_new && pos >= c0 && pos < c0 + PAGE_TOKENS) {
+                const int t = pos - c0;
+                put_k<KT>(sK, t, d, s_newk[d]);
+                put_v<VT>(sV, t, d, s_newv[d]);
+                if (KT == KV_T_Q8 && d < 4) *reinterpret_cast<uint16_t *>(sK + ks_off(t, d)) = s_newks[d];
+                if (VT == KV_T_Q8 && d < 4) *reinterpret_cast<uint16_t *>(sV + vs_off(t, d)) = s_newvs[d];
             }
             __syncthreads();
         }
-
         const int tb = c0 + 16 * warp;   // this warp's 16 tokens
-        if (tb < T1) {
-            const uint8_t *sK = st;
-            const uint8_t *sV = st + Lay::K_BYTES;
-            // ---- scores S[head][token], tokens of n-tile nt, slot c: 4(c>>1) + 2nt + (c&1)
+        if (ok && tb < T1) {
             float S[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; nt++) {
-                const int tr = 16 * warp + 4 * (gid >> 1) + 2 * nt + (gid & 1);
-#pragma unroll
-                for (int i = 0; i < 4; i++) S[nt][i] = 0.0f;
-                if (KVT == 0) {
-#pragma unroll
-                    for (int st8 = 0; st8 < 8; st8++) {
-                        uint2 kb = *reinterpret_cast<const uint2 *>(sK + tr * Lay::K_STRIDE + (16 * st8 + 4 * tig) * 2);
-                        mma16816(S[nt], qa[st8], kb.x, kb.y, S[nt]);
-                    }
-                } else {
-                    const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES);
-                    const int ta = 16 * warp + 4 * tig + 2 * nt;   // tokens of columns 2tig, 2tig+1
-                    // the four block scales of tokens ta and ta + 1
-                    const uint2 ksa = *reinterpret_cast<const uint2 *>(sKs + ta * 4);
-                    const uint2 ksb = *reinterpret_cast<const uint2 *>(sKs + (ta + 1) * 4);
-                    const float2 ka01 = __half22float2(u32_as_h2(ksa.x)), ka23 = __half22float2(u32_as_h2(ksa.y));
-                    const float2 kb01 = __half22float2(u32_as_h2(ksb.x)), kb23 = __half22float2(u32_as_h2(ksb.y));
-                    const float kas[4] = {ka01.x, ka01.y, ka23.x, ka23.y};
-                    const float kbs[4] = {kb01.x, kb01.y, kb23.x, kb23.y};
-#pragma unroll
-                    for (int bl = 0; bl < 4; bl++) {
-                        float tmp[4];
-#pragma unroll
-                        for (int hs = 0; hs < 2; hs++) {
-                            const int st8 = 2 * bl + hs;
-                            uint32_t w = *reinterpret_cast<const uint32_t *>(sK + tr * Lay::K_STRIDE + 16 * st8 + 4 * tig);
-                            uint32_t b0, b1;
-                            codes4_to_h2(w, b0, b1);
-                            if (hs) mma16816(tmp, qa[st8], b0, b1, tmp);
-                            else mma16816(tmp, qa[st8], b0, b1, zero4);
-                        }
-                        const float ka = kas[bl], kb = kbs[bl];
-                        S[nt][0] += ka * tmp[0];
-                        S[nt][1] += kb * tmp[1];
-                        S[nt][2] += ka * tmp[2];
-                        S[nt][3] += kb * tmp[3];
-                    }
-                }
-            }
-            // ---- online softmax on this tile (head gid, tokens 4tig + {0,1,2,3})
-            float sc[4];
-            sc[0] = S[0][0] + S[0][2];
-            sc[1] = S[0][1] + S[0][3];
-            sc[2] = S[1][0] + S[1][2];
-            sc[3] = S[1][1] + S[1][3];
+            qk_tile<KT>(sK, warp, gid, tig, qa, S);
+            // ---- online softmax on this tile (head gid, tokens tb + 4 tig + {0..3})
+            float sc[4] = {S[0][0] + S[0][2], S[0][1] + S[0][3], S[1][0] + S[1][2], S[1][1] + S[1][3]};
             if (gid >= GROUP) sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;   // zero A rows: no head
             if (tb + 16 > T1)   // the range's last tile may end early
 #pragma unroll
@@ -545,9 +474,8 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
             mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 1));
             mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 2));
-            // scores are in log2 units (q carries log2(e)/sqrt(128)); the output
-            // is rescaled only when some head's running max grew (alpha = 1
-            // exactly otherwise), which after the first tiles is rare
+            // the output is rescaled only when some head's running max grew
+            // (alpha = 1 exactly otherwise), which after the first tiles is rare
             const float m_new = fmaxf(m_run, mt);
             const bool grow = m_new > m_run;
             const float alpha = grow ? exp2f(m_run - m_new) : 1.0f;   // m_run = -inf -> 0
@@ -563,56 +491,19 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
                 for (int dn = 0; dn < 16; dn++)
 #pragma unroll
                     for (int i = 0; i < 4; i++) oacc[dn][i] *= alpha;
-            // ---- output += P V
-            if (KVT == 0) {
-                uint32_t pa[4];
-                __half2 h01 = __floats2half2_rn(pr[0], pr[1]), h23 = __floats2half2_rn(pr[2], pr[3]);
-                float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                pa[0] = h2_as_u32(h01);
-                pa[1] = h2_as_u32(__floats2half2_rn(pr[0] - f01.x, pr[1] - f01.y));
-                pa[2] = h2_as_u32(h23);
-                pa[3] = h2_as_u32(__floats2half2_rn(pr[2] - f23.x, pr[3] - f23.y));
-#pragma unroll
-                for (int dn = 0; dn < 16; dn++) {
-                    const int d = 8 * dn + gid;
-                    uint2 vb = *reinterpret_cast<const uint2 *>(sV + d * Lay::V_STRIDE + (16 * warp + 4 * tig) * 2);
-                    mma16816(oacc[dn], pa, vb.x, vb.y, oacc[dn]);
-                }
-            } else {
-                const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + Lay::K_BYTES + Lay::V_BYTES + Lay::KS_BYTES);
-                const int tl = 16 * warp + 4 * tig;
-#pragma unroll
-                for (int bl = 0; bl < 4; bl++) {
-                    const uint2 vsc = *reinterpret_cast<const uint2 *>(sVs + bl * ATT_CHUNK + tl);   // tokens tl..tl+3
-                    const float2 v01 = __half22float2(u32_as_h2(vsc.x)), v23 = __half22float2(u32_as_h2(vsc.y));
-                    const float q4[4] = {pr[0] * v01.x, pr[1] * v01.y, pr[2] * v23.x, pr[3] * v23.y};
-                    uint32_t pa[4];
-                    __half2 h01 = __floats2half2_rn(q4[0], q4[1]), h23 = __floats2half2_rn(q4[2], q4[3]);
-                    float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                    pa[0] = h2_as_u32(h01);
-                    pa[1] = h2_as_u32(__floats2half2_rn(q4[0] - f01.x, q4[1] - f01.y));
-                    pa[2] = h2_as_u32(h23);
-                    pa[3] = h2_as_u32(__floats2half2_rn(q4[2] - f23.x, q4[3] - f23.y));
-#pragma unroll
-                    for (int dq = 0; dq < 4; dq++) {
-                        const int dn = 4 * bl + dq, d = 8 * dn + gid;
-                        uint32_t w = *reinterpret_cast<const uint32_t *>(sV + d * Lay::V_STRIDE + tl);
-                        uint32_t b0, b1;
-                        codes4_to_h2(w, b0, b1);
-                        mma16816(oacc[dn], pa, b0, b1, oacc[dn]);
-                    }
-                }
-            }
+            pv_tile<VT>(sV, warp, gid, tig, pr, oacc);
         }
-        slot = slot + 1 == NS ? 0 : slot + 1;
     }
-    cp_async_wait<0>();
     tl_max(p.tl, 6);
+    __syncthreads();
+    if (s_bad && threadIdx.x == 0)   // copies still in flight land before the ring is reused
+        for (int i = max(0, sent - NS); i < sent; i++)
+            att_wait(&full[i % NS], (uint32_t)(i / NS) & 1u, ATT_WAIT_LIMIT);
 
-    // ---- merge the 4 warps of this CTA (smem reused after the stages)
-    float *wm = reinterpret_cast<float *>(smem);          // [4 warps][4 heads]
+    // ---- merge the 4 warps of this CTA (shared memory reused after the stages)
+    float *wm = reinterpret_cast<float *>(smem);   // [4 warps][4 heads]
     float *wl = wm + 16;
-    float *wo = wl + 16;                                   // [4][4][128]
+    float *wo = wl + 16;                            // [4][4][128]
     float l_tot = l_run;
     l_tot += __shfl_xor_sync(AFULL, l_tot, 1);
     l_tot += __shfl_xor_sync(AFULL, l_tot, 2);
@@ -632,8 +523,8 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         for (int w = 0; w < 4; w++) M = fmaxf(M, wm[w * 4 + head]);
         float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int w = 0; w < 4; w++) {
-            float mw = wm[w * 4 + head];
-            float f = mw == -INFINITY ? 0.0f : exp2f(mw - M);
+            const float mw = wm[w * 4 + head];
+            const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M);
             L += f * wl[w * 4 + head];
             for (int e = 0; e < 4; e++) O[e] += f * wo[(w * 4 + head) * HD + d0 + e];
         }
@@ -645,8 +536,8 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     cluster_arrive_release();   // the partials in s_part (shared memory only)
     cluster_wait_acquire();
     if (rank == 0) {
-        // issue every peer's loads before using any (distributed shared memory
-        // latency is paid once, not once per rank)
+        // issue every peer's loads before using any (the distributed shared
+        // memory latency is paid once, not once per rank)
         float mr[16], lr[16];
         float4 orr[16];
 #pragma unroll
@@ -671,70 +562,117 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             L += f * lr[r];
             O[0] += f * orr[r].x; O[1] += f * orr[r].y; O[2] += f * orr[r].z; O[3] += f * orr[r].w;
         }
-        const float inv = 1.0f / L;
-        const int qd = p.nq * HD;
-        const int kcol = (GROUP * g + head) * HD + d0;   // column of o, the O projection's input
-        float y[4];
-        for (int e = 0; e < 4; e++) y[e] = O[e] * inv;
-        float *o = p.o + (size_t)b * qd + kcol;
-        for (int e = 0; e < 4; e++) o[e] = y[e];
-        // the O projection's operand as fp16 hi + lo parts (elements 4..7 of every
-        // 8 stored /16) and the per-32 sub-block sums, as the GEMM prep writes them
-        __half h[4], hl[4];
-        float part = 0.0f;
-        for (int e = 0; e < 4; e++) {
-            h[e] = __float2half_rn(y[e]);
-            hl[e] = __float2half_rn((y[e] - __half2float(h[e])) * LO_SCALE);
-            part += y[e];
-        }
-        if (d0 & 4)
-            for (int e = 0; e < 4; e++) {
-                h[e] = __hmul(h[e], __float2half(0.0625f));
-                hl[e] = __hmul(hl[e], __float2half(0.0625f));
+        bool finish = nseg == 1;
+        if (!finish) {
+            // several segments: this one's partial goes to global memory; the
+            // last segment of the (row, kv head) to arrive merges them all, in
+            // segment order
+            float *mine = p.seg_part + ((size_t)z * p.kv.n_kv + g) * SEG_PART + head * (HD + 4);
+            if ((threadIdx.x & 31) == 0) { mine[0] = M; mine[1] = L; }
+            *reinterpret_cast<float4 *>(mine + 4 + d0) = make_float4(O[0], O[1], O[2], O[3]);
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int *ticket = p.seg_ticket + b * p.kv.n_kv + g;
+                s_last = atomicAdd(ticket, 1) == nseg - 1;
+                if (s_last) *ticket = 0;   // every segment has arrived: ready for the next launch
+                __threadfence();
             }
-        const size_t ai = act_chunk(kcol >> 8, b, (kcol & 255) >> 3, p.oBp) + (kcol & 7);
-        *reinterpret_cast<uint2 *>(p.o16 + ai) =
-            make_uint2(h2_as_u32(__halves2half2(h[0], h[1])), h2_as_u32(__halves2half2(h[2], h[3])));
-        *reinterpret_cast<uint2 *>(p.o16lo + ai) =
-            make_uint2(h2_as_u32(__halves2half2(hl[0], hl[1])), h2_as_u32(__halves2half2(hl[2], hl[3])));
-        part += __shfl_xor_sync(AFULL, part, 1);
-        part += __shfl_xor_sync(AFULL, part, 2);
-        part += __shfl_xor_sync(AFULL, part, 4);
-        if ((lane & 7) == 0) store_sum(p.osx, kcol >> 8, b, (kcol >> 5) & 7, p.oBp, part);
+            __syncthreads();
+            finish = s_last != 0;
+            if (finish) {
+                const int z0 = z - seg;
+                M = -INFINITY;
+                for (int s = 0; s < nseg; s++)
+                    M = fmaxf(M, __ldcg(p.seg_part + ((size_t)(z0 + s) * p.kv.n_kv + g) * SEG_PART + head * (HD + 4)));
+                L = 0.0f;
+                O[0] = O[1] = O[2] = O[3] = 0.0f;
+                for (int s = 0; s < nseg; s++) {
+                    const float *ps = p.seg_part + ((size_t)(z0 + s) * p.kv.n_kv + g) * SEG_PART + head * (HD + 4);
+                    const float ms = __ldcg(ps);
+                    const float f = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+                    L += f * __ldcg(ps + 1);
+                    const float4 os = __ldcg(reinterpret_cast<const float4 *>(ps + 4 + d0));
+                    O[0] += f * os.x; O[1] += f * os.y; O[2] += f * os.z; O[3] += f * os.w;
+                }
+            }
+        }
+        if (finish) {
+            const float inv = 1.0f / L;
+            const int qd = p.nq * HD;
+            const int kcol = (GROUP * g + head) * HD + d0;   // column of o, the O projection's input
+            float y[4];
+            for (int e = 0; e < 4; e++) y[e] = O[e] * inv;
+            float *o = p.o + (size_t)b * qd + kcol;
+            for (int e = 0; e < 4; e++) o[e] = y[e];
+            // the O projection's operand as fp16 hi + lo parts (elements 4..7 of
+            // every 8 stored / 16) and the per-32 sub-block sums, as the GEMM
+            // prep writes them
+            __half h[4], hl[4];
+            float part = 0.0f;
+            for (int e = 0; e < 4; e++) {
+                h[e] = __float2half_rn(y[e]);
+                hl[e] = __float2half_rn((y[e] - __half2float(h[e])) * LO_SCALE);
+                part += y[e];
+            }
+            if (d0 & 4)
+                for (int e = 0; e < 4; e++) {
+                    h[e] = __hmul(h[e], __float2half(0.0625f));
+                    hl[e] = __hmul(hl[e], __float2half(0.0625f));
+                }
+            const size_t ai = act_chunk(kcol >> 8, b, (kcol & 255) >> 3, p.oBp) + (kcol & 7);
+            *reinterpret_cast<uint2 *>(p.o16 + ai) =
+                make_uint2(h2_as_u32(__halves2half2(h[0], h[1])), h2_as_u32(__halves2half2(h[2], h[3])));
+            *reinterpret_cast<uint2 *>(p.o16lo + ai) =
+                make_uint2(h2_as_u32(__halves2half2(hl[0], hl[1])), h2_as_u32(__halves2half2(hl[2], hl[3])));
+            part += __shfl_xor_sync(AFULL, part, 1);
+            part += __shfl_xor_sync(AFULL, part, 2);
+            part += __shfl_xor_sync(AFULL, part, 4);
+            if ((lane & 7) == 0) store_sum(p.osx, kcol >> 8, b, (kcol >> 5) & 7, p.oBp, part);
+        }
     }
     tl_max(p.tl, 7);
     // peers keep their partials alive until rank 0 has read them (its reads
     // have returned by the time it arrives; nothing needs ordering)
     cluster_arrive_relaxed();
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    // a step whose inputs a device check flagged (or that follows one before
-    // zdec_sync) changes no cache state: the status word is final by now,
-    // every kernel that sets it having completed before this kernel's wait
-    if (has_new && warp == 0 && (*(volatile uint32_t *)p.status & STATUS_STATE_ERRORS) == 0) store_new();
+    // the appended token into its page, unless a device check flagged the step
+    // (the status word is final by now: every kernel that sets it completed
+    // before this kernel's dependency wait)
+    if (has_new && warp == 0 && (*(volatile uint32_t *)p.status & STATUS_STATE_ERRORS) == 0) {
+        const int page = kv_page(p.kv, slot, pos);
+        if (kv_page_ok(p.kv, page)) {
+            uint8_t *k = p.kv.base + (size_t)page * p.kv.page_bytes + coff, *v = k + KB;
+            const int t = pos & (PAGE_TOKENS - 1);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int d = lane + 32 * i;
+                put_k<KT>(k, t, d, s_newk[d]);
+                put_v<VT>(v, t, d, s_newv[d]);
+                if (lane == 0) {
+                    if (KT == KV_T_Q8) *reinterpret_cast<uint16_t *>(k + ks_off(t, i)) = s_newks[i];
+                    if (VT == KV_T_Q8) *reinterpret_cast<uint16_t *>(v + vs_off(t, i)) = s_newvs[i];
+                }
+            }
+        }
+    }
     tl_end(p.tl);
 }
 
-cudaError_t attention_setup(int kv_dtype) {
-    int smem = (int)attention_smem_bytes(kv_dtype, att_max_stages(kv_dtype));
-    cudaError_t e;
-    if (kv_dtype == 0) {
-        e = cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attention_kernel<0>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    } else {
-        e = cudaFuncSetAttribute(attention_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attention_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    }
+// ------------------------------------------------------------------ dispatch ---
+template <int KT, int VT>
+static cudaError_t set_attrs() {
+    const int smem = (int)attention_smem_bytes(KT, VT, att_max_stages(KT, VT));
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<KT, VT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attention_kernel<KT, VT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
-
-int attention_max_clusters(int kv_dtype, int stages, int cs) {
-    if (cs < 1 || cs > 16 || stages < 2 || stages > att_max_stages(kv_dtype)) return 0;
+template <int KT, int VT>
+static int max_clusters(int stages, int cs, int nkv) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, 8, 1);
+    cfg.gridDim = dim3(cs, nkv, 8);
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = attention_smem_bytes(kv_dtype, stages);
+    cfg.dynamicSmemBytes = attention_smem_bytes(KT, VT, stages);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
@@ -743,94 +681,145 @@ int attention_max_clusters(int kv_dtype, int stages, int cs) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    cudaError_t e = kv_dtype ? cudaOccupancyMaxActiveClusters(&n, attention_kernel<1>, &cfg)
-                             : cudaOccupancyMaxActiveClusters(&n, attention_kernel<0>, &cfg);
-    if (e != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attention_kernel<KT, VT>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
+template <int KT, int VT>
+static cudaError_t launch_kt(const AttnParams &p, bool pdl, cudaStream_t s, int nz) {
+    return launch_k(attention_kernel<KT, VT>, dim3(p.cs, p.kv.n_kv, nz), dim3(128),
+                    attention_smem_bytes(KT, VT, p.stages), pdl, p.cs, s, p);
+}
 
-cudaError_t launch_attention(const AttnParams &p0, bool pdl, cudaStream_t stream) {
+// Evaluates CALL(KT, VT) for the runtime type pair (kt, vt) and returns it.
+#define ZDEC_KV_DISPATCH(kt, vt, CALL)                                                   \
+    switch ((kt) * 3 + (vt)) {                                                           \
+        case 0: return CALL(0, 0); case 1: return CALL(0, 1); case 2: return CALL(0, 2); \
+        case 3: return CALL(1, 0); case 4: return CALL(1, 1); case 5: return CALL(1, 2); \
+        case 6: return CALL(2, 0); case 7: return CALL(2, 1); case 8: return CALL(2, 2); \
+        default: break;                                                                  \
+    }
+
+cudaError_t attention_setup(int kt, int vt) {
+#define ZDEC_SET(a, b) set_attrs<a, b>()
+    ZDEC_KV_DISPATCH(kt, vt, ZDEC_SET)
+#undef ZDEC_SET
+    return cudaErrorInvalidValue;
+}
+
+int attention_max_clusters(int kt, int vt, int stages, int cs, int nkv) {
+    if (cs < 1 || cs > 16 || kt < 0 || kt > 2 || vt < 0 || vt > 2 || stages < 2 || stages > att_max_stages(kt, vt))
+        return 0;
+#define ZDEC_MC(a, b) max_clusters<a, b>(stages, cs, nkv)
+    ZDEC_KV_DISPATCH(kt, vt, ZDEC_MC)
+#undef ZDEC_MC
+    return 0;
+}
+
+int attention_stage_limit(int kt, int vt) { return att_max_stages(kt, vt); }
+
+cudaError_t launch_attention(const AttnParams &p0, int nz, bool pdl, cudaStream_t stream) {
     AttnParams p = p0;
-    if (p.cs < 1 || p.cs > 16) return cudaErrorInvalidValue;
-    if (p.stages == 0) p.stages = attention_default_stages(p.kv.kv_dtype);
-    if (p.stages < 2 || p.stages > att_max_stages(p.kv.kv_dtype)) return cudaErrorInvalidValue;
-    dim3 grid(p.cs, p.kv.n_kv, p.B), block(128);
-    size_t smem = attention_smem_bytes(p.kv.kv_dtype, p.stages);
-    if (p.kv.kv_dtype == 0) return launch_k(attention_kernel<0>, grid, block, smem, pdl, p.cs, stream, p);
-    return launch_k(attention_kernel<1>, grid, block, smem, pdl, p.cs, stream, p);
+    const int kt = p.kv.k_type, vt = p.kv.v_type;
+    if (p.cs < 1 || p.cs > 16 || kt < 0 || kt > 2 || vt < 0 || vt > 2 || p.B < 1 || p.B > MAX_B)
+        return cudaErrorInvalidValue;
+    if (nz < p.B || (nz > p.B && (!p.seg_part || !p.seg_ticket))) return cudaErrorInvalidValue;
+    if (p.stages == 0) p.stages = attention_default_stages(kt, vt);
+    if (p.stages < 2 || p.stages > att_max_stages(kt, vt)) return cudaErrorInvalidValue;
+    if (p.seg_min < 1) p.seg_min = 1;
+#define ZDEC_LA(a, b) launch_kt<a, b>(p, pdl, stream, nz)
+    ZDEC_KV_DISPATCH(kt, vt, ZDEC_LA)
+#undef ZDEC_LA
+    return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------ bulk append ---
 // One warp per (layer, token, kv head); lane holds dims lane + 32 i, i.e.
-// element `lane` of Q8_0 block i.
-__global__ void kv_append_kernel(const KvArena a, int slot, int t0, int n,
-                                 const uint16_t *__restrict__ k16, const uint16_t *__restrict__ v16) {
-    long w = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    int lane = threadIdx.x & 31;
-    if (w >= (long)a.n_layers * n * a.n_kv) return;
-    int g = (int)(w % a.n_kv);
-    int t = (int)((w / a.n_kv) % n);
-    int l = (int)(w / ((long)a.n_kv * n));
+// element `lane` of Q8_0 block i.  Every page the tokens land in is already
+// assigned to the slot (the host allocates pages before it enqueues this).
+template <int KT, int VT>
+__global__ void kv_append_kernel(const KvPool a, int slot, int t0, int n, const uint16_t *__restrict__ k16,
+                                 const uint16_t *__restrict__ v16, uint32_t *status) {
+    constexpr uint32_t KB = kv_region_bytes(KT);
+    const long w = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= (long)a.n_layers * n * a.n_kv) return;   // whole warps: the grid covers 32 lanes per item
+    const int g = (int)(w % a.n_kv);
+    const int t = (int)((w / a.n_kv) % n);
+    const int l = (int)(w / ((long)a.n_kv * n));
     const uint16_t *ks = k16 + (((size_t)l * n + t) * a.n_kv + g) * HD;
     const uint16_t *vs = v16 + (((size_t)l * n + t) * a.n_kv + g) * HD;
-    size_t pi = plane_index(a, slot, l, g);
-    int pos = t0 + t;
+    const int pos = t0 + t;
+    const int page = kv_page(a, slot, pos);
+    if (!kv_page_ok(a, page)) {
+        if (lane == 0) atomicOr(status, STATUS_PAGE);
+        return;
+    }
+    uint8_t *k = a.base + (size_t)page * a.page_bytes + kv_chunk_off(a, l, g), *v = k + KB;
+    const int tl = pos & (PAGE_TOKENS - 1);
+#pragma unroll
     for (int i = 0; i < 4; i++) {
-        int d = lane + 32 * i;
-        uint16_t kb = ks[d], vb = vs[d];
-        if (a.kv_dtype == 0) {
-            *reinterpret_cast<uint16_t *>(a.k + pi * a.Lp * (HD * 2) + kv_k16_off(pos, d)) = kb;
-            *reinterpret_cast<uint16_t *>(a.v + pi * a.Lp * (HD * 2) + kv_v16_off(d, pos)) = vb;
-        } else {
-            uint16_t ksb, vsb;
-            int8_t kc = q8_0_lane(__ushort_as_half(kb), ksb);
-            int8_t vc = q8_0_lane(__ushort_as_half(vb), vsb);
-            *reinterpret_cast<int8_t *>(a.k + pi * a.Lp * HD + kv_k8_off(pos, d)) = kc;
-            *reinterpret_cast<int8_t *>(a.v + pi * a.Lp * HD + kv_v8_off(d, pos)) = vc;
-            if (lane == 0) {
-                *reinterpret_cast<uint16_t *>(a.ks + pi * a.Lp * 8 + kv_ks_off(pos, i)) = ksb;
-                *reinterpret_cast<uint16_t *>(a.vs + pi * a.Lp * 8 + kv_vs_off(i, pos)) = vsb;
-            }
+        const int d = lane + 32 * i;
+        uint16_t ksb = 0, vsb = 0;
+        const uint16_t kc = encode_lane<KT>(__ushort_as_half(ks[d]), ksb);
+        const uint16_t vc = encode_lane<VT>(__ushort_as_half(vs[d]), vsb);
+        put_k<KT>(k, tl, d, kc);
+        put_v<VT>(v, tl, d, vc);
+        if (lane == 0) {
+            if (KT == KV_T_Q8) *reinterpret_cast<uint16_t *>(k + ks_off(tl, i)) = ksb;
+            if (VT == KV_T_Q8) *reinterpret_cast<uint16_t *>(v + vs_off(tl, i)) = vsb;
         }
     }
 }
 
-cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const uint16_t *k16,
-                             const uint16_t *v16, cudaStream_t stream) {
-    long warps = (long)a.n_layers * n * a.n_kv;
-    if (warps == 0) return cudaSuccess;
-    kv_append_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(a, slot, t0, n, k16, v16);
+template <int KT, int VT>
+static cudaError_t append_kt(const KvPool &a, int slot, int t0, int n, const uint16_t *k16, const uint16_t *v16,
+                             uint32_t *status, cudaStream_t stream) {
+    const long warps = (long)a.n_layers * n * a.n_kv;
+    kv_append_kernel<KT, VT><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(a, slot, t0, n, k16, v16, status);
     return cudaGetLastError();
 }
 
-// One thread per (token, kv head, dim) of one layer.
-__global__ void kv_read_kernel(const KvArena a, int slot, int layer, int t0, int n, uint8_t *k,
-                               uint8_t *v, uint16_t *ks, uint16_t *vs) {
-    long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+cudaError_t launch_kv_append(const KvPool &a, int slot, int t0, int n, const uint16_t *k16, const uint16_t *v16,
+                             uint32_t *status, cudaStream_t stream) {
+    if ((long)a.n_layers * n * a.n_kv == 0) return cudaSuccess;
+#define ZDEC_AP(x, y) append_kt<x, y>(a, slot, t0, n, k16, v16, status, stream)
+    ZDEC_KV_DISPATCH(a.k_type, a.v_type, ZDEC_AP)
+#undef ZDEC_AP
+    return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ read-back ---
+// One thread per (token, kv head, dim) of one layer: canonical token-major
+// rows; fp16 bits, Q8_0 codes (the stored offset removed) with their scales
+// [n][n_kv][4], or e4m3 codes.  Tokens without a page read as zero.
+__global__ void kv_read_kernel(const KvPool a, int slot, int layer, int t0, int n, uint8_t *k, uint8_t *v,
+                               uint16_t *ks, uint16_t *vs) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)n * a.n_kv * HD) return;
-    int d = (int)(i % HD), g = (int)((i / HD) % a.n_kv), t = (int)(i / ((long)HD * a.n_kv));
-    size_t pi = plane_index(a, slot, layer, g);
-    int pos = t0 + t;
-    if (a.kv_dtype == 0) {
-        reinterpret_cast<uint16_t *>(k)[i] = *reinterpret_cast<const uint16_t *>(a.k + pi * a.Lp * (HD * 2) + kv_k16_off(pos, d));
-        reinterpret_cast<uint16_t *>(v)[i] = *reinterpret_cast<const uint16_t *>(a.v + pi * a.Lp * (HD * 2) + kv_v16_off(d, pos));
-    } else {
-        k[i] = a.k[pi * a.Lp * HD + kv_k8_off(pos, d)];
-        v[i] = a.v[pi * a.Lp * HD + kv_v8_off(d, pos)];
-        if ((d & 31) == 0) {
-            size_t o = ((size_t)t * a.n_kv + g) * 4 + (d >> 5);
-            ks[o] = *reinterpret_cast<const uint16_t *>(a.ks + pi * a.Lp * 8 + kv_ks_off(pos, d >> 5));
-            vs[o] = *reinterpret_cast<const uint16_t *>(a.vs + pi * a.Lp * 8 + kv_vs_off(d >> 5, pos));
-        }
+    const int d = (int)(i % HD), g = (int)((i / HD) % a.n_kv), t = (int)(i / ((long)HD * a.n_kv));
+    const int pos = t0 + t;
+    const int page = kv_page(a, slot, pos);
+    const bool ok = kv_page_ok(a, page);
+    const uint8_t *kr = ok ? a.base + (size_t)page * a.page_bytes + kv_chunk_off(a, layer, g) : nullptr;
+    const uint8_t *vr = ok ? kr + kv_region_bytes(a.k_type) : nullptr;
+    const int tl = pos & (PAGE_TOKENS - 1);
+    const size_t so = ((size_t)t * a.n_kv + g) * 4 + (d >> 5);
+    if (a.k_type == KV_T_F16) reinterpret_cast<uint16_t *>(k)[i] = ok ? *reinterpret_cast<const uint16_t *>(kr + k16_off(tl, d)) : 0;
+    else k[i] = ok ? (uint8_t)(kr[k8_off(tl, d)] ^ (a.k_type == KV_T_Q8 ? 0x80 : 0)) : 0;
+    if (a.v_type == KV_T_F16) reinterpret_cast<uint16_t *>(v)[i] = ok ? *reinterpret_cast<const uint16_t *>(vr + v16_off(tl, d)) : 0;
+    else v[i] = ok ? (uint8_t)(vr[v8_off(tl, d)] ^ (a.v_type == KV_T_Q8 ? 0x80 : 0)) : 0;
+    if ((d & 31) == 0) {
+        if (a.k_type == KV_T_Q8) ks[so] = ok ? *reinterpret_cast<const uint16_t *>(kr + ks_off(tl, d >> 5)) : 0;
+        if (a.v_type == KV_T_Q8) vs[so] = ok ? *reinterpret_cast<const uint16_t *>(vr + vs_off(tl, d >> 5)) : 0;
     }
 }
 
-cudaError_t launch_kv_read(const KvArena &a, int slot, int layer, int t0, int n, uint8_t *k,
-                           uint8_t *v, uint16_t *ks, uint16_t *vs, cudaStream_t stream) {
-    long total = (long)n * a.n_kv * HD;
+cudaError_t launch_kv_read(const KvPool &a, int slot, int layer, int t0, int n, uint8_t *k, uint8_t *v,
+                           uint16_t *ks, uint16_t *vs, cudaStream_t stream) {
+    const long total = (long)n * a.n_kv * HD;
     if (total == 0) return cudaSuccess;
     kv_read_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(a, slot, layer, t0, n, k, v, ks, vs);
     return cudaGetLastError();

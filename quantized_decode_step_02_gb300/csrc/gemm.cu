@@ -820,7 +820,8 @@ cudaError_t launch_gemm(const GemmParams &p, int epi, int impl, bool pdl, cudaSt
 // --------------------------------------------------------- argmax final ---
 __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *__restrict__ idxs,
                                     int nparts, int B, int32_t *ids, const int32_t *positions,
-                                    int32_t *len_dev, const uint32_t *status, unsigned long long *tl) {
+                                    const int32_t *slots, int32_t *len_dev, const uint32_t *status,
+                                    unsigned long long *tl) {
     tl_min(tl, 0);
     pdl_launch_dependents();
     pdl_wait();
@@ -848,16 +849,17 @@ __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *_
             if (sv[w] > bv || (sv[w] == bv && si[w] < bi)) { bv = sv[w]; bi = si[w]; }
         ids[b] = bi == 0x7FFFFFFF ? 0 : bi;
         // the length advances only for a step no device check has flagged
-        if ((*(volatile const uint32_t *)status & STATUS_STATE_ERRORS) == 0) len_dev[b] = positions[b] + 1;
+        if ((*(volatile const uint32_t *)status & STATUS_STATE_ERRORS) == 0) len_dev[slots[b]] = positions[b] + 1;
         tl_end(tl);
     }
 }
 
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
-                                int32_t *ids, const int32_t *positions, int32_t *len_dev,
-                                const uint32_t *status, bool pdl, cudaStream_t stream, unsigned long long *tl) {
+                                int32_t *ids, const int32_t *positions, const int32_t *slots,
+                                int32_t *len_dev, const uint32_t *status, bool pdl, cudaStream_t stream,
+                                unsigned long long *tl) {
     return launch_k(argmax_final_kernel, dim3(B), dim3(256), 0, pdl, 1, stream, amax_val, amax_idx,
-                    nparts, B, ids, positions, len_dev, status, tl);
+                    nparts, B, ids, positions, slots, len_dev, status, tl);
 }
 
 }  // namespace zdec

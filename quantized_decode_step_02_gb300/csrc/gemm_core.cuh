@@ -1,7 +1,7 @@
-// gemm_core.cuh -- the per-stage Q4_K x activation arithmetic shared by the
-// projection kernel (gemm.cu) and the persistent step kernel (step.cu): the
-// stage buffer layout, the tile-block decode into mma A fragments, and one
-// warp's contribution of a 16-row tile block times the staged activations.
+// gemm_core.cuh -- the per-stage Q4_K x activation arithmetic of the
+// projection kernel (gemm.cu): the stage buffer layout, the tile-block decode
+// into mma A fragments, and one warp's contribution of a 16-row tile block
+// times the staged activations.
 #pragma once
 #include "zdec_kernels.cuh"
 

@@ -169,7 +169,7 @@ cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int 
 // ---------------------------------------------------------------- embed ---
 // Block b gathers row tokens[b] of the tied embedding: thread = (sb, sub-block).
 __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
-                             const int32_t *tokens, const int32_t *positions,
+                             const int32_t *tokens, const int32_t *positions, const int32_t *slots,
                              const int32_t *len_dev, uint32_t *status, int B,
                              float *__restrict__ x, int ldx, const float *__restrict__ gain,
                              __half *u, __half *ulo, __half *usx, int Bp, float *part,
@@ -182,7 +182,7 @@ __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
     int b = blockIdx.x;
     if (b >= B) return;
     int tok = tokens[b];
-    if (threadIdx.x == 0 && positions[b] != len_dev[b]) atomicOr(status, STATUS_POSITION);
+    if (threadIdx.x == 0 && positions[b] != len_dev[slots[b]]) atomicOr(status, STATUS_POSITION);
     if (tok < 0 || tok >= vocab) {               // flagged; row 0 keeps the step well defined
         if (threadIdx.x == 0) atomicOr(status, STATUS_TOKEN);
         tok = 0;
@@ -224,11 +224,12 @@ __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
 }
 
 cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
-                         const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
-                         float *x, int ldx, const float *gain, __half *u, __half *ulo, __half *usx,
-                         int Bp, float *part, bool pdl, cudaStream_t stream, unsigned long long *tl) {
+                         const int32_t *positions, const int32_t *slots, const int32_t *len_dev,
+                         uint32_t *status, int B, float *x, int ldx, const float *gain, __half *u,
+                         __half *ulo, __half *usx, int Bp, float *part, bool pdl, cudaStream_t stream,
+                         unsigned long long *tl) {
     return launch_k(embed_kernel, dim3(B), dim3(128), 0, pdl, 1, stream, E, nsb, vocab, tokens,
-                    positions, len_dev, status, B, x, ldx, gain, u, ulo, usx, Bp, part, tl);
+                    positions, slots, len_dev, status, B, x, ldx, gain, u, ulo, usx, Bp, part, tl);
 }
 
 }  // namespace zdec

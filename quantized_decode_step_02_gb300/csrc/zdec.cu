@@ -1,8 +1,9 @@
 // zdec.cu -- host runtime behind include/zdec.h: weight upload + repack, the
-// KV arena, the per-step workspace, the launch sequence of one decode step
-// (replayed as a CUDA graph whose kernel edges are programmatic, so each
-// kernel's weight prefetch overlaps its predecessor's tail), and the
-// read-backs the parity tests use.
+// paged KV pool (block tables, a page allocator, sequence slots), the
+// per-step workspace, the launch sequence of one decode step (replayed as a
+// CUDA graph whose kernel edges are programmatic, so each kernel's weight
+// prefetch overlaps its predecessor's tail), and the read-backs the parity
+// tests use.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -59,6 +60,7 @@ int pick_cs(int groups, int nsb, Slots slots_of, int max_cs = 16) {
 int batch_class(int B) { return B == 1 ? 0 : (B <= 4 ? 1 : (B <= 8 ? 2 : (B <= 16 ? 3 : 4))); }
 constexpr int CLASS_B[5] = {1, 4, 8, 16, 32};
 enum { MAT_QKV, MAT_O, MAT_GU, MAT_DOWN, MAT_LM, N_MAT };
+constexpr int MAX_SEGS = 4;   // attention segment slots per row of a step, at most
 
 struct LayerW {
     uint8_t *qkv, *o, *gu, *down;
@@ -70,11 +72,15 @@ struct Launch {      // one entry of a profiled step
     cudaEvent_t t0, t1;
 };
 
+struct AttnPlan {    // attention launch shape for a batch size
+    int cs, segs, stages;
+};
+
 }  // namespace
 
 struct zdec_ctx {
     zdec_model_desc d{};
-    int kv_dtype = 0, max_B = 0, max_L = 0, Lp = 0, Bp_max = 0;
+    int k_type = 0, v_type = 0, max_B = 0, max_L = 0, Bp_max = 0;
     int qd = 0, kvd = 0, qkv_ld = 0, nsb_h = 0, nsb_f = 0, nsb_q = 0, nrt_vocab = 0;
     int num_sms = 0;
     cudaStream_t stream = nullptr;
@@ -85,16 +91,23 @@ struct zdec_ctx {
     uint8_t *embed = nullptr;
     float *final_norm = nullptr;
     std::vector<LayerW> L;
-    KvArena arena{};
-    size_t arena_bytes = 0;
-    std::vector<void *> arena_allocs;
+    // paged KV pool
+    KvPool pool{};
+    uint8_t *pool_mem = nullptr;
+    size_t pool_bytes = 0;
+    int max_pages = 0;                 // block-table entries per slot
+    std::vector<int> free_pages;       // stack of free page indices
+    int32_t *table_host = nullptr;     // pinned mirror of the block tables [max_B][max_pages]
+    int32_t *table_dev = nullptr;
     float2 *rope = nullptr;
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *x = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *logits = nullptr;
-    float *part = nullptr, *amax_v = nullptr;
-    int *amax_i = nullptr, *tickets = nullptr;
+    float *amax_v = nullptr;
+    int *amax_i = nullptr;
     float *rms_part = nullptr;          // per-group sums of x^2 feeding the next RMSNorm scale
+    float *seg_part = nullptr;          // attention partials of rows cut into several segments
+    int *seg_ticket = nullptr;
     // GEMM act planes (hi, lo) and sub-block sums: x* for the normed residual,
     // o* for the attention output, a* for the SwiGLU output
     __half *x16 = nullptr, *x16lo = nullptr, *sx = nullptr;
@@ -102,39 +115,28 @@ struct zdec_ctx {
     __half *a16 = nullptr, *a16lo = nullptr, *asx = nullptr;
     int cs_tab[4][5][N_MAT] = {};   // K split per (projection kernel, batch class, matrix); 0: unset
     int32_t *tok_dev = nullptr, *pos_dev = nullptr, *ids_dev = nullptr, *len_dev = nullptr;
+    int32_t *slots_dev = nullptr;      // [max_B] cache slot of each row of a step
+    int32_t *ident_dev = nullptr;      // [max_B] 0, 1, 2, ...
     uint32_t *status = nullptr;
     uint4 *qfrag = nullptr;            // [max_B][n_q][32] query fragments (QKV epilogue -> attention)
     int32_t *pinned_io = nullptr;      // [2*max_B] staging of host tokens/positions
     // host state
     std::vector<int> len_host;
+    std::vector<int32_t> slots_cur;    // the row -> slot map slots_dev holds (its first slots_n rows)
+    int slots_n = 0;
     int gemm_impl = 0, matvec_max_B = 0;
     int b1_impl = 3;                   // projection kernel at B = 1 (ZDEC_B1_IMPL)
     size_t prefetch_cap = 0;   // bytes of the next matrix a GEMM warms in L2 (0: off; ZDEC_L2_PREFETCH_MB)
     long long wait_limit = 0;  // projection stage-wait bound in clock cycles (0: the kernels' ~2 s)
-    std::map<std::tuple<int, const void *, int>, cudaGraphExec_t> graphs;
+    std::map<std::tuple<int, const void *, int, int>, cudaGraphExec_t> graphs;   // (B, logits, impl, segments)
     std::string err;
-    int last_kernels = 0, last_splits = 0;
+    int last_kernels = 0, last_splits = 0, last_segs = 0;
     // instrumentation of the next/current eager step
     std::vector<Launch> *prof = nullptr;
     float *capture_dev_host = nullptr;   // pinned [L+1][B][H] while a capture is armed
     float *capture_user = nullptr;       // [B][L+1][H]
-    // persistent step kernel (step.cu)
-    int engine = ZDEC_ENGINE_AUTO, last_engine = ZDEC_ENGINE_KERNELS;
-    int step_grid = 0;                   // CTAs (0: the persistent kernel is unavailable)
-    int step_slots[2] = {0, 0};          // ring slots for B <= 4 and B <= 8
-    void *step_buf = nullptr;            // its buffers (one allocation)
-    StepLayerW *d_layers = nullptr;
-    float *s_q = nullptr, *s_gpart = nullptr, *s_apart = nullptr, *s_rms_ffn = nullptr, *s_capture = nullptr;
-    __half *g16 = nullptr, *g16lo = nullptr, *gsx = nullptr;
-    int *s_cnt = nullptr, *s_ok = nullptr, *s_abort = nullptr;
-    int s_ncnt = 0;
-    bool persistent_eager = false;       // its CUDA graph capture failed: launch it directly
-    int step_pf_items = 0;               // L2 prefetch distance (items per CTA; ZDEC_STEP_PF_ITEMS)
-    int step_att_min = 8;                // attention units per CTA at least (ZDEC_STEP_ATT_MIN)
-    unsigned long long *trace = nullptr; // phase timeline of the last persistent step, or null
-    size_t trace_entries = 0;
     bool trace_on = false;               // tracing requested (zdec_set_trace)
-    unsigned long long *ktl = nullptr;   // kernel engine: [launches][4] timeline of the last step
+    unsigned long long *ktl = nullptr;   // [launches][8] timeline of the last traced step
     unsigned long long *ktl_init = nullptr;   // pinned: its initial values
     size_t ktl_entries = 0;
     std::vector<int> ktl_kinds;          // kernel kind of each launch of the last traced step
@@ -180,11 +182,11 @@ static void free_ctx(zdec_ctx *ctx) {
     if (!ctx) return;
     for (auto &kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
     cudaFree(ctx->wbuf);
-    for (void *p : ctx->arena_allocs) cudaFree(p);
+    cudaFree(ctx->pool_mem);
+    cudaFree(ctx->table_dev);
+    cudaFreeHost(ctx->table_host);
     cudaFree(ctx->rope);
     cudaFree(ctx->ws);
-    cudaFree(ctx->step_buf);
-    cudaFree(ctx->trace);
     cudaFree(ctx->ktl);
     cudaFreeHost(ctx->ktl_init);
     cudaFreeHost(ctx->pinned_io);
@@ -244,96 +246,20 @@ static zdec_status upload_weights(zdec_ctx *ctx, const zdec_weights *w) {
     return done(ZDEC_OK);
 }
 
-// Ring slots and CTAs of the persistent step kernel, and its buffers.  The
-// kernel runs two CTAs per SM when they fit (one otherwise); it is left
-// unavailable (step_grid = 0) when the device cannot launch it cooperatively,
-// or when the attention output width differs from the hidden size.
-static zdec_status step_configure(zdec_ctx *ctx) {
-    const zdec_model_desc &d = ctx->d;
-    int dev = 0, coop = 0, smem_sm = 0, reserved = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-    if (getenv("ZDEC_NO_PERSISTENT") || !coop || ctx->qd != d.hidden || ctx->num_sms < 1) return ZDEC_OK;
-    if (const char *e = getenv("ZDEC_STEP_PF_ITEMS")) ctx->step_pf_items = std::max(0, atoi(e));
-    if (const char *e = getenv("ZDEC_STEP_ATT_MIN")) ctx->step_att_min = std::max(1, atoi(e));
-    int per_sm = 2;
-    for (int v = 0; v < 2; v++) {
-        const int B = v ? STEP_MAX_B : 4;
-        const size_t static_smem = 11 * 1024;   // the kernel's own __shared__ state
-        int slots = (int)(((size_t)smem_sm / 2 - reserved - static_smem) / (step_slot_bytes(B) + 16));
-        // the attention's warp pairs need a slot count divisible by their number (<= 4)
-        slots = std::max(2, std::min(8, slots));
-        if (slots == 5) slots = 4;
-        if (slots == 7) slots = 6;
-        int fit = 0;
-        while (true) {
-            if (step_setup(B, ctx->kv_dtype, slots, &fit) != cudaSuccess) {
-                cudaGetLastError();
-                return ZDEC_OK;
-            }
-            if (fit >= 2 || slots <= 2) break;
-            slots = slots == 6 ? 4 : slots - 1;
-        }
-        if (fit < 1) return ZDEC_OK;
-        per_sm = std::min(per_sm, fit);
-        ctx->step_slots[v] = slots;
-    }
-    const int grid = per_sm * ctx->num_sms;
-    const int H = d.hidden, NL = d.n_layers, Bm = std::min(ctx->max_B, STEP_MAX_B);
-    ctx->s_ncnt = step_counter_count(NL, H, d.ffn, d.vocab, d.n_q_heads, d.n_kv_heads);
-    size_t w = 0;
-    auto t = [&](size_t bytes) { size_t o = w; w = align_up(w + bytes, 256); return o; };
-    auto plane = [&](int K) { return (size_t)(K / QK) * Bm * 256 * 2; };
-    const size_t o_layers = t(sizeof(StepLayerW) * NL);
-    const size_t o_q = t((size_t)Bm * ctx->qd * 4);
-    const size_t o_gp = t(step_gpart_floats(H, d.ffn, d.vocab, d.n_q_heads, d.n_kv_heads, Bm, grid) * 4);
-    const size_t o_ap = t(step_apart_floats(d.n_kv_heads, Bm, grid) * 4);
-    const size_t o_rf = t((size_t)(H / 128) * MAX_B * 4);
-    const size_t o_cap = t((size_t)(NL + 1) * Bm * H * 4);
-    const size_t o_g = t(plane(H)), o_glo = t(plane(H)), o_gsx = t((size_t)(H / QK) * Bm * 16 * 2);
-    const size_t o_cnt = t((size_t)ctx->s_ncnt * 4), o_ok = t(4), o_ab = t(4);
-    if (cudaMalloc(&ctx->step_buf, w) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(nullptr, ZDEC_ERR_OOM, "cannot allocate %zu bytes for the step kernel", w);
-    }
-    uint8_t *b = (uint8_t *)ctx->step_buf;
-    ctx->d_layers = (StepLayerW *)(b + o_layers);
-    ctx->s_q = (float *)(b + o_q);
-    ctx->s_gpart = (float *)(b + o_gp);
-    ctx->s_apart = (float *)(b + o_ap);
-    ctx->s_rms_ffn = (float *)(b + o_rf);
-    ctx->s_capture = (float *)(b + o_cap);
-    ctx->g16 = (__half *)(b + o_g);
-    ctx->g16lo = (__half *)(b + o_glo);
-    ctx->gsx = (__half *)(b + o_gsx);
-    ctx->s_cnt = (int *)(b + o_cnt);
-    ctx->s_ok = (int *)(b + o_ok);
-    ctx->s_abort = (int *)(b + o_ab);
-    std::vector<StepLayerW> lw(NL);
-    for (int l = 0; l < NL; l++)
-        lw[l] = {ctx->L[l].qkv, ctx->L[l].o, ctx->L[l].gu, ctx->L[l].down, ctx->L[l].attn_norm, ctx->L[l].ffn_norm};
-    if (cudaMemsetAsync(ctx->step_buf, 0, w, ctx->stream) != cudaSuccess ||
-        cudaMemcpyAsync(ctx->d_layers, lw.data(), sizeof(StepLayerW) * NL, cudaMemcpyHostToDevice, ctx->stream) !=
-            cudaSuccess ||
-        cudaStreamSynchronize(ctx->stream) != cudaSuccess)
-        return fail(nullptr, ZDEC_ERR_CUDA, "step kernel buffers: %s", cudaGetErrorString(cudaGetLastError()));
-    ctx->step_grid = grid;
-    return ZDEC_OK;
-}
+static bool kv_type_ok(int t) { return t == ZDEC_KV_F16 || t == ZDEC_KV_Q8_0 || t == ZDEC_KV_FP8; }
 
-extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights,
-                                   zdec_kv_dtype kv_dtype, int max_B, int max_L, void *cuda_stream,
-                                   zdec_ctx **out) {
+extern "C" zdec_status zdec_create_cache(const zdec_model_desc *desc, const zdec_weights *weights,
+                                         const zdec_cache_desc *cache, void *cuda_stream, zdec_ctx **out) {
     zdec_ctx *ctx = nullptr;
-    if (!desc || !weights || !out) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    if (!desc || !weights || !cache || !out) return fail(ctx, ZDEC_ERR_ARG, "null argument");
     *out = nullptr;
     zdec_status vs = validate_desc(desc);
     if (vs != ZDEC_OK) return vs;
-    if (kv_dtype != ZDEC_KV_F16 && kv_dtype != ZDEC_KV_Q8_0) return fail(ctx, ZDEC_ERR_ARG, "bad kv_dtype");
+    if (!kv_type_ok(cache->k_type) || !kv_type_ok(cache->v_type)) return fail(ctx, ZDEC_ERR_ARG, "bad K or V cache type");
+    const int max_B = cache->max_B, max_L = cache->max_L;
     if (max_B < 1 || max_B > MAX_B) return fail(ctx, ZDEC_ERR_ARG, "max_B must be in [1, %d]", MAX_B);
     if (max_L < 1) return fail(ctx, ZDEC_ERR_ARG, "max_L must be >= 1");
+    if (cache->pool_tokens < 0) return fail(ctx, ZDEC_ERR_ARG, "pool_tokens must be >= 0");
     if (!weights->embed || !weights->final_norm || !weights->attn_norm || !weights->ffn_norm ||
         !weights->wq || !weights->wk || !weights->wv || !weights->wo || !weights->w_gate ||
         !weights->w_up || !weights->w_down)
@@ -342,10 +268,10 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     ctx = new zdec_ctx();
     ctx->d = *desc;
     const zdec_model_desc &d = ctx->d;
-    ctx->kv_dtype = kv_dtype;
+    ctx->k_type = cache->k_type;
+    ctx->v_type = cache->v_type;
     ctx->max_B = max_B;
     ctx->max_L = max_L;
-    ctx->Lp = (int)align_up((size_t)max_L, ATT_CHUNK);
     ctx->Bp_max = (int)align_up((size_t)max_B, 8);
     ctx->qd = d.n_q_heads * d.head_dim;
     ctx->kvd = d.n_kv_heads * d.head_dim;
@@ -396,31 +322,40 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
         ctx->L[l] = {ctx->wbuf + oq[l], ctx->wbuf + oo[l], ctx->wbuf + og[l], ctx->wbuf + od[l],
                      reinterpret_cast<float *>(ctx->wbuf + on1[l]), reinterpret_cast<float *>(ctx->wbuf + on2[l])};
 
-    // ---- KV arena
-    KvArena &a = ctx->arena;
-    a.kv_dtype = kv_dtype;
-    a.n_layers = NL;
-    a.n_kv = d.n_kv_heads;
-    a.Lp = ctx->Lp;
-    size_t planes = (size_t)max_B * NL * d.n_kv_heads;
-    size_t kb = planes * ctx->Lp * HD * (kv_dtype ? 1 : 2);
-    std::vector<std::pair<uint8_t **, size_t>> want = {{&a.k, kb}, {&a.v, kb}};
-    if (kv_dtype) {
-        want.push_back({&a.ks, planes * ctx->Lp * 4 * 2});
-        want.push_back({&a.vs, planes * ctx->Lp * 4 * 2});
-    }
-    for (auto &w : want) {
-        void *p = nullptr;
-        if (cudaMalloc(&p, w.second) != cudaSuccess) {
+    // ---- paged KV pool: pages of 64 tokens (all layers and kv heads, K and V),
+    // one block table per slot
+    {
+        KvPool &p = ctx->pool;
+        p.k_type = ctx->k_type;
+        p.v_type = ctx->v_type;
+        p.n_layers = NL;
+        p.n_kv = d.n_kv_heads;
+        p.page_bytes = (size_t)NL * d.n_kv_heads * (kv_region_bytes(p.k_type) + kv_region_bytes(p.v_type));
+        ctx->max_pages = (max_L + PAGE_TOKENS - 1) / PAGE_TOKENS;
+        const long long want = cache->pool_tokens > 0 ? cache->pool_tokens : (long long)max_B * ctx->max_pages * PAGE_TOKENS;
+        const long long pages = (want + PAGE_TOKENS - 1) / PAGE_TOKENS;
+        if (pages > (1LL << 30)) return bail(fail(nullptr, ZDEC_ERR_ARG, "pool of %lld pages is too large", pages));
+        p.n_pages = (int)pages;
+        p.max_pages = ctx->max_pages;
+        ctx->pool_bytes = (size_t)p.n_pages * p.page_bytes;
+        if (cudaMalloc(&ctx->pool_mem, ctx->pool_bytes) != cudaSuccess) {
             cudaGetLastError();
-            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate the KV arena (%zu bytes for max_B=%d, max_L=%d)",
-                             w.second, max_B, max_L));
+            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate the KV pool (%zu bytes: %d pages of %zu)",
+                             ctx->pool_bytes, p.n_pages, p.page_bytes));
         }
-        ctx->arena_allocs.push_back(p);
-        *w.first = (uint8_t *)p;
-        ctx->arena_bytes += w.second;
-        if (cudaMemsetAsync(p, 0, w.second, ctx->stream) != cudaSuccess)
-            return bail(fail(nullptr, ZDEC_ERR_CUDA, "arena memset failed"));
+        p.base = ctx->pool_mem;
+        const size_t tb = (size_t)max_B * ctx->max_pages * sizeof(int32_t);
+        if (cudaMalloc(&ctx->table_dev, tb) != cudaSuccess || cudaMallocHost(&ctx->table_host, tb) != cudaSuccess) {
+            cudaGetLastError();
+            return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate the block tables"));
+        }
+        for (size_t i = 0; i < (size_t)max_B * ctx->max_pages; i++) ctx->table_host[i] = -1;
+        if (cudaMemsetAsync(ctx->pool_mem, 0, ctx->pool_bytes, ctx->stream) != cudaSuccess ||
+            cudaMemcpyAsync(ctx->table_dev, ctx->table_host, tb, cudaMemcpyHostToDevice, ctx->stream) != cudaSuccess)
+            return bail(fail(nullptr, ZDEC_ERR_CUDA, "KV pool initialisation failed"));
+        p.table = ctx->table_dev;
+        ctx->free_pages.resize(p.n_pages);
+        for (int i = 0; i < p.n_pages; i++) ctx->free_pages[i] = p.n_pages - 1 - i;   // page 0 taken first
     }
 
     // ---- RoPE table [max_L][64] (cos, sin), angles in double
@@ -443,23 +378,22 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     // ---- workspace
     {
         const int Bm = max_B, Bp = ctx->Bp_max;
-        const int Kmax = std::max({H, F, ctx->qd});
         int lm_grid = n_groups(ctx->nrt_vocab) * 8;   // any cluster split of the LM head
         size_t w = 0;
         auto t = [&](size_t bytes) { size_t o = w; w = align_up(w + bytes, 256); return o; };
         size_t ox = t((size_t)Bm * H * 4), oqkv = t((size_t)Bm * ctx->qkv_ld * 4), oo2 = t((size_t)Bm * ctx->qd * 4);
         size_t oact = t((size_t)Bm * F * 4), olog = t((size_t)Bm * d.vocab * 4);
-        size_t opart = t((size_t)Bm * d.n_kv_heads * 64 * 4 * (HD + 2) * 4);
         size_t oav = t((size_t)lm_grid * MAX_B * 4), oai = t((size_t)lm_grid * MAX_B * 4);
-        size_t otk = t((size_t)Bm * d.n_kv_heads * 4);
         size_t orms = t((size_t)(n_groups(H / 16) + 1) * MAX_B * 4);
+        size_t osp = t((size_t)Bm * MAX_SEGS * d.n_kv_heads * 4 * (HD + 4) * 4);
+        size_t ost = t((size_t)MAX_B * d.n_kv_heads * 4);
         auto plane = [&](int K) { return (size_t)(K / QK) * Bp * 256 * 2; };
         auto sums = [&](int K) { return (size_t)(K / QK) * Bp * 16 * 2; };
         size_t ox16 = t(plane(H)), ox16lo = t(plane(H)), osx = t(sums(H));
         size_t oo16 = t(plane(ctx->qd)), oo16lo = t(plane(ctx->qd)), oosx = t(sums(ctx->qd));
         size_t oa16 = t(plane(F)), oa16lo = t(plane(F)), oasx = t(sums(F));
-        (void)Kmax;
-        size_t otok = t(Bm * 4), opos = t(Bm * 4), oids = t(Bm * 4), olen = t(Bm * 4), ost = t(4);
+        size_t otok = t(Bm * 4), opos = t(Bm * 4), oids = t(Bm * 4), olen = t(Bm * 4), ostat = t(4);
+        size_t oslot = t(Bm * 4), oident = t(Bm * 4);
         size_t oqf = t((size_t)Bm * d.n_q_heads * 32 * 16);
         ctx->ws_bytes = w;
         if (cudaMalloc(&ctx->ws, w) != cudaSuccess) {
@@ -468,20 +402,30 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
         }
         uint8_t *b = (uint8_t *)ctx->ws;
         ctx->x = (float *)(b + ox); ctx->qkv = (float *)(b + oqkv); ctx->o = (float *)(b + oo2);
-        ctx->act = (float *)(b + oact); ctx->logits = (float *)(b + olog); ctx->part = (float *)(b + opart);
-        ctx->amax_v = (float *)(b + oav); ctx->amax_i = (int *)(b + oai); ctx->tickets = (int *)(b + otk);
+        ctx->act = (float *)(b + oact); ctx->logits = (float *)(b + olog);
+        ctx->amax_v = (float *)(b + oav); ctx->amax_i = (int *)(b + oai);
         ctx->rms_part = (float *)(b + orms);
+        ctx->seg_part = (float *)(b + osp); ctx->seg_ticket = (int *)(b + ost);
         ctx->x16 = (__half *)(b + ox16); ctx->x16lo = (__half *)(b + ox16lo); ctx->sx = (__half *)(b + osx);
         ctx->o16 = (__half *)(b + oo16); ctx->o16lo = (__half *)(b + oo16lo); ctx->osx = (__half *)(b + oosx);
         ctx->a16 = (__half *)(b + oa16); ctx->a16lo = (__half *)(b + oa16lo); ctx->asx = (__half *)(b + oasx);
         ctx->tok_dev = (int32_t *)(b + otok); ctx->pos_dev = (int32_t *)(b + opos);
         ctx->ids_dev = (int32_t *)(b + oids); ctx->len_dev = (int32_t *)(b + olen);
-        ctx->status = (uint32_t *)(b + ost);
+        ctx->status = (uint32_t *)(b + ostat);
+        ctx->slots_dev = (int32_t *)(b + oslot); ctx->ident_dev = (int32_t *)(b + oident);
         ctx->qfrag = (uint4 *)(b + oqf);
         if (cudaMemsetAsync(ctx->ws, 0, w, ctx->stream) != cudaSuccess)
             return bail(fail(nullptr, ZDEC_ERR_CUDA, "workspace memset failed"));
         if (cudaMallocHost(&ctx->pinned_io, 2 * Bm * sizeof(int32_t)) != cudaSuccess)
             return bail(fail(nullptr, ZDEC_ERR_OOM, "cannot allocate pinned staging"));
+        std::vector<int32_t> ident(Bm);
+        for (int i = 0; i < Bm; i++) ident[i] = i;
+        if (cudaStreamSynchronize(ctx->stream) != cudaSuccess ||
+            cudaMemcpy(ctx->ident_dev, ident.data(), Bm * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(ctx->slots_dev, ident.data(), Bm * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+            return bail(fail(nullptr, ZDEC_ERR_CUDA, "slot map upload failed"));
+        ctx->slots_cur = ident;
+        ctx->slots_n = Bm;
     }
     {
         // K splits of every projection for every kernel and batch class, from
@@ -509,12 +453,8 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
                                 ctx->cs_tab[impl][c][0], ctx->cs_tab[impl][c][1], ctx->cs_tab[impl][c][2],
                                 ctx->cs_tab[impl][c][3], ctx->cs_tab[impl][c][4]);
     }
-    if (attention_setup(kv_dtype) != cudaSuccess)
+    if (attention_setup(ctx->k_type, ctx->v_type) != cudaSuccess)
         return bail(fail(nullptr, ZDEC_ERR_CUDA, "attention smem attribute failed"));
-    {
-        zdec_status ss = step_configure(ctx);
-        if (ss != ZDEC_OK) return bail(ss);
-    }
 
     zdec_status us = upload_weights(ctx, weights);
     if (us != ZDEC_OK) {
@@ -527,6 +467,18 @@ extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weigh
     return ZDEC_OK;
 }
 
+extern "C" zdec_status zdec_create(const zdec_model_desc *desc, const zdec_weights *weights,
+                                   zdec_kv_dtype kv_dtype, int max_B, int max_L, void *cuda_stream,
+                                   zdec_ctx **out) {
+    zdec_cache_desc c{};
+    c.k_type = kv_dtype;
+    c.v_type = kv_dtype;
+    c.max_B = max_B;
+    c.max_L = max_L;
+    c.pool_tokens = 0;
+    return zdec_create_cache(desc, weights, &c, cuda_stream, out);
+}
+
 extern "C" void zdec_destroy(zdec_ctx *ctx) {
     if (!ctx) return;
     cudaStreamSynchronize(ctx->stream);
@@ -535,6 +487,50 @@ extern "C" void zdec_destroy(zdec_ctx *ctx) {
 
 extern "C" const char *zdec_last_error(const zdec_ctx *ctx) { return ctx ? ctx->err.c_str() : g_global_error.c_str(); }
 extern "C" const char *zdec_last_global_error(void) { return g_global_error.c_str(); }
+
+// -------------------------------------------------------------- pages ---
+// Pages for tokens [t0, t1) of `slot`, taken from the free list where the
+// slot has none; the entries set are appended to `fresh`.  On a shortage it
+// returns the pages it took and fails with ZDEC_ERR_CAPACITY.
+static zdec_status take_pages(zdec_ctx *ctx, int slot, long t0, long t1, std::vector<int> &fresh) {
+    if (t1 <= t0) return ZDEC_OK;
+    const size_t first = fresh.size();
+    for (long pg = t0 / PAGE_TOKENS; pg <= (t1 - 1) / PAGE_TOKENS; pg++) {
+        const int e = slot * ctx->max_pages + (int)pg;
+        if (ctx->table_host[e] >= 0) continue;
+        if (ctx->free_pages.empty()) {
+            for (size_t i = first; i < fresh.size(); i++) {
+                ctx->free_pages.push_back(ctx->table_host[fresh[i]]);
+                ctx->table_host[fresh[i]] = -1;
+            }
+            fresh.resize(first);
+            return fail(ctx, ZDEC_ERR_CAPACITY, "the KV pool has no free page (%d pages of %d tokens)",
+                        ctx->pool.n_pages, PAGE_TOKENS);
+        }
+        ctx->table_host[e] = ctx->free_pages.back();
+        ctx->free_pages.pop_back();
+        fresh.push_back(e);
+    }
+    return ZDEC_OK;
+}
+
+// Pages listed in `fresh` back to the free list (their entries unset).
+static void give_back_pages(zdec_ctx *ctx, std::vector<int> &fresh) {
+    for (int e : fresh) {
+        ctx->free_pages.push_back(ctx->table_host[e]);
+        ctx->table_host[e] = -1;
+    }
+    fresh.clear();
+}
+
+// Block-table entries the host changed, into the device tables (in stream order).
+static cudaError_t push_pages(zdec_ctx *ctx, const std::vector<int> &fresh) {
+    for (int e : fresh) {
+        cudaError_t r = cudaMemcpyAsync(ctx->table_dev + e, ctx->table_host + e, 4, cudaMemcpyHostToDevice, ctx->stream);
+        if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+}
 
 // ------------------------------------------------------------- append ---
 extern "C" zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, const void *k_f16,
@@ -546,32 +542,34 @@ extern "C" zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, cons
         return fail(ctx, ZDEC_ERR_CAPACITY, "sequence %d: %d + %d tokens exceed max_L %d", seq,
                     ctx->len_host[seq], n_tokens, ctx->max_L);
     if (n_tokens == 0) return ZDEC_OK;
+    const int t0 = ctx->len_host[seq];
     const zdec_model_desc &d = ctx->d;
-    size_t bytes = (size_t)d.n_layers * n_tokens * d.n_kv_heads * HD * 2;
-    const uint16_t *kd = (const uint16_t *)k_f16, *vd = (const uint16_t *)v_f16;
+    const size_t bytes = (size_t)d.n_layers * n_tokens * d.n_kv_heads * HD * 2;
     void *tmp = nullptr;
-    if (!on_device) {
-        if (cudaMalloc(&tmp, 2 * bytes) != cudaSuccess) {
-            cudaGetLastError();
-            return fail(ctx, ZDEC_ERR_OOM, "cannot stage %zu bytes of KV", 2 * bytes);
-        }
-        CK(cudaMemcpyAsync(tmp, k_f16, bytes, cudaMemcpyHostToDevice, ctx->stream));
-        CK(cudaMemcpyAsync((uint8_t *)tmp + bytes, v_f16, bytes, cudaMemcpyHostToDevice, ctx->stream));
+    if (!on_device && cudaMalloc(&tmp, 2 * bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ctx, ZDEC_ERR_OOM, "cannot stage %zu bytes of KV", 2 * bytes);
+    }
+    std::vector<int> fresh;
+    zdec_status ps = take_pages(ctx, seq, t0, (long)t0 + n_tokens, fresh);
+    if (ps != ZDEC_OK) {
+        cudaFree(tmp);
+        return ps;
+    }
+    const uint16_t *kd = (const uint16_t *)k_f16, *vd = (const uint16_t *)v_f16;
+    cudaError_t e = push_pages(ctx, fresh);
+    if (e == cudaSuccess && tmp) {
+        e = cudaMemcpyAsync(tmp, k_f16, bytes, cudaMemcpyHostToDevice, ctx->stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync((uint8_t *)tmp + bytes, v_f16, bytes, cudaMemcpyHostToDevice, ctx->stream);
         kd = (const uint16_t *)tmp;
         vd = (const uint16_t *)((uint8_t *)tmp + bytes);
     }
-    int t0 = ctx->len_host[seq];
-    cudaError_t e = launch_kv_append(ctx->arena, seq, t0, n_tokens, kd, vd, ctx->stream);
+    if (e == cudaSuccess) e = launch_kv_append(ctx->pool, seq, t0, n_tokens, kd, vd, ctx->status, ctx->stream);
     int32_t newlen = t0 + n_tokens;
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(ctx->len_dev + seq, &newlen, 4, cudaMemcpyHostToDevice, ctx->stream);
-    if (!on_device) {
-        cudaError_t e2 = cudaStreamSynchronize(ctx->stream);
-        cudaFree(tmp);
-        if (e == cudaSuccess) e = e2;
-    } else if (e == cudaSuccess) {
-        e = cudaStreamSynchronize(ctx->stream);   // the host length source is read asynchronously
-    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->len_dev + seq, &newlen, 4, cudaMemcpyHostToDevice, ctx->stream);
+    cudaError_t e2 = cudaStreamSynchronize(ctx->stream);   // the host length source is read asynchronously
+    cudaFree(tmp);
+    if (e == cudaSuccess) e = e2;
     if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "append_kv: %s", cudaGetErrorString(e));
     ctx->len_host[seq] = newlen;
     return ZDEC_OK;
@@ -580,7 +578,18 @@ extern "C" zdec_status zdec_append_kv(zdec_ctx *ctx, int seq, int n_tokens, cons
 extern "C" zdec_status zdec_reset_seq(zdec_ctx *ctx, int seq) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
     if (seq < 0 || seq >= ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "seq %d out of range", seq);
+    CK(cudaStreamSynchronize(ctx->stream));   // no step in flight still reads the slot's pages
+    std::vector<int> freed;
+    for (int pg = 0; pg < ctx->max_pages; pg++) {
+        const int e = seq * ctx->max_pages + pg;
+        if (ctx->table_host[e] >= 0) {
+            ctx->free_pages.push_back(ctx->table_host[e]);
+            ctx->table_host[e] = -1;
+            freed.push_back(e);
+        }
+    }
     int32_t zero = 0;
+    CK(push_pages(ctx, freed));
     CK(cudaMemcpyAsync(ctx->len_dev + seq, &zero, 4, cudaMemcpyHostToDevice, ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
     ctx->len_host[seq] = 0;
@@ -595,38 +604,55 @@ extern "C" zdec_status zdec_seq_len(const zdec_ctx *ctx, int seq, int *len) {
 }
 
 // --------------------------------------------------------------- step ---
-// Attention split (cluster size, 1..16; ZDEC_ATT_CS forces one): the split
-// of least modelled time over the B x n_kv clusters, waves x (chunks per CTA
-// + 1 for the CTA's query load and merge) for a nominal 64 chunks per
-// sequence, the waves from the occupancy API's co-resident clusters (which
-// must each fit one GPC: 64 clusters of 6 Q8_0 CTAs fit at once, of 7 not).
-static int attn_stages(const zdec_ctx *ctx, int B);
-static int attn_cluster(const zdec_ctx *ctx, int B) {
-    static const int forced = getenv("ZDEC_ATT_CS") ? atoi(getenv("ZDEC_ATT_CS")) : 0;
-    if (forced >= 1 && forced <= 16) return forced;
-    const int clusters = B * ctx->d.n_kv_heads, stages = attn_stages(ctx, B);
-    int best = 1;
-    double best_t = 1e30;
-    for (int cs = 1; cs <= 16; cs++) {
-        const int maxc = attention_max_clusters(ctx->kv_dtype, stages, cs);
-        if (maxc <= 0) continue;
-        const double t = (double)((clusters + maxc - 1) / maxc) * (64.0 / cs + 1.0);
-        if (t < best_t - 1e-9) { best_t = t; best = cs; }
-    }
-    if (getenv("ZDEC_PRINT_SPLITS")) fprintf(stderr, "zdec attention B=%d: %d stages, split %d\n", B, stages, best);
-    return best;
-}
-
-// Attention chunks in flight per CTA (ZDEC_ATT_STAGES overrides).  A deeper
-// ring pays off only where the attention dominates the step; elsewhere its
-// shared memory keeps the neighbouring projections' CTAs (which prefetch
-// their weights) off the SMs.  Measured: batch of one, two stages; batch of
-// eight, two for an fp16 cache (a third would drop to one CTA per SM) and
-// three for Q8_0 (still three CTAs per SM).
+// Attention ring depth.  A deeper ring pays off only where the attention
+// dominates the step; elsewhere its shared memory keeps the neighbouring
+// projections' CTAs (which prefetch their weights) off the SMs.
 static int attn_stages(const zdec_ctx *ctx, int B) {
     static const int env = getenv("ZDEC_ATT_STAGES") ? atoi(getenv("ZDEC_ATT_STAGES")) : 0;
-    if (env >= 2) return std::min(env, ctx->kv_dtype ? 8 : 5);
-    return (B > 4 && ctx->kv_dtype) ? 3 : 2;
+    const int lim = attention_stage_limit(ctx->k_type, ctx->v_type);
+    if (env >= 2) return std::min(env, lim);
+    const bool f16 = ctx->k_type == ZDEC_KV_F16 && ctx->v_type == ZDEC_KV_F16;
+    return std::min(lim, (B > 4 && !f16) ? 3 : 2);
+}
+// Segment slots per row for a step whose rows hold these many tokens: one
+// when the rows are about even (a cut row pays a cross-segment merge, ~3 us
+// at B = 1 measured), up to MAX_SEGS when the longest row is that many times
+// the mean, so that its clusters take about a mean row's work each.
+static int attn_segments(const zdec_ctx *ctx, int B) {
+    static const int f_seg = getenv("ZDEC_ATT_SEGS") ? atoi(getenv("ZDEC_ATT_SEGS")) : 0;
+    if (f_seg >= 1) return std::min(f_seg, MAX_SEGS);
+    long sum = 0, mx = 0;
+    for (int b = 0; b < B; b++) {
+        const long n = ctx->len_host[ctx->slots_cur[b]] + 1;
+        sum += n;
+        mx = std::max(mx, n);
+    }
+    const double ratio = sum > 0 ? (double)mx * B / (double)sum : 1.0;
+    return std::max(1, std::min(MAX_SEGS, (int)(ratio + 0.5)));
+}
+// Attention launch shape for a batch of B rows cut into `segs` segment slots
+// per row: the cluster size cs (ranks per segment) of least modelled time,
+// waves x (chunks per CTA + 1 for the query load and the cluster merge), for
+// a nominal 64 chunks per row, the waves from the occupancy API's co-resident
+// clusters (which must each fit one GPC).  ZDEC_ATT_CS forces one.
+static AttnPlan attn_plan(const zdec_ctx *ctx, int B, int segs) {
+    static const int f_cs = getenv("ZDEC_ATT_CS") ? atoi(getenv("ZDEC_ATT_CS")) : 0;
+    AttnPlan best{1, segs, attn_stages(ctx, B)};
+    double best_t = 1e30;
+    for (int m = segs; m <= segs; m++) {
+        for (int cs = 1; cs <= 16; cs++) {
+            if (f_cs >= 1 && f_cs <= 16 && cs != f_cs) continue;
+            const int maxc = attention_max_clusters(ctx->k_type, ctx->v_type, best.stages, cs, ctx->d.n_kv_heads);
+            if (maxc <= 0) continue;
+            const int clusters = B * ctx->d.n_kv_heads * m;
+            const double t = (double)((clusters + maxc - 1) / maxc) * (64.0 / (m * cs) + 1.0);
+            if (t < best_t - 1e-9) { best_t = t; best.cs = cs; best.segs = m; }
+        }
+    }
+    if (getenv("ZDEC_PRINT_SPLITS"))
+        fprintf(stderr, "zdec attention B=%d: %d stages, cluster %d, %d segment slot(s) per row\n", B, best.stages,
+                best.cs, best.segs);
+    return best;
 }
 
 static int pick_impl(const zdec_ctx *ctx, int B) {
@@ -638,8 +664,9 @@ static int pick_impl(const zdec_ctx *ctx, int B) {
     return B <= ctx->matvec_max_B ? 1 : 2;
 }
 
-// Enqueue the whole step for rows 0..B-1.  logits_out may be null.
-static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pdl) {
+// Enqueue the whole step for rows 0..B-1 (row b uses cache slot slots_dev[b]),
+// the attention cut into `segs` segment slots per row.  logits_out may be null.
+static cudaError_t enqueue_step(zdec_ctx *ctx, int B, int segs, float *logits_out, bool pdl) {
     const zdec_model_desc &d = ctx->d;
     const int H = d.hidden, F = d.ffn;
     const int impl = pick_impl(ctx, B);
@@ -684,7 +711,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     const int Bp0 = ctx->Bp_max;
     const int bc = batch_class(B);   // split-table row
     auto split = [&](int m) { const int c = ctx->cs_tab[impl][bc][m]; return c > 0 ? c : 1; };
-    STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev,
+    STEP(ZDEC_KERNEL_EMBED, launch_embed(ctx->embed, ctx->nsb_h, d.vocab, ctx->tok_dev, ctx->pos_dev, ctx->slots_dev,
                                          ctx->len_dev, ctx->status, B, ctx->x, H, ctx->L[0].attn_norm,
                                          ctx->x16, ctx->x16lo, ctx->sx, Bp0, ctx->rms_part, pdl, s, tlk));
     if ((e = capture_x(0)) != cudaSuccess) return e;
@@ -710,16 +737,19 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         gp.pf_ptr = W;
         gp.pf_bytes = std::min(tile_bytes(nrt, nsb), ctx->prefetch_cap);
     };
+    const AttnPlan plan = attn_plan(ctx, B, segs);
     AttnParams ap{};
-    ap.kv = ctx->arena;
+    ap.kv = ctx->pool;
     ap.nq = d.n_q_heads;
     ap.positions = ctx->pos_dev;
+    ap.slots = ctx->slots_dev;
     ap.qkv = ctx->qkv;
     ap.qkv_ld = ctx->qkv_ld;
     ap.rope = ctx->rope;
     ap.append = 1;
-    ap.cs = attn_cluster(ctx, B);
-    ap.stages = attn_stages(ctx, B);
+    ap.cs = plan.cs;
+    ap.seg_min = 2;
+    ap.stages = plan.stages;
     ap.o = ctx->o;
     ap.o16 = ctx->o16;
     ap.o16lo = ctx->o16lo;
@@ -729,6 +759,9 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     ap.max_L = ctx->max_L;
     ap.status = ctx->status;
     ap.q_frag = ctx->qfrag;   // written by the QKV projection's epilogue
+    ap.seg_part = ctx->seg_part;
+    ap.seg_ticket = ctx->seg_ticket;
+    const int nz = B * plan.segs;
     // RMSNorm never runs as its own kernel: the producer of the residual (the
     // embedding gather, the O and down projections) writes gain*x as the next
     // projection's operand plus per-group sums of x^2, and the consumer scales
@@ -752,8 +785,8 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
         STEP(ZDEC_KERNEL_GEMM_QKV, (gp.tl = tlk, launch_gemm(gp, EPI_STORE, impl, pdl, s)));
         gp.q_frag = nullptr;
         ap.layer = l;
-        STEP(ZDEC_KERNEL_ATTENTION, (ap.tl = tlk, launch_attention(ap, pdl, s)));
-        plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention combine
+        STEP(ZDEC_KERNEL_ATTENTION, (ap.tl = tlk, launch_attention(ap, nz, pdl, s)));
+        plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention merge
         matrix(lw.o, H, H / 16, ctx->nsb_q, split(MAT_O));
         prefetch(lw.gu, F / 8, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
@@ -783,117 +816,76 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, float *logits_out, bool pd
     gp.amax_val = ctx->amax_v; gp.amax_idx = ctx->amax_i;
     STEP(ZDEC_KERNEL_GEMM_LMHEAD, (gp.tl = tlk, launch_gemm(gp, EPI_LMHEAD, impl, pdl, s)));
     STEP(ZDEC_KERNEL_ARGMAX, launch_argmax_final(ctx->amax_v, ctx->amax_i, n_groups(ctx->nrt_vocab), B, ctx->ids_dev,
-                                                 ctx->pos_dev, ctx->len_dev, ctx->status, pdl, s, tlk));
+                                                 ctx->pos_dev, ctx->slots_dev, ctx->len_dev, ctx->status, pdl, s, tlk));
 #undef STEP
     ctx->last_kernels = nk;
-    ctx->last_splits = ap.cs;
+    ctx->last_splits = plan.cs;
+    ctx->last_segs = plan.segs;
     return cudaSuccess;
 }
 
-// The persistent kernel runs this step?
-static bool use_persistent(const zdec_ctx *ctx, int B) {
-    return ctx->engine == ZDEC_ENGINE_PERSISTENT && ctx->step_grid > 0 && B <= STEP_MAX_B;
-}
-
-// The whole step as the prep kernel + the persistent step kernel.
-static cudaError_t enqueue_step_persistent(zdec_ctx *ctx, int B, float *logits_out) {
-    const zdec_model_desc &d = ctx->d;
-    StepParams p{};
-    p.n_layers = d.n_layers;
-    p.hidden = d.hidden;
-    p.ffn = d.ffn;
-    p.vocab = d.vocab;
-    p.n_q = d.n_q_heads;
-    p.n_kv = d.n_kv_heads;
-    p.eps = d.rms_eps;
-    p.layers = ctx->d_layers;
-    p.embed = ctx->embed;
-    p.lm = ctx->embed;
-    p.final_norm = ctx->final_norm;
-    p.rope = ctx->rope;
-    p.kv = ctx->arena;
-    p.max_L = ctx->max_L;
-    p.B = B;
-    p.tokens = ctx->tok_dev;
-    p.positions = ctx->pos_dev;
-    p.logits = logits_out;
-    p.ids = ctx->ids_dev;
-    p.capture = ctx->capture_dev_host ? ctx->s_capture : nullptr;
-    p.x = ctx->x;
-    p.u16 = ctx->x16; p.u16lo = ctx->x16lo; p.usx = ctx->sx;
-    p.g16 = ctx->g16; p.g16lo = ctx->g16lo; p.gsx = ctx->gsx;
-    p.o16 = ctx->o16; p.o16lo = ctx->o16lo; p.osx = ctx->osx;
-    p.a16 = ctx->a16; p.a16lo = ctx->a16lo; p.asx = ctx->asx;
-    p.rms_attn = ctx->rms_part;
-    p.rms_ffn = ctx->s_rms_ffn;
-    p.q = ctx->s_q;
-    p.gpart = ctx->s_gpart;
-    p.apart = ctx->s_apart;
-    p.amax_val = ctx->amax_v;
-    p.amax_idx = ctx->amax_i;
-    p.cnt = ctx->s_cnt;
-    p.n_cnt = ctx->s_ncnt;
-    p.step_ok = ctx->s_ok;
-    p.abort_flag = ctx->s_abort;
-    p.status = ctx->status;
-    p.slots = ctx->step_slots[B <= 4 ? 0 : 1];
-    p.slot_bytes = step_slot_bytes(B);
-    p.pf_items = ctx->step_pf_items;
-    p.att_min_units = ctx->step_att_min;
-    p.trace = ctx->trace_on ? ctx->trace : nullptr;
-    cudaStream_t s = ctx->stream;
-    cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (ctx->prof) {
-        cudaEventCreate(&e0);
-        cudaEventCreate(&e1);
-        cudaEventRecord(e0, s);
-    }
-    cudaError_t e = launch_step(p, ctx->step_grid, ctx->len_dev, s);
-    if (ctx->prof) {
-        cudaEventRecord(e1, s);
-        ctx->prof->push_back(Launch{ZDEC_KERNEL_STEP, e0, e1});
-    }
-    if (e != cudaSuccess) return e;
-    if (ctx->capture_dev_host)
-        e = cudaMemcpyAsync(ctx->capture_dev_host, ctx->s_capture, (size_t)(d.n_layers + 1) * B * d.hidden * 4,
-                            cudaMemcpyDeviceToHost, s);
-    ctx->last_kernels = 2;
-    ctx->last_splits = 0;
-    return e;
-}
-
-static cudaError_t enqueue_any(zdec_ctx *ctx, int B, float *logits_out, bool pdl) {
-    if (use_persistent(ctx, B)) {
-        ctx->last_engine = ZDEC_ENGINE_PERSISTENT;
-        return enqueue_step_persistent(ctx, B, logits_out);
-    }
-    ctx->last_engine = ZDEC_ENGINE_KERNELS;
-    return enqueue_step(ctx, B, logits_out, pdl);
-}
-
-static zdec_status check_step_args(zdec_ctx *ctx, int B, const int32_t *tokens, const int32_t *positions,
-                                   int32_t *ids) {
+// Host checks of a step: row count, distinct in-range slots, room in every
+// slot, and a page for every new token (taken here; `fresh` lists the block
+// table entries set).  On failure nothing has changed.
+static zdec_status check_step_args(zdec_ctx *ctx, int B, const int32_t *slots, const int32_t *tokens,
+                                   const int32_t *positions, int32_t *ids, std::vector<int> &fresh) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
     if (B < 1 || B > ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "B=%d outside [1, %d]", B, ctx->max_B);
     if (!tokens || !positions || !ids) return fail(ctx, ZDEC_ERR_ARG, "null tokens/positions/ids");
-    for (int b = 0; b < B; b++)
-        if (ctx->len_host[b] + 1 > ctx->max_L)
-            return fail(ctx, ZDEC_ERR_CAPACITY, "sequence %d is full (%d tokens)", b, ctx->max_L);
-    if (ctx->engine == ZDEC_ENGINE_PERSISTENT && !use_persistent(ctx, B))
-        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the persistent step kernel is unavailable for B=%d", B);
+    std::vector<char> used(ctx->max_B, 0);
+    for (int b = 0; b < B; b++) {
+        const int s = slots ? slots[b] : b;
+        if (s < 0 || s >= ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "slots[%d] = %d outside [0, %d)", b, s, ctx->max_B);
+        if (used[s]) return fail(ctx, ZDEC_ERR_ARG, "slot %d appears twice in one step", s);
+        used[s] = 1;
+    }
+    for (int b = 0; b < B; b++) {
+        const int s = slots ? slots[b] : b;
+        if (ctx->len_host[s] + 1 > ctx->max_L)
+            return fail(ctx, ZDEC_ERR_CAPACITY, "slot %d is full (%d tokens)", s, ctx->max_L);
+    }
+    for (int b = 0; b < B; b++) {
+        const int s = slots ? slots[b] : b;
+        zdec_status ps = take_pages(ctx, s, ctx->len_host[s], (long)ctx->len_host[s] + 1, fresh);
+        if (ps != ZDEC_OK) {   // the pages earlier rows took go back
+            give_back_pages(ctx, fresh);
+            return ps;
+        }
+    }
     return ZDEC_OK;
 }
 
-// Stage inputs: host pointers are validated and copied through pinned memory.
+// The row -> slot map of this step into slots_dev (only when it changed; it
+// then waits for the steps in flight, which read the old map).
+static zdec_status set_slots(zdec_ctx *ctx, int B, const int32_t *slots) {
+    bool same = B <= ctx->slots_n;
+    for (int b = 0; same && b < B; b++) same = ctx->slots_cur[b] == (slots ? slots[b] : b);
+    if (same) return ZDEC_OK;
+    CK(cudaStreamSynchronize(ctx->stream));
+    for (int b = 0; b < B; b++) ctx->slots_cur[b] = slots ? slots[b] : b;
+    CK(cudaMemcpy(ctx->slots_dev, ctx->slots_cur.data(), B * 4, cudaMemcpyHostToDevice));
+    ctx->slots_n = B;
+    return ZDEC_OK;
+}
+
+// Host-I/O input checks (before anything is enqueued): every row's position
+// is its slot's length, every token is in the vocabulary.
+static zdec_status check_host_inputs(zdec_ctx *ctx, int B, const int32_t *slots, const int32_t *tokens,
+                                     const int32_t *positions) {
+    for (int b = 0; b < B; b++) {
+        const int s = slots ? slots[b] : b;
+        if (positions[b] != ctx->len_host[s])
+            return fail(ctx, ZDEC_ERR_POSITION, "positions[%d] = %d but slot %d holds %d tokens", b, positions[b], s,
+                        ctx->len_host[s]);
+        if (tokens[b] < 0 || tokens[b] >= ctx->d.vocab)
+            return fail(ctx, ZDEC_ERR_ARG, "tokens[%d] = %d outside the vocabulary", b, tokens[b]);
+    }
+    return ZDEC_OK;
+}
+
+// Stage inputs: host inputs go through pinned memory.
 static zdec_status stage_inputs(zdec_ctx *ctx, int B, const int32_t *tokens, const int32_t *positions, bool host) {
     if (host) {
-        for (int b = 0; b < B; b++) {
-            if (positions[b] != ctx->len_host[b])
-                return fail(ctx, ZDEC_ERR_POSITION, "positions[%d] = %d but sequence %d holds %d tokens", b,
-                            positions[b], b, ctx->len_host[b]);
-            if (tokens[b] < 0 || tokens[b] >= ctx->d.vocab)
-                return fail(ctx, ZDEC_ERR_ARG, "tokens[%d] = %d outside the vocabulary", b, tokens[b]);
-        }
         CK(cudaStreamSynchronize(ctx->stream));   // the pinned staging may still be in flight
         memcpy(ctx->pinned_io, tokens, B * 4);
         memcpy(ctx->pinned_io + ctx->max_B, positions, B * 4);
@@ -906,35 +898,44 @@ static zdec_status stage_inputs(zdec_ctx *ctx, int B, const int32_t *tokens, con
     return ZDEC_OK;
 }
 
-extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tokens,
-                                        const int32_t *positions, float *logits, int32_t *ids, int flags) {
-    zdec_status st = check_step_args(ctx, B, tokens, positions, ids);
+// Everything before the kernels of a step: host checks, pages, the slot map
+// and the inputs.  When it fails the step has changed nothing.
+static zdec_status prepare_step(zdec_ctx *ctx, int B, const int32_t *slots, const int32_t *tokens,
+                                const int32_t *positions, int32_t *ids, bool host) {
+    std::vector<int> fresh;
+    zdec_status st = check_step_args(ctx, B, slots, tokens, positions, ids, fresh);
     if (st != ZDEC_OK) return st;
+    if (host) st = check_host_inputs(ctx, B, slots, tokens, positions);
+    if (st == ZDEC_OK) st = set_slots(ctx, B, slots);
+    if (st == ZDEC_OK) st = stage_inputs(ctx, B, tokens, positions, host);
+    if (st != ZDEC_OK) {
+        give_back_pages(ctx, fresh);
+        return st;
+    }
+    cudaError_t e = push_pages(ctx, fresh);
+    if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "block table update: %s", cudaGetErrorString(e));
+    return ZDEC_OK;
+}
+
+static zdec_status run_step(zdec_ctx *ctx, int B, const int32_t *slots, const int32_t *tokens,
+                            const int32_t *positions, float *logits, int32_t *ids, int flags) {
     const bool host = flags & ZDEC_STEP_HOST_IO;
-    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host || ctx->trace_on ||
-                       (ctx->persistent_eager && use_persistent(ctx, B));
-    st = stage_inputs(ctx, B, tokens, positions, host);
+    zdec_status st = prepare_step(ctx, B, slots, tokens, positions, ids, host);
     if (st != ZDEC_OK) return st;
+    const bool eager = (flags & ZDEC_STEP_EAGER) || ctx->capture_dev_host || ctx->trace_on;
     float *lg = host ? (logits ? ctx->logits : nullptr) : logits;
-    const int impl = use_persistent(ctx, B) ? 3 : pick_impl(ctx, B);
+    const int impl = pick_impl(ctx, B);
+    const int segs = attn_segments(ctx, B);
     if (eager) {
-        CK(enqueue_any(ctx, B, lg, true));
+        CK(enqueue_step(ctx, B, segs, lg, true));
     } else {
-        auto key = std::make_tuple(B, (const void *)lg, impl);
+        auto key = std::make_tuple(B, (const void *)lg, impl, segs);
         auto it = ctx->graphs.find(key);
         if (it == ctx->graphs.end()) {
             cudaGraph_t graph;
             CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
-            cudaError_t e = enqueue_any(ctx, B, lg, true);
+            cudaError_t e = enqueue_step(ctx, B, segs, lg, true);
             cudaError_t e2 = cudaStreamEndCapture(ctx->stream, &graph);
-            if ((e != cudaSuccess || e2 != cudaSuccess) && impl == 3) {
-                // a cooperative launch that cannot be captured: run the persistent engine without graphs
-                if (e2 == cudaSuccess) cudaGraphDestroy(graph);
-                cudaGetLastError();
-                ctx->persistent_eager = true;
-                CK(enqueue_any(ctx, B, lg, true));
-                goto launched;
-            }
             if (e != cudaSuccess || e2 != cudaSuccess) {
                 if (e2 == cudaSuccess) cudaGraphDestroy(graph);
                 return fail(ctx, ZDEC_ERR_CUDA, "step capture: %s", cudaGetErrorString(e != cudaSuccess ? e : e2));
@@ -947,7 +948,6 @@ extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tok
         }
         CK(cudaGraphLaunch(it->second, ctx->stream));
     }
-launched:
     if (host) {
         if (logits)
             CK(cudaMemcpyAsync(logits, ctx->logits, (size_t)B * ctx->d.vocab * 4, cudaMemcpyDeviceToHost, ctx->stream));
@@ -955,7 +955,7 @@ launched:
     } else {
         CK(cudaMemcpyAsync(ids, ctx->ids_dev, B * 4, cudaMemcpyDeviceToDevice, ctx->stream));
     }
-    for (int b = 0; b < B; b++) ctx->len_host[b]++;
+    for (int b = 0; b < B; b++) ctx->len_host[ctx->slots_cur[b]]++;
     if (ctx->capture_dev_host) {   // armed hidden-state capture: wait and reorder
         cudaError_t e = cudaStreamSynchronize(ctx->stream);
         const int H = ctx->d.hidden, NL1 = ctx->d.n_layers + 1;
@@ -973,6 +973,17 @@ launched:
     return ZDEC_OK;
 }
 
+extern "C" zdec_status zdec_decode_step(zdec_ctx *ctx, int B, const int32_t *tokens,
+                                        const int32_t *positions, float *logits, int32_t *ids, int flags) {
+    return run_step(ctx, B, nullptr, tokens, positions, logits, ids, flags);
+}
+
+extern "C" zdec_status zdec_decode_step_slots(zdec_ctx *ctx, int B, const int32_t *slots, const int32_t *tokens,
+                                              const int32_t *positions, float *logits, int32_t *ids, int flags) {
+    if (ctx && !slots) return fail(ctx, ZDEC_ERR_ARG, "null slots");
+    return run_step(ctx, B, slots, tokens, positions, logits, ids, flags);
+}
+
 extern "C" zdec_status zdec_sync(zdec_ctx *ctx) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
     CK(cudaStreamSynchronize(ctx->stream));
@@ -987,9 +998,10 @@ extern "C" zdec_status zdec_sync(zdec_ctx *ctx) {
         CK(cudaMemcpy(len.data(), ctx->len_dev, ctx->max_B * sizeof(int32_t), cudaMemcpyDeviceToHost));
         for (int b = 0; b < ctx->max_B; b++) ctx->len_host[b] = len[b];
         if (st & STATUS_TIMEOUT) return fail(ctx, ZDEC_ERR_TIMEOUT, "a bounded device wait gave up");
-        return fail(ctx, ZDEC_ERR_DEVICE, "device check failed (status 0x%x:%s%s)", st,
+        return fail(ctx, ZDEC_ERR_DEVICE, "device check failed (status 0x%x:%s%s%s)", st,
                     (st & STATUS_POSITION) ? " position != cached length" : "",
-                    (st & STATUS_TOKEN) ? " token outside the vocabulary" : "");
+                    (st & STATUS_TOKEN) ? " token outside the vocabulary" : "",
+                    (st & STATUS_PAGE) ? " cached token without a KV page" : "");
     }
     return ZDEC_OK;
 }
@@ -1014,15 +1026,18 @@ extern "C" zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl) {
 extern "C" zdec_status zdec_get_info(const zdec_ctx *ctx, zdec_info *info) {
     if (!ctx || !info) return fail(nullptr, ZDEC_ERR_ARG, "null argument");
     info->weight_bytes = ctx->wbytes;
-    info->arena_bytes = ctx->arena_bytes;
+    info->arena_bytes = ctx->pool_bytes;
     info->workspace_bytes = ctx->ws_bytes;
-    info->kv_bytes_per_token = (size_t)ctx->d.n_layers * ctx->d.n_kv_heads * HD * 2 * (ctx->kv_dtype ? 1 : 2) +
-                               (ctx->kv_dtype ? (size_t)ctx->d.n_layers * ctx->d.n_kv_heads * 4 * 2 * 2 : 0);
+    info->kv_bytes_per_token = ctx->pool.page_bytes / PAGE_TOKENS;
     info->kernels_per_step = ctx->last_kernels;
     info->attn_splits = ctx->last_splits;
     info->matvec_max_B = ctx->matvec_max_B;
-    info->engine = ctx->last_engine;
-    info->step_ctas = ctx->step_grid;
+    info->attn_segments = ctx->last_segs;
+    info->k_type = ctx->k_type;
+    info->v_type = ctx->v_type;
+    info->page_tokens = PAGE_TOKENS;
+    info->pool_pages = ctx->pool.n_pages;
+    info->free_pages = (int)ctx->free_pages.size();
     return ZDEC_OK;
 }
 
@@ -1030,27 +1045,16 @@ extern "C" zdec_status zdec_set_trace(zdec_ctx *ctx, int on) {
     if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
     CK(cudaStreamSynchronize(ctx->stream));
     if (!on) {
-        cudaFree(ctx->trace);
         cudaFree(ctx->ktl);
         cudaFreeHost(ctx->ktl_init);
-        ctx->trace = nullptr;
         ctx->ktl = nullptr;
         ctx->ktl_init = nullptr;
-        ctx->trace_entries = ctx->ktl_entries = 0;
+        ctx->ktl_entries = 0;
         ctx->trace_on = false;
         return ZDEC_OK;
     }
     if (ctx->trace_on) return ZDEC_OK;
-    if (ctx->step_grid > 0) {   // persistent engine: [ctas][phases][8]
-        const size_t n = (size_t)ctx->step_grid * (2 + 5 * ctx->d.n_layers) * 8;
-        if (cudaMalloc(&ctx->trace, n * 8) != cudaSuccess) {
-            cudaGetLastError();
-            return fail(ctx, ZDEC_ERR_OOM, "cannot allocate the step trace");
-        }
-        CK(cudaMemsetAsync(ctx->trace, 0, n * 8, ctx->stream));
-        ctx->trace_entries = n;
-    }
-    // kernel engine: [launches][8] = (first start, first past the wait, last end, kind, milestones)
+    // [launches][8] = (first start, first past the wait, last end, kind, milestones)
     const size_t nk = (size_t)(3 + 5 * ctx->d.n_layers) * 8;
     if (cudaMalloc(&ctx->ktl, nk * 8) != cudaSuccess || cudaMallocHost(&ctx->ktl_init, nk * 8) != cudaSuccess) {
         cudaGetLastError();
@@ -1064,37 +1068,24 @@ extern "C" zdec_status zdec_set_trace(zdec_ctx *ctx, int on) {
 
 extern "C" zdec_status zdec_debug_step_trace(zdec_ctx *ctx, uint64_t *out_host, size_t cap, size_t *n) {
     if (!ctx || !n) return fail(nullptr, ZDEC_ERR_ARG, "null argument");
-    const bool pers = ctx->last_engine == ZDEC_ENGINE_PERSISTENT;
-    *n = !ctx->trace_on ? 0 : (pers ? ctx->trace_entries : ctx->ktl_entries);
+    *n = ctx->trace_on ? ctx->ktl_entries : 0;
     if (!ctx->trace_on || !out_host || *n == 0) return ZDEC_OK;   // size query
     if (cap < *n) return fail(ctx, ZDEC_ERR_ARG, "trace needs %zu entries", *n);
     CK(cudaStreamSynchronize(ctx->stream));
-    CK(cudaMemcpy(out_host, pers ? ctx->trace : ctx->ktl, *n * 8, cudaMemcpyDeviceToHost));
-    if (!pers)
-        for (size_t i = 0; i < *n / 8; i++) out_host[8 * i + 3] = i < ctx->ktl_kinds.size() ? ctx->ktl_kinds[i] : 0;
-    return ZDEC_OK;
-}
-
-extern "C" zdec_status zdec_set_engine(zdec_ctx *ctx, int engine) {
-    if (!ctx) return fail(nullptr, ZDEC_ERR_ARG, "null context");
-    if (engine < ZDEC_ENGINE_AUTO || engine > ZDEC_ENGINE_PERSISTENT) return fail(ctx, ZDEC_ERR_ARG, "bad engine %d", engine);
-    if (engine == ZDEC_ENGINE_PERSISTENT && ctx->step_grid == 0)
-        return fail(ctx, ZDEC_ERR_UNSUPPORTED, "the persistent step kernel is unavailable on this device/model");
-    ctx->engine = engine;
+    CK(cudaMemcpy(out_host, ctx->ktl, *n * 8, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < *n / 8; i++) out_host[8 * i + 3] = i < ctx->ktl_kinds.size() ? ctx->ktl_kinds[i] : 0;
     return ZDEC_OK;
 }
 
 extern "C" zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *tokens_dev,
                                          const int32_t *positions_dev, float *logits_dev, int32_t *ids_dev,
                                          int *kind, float *ms, int cap, int *n) {
-    zdec_status st = check_step_args(ctx, B, tokens_dev, positions_dev, ids_dev);
-    if (st != ZDEC_OK) return st;
-    if (!n || (cap > 0 && (!kind || !ms))) return fail(ctx, ZDEC_ERR_ARG, "null output");
-    st = stage_inputs(ctx, B, tokens_dev, positions_dev, false);
+    if (ctx && (!n || (cap > 0 && (!kind || !ms)))) return fail(ctx, ZDEC_ERR_ARG, "null output");
+    zdec_status st = prepare_step(ctx, B, nullptr, tokens_dev, positions_dev, ids_dev, false);
     if (st != ZDEC_OK) return st;
     std::vector<Launch> launches;
     ctx->prof = &launches;
-    cudaError_t e = enqueue_any(ctx, B, logits_dev, false);
+    cudaError_t e = enqueue_step(ctx, B, attn_segments(ctx, B), logits_dev, false);
     ctx->prof = nullptr;
     if (e == cudaSuccess) e = cudaMemcpyAsync(ids_dev, ctx->ids_dev, B * 4, cudaMemcpyDeviceToDevice, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
@@ -1107,7 +1098,7 @@ extern "C" zdec_status zdec_profile_step(zdec_ctx *ctx, int B, const int32_t *to
     }
     *n = (int)launches.size();
     if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "profile step: %s", cudaGetErrorString(e));
-    for (int b = 0; b < B; b++) ctx->len_host[b]++;
+    for (int b = 0; b < B; b++) ctx->len_host[ctx->slots_cur[b]]++;
     return zdec_sync(ctx);
 }
 
@@ -1172,25 +1163,38 @@ extern "C" zdec_status zdec_debug_dequant(zdec_ctx *ctx, int which, int layer, i
 extern "C" zdec_status zdec_debug_read_kv(zdec_ctx *ctx, int seq, int layer, int t0, int n, void *k, void *v,
                                           void *ks, void *vs) {
     if (!ctx || !k || !v) return fail(ctx, ZDEC_ERR_ARG, "null argument");
-    if (ctx->kv_dtype && (!ks || !vs)) return fail(ctx, ZDEC_ERR_ARG, "Q8_0 read needs scale buffers");
+    if ((ctx->k_type == ZDEC_KV_Q8_0 && !ks) || (ctx->v_type == ZDEC_KV_Q8_0 && !vs))
+        return fail(ctx, ZDEC_ERR_ARG, "a Q8_0 tensor's read needs its scale buffer");
     if (seq < 0 || seq >= ctx->max_B || layer < 0 || layer >= ctx->d.n_layers || t0 < 0 || n < 0 ||
         t0 + n > ctx->max_L)
         return fail(ctx, ZDEC_ERR_ARG, "range out of bounds");
     if (n == 0) return ZDEC_OK;
     const int nkv = ctx->d.n_kv_heads;
-    size_t es = ctx->kv_dtype ? 1 : 2;
-    size_t kb = (size_t)n * nkv * HD * es, sb = ctx->kv_dtype ? (size_t)n * nkv * 4 * 2 : 0;
+    const size_t kb = (size_t)n * nkv * HD * (ctx->k_type == ZDEC_KV_F16 ? 2 : 1);
+    const size_t vb = (size_t)n * nkv * HD * (ctx->v_type == ZDEC_KV_F16 ? 2 : 1);
+    const size_t sb = (size_t)n * nkv * 4 * 2;
     uint8_t *buf = nullptr;
-    if (cudaMalloc(&buf, 2 * kb + 2 * sb + 16) != cudaSuccess) { cudaGetLastError(); return fail(ctx, ZDEC_ERR_OOM, "debug buffer"); }
-    uint16_t *dks = sb ? (uint16_t *)(buf + 2 * kb) : nullptr, *dvs = sb ? (uint16_t *)(buf + 2 * kb + sb) : nullptr;
-    cudaError_t e = launch_kv_read(ctx->arena, seq, layer, t0, n, buf, buf + kb, dks, dvs, ctx->stream);
+    if (cudaMalloc(&buf, kb + vb + 2 * sb + 16) != cudaSuccess) { cudaGetLastError(); return fail(ctx, ZDEC_ERR_OOM, "debug buffer"); }
+    uint16_t *dks = (uint16_t *)(buf + kb + vb), *dvs = (uint16_t *)(buf + kb + vb + sb);
+    cudaError_t e = launch_kv_read(ctx->pool, seq, layer, t0, n, buf, buf + kb, dks, dvs, ctx->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(k, buf, kb, cudaMemcpyDeviceToHost, ctx->stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(v, buf + kb, kb, cudaMemcpyDeviceToHost, ctx->stream);
-    if (e == cudaSuccess && sb) e = cudaMemcpyAsync(ks, dks, sb, cudaMemcpyDeviceToHost, ctx->stream);
-    if (e == cudaSuccess && sb) e = cudaMemcpyAsync(vs, dvs, sb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(v, buf + kb, vb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess && ctx->k_type == ZDEC_KV_Q8_0) e = cudaMemcpyAsync(ks, dks, sb, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess && ctx->v_type == ZDEC_KV_Q8_0) e = cudaMemcpyAsync(vs, dvs, sb, cudaMemcpyDeviceToHost, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
     cudaFree(buf);
     if (e != cudaSuccess) return fail(ctx, ZDEC_ERR_CUDA, "kv read: %s", cudaGetErrorString(e));
+    return ZDEC_OK;
+}
+
+extern "C" zdec_status zdec_debug_block_table(zdec_ctx *ctx, int seq, int32_t *pages_host, int cap, int *n) {
+    if (!ctx || !n) return fail(ctx, ZDEC_ERR_ARG, "null argument");
+    if (seq < 0 || seq >= ctx->max_B) return fail(ctx, ZDEC_ERR_ARG, "seq %d out of range", seq);
+    *n = ctx->max_pages;
+    if (!pages_host) return ZDEC_OK;
+    if (cap < ctx->max_pages) return fail(ctx, ZDEC_ERR_ARG, "the table needs %d entries", ctx->max_pages);
+    CK(cudaStreamSynchronize(ctx->stream));
+    CK(cudaMemcpy(pages_host, ctx->table_dev + (size_t)seq * ctx->max_pages, ctx->max_pages * 4, cudaMemcpyDeviceToHost));
     return ZDEC_OK;
 }
 
@@ -1217,16 +1221,23 @@ extern "C" zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, con
     const int qd = ctx->qd;
     CK(cudaMemcpy2DAsync(ctx->qkv, ctx->qkv_ld * 4, q_host, qd * 4, qd * 4, B, cudaMemcpyHostToDevice, ctx->stream));
     CK(cudaMemcpyAsync(ctx->pos_dev, positions_host, B * 4, cudaMemcpyHostToDevice, ctx->stream));
+    std::vector<int32_t> saved(ctx->slots_cur);   // the segment choice reads rows 0..B-1 as slots 0..B-1
+    for (int b = 0; b < B; b++) ctx->slots_cur[b] = b;
+    const AttnPlan plan = attn_plan(ctx, B, attn_segments(ctx, B));
+    ctx->slots_cur = saved;
     AttnParams ap{};
-    ap.kv = ctx->arena;
+    ap.kv = ctx->pool;
     ap.layer = layer;
     ap.nq = ctx->d.n_q_heads;
     ap.positions = ctx->pos_dev;
+    ap.slots = ctx->ident_dev;   // row b reads slot b
     ap.qkv = ctx->qkv;
     ap.qkv_ld = ctx->qkv_ld;
     ap.rope = ctx->rope;
     ap.append = 0;
-    ap.cs = attn_cluster(ctx, B);
+    ap.cs = plan.cs;
+    ap.seg_min = 2;
+    ap.stages = plan.stages;
     ap.o = ctx->o;
     ap.o16 = ctx->o16;
     ap.o16lo = ctx->o16lo;
@@ -1235,7 +1246,9 @@ extern "C" zdec_status zdec_debug_attention(zdec_ctx *ctx, int layer, int B, con
     ap.B = B;
     ap.max_L = ctx->max_L;
     ap.status = ctx->status;
-    CK(launch_attention(ap, false, ctx->stream));
+    ap.seg_part = ctx->seg_part;
+    ap.seg_ticket = ctx->seg_ticket;
+    CK(launch_attention(ap, B * plan.segs, false, ctx->stream));
     CK(cudaMemcpyAsync(o_host, ctx->o, (size_t)B * qd * 4, cudaMemcpyDeviceToHost, ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
     return ZDEC_OK;

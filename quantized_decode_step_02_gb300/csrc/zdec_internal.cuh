@@ -67,40 +67,6 @@ __host__ __device__ __forceinline__ size_t act_sum(int sb, int b, int j, int lo,
     return (((size_t)sb * Bp + b) * 4 + (j >> 1)) * 4 + (lo ? 2 : 0) + (j & 1);
 }
 
-// KV arena layout.  Every (sequence slot, layer, kv head) owns one plane per
-// tensor, Lp tokens long (Lp a multiple of KU).  Tokens are grouped in units of
-// KU = 32 so that one unit of every tensor is a contiguous run of bytes (a
-// single bulk copy), and 16-byte segments inside a row are XOR-swizzled so
-// that the rows the attention's mma fragments read together fall in
-// different shared-memory banks once a unit is copied verbatim:
-//   fp16 K   [Lp][128] half: segment s (8 dims) of token t at s ^ (t & 7)
-//   fp16 V   [Lp/32][128 dims][32 tokens] half: segment s (8 tokens) of dim
-//            row d at s ^ ((d >> 1) & 3)
-//   Q8_0 K   [Lp][128] int8 codes: segment s (16 dims) at s ^ (t & 7);
-//            scales [Lp][4] fp16 (one per 32 dims)
-//   Q8_0 V   [Lp/32][128 dims][32 tokens] int8 codes: segment s (16 tokens)
-//            at s ^ ((d >> 2) & 1); scales [Lp/32][4 blocks][32 tokens] fp16
-// Offsets are in bytes from the start of the plane.
-constexpr int KU = 32;
-__host__ __device__ __forceinline__ size_t kv_k16_off(int t, int d) {
-    return (size_t)t * 256 + ((((d >> 3) ^ (t & 7)) << 4) | ((d & 7) << 1));
-}
-__host__ __device__ __forceinline__ size_t kv_v16_off(int d, int t) {
-    const int tt = t & (KU - 1);
-    return ((size_t)(t >> 5) * HD + d) * 64 + ((((tt >> 3) ^ ((d >> 1) & 3)) << 4) | ((tt & 7) << 1));
-}
-__host__ __device__ __forceinline__ size_t kv_k8_off(int t, int d) {
-    return (size_t)t * 128 + ((((d >> 4) ^ (t & 7)) << 4) | (d & 15));
-}
-__host__ __device__ __forceinline__ size_t kv_v8_off(int d, int t) {
-    const int tt = t & (KU - 1);
-    return ((size_t)(t >> 5) * HD + d) * 32 + ((((tt >> 4) ^ ((d >> 2) & 1)) << 4) | (tt & 15));
-}
-__host__ __device__ __forceinline__ size_t kv_ks_off(int t, int blk) { return (size_t)t * 8 + blk * 2; }
-__host__ __device__ __forceinline__ size_t kv_vs_off(int blk, int t) {
-    return (((size_t)(t >> 5) * 4 + blk) * KU + (t & (KU - 1))) * 2;
-}
-
 // offset -> nibble position inside a lane word, and back
 __host__ __device__ constexpr int nib_of_off(int o) {
     return o == 0 ? 0 : o == 4 ? 1 : o == 2 ? 2 : o == 6 ? 3 : o == 1 ? 4 : o == 5 ? 5 : o == 3 ? 6 : 7;
@@ -301,10 +267,11 @@ __device__ __forceinline__ void tl_max(unsigned long long *tl, int k) {
 }
 
 // ------------------------------------------------------- device status ---
-enum : uint32_t { STATUS_POSITION = 1u, STATUS_CAPACITY = 2u, STATUS_TIMEOUT = 4u, STATUS_TOKEN = 8u };
+enum : uint32_t { STATUS_POSITION = 1u, STATUS_CAPACITY = 2u, STATUS_TIMEOUT = 4u, STATUS_TOKEN = 8u,
+                  STATUS_PAGE = 16u /* a cached token without a KV page */ };
 // Any of these makes the step (and every later step until the host clears the
 // word) leave the KV cache and the device lengths untouched.
-constexpr uint32_t STATUS_STATE_ERRORS = STATUS_POSITION | STATUS_CAPACITY | STATUS_TIMEOUT | STATUS_TOKEN;
+constexpr uint32_t STATUS_STATE_ERRORS = STATUS_POSITION | STATUS_CAPACITY | STATUS_TIMEOUT | STATUS_TOKEN | STATUS_PAGE;
 
 
 }  // namespace zdec

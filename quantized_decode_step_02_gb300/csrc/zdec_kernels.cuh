@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <utility>
 
+#include "kv_pool.cuh"
 #include "zdec_internal.cuh"
 
 namespace zdec {
@@ -26,14 +27,16 @@ cudaError_t launch_export_canonical(const uint8_t *tiles, int row_map, int nsb, 
                                     int nrows, uint8_t *dst, cudaStream_t stream);
 cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int row0, int nrows,
                                 float *dst, cudaStream_t stream);
-// x[b][:] = dequant(E[tokens[b]]) for b < B; also checks positions against
-// the device lengths (status bit STATUS_POSITION on mismatch).
+// x[b][:] = dequant(E[tokens[b]]) for b < B; also checks each row's position
+// against the device length of its slot, len_dev[slots[b]] (status bit
+// STATUS_POSITION on mismatch) and its token against the vocabulary.
 // It also writes the first projection's operand gain*x (act planes, row pitch
 // Bp) and the sum of x^2 of each row into part[b] (one partial per row).
 cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *tokens,
-                         const int32_t *positions, const int32_t *len_dev, uint32_t *status, int B,
-                         float *x, int ldx, const float *gain, __half *u, __half *ulo, __half *usx,
-                         int Bp, float *part, bool pdl, cudaStream_t stream, unsigned long long *tl = nullptr);
+                         const int32_t *positions, const int32_t *slots, const int32_t *len_dev,
+                         uint32_t *status, int B, float *x, int ldx, const float *gain, __half *u,
+                         __half *ulo, __half *usx, int Bp, float *part, bool pdl, cudaStream_t stream,
+                         unsigned long long *tl = nullptr);
 
 // --------------------------------------------------------------- gemm.cu
 enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LMHEAD = 3 };
@@ -97,34 +100,27 @@ int gemm_cluster_slots(int B, int impl, int epi, int cs);
 cudaError_t launch_prep(const float *src, int lds, int K, const float *gain, float eps, int B, int Bp,
                         __half *hi, __half *lo, __half *sums, bool pdl, cudaStream_t stream);
 // ids[b] = argmax over the per-CTA partials (lowest index on ties); also
-// advances the device lengths, len_dev[b] = positions[b] + 1, unless the
-// status word holds an error (then the step changes no length).
+// advances the device length of each row's slot, len_dev[slots[b]] =
+// positions[b] + 1, unless the status word holds an error (then the step
+// changes no length).
 cudaError_t launch_argmax_final(const float *amax_val, const int *amax_idx, int nparts, int B,
-                                int32_t *ids, const int32_t *positions, int32_t *len_dev,
-                                const uint32_t *status, bool pdl, cudaStream_t stream,
+                                int32_t *ids, const int32_t *positions, const int32_t *slots,
+                                int32_t *len_dev, const uint32_t *status, bool pdl, cudaStream_t stream,
                                 unsigned long long *tl = nullptr);
 
 // ---------------------------------------------------------- attention.cu
-struct KvArena {
-    int kv_dtype;          // 0 fp16, 1 Q8_0
-    int n_layers, n_kv, Lp;
-    // one plane per (slot, layer, kv head), plane index (slot*n_layers + layer)*n_kv + g;
-    // the layout inside a plane is given by kv_*_off (zdec_internal.cuh)
-    uint8_t *k;            // fp16 Lp*256 bytes per plane; Q8: int8 codes, Lp*128
-    uint8_t *v;            // fp16 Lp*256 bytes (unit-tiled V^T); Q8: Lp*128
-    uint8_t *ks;           // Q8: Lp*8 bytes per plane (K scales)
-    uint8_t *vs;           // Q8: Lp*8 bytes per plane (V scales, unit-tiled)
-};
 struct AttnParams {
-    KvArena kv;
+    KvPool kv;
     int layer;
     int nq;                // query heads (= 4 * n_kv)
-    const int32_t *positions;
+    const int32_t *positions;   // [B] position of each row's new token
+    const int32_t *slots;       // [B] cache slot of each row
     const float *qkv;      // [B][qkv_ld]: q (nq*128), k (n_kv*128), v (n_kv*128)
     int qkv_ld;
     const float2 *rope;    // [max_L][64] (cos, sin)
     int append;            // 1: rotate q/k at pos and append k, v; 0: q already rotated, no append
-    int cs;                // CTAs per (b, kv head): one thread-block cluster (1..16)
+    int cs;                // CTAs per (segment, kv head): one thread-block cluster (1..16)
+    int seg_min;           // fewest 64-token chunks a segment takes (when rows are long enough)
     float *o;              // [B][nq*128]
     __half *o16;           // act planes (hi, lo) and sums of the O projection's input
     __half *o16lo;
@@ -132,86 +128,34 @@ struct AttnParams {
     int oBp;               // their row pitch
     int B;
     int max_L;             // positions >= max_L are ignored (the step is flagged elsewhere)
-    uint32_t *status;      // device status word (bounded-wait timeouts)
+    uint32_t *status;      // device status word
     unsigned long long *tl;   // launch timeline slot (zdec_internal.cuh) or null
     const uint4 *q_frag;   // query fragments prepared by the QKV projection (GemmParams), or null
-    int stages;            // 64-token chunks in flight per CTA (2..8; 0: the KV type's default)
+    int stages;            // 64-token chunks in flight per CTA (2..; 0: the type pair's default)
+    float *seg_part;       // [segment slots][n_kv][4][132] partials of rows cut into several segments
+    int *seg_ticket;       // [MAX_B][n_kv] arrival counters, zero between launches
 };
-cudaError_t launch_attention(const AttnParams &p, bool pdl, cudaStream_t stream);
-// Raise the attention kernel's dynamic shared-memory limit (once, before capture).
-cudaError_t attention_setup(int kv_dtype);
+// grid (cs, n_kv, nz): nz >= B segment slots (nz > B needs seg_part / seg_ticket).
+cudaError_t launch_attention(const AttnParams &p, int nz, bool pdl, cudaStream_t stream);
+// Raise the attention kernel's dynamic shared-memory limit for a (K, V) type
+// pair (once, before capture).
+cudaError_t attention_setup(int k_type, int v_type);
 // Dynamic shared memory of a launch with `stages` chunks in flight (0: default).
-size_t attention_smem_bytes(int kv_dtype, int stages = 0);
-int attention_default_stages(int kv_dtype);
+size_t attention_smem_bytes(int k_type, int v_type, int stages);
+int attention_default_stages(int k_type, int v_type);
+int attention_stage_limit(int k_type, int v_type);
 // Clusters of cs attention CTAs (with `stages` chunks in flight) the GPU holds
 // at once, from the occupancy API (0: not launchable).  Needs attention_setup.
-int attention_max_clusters(int kv_dtype, int stages, int cs);
-// Bulk append of fp16 K/V [n_layers][n][n_kv][128] (device) at tokens t0.. of slot.
-cudaError_t launch_kv_append(const KvArena &a, int slot, int t0, int n, const uint16_t *k16,
-                             const uint16_t *v16, cudaStream_t stream);
-// Canonical read-back: [n][n_kv][128] (+ scales [n][n_kv][4]) for one layer.
-cudaError_t launch_kv_read(const KvArena &a, int slot, int layer, int t0, int n, uint8_t *k,
+int attention_max_clusters(int k_type, int v_type, int stages, int cs, int n_kv);
+// Bulk append of fp16 K/V [n_layers][n][n_kv][128] (device) at tokens t0.. of
+// a slot, encoded per tensor type; every page must be assigned already.
+cudaError_t launch_kv_append(const KvPool &a, int slot, int t0, int n, const uint16_t *k16,
+                             const uint16_t *v16, uint32_t *status, cudaStream_t stream);
+// Canonical read-back of one layer: [n][n_kv][128] fp16 bits, or one-byte
+// codes (Q8_0 without its storage offset, e4m3), plus Q8_0 scales [n][n_kv][4].
+cudaError_t launch_kv_read(const KvPool &a, int slot, int layer, int t0, int n, uint8_t *k,
                            uint8_t *v, uint16_t *ks, uint16_t *vs, cudaStream_t stream);
 
-// ---------------------------------------------------------------- step.cu
-// The whole decode step as one persistent kernel (B <= STEP_MAX_B).
-constexpr int STEP_MAX_B = 8;
-struct StepLayerW {
-    const uint8_t *qkv, *o, *gu, *down;   // grouped tile blocks
-    const float *attn_norm, *ffn_norm;
-};
-struct StepParams {
-    int n_layers, hidden, ffn, vocab, n_q, n_kv;
-    float eps;
-    const StepLayerW *layers;   // device [n_layers]
-    const uint8_t *embed, *lm;
-    const float *final_norm;
-    const float2 *rope;         // [max_L][64] (cos, sin)
-    KvArena kv;
-    int max_L;
-    int B;
-    const int32_t *tokens, *positions;
-    float *logits;              // [B][vocab] or null
-    int32_t *ids;               // [B]
-    float *capture;             // [n_layers+1][B][hidden] or null
-    // workspace
-    float *x;                   // [B][hidden] residual stream
-    __half *u16, *u16lo, *usx;  // gain*x planes: QKV and LM head input
-    __half *g16, *g16lo, *gsx;  // ffn-gain*x planes: gate/up input
-    __half *o16, *o16lo, *osx;  // attention output planes: O input
-    __half *a16, *a16lo, *asx;  // SwiGLU planes: down input
-    float *rms_attn, *rms_ffn;  // [hidden/128][MAX_B] partial sums of x^2
-    float *q;                   // [B][n_q][128] rotated, scaled queries
-    float *gpart;               // GEMM piece partials [(groups + grid)][B][128]
-    float *apart;               // attention piece partials [(B*n_kv + grid)][4][HD + 4]
-    float *amax_val;            // [lm groups][MAX_B]
-    int *amax_idx;
-    int *cnt;                   // step counters (zeroed by the prep kernel)
-    int n_cnt;
-    const int *step_ok;         // set by the prep kernel
-    int *abort_flag;
-    uint32_t *status;
-    int slots;                  // ring slots per CTA
-    int slot_bytes;
-    int pf_items;               // items each CTA prefetches into L2 ahead of its ring (0: none)
-    int att_min_units;          // attention units per CTA at least (fewer CTAs for short work)
-    unsigned long long *trace;  // [grid][phases][8] timestamps (null: off), see step.cu
-};
-int step_counter_count(int n_layers, int hidden, int ffn, int vocab, int n_q, int n_kv);
-size_t step_gpart_floats(int hidden, int ffn, int vocab, int n_q, int n_kv, int B, int grid);
-size_t step_apart_floats(int n_kv, int B, int grid);
-int step_lm_groups(int vocab);
-// Shared memory per CTA for `slots` ring slots at batch B.
-size_t step_smem_bytes(int B, int slots);
-int step_slot_bytes(int B);
-// Validate inputs, zero the counters, advance the lengths (prep kernel), then
-// the persistent kernel over `grid` CTAs (cooperative launch).
-cudaError_t launch_step(const StepParams &p, int grid, int32_t *len_dev, cudaStream_t stream);
-// Configure the kernels (shared-memory limit) and report how many CTAs of the
-// step kernel fit on one SM for `slots` ring slots at batch B.
-cudaError_t step_setup(int B, int kv_dtype, int slots, int *ctas_per_sm);
-
-// Launch helper with the programmatic-stream-serialization attribute.
 // Launch helper: optional programmatic stream serialization and a 1-D cluster
 // of `cluster` CTAs along x (1 = no cluster).
 template <typename... KArgs, typename... Args>

@@ -57,6 +57,23 @@ def test_create_rejects_bad_shapes_before_any_cuda_call():
     assert b"null weight" in z.load_library().zdec_last_global_error()
 
 
+def test_create_cache_rejects_bad_cache_descriptions():
+    """Bad K/V types, slot counts, lengths and pool sizes fail with
+    ZDEC_ERR_ARG before anything is allocated."""
+    lib = z.load_library()
+    small = z.ModelDesc(n_layers=1, hidden=512, n_q_heads=4, n_kv_heads=1, head_dim=128, ffn=512, vocab=10)._c()
+    w = z._Weights()
+    h = ctypes.c_void_p()
+    cases = [((3, 0, 1, 16, 0), b"type"), ((0, -1, 1, 16, 0), b"type"), ((0, 0, 0, 16, 0), b"max_B"),
+             ((0, 0, 33, 16, 0), b"max_B"), ((0, 2, 1, 0, 0), b"max_L"), ((1, 2, 1, 16, -1), b"pool_tokens"),
+             ((2, 1, 1, 16, 64), b"null weight")]
+    for args, msg in cases:
+        c = z._Cache(*args)
+        assert lib.zdec_create_cache(ctypes.byref(small), ctypes.byref(w), ctypes.byref(c), None,
+                                     ctypes.byref(h)) == -1, args
+        assert msg in lib.zdec_last_global_error(), (args, lib.zdec_last_global_error())
+
+
 def test_null_context_calls_fail_cleanly():
     lib = z.load_library()
     assert lib.zdec_sync(None) == -1

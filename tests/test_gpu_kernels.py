@@ -1,7 +1,8 @@
 """Kernel-level parity on the GPU through the C ABI against the CPU oracle:
 Q4_K repack/unpack (bit-exact), dequantization (bit-exact), the dense Q4_K
-projection (matvec and mma.sync GEMM), the split-K attention over fp16 and
-Q8_0 caches, and Q8_0 quantize-on-append (bit-exact codes and scales)."""
+projection (matvec and mma.sync GEMM), the split-K attention over fp16, Q8_0
+and FP8 caches (also K and V of different types), and encode-on-append
+(bit-exact Q8_0 codes and scales, e4m3 codes)."""
 import numpy as np
 import pytest
 
@@ -130,18 +131,20 @@ ATT = ModelDesc(n_layers=1, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=12
                 vocab=256)
 
 
-@pytest.mark.parametrize("kv_dtype", [0, 1])
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2, (1, 0), (0, 2), (2, 1)])
 @pytest.mark.parametrize("lengths", [[256], [1, 65, 700], [64, 128, 5000, 33]])
 def test_attention_matches_oracle(kv_dtype, lengths):
-    """GQA 32q/8kv, head_dim 128; lengths are cached tokens per sequence and the
+    """GQA 32q/8kv, head_dim 128, over fp16, Q8_0 and FP8 caches (one type, or
+    one for K and one for V); lengths are cached tokens per sequence and the
     query attends over all of them (positions = length - 1)."""
     B = len(lengths)
     w = cached_model(ATT, 3)
     max_L = max(lengths) + 1
     dec = z.Decoder(ATT, w, kv_dtype, max_B=B, max_L=max_L)
+    seed = 30 + (kv_dtype if isinstance(kv_dtype, int) else 3 * kv_dtype[0] + kv_dtype[1])
     kvs = []
     for b, L in enumerate(lengths):
-        k, v = make_kv_history(ATT, 30 + kv_dtype, b, L)
+        k, v = make_kv_history(ATT, seed, b, L)
         dec.append_kv(b, k, v)
         kv = oracle.KV(odesc(ATT), max_L, kv_dtype)
         kv.append(k, v)
@@ -173,22 +176,42 @@ def _special_fp16_rows(n_layers, n, nkv):
     return x.view(np.uint16)
 
 
-def test_q8_0_append_bit_exact():
+def _check_encoded(x16, codes, scales, kind):
+    """Stored codes (and Q8_0 scales) of fp16 rows [t][g][128] against the oracle's encoders."""
+    for t in range(x16.shape[0]):
+        for g in range(x16.shape[1]):
+            if kind == z.KV_F16:
+                assert np.array_equal(codes[t, g], x16[t, g]), (t, g)
+            elif kind == z.KV_Q8_0:
+                rs, rq = oracle.q8_0_quantize(x16[t, g])
+                assert np.array_equal(scales[t, g], rs) and np.array_equal(codes[t, g], rq), (t, g)
+            else:
+                ref = np.array([oracle.e4m3_from_half(int(h)) for h in x16[t, g]], np.uint8)
+                assert np.array_equal(codes[t, g], ref), (t, g)
+
+
+@pytest.mark.parametrize("types", [(1, 1), (2, 2), (1, 2), (2, 0), (0, 1)])
+def test_append_encodes_bit_exact(types):
+    """Bulk append through the C ABI encodes each tensor by its own type,
+    bit-exact against the oracle's Q8_0 quantizer and e4m3 conversion (ties,
+    all-zero blocks, subnormals, +-65504 saturating to +-448 in e4m3), across
+    a page boundary."""
     d = SMALL
     w = cached_model(d, 21)
-    dec = z.Decoder(d, w, z.KV_Q8_0, max_B=2, max_L=64)
-    k = _special_fp16_rows(d.n_layers, 7, d.n_kv_heads)
+    dec = z.Decoder(d, w, types, max_B=2, max_L=160)
+    k = _special_fp16_rows(d.n_layers, 70, d.n_kv_heads)
     v = np.flip(k, axis=-1).copy()
-    dec.append_kv(1, k, v)
+    dec.append_kv(1, k[:, :3], v[:, :3])
+    dec.append_kv(1, k[:, 3:], v[:, 3:])   # the second call crosses into the second page
     for layer in range(d.n_layers):
-        kq, vq, ks, vs = dec.read_kv(1, layer, 0, 7)
-        for t in range(7):
-            for g in range(d.n_kv_heads):
-                rs, rq = oracle.q8_0_quantize(k[layer, t, g])
-                assert np.array_equal(ks[t, g], rs) and np.array_equal(kq[t, g], rq), (layer, t, g)
-                rs, rq = oracle.q8_0_quantize(v[layer, t, g])
-                assert np.array_equal(vs[t, g], rs) and np.array_equal(vq[t, g], rq), (layer, t, g)
-    assert dec.seq_len(1) == 7 and dec.seq_len(0) == 0
+        got = dec.read_kv(1, layer, 0, 70)
+        ks = got[2] if len(got) == 4 else None
+        vs = got[3] if len(got) == 4 else None
+        _check_encoded(k[layer], got[0], ks, types[0])
+        _check_encoded(v[layer], got[1], vs, types[1])
+    assert dec.seq_len(1) == 70 and dec.seq_len(0) == 0
+    assert (dec.block_table(1)[:2] >= 0).all() and (dec.block_table(1)[2:] < 0).all()
+    assert (dec.block_table(0) < 0).all()
     dec.close()
 
 
