@@ -359,7 +359,6 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_bad;
     __shared__ uint64_t red_bar;   // rank 0 of a cluster: the peers' partial tiles have landed
-    __shared__ uint32_t s_done[8];  // pipe 1: warps done with each ring slot (running count)
     __shared__ int s_issued;        // stages whose copies have been issued
     __shared__ float s_gain[128];   // RESID with next_gain: the group's gain rows
     __shared__ float s_rms[MAX_B];  // RMSNorm scale per batch row (consumers of a folded norm)
@@ -375,20 +374,21 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     const uint32_t sbyt = lay.bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)D * sbyt);
     const uint8_t *gW = p.W + (size_t)grp * p.nsb * GROUP_BYTES;
-    auto stage = [&](int i) { return smem + (size_t)(i % D) * sbyt; };
-    auto issue_w = [&](int i) {
-        mbar_expect_tx(&full[i % D], tx);
-        bulk_g2s(stage(i), gW + (size_t)(s0 + i) * GROUP_BYTES, GROUP_BYTES, &full[i % D]);
+    // Stage i of the CTA's range lives in ring slot i % D; the loop tracks
+    // slot and phase parity incrementally, so no division runs per stage.
+    auto slot_ptr = [&](int slot) { return smem + (uint32_t)slot * sbyt; };
+    auto issue_w = [&](int slot, int i) {   // weights of stage i into `slot`
+        mbar_expect_tx(&full[slot], tx);
+        bulk_g2s(slot_ptr(slot), gW + (size_t)(s0 + i) * GROUP_BYTES, GROUP_BYTES, &full[slot]);
     };
-    auto issue_act = [&](int i) {
-        uint8_t *st = stage(i) + GROUP_BYTES;
+    auto issue_act = [&](int slot, int i) {   // the activation rows of stage i into `slot`
+        uint8_t *st = slot_ptr(slot);
         const size_t sb = (size_t)(s0 + i);
-        bulk_g2s(st + (lay.hi - GROUP_BYTES), p.x16 + sb * p.Bp * 256, abytes, &full[i % D]);
-        bulk_g2s(st + (lay.lo - GROUP_BYTES), p.x16lo + sb * p.Bp * 256, abytes, &full[i % D]);
-        bulk_g2s(st + (lay.sums - GROUP_BYTES), p.sx + sb * p.Bp * 16, sbytes, &full[i % D]);
+        bulk_g2s(st + lay.hi, p.x16 + sb * p.Bp * 256, abytes, &full[slot]);
+        bulk_g2s(st + lay.lo, p.x16lo + sb * p.Bp * 256, abytes, &full[slot]);
+        bulk_g2s(st + lay.sums, p.sx + sb * p.Bp * 16, sbytes, &full[slot]);
     };
     tl_min(p.tl, 0);
-    if (threadIdx.x < 8) s_done[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         s_bad = 0;
         for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
@@ -423,13 +423,19 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     const uint32_t swz = (uint32_t)tig | ((uint32_t)((g >> 1) & 1) << 2);
     uint32_t sum_off = (g & 1) ? lay.zero + (uint32_t)tig * 8u
                                : lay.sums + (uint32_t)(g >> 1) * 32u + (uint32_t)tig * 8u;
+    MvOff mvo{};
     if (IMPL == 3) {   // B column g carries sub-block data only in lane group tig = g/2 (see stage_mv)
         act_off = (g == 2 * tig ? lay.hi : (g == 2 * tig + 1 ? lay.lo : lay.hi + 512u)) + (uint32_t)tig * 128u;
         sum_off = lay.sums + (uint32_t)tig * 8u;
+        mvo.codes = (uint32_t)warp * TILE_BYTES + 16u * (uint32_t)lane;
+        mvo.meta = (uint32_t)warp * TILE_BYTES + TILE_CODE_BYTES + 8u * (uint32_t)lane;
+#pragma unroll
+        for (int pw = 0; pw < 4; pw++) mvo.act[pw] = act_off + (((uint32_t)pw ^ (uint32_t)tig) << 4);
+        mvo.sums = sum_off;
     }
     const int pre = min(D, n);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < pre; i++) issue_w(i);
+        for (int i = 0; i < pre; i++) issue_w(i, i);
         s_issued = pre;
     }
     // epilogue inputs that no earlier kernel of the step writes (weights, the
@@ -452,7 +458,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     tl_min(p.tl, 1);
     tl_max(p.tl, 4);
     if (threadIdx.x == 0)
-        for (int i = 0; i < pre; i++) issue_act(i);
+        for (int i = 0; i < pre; i++) issue_act(i, i);
     // the epilogue's inputs from earlier kernels, fetched now so that their
     // latency hides behind the K loop: this lane's partial sums of x^2 per
     // batch row (RMSNorm scale) and the residual rows it will update
@@ -492,71 +498,64 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     float accr[NB][2];
 #pragma unroll
     for (int c = 0; c < NB; c++) accr[c][0] = accr[c][1] = 0.0f;
-    float ymv[2] = {0.0f, 0.0f};
-    // two stages per step: their loads, dequant and MMAs are independent, which
-    // gives each warp two dependency chains to interleave, and halves the
-    // block-wide syncs that release stages for refilling
+    float ymq[2] = {0.0f, 0.0f}, ymm[2] = {0.0f, 0.0f};   // IMPL 3: code and min terms (stage_mv)
+    // one stage per step (p.pair = 0): each slot is refilled as soon as every
+    // warp is done with it, so the D - 1 stages ahead of the one computed stay
+    // in flight; or two (p.pair = 1): their loads, dequant and MMAs are
+    // independent, giving each warp two dependency chains, and the block-wide
+    // syncs halve, but the pair's second slot refills one stage later
     bool ok = true;
     const long long wlim = p.wait_limit > 0 ? p.wait_limit : GEMM_WAIT_LIMIT;
     // wait_limit < 0 (tests): the first stage wait counts as run out at once,
     // so the give-up path (status, drain of the copies in flight, return)
     // runs deterministically, without racing the copies
-    auto expired = [&](int i, int parity_i) {
+    auto expired = [&](int i, int slot, uint32_t parity) {
         if (p.wait_limit < 0 && i == 0) {
             if (p.status) atomicOr(p.status, STATUS_TIMEOUT);
             return true;
         }
-        return !wait_stage(&full[parity_i % D], (uint32_t)(parity_i / D) & 1u, p.status, wlim);
+        return !wait_stage(&full[slot], parity, p.status, wlim);
     };
-    if (p.pipe == 1) {
-        // each warp takes the stages in order; the last warp done with a stage
-        // refills its slot, so no block-wide barrier stalls the ring
-        for (int i = 0; i < n; i++) {
-            if (ok && expired(i, i)) { ok = false; s_bad = 1; }
-            if (i == 0) tl_max(p.tl, 5);
-            if (ok && rt < p.nrt) {
-                if (IMPL == 2) stage_mma<NA, GemmChains<NT>::v>(stage(i), warp, lane, act_off, sum_off, swz, acc);
-                else if (IMPL == 3) stage_mv(stage(i), warp, lane, act_off, sum_off, ymv);
-                else stage_fma<NB>(stage(i), warp, lane, lay, accr);
-            }
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();   // this warp's reads of the slot precede its refill
-                const uint32_t prev = atomicAdd(&s_done[i % D], 1u);
-                if ((prev & 7u) == 7u && i + D < n && !*((volatile int *)&s_bad)) {
-                    __threadfence_block();
-                    issue_w(i + D);
-                    issue_act(i + D);
-                    atomicMax(&s_issued, i + D + 1);
-                }
-            }
-        }
-        __syncthreads();
-    } else
-    for (int i = 0; i < n; i += 2) {
-        const bool two = i + 1 < n;
-        if (ok && expired(i, i)) { ok = false; s_bad = 1; }
+    const bool live = rt < p.nrt;   // the group's last row tiles may be padding
+    int sa = 0;                     // ring slot of stage i
+    uint32_t pa = 0;                // its phase parity
+    const int step = p.pair ? 2 : 1;
+    for (int i = 0; i < n; i += step) {
+        const bool two = p.pair && i + 1 < n;
+        int sb = sa + 1;            // stage i + 1
+        uint32_t pb = pa;
+        if (sb == D) { sb = 0; pb ^= 1u; }
+        if (ok && expired(i, sa, pa)) { ok = false; s_bad = 1; }
         if (i == 0) tl_max(p.tl, 5);
-        if (two && ok && expired(i + 1, i + 1)) {
+        if (two && ok && expired(i + 1, sb, pb)) {
             ok = false;
             s_bad = 1;
         }
-        if (ok && rt < p.nrt) {
+        if (ok && live) {
+            const uint8_t *st_a = slot_ptr(sa), *st_b = slot_ptr(sb);
             if (IMPL == 2) {
-                stage_mma<NA, GemmChains<NT>::v>(stage(i), warp, lane, act_off, sum_off, swz, acc);
-                if (two) stage_mma<NA, GemmChains<NT>::v>(stage(i + 1), warp, lane, act_off, sum_off, swz, acc);
+                stage_mma<NA, GemmChains<NT>::v>(st_a, warp, lane, act_off, sum_off, swz, acc);
+                if (two) stage_mma<NA, GemmChains<NT>::v>(st_b, warp, lane, act_off, sum_off, swz, acc);
             } else if (IMPL == 3) {
-                stage_mv(stage(i), warp, lane, act_off, sum_off, ymv);
-                if (two) stage_mv(stage(i + 1), warp, lane, act_off, sum_off, ymv);
+                stage_mv(st_a, mvo, tig, ymq, ymm);
+                if (two) stage_mv(st_b, mvo, tig, ymq, ymm);
             } else {
-                stage_fma<NB>(stage(i), warp, lane, lay, accr);
-                if (two) stage_fma<NB>(stage(i + 1), warp, lane, lay, accr);
+                stage_fma<NB>(st_a, warp, lane, lay, accr);
+                if (two) stage_fma<NB>(st_b, warp, lane, lay, accr);
             }
         }
-        __syncthreads();
+        __syncthreads();   // every warp is done with both slots: refill them
         if (threadIdx.x == 0 && !s_bad) {
-            if (i + D < n) { issue_w(i + D); issue_act(i + D); s_issued = i + D + 1; }
-            if (two && i + 1 + D < n) { issue_w(i + 1 + D); issue_act(i + 1 + D); s_issued = i + D + 2; }
+            if (i + D < n) { issue_w(sa, i + D); issue_act(sa, i + D); s_issued = i + D + 1; }
+            if (two && i + 1 + D < n) { issue_w(sb, i + 1 + D); issue_act(sb, i + 1 + D); s_issued = i + D + 2; }
+        }
+        if (p.pair) {               // stage i + 2
+            sa = sb + 1;
+            pa = pb;
+            if (sa == D) { sa = 0; pa ^= 1u; }
+        } else {                    // stage i + 1
+            sa = sb;
+            pa = pb;
         }
     }
     tl_max(p.tl, 6);
@@ -576,8 +575,10 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
             y[nt][1] = acc[nt < NA ? nt : 0][2] + acc[nt < NA ? nt : 0][3] * LO_UNSCALE;
         }
     } else if (IMPL == 3) {   // the row's four lanes, then batch row 0 in lane tig 0
+        float ymv[2];
 #pragma unroll
         for (int r = 0; r < 2; r++) {
+            ymv[r] = fmaf(16777216.0f, ymq[r], -ymm[r]);   // the codes carried 2^-24
             ymv[r] += __shfl_xor_sync(FULL, ymv[r], 1);
             ymv[r] += __shfl_xor_sync(FULL, ymv[r], 2);
         }

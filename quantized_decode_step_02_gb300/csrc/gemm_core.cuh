@@ -164,22 +164,26 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int warp, int lane,
 //      2t + h (e = 0: hi plane, 1: lo plane) in the k-slots of lane group
 //      tig = t and zeros elsewhere.  A lane (g, tig) loads real activations
 //      only when g = 2 tig (hi) or g = 2 tig + 1 (lo); the other lanes read a
-//      zero row (act_off, see the kernels).
+//      zero row.
 // D[row][2t + e] is then 2^-24 times the code-times-activation sum of one
 // sub-block, and the C fragment hands lane (g, tig) exactly its own two
-// sub-blocks for rows g and g + 8, which it scales by d*sc and offsets by
-// dmin*m*S in fp32: y[rho] += d sc 2^24 D - dmin m S_j.
-// y holds this lane's share of rows g, g + 8 (sub-blocks 2tig, 2tig+1 of
-// every super-block); the four lanes of a row are summed by the caller.
-__device__ __forceinline__ void stage_mv(const uint8_t *st, int warp, int lane, uint32_t act_off, uint32_t sum_off,
-                                         float (&y)[2]) {
-    const int tig = lane & 3;
-    const uint8_t *tile = st + warp * TILE_BYTES;
-    const uint8_t *act = st + act_off;
+// sub-blocks for rows g and g + 8.
+// Lane offsets inside a stage, fixed for the whole kernel.
+struct MvOff {
+    uint32_t codes;    // warp's tile block + 16 * lane
+    uint32_t meta;     // warp's tile block + 2048 + 8 * lane
+    uint32_t act[4];   // B-fragment row of word pair p (swizzled by tig); + 64 for sub-block h = 1
+    uint32_t sums;     // this lane group's sub-block sums
+};
+// Accumulates this lane's share of rows g, g + 8 (sub-blocks 2 tig, 2 tig + 1
+// of every super-block): yq += d * sum_j sc_j * D_j (still carrying 2^-24) and
+// ym += dmin * sum_j m_j * S_j; the row is 2^24 yq - ym summed over its four
+// lanes (done by the caller after the K loop).
+__device__ __forceinline__ void stage_mv(const uint8_t *st, const MvOff &o, int tig, float (&yq)[2], float (&ym)[2]) {
     uint4 q[4];
 #pragma unroll
-    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(tile + c * 512 + 16 * lane);
-    const uint2 mt = *reinterpret_cast<const uint2 *>(tile + TILE_CODE_BYTES + 8 * lane);
+    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(st + o.codes + c * 512);
+    const uint2 mt = *reinterpret_cast<const uint2 *>(st + o.meta);
     // d, dmin of rows g, g+8 (four nibble quarters spread over the tig lanes)
     uint32_t dq = ((mt.x >> 12) & 0xFu) | ((mt.x >> 24) & 0xF0u) | ((mt.y >> 4) & 0xF00u) | ((mt.y >> 16) & 0xF000u);
     const uint32_t other = __shfl_xor_sync(FULL, dq, 1);
@@ -204,24 +208,25 @@ __device__ __forceinline__ void stage_mv(const uint8_t *st, int warp, int lane, 
             const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
             const uint32_t a[4] = {w0 & 0x000F000Fu, w1 & 0x000F000Fu, s0 & 0x000F000Fu, s1 & 0x000F000Fu};
             const uint32_t a16[4] = {w0 & 0x00F000F0u, w1 & 0x00F000F0u, s0 & 0x00F000F0u, s1 & 0x00F000F0u};
-            const uint4 xv = *reinterpret_cast<const uint4 *>(act + (((uint32_t)(h * 4 + pidx) ^ (uint32_t)tig) << 4));
+            const uint4 xv = *reinterpret_cast<const uint4 *>(st + o.act[pidx] + h * 64);
             mma16816(D[h][c & 1], a, xv.x, xv.y, D[h][c & 1]);
             mma16816(D[h][c & 1], a16, xv.z, xv.w, D[h][c & 1]);
         }
     }
-    const uint2 sv = *reinterpret_cast<const uint2 *>(st + sum_off);   // (S hi 2tig, 2tig+1, S lo 2tig, 2tig+1)
+    const uint2 sv = *reinterpret_cast<const uint2 *>(st + o.sums);   // (S hi 2tig, 2tig+1, S lo 2tig, 2tig+1)
     const float2 shi = __half22float2(u32_as_h2(sv.x)), slo = __half22float2(u32_as_h2(sv.y));
-    const float S[2] = {shi.x + slo.x, shi.y + slo.y};
-    const float dg = fg.x * 16777216.0f, d8 = f8.x * 16777216.0f;   // the codes carry 2^-24
+    const float S0 = shi.x + slo.x, S1 = shi.y + slo.y;
 #pragma unroll
-    for (int h = 0; h < 2; h++) {
-        const int sh = 16 * h;   // sub-block 2tig + h: fields at bits 0 / 16 (sc) and 6 / 22 (m)
-        const float scg = (float)((mt.x >> sh) & 63u), sc8 = (float)((mt.y >> sh) & 63u);
-        const float mg = (float)((mt.x >> (sh + 6)) & 63u), m8 = (float)((mt.y >> (sh + 6)) & 63u);
-        const float vg = (D[h][0][0] + D[h][1][0]) + (D[h][0][1] + D[h][1][1]) * LO_UNSCALE;
-        const float v8 = (D[h][0][2] + D[h][1][2]) + (D[h][0][3] + D[h][1][3]) * LO_UNSCALE;
-        y[0] += (dg * scg) * vg - (fg.y * mg) * S[h];
-        y[1] += (d8 * sc8) * v8 - (f8.y * m8) * S[h];
+    for (int r = 0; r < 2; r++) {   // row g (meta low word), row g + 8 (high word)
+        const uint32_t w = r ? mt.y : mt.x;
+        // sub-block 2tig: sc bits 0-5, m bits 6-11; 2tig+1: sc 16-21, m 22-27
+        const float sc0 = (float)(w & 63u), m0 = (float)((w >> 6) & 63u);
+        const float sc1 = (float)((w >> 16) & 63u), m1 = (float)((w >> 22) & 63u);
+        const float v0 = (D[0][0][2 * r] + D[0][1][2 * r]) + (D[0][0][2 * r + 1] + D[0][1][2 * r + 1]) * LO_UNSCALE;
+        const float v1 = (D[1][0][2 * r] + D[1][1][2 * r]) + (D[1][0][2 * r + 1] + D[1][1][2 * r + 1]) * LO_UNSCALE;
+        const float dd = r ? f8.x : fg.x, dm = r ? f8.y : fg.y;
+        yq[r] = fmaf(dd, fmaf(sc1, v1, sc0 * v0), yq[r]);
+        ym[r] = fmaf(dm, fmaf(m1, S1, m0 * S0), ym[r]);
     }
 }
 

@@ -29,11 +29,10 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Bytes of a matrix of rows16 row tiles in the grouped layout (padded to whole groups).
 size_t tile_bytes(int rows16, int nsb) { return (size_t)n_groups(rows16) * nsb * GROUP_BYTES; }
 
-// Projection pipeline mode (GemmParams::pipe): 0 (stage pairs) unless
-// ZDEC_GEMM_PIPE=1; pairs measured faster, their two independent stages
-// giving each warp more instruction-level parallelism.
-int gemm_pipe_mode() {
-    static const int mode = getenv("ZDEC_GEMM_PIPE") ? (atoi(getenv("ZDEC_GEMM_PIPE")) ? 1 : 0) : 0;
+// Stages a projection consumes per loop step (GemmParams::pair): ZDEC_GEMM_STEP
+// = 1 or 2.
+int gemm_pair_mode() {
+    static const int mode = getenv("ZDEC_GEMM_STEP") ? (atoi(getenv("ZDEC_GEMM_STEP")) == 2 ? 1 : 0) : 1;
     return mode;
 }
 
@@ -42,14 +41,17 @@ int gemm_pipe_mode() {
 // least modelled time, waves x (super-blocks per CTA + 2 for a CTA's fixed
 // ramp, reduction and epilogue).  32 row groups of 56 super-blocks split 14
 // ways fill 448 of 456 slots in one wave of 4 super-blocks per CTA.
+// grid_cap > 0 keeps the grid within that many CTAs (where any split does),
+// leaving SM room for the next kernels of the step to become resident early.
 template <typename Slots>
-int pick_cs(int groups, int nsb, Slots slots_of, int max_cs = 16) {
+int pick_cs(int groups, int nsb, Slots slots_of, int max_cs = 16, int grid_cap = 0) {
     if (groups <= 0) return 1;
     int best = 1;
     double best_t = 1e30;
     for (int cs = 1; cs <= std::min(max_cs, std::max(1, nsb / 2)); cs++) {
         const int slots = slots_of(cs);
         if (slots <= 0) continue;   // the split cannot be launched
+        if (grid_cap > 0 && cs > 1 && (long)groups * cs > grid_cap) continue;
         const long waves = ((long)groups * cs + slots - 1) / slots;
         const double t = (double)waves * ((double)nsb / cs + 2.0);
         if (t < best_t - 1e-9) { best_t = t; best = cs; }
@@ -432,6 +434,9 @@ extern "C" zdec_status zdec_create_cache(const zdec_model_desc *desc, const zdec
         // the occupancy API (ZDEC_CS_MAX: largest split, default 16, a
         // non-portable cluster size)
         const int csmax = getenv("ZDEC_CS_MAX") ? std::max(1, std::min(16, atoi(getenv("ZDEC_CS_MAX")))) : 16;
+        // ZDEC_GRID_CAP: projection grids of at most this many CTAs per SM (0: no cap)
+        const double gcap = getenv("ZDEC_GRID_CAP") ? atof(getenv("ZDEC_GRID_CAP")) : 0.0;
+        const int grid_cap = gcap > 0 ? std::max(1, (int)(gcap * ctx->num_sms)) : 0;
         const int groups[N_MAT] = {n_groups(ctx->qkv_ld / 16), n_groups(H / 16), n_groups(F / 8), n_groups(H / 16),
                                    n_groups(ctx->nrt_vocab)};
         const int nsb[N_MAT] = {ctx->nsb_h, ctx->nsb_q, ctx->nsb_h, ctx->nsb_f, ctx->nsb_h};
@@ -442,9 +447,19 @@ extern "C" zdec_status zdec_create_cache(const zdec_model_desc *desc, const zdec
                 if ((impl == 3 && Bc != 1) || (impl == 1 && Bc > 4)) continue;
                 for (int m = 0; m < N_MAT; m++)
                     ctx->cs_tab[impl][c][m] = pick_cs(
-                        groups[m], nsb[m], [&](int cs) { return gemm_cluster_slots(Bc, impl, epi[m], cs); }, csmax);
+                        groups[m], nsb[m], [&](int cs) { return gemm_cluster_slots(Bc, impl, epi[m], cs); }, csmax,
+                        m == MAT_LM ? 0 : grid_cap);
             }
         cudaGetLastError();
+        // ZDEC_SPLITS=q,o,gu,down,lm forces per-matrix splits (0 keeps the model's)
+        if (const char *e = getenv("ZDEC_SPLITS")) {
+            int f[N_MAT] = {0, 0, 0, 0, 0};
+            sscanf(e, "%d,%d,%d,%d,%d", &f[0], &f[1], &f[2], &f[3], &f[4]);
+            for (int impl = 1; impl <= 3; impl++)
+                for (int c = 0; c < 5; c++)
+                    for (int m = 0; m < N_MAT; m++)
+                        if (f[m] >= 1 && f[m] <= 16 && ctx->cs_tab[impl][c][m]) ctx->cs_tab[impl][c][m] = f[m];
+        }
         if (getenv("ZDEC_PRINT_SPLITS"))   // impl, batch class: splits of qkv, o, gate/up, down, lm head
             for (int impl = 1; impl <= 3; impl++)
                 for (int c = 0; c < 5; c++)
@@ -722,7 +737,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, int segs, float *logits_ou
     gp.out_Bp = Bp;
     gp.status = ctx->status;
     gp.wait_limit = ctx->wait_limit;
-    gp.pipe = gemm_pipe_mode();
+    gp.pair = gemm_pair_mode();
     // Every projection takes its activation as fp16 hi + lo planes (~22 bits):
     // the new K/V rows are rounded and quantized, and over dozens of layers a
     // single fp16 operand would drift past the parity tolerance.
@@ -1312,7 +1327,7 @@ static zdec_status run_q4k_gemm(const void *repacked_dev, int N, int K, const fl
     gp.out = y_dev;
     gp.ldo = N;
     gp.cs = pick_cs(n_groups(N / 16), K / QK, [&](int cs) { return gemm_cluster_slots(B, impl, EPI_STORE, cs); });
-    gp.pipe = gemm_pipe_mode();
+    gp.pair = gemm_pair_mode();
     CK(launch_gemm(gp, EPI_STORE, impl, false, s));
     return ZDEC_OK;
 }

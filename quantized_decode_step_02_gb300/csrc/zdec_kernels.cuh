@@ -67,8 +67,7 @@ struct GemmParams {
     int *amax_idx;
     int cs;                // K split over a cluster of cs CTAs (1..16)
     int stages;            // pipeline depth (set by the launcher)
-    int pipe;              // 0: stages consumed in pairs, refilled after a block barrier;
-                           // 1: each stage refilled by the last warp done with it
+    int pair;              // 1: stages consumed two at a time; 0: one at a time
     uint32_t red_off;      // cluster rank 0's area for the peers' partial tiles (set by the launcher)
     int red_alias;         // 1: that area is rank 0's stage ring, written once its K loop is done
     const uint8_t *pf_ptr; // read-only bytes the next kernel streams (L2 prefetch), or null

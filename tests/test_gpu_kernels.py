@@ -101,26 +101,6 @@ def test_gemm_mma_shapes_and_ragged_batch(N, K, B):
     _gemm_case(N, K, B, 2, N + K + B)
 
 
-def test_gemm_per_stage_refill_pipeline():
-    """The optional pipeline that refills each stage from the last warp done
-    with it (ZDEC_GEMM_PIPE=1, read once per process, so run in a child
-    process) against the oracle: every kernel, ragged batches, a split-K
-    cluster and a multi-stage K loop."""
-    import os
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    code = ("from tests.test_gpu_kernels import _gemm_case\n"
-            "for N, K, B, impl in [(4096, 4096, 1, 3), (4096, 14336, 1, 3), (2048, 4096, 3, 2), "
-            "(6144, 4096, 8, 2), (512, 512, 32, 2), (2048, 2048, 2, 1)]:\n"
-            "    _gemm_case(N, K, B, impl, N + K + B)\n"
-            "print('ok')\n")
-    env = dict(os.environ, ZDEC_GEMM_PIPE="1")
-    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
-                       timeout=600)
-    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
-
-
 @pytest.mark.parametrize("B", [1, 2, 3, 4])
 def test_gemm_matvec_batches(B):
     _gemm_case(2048, 2048, B, 1, 40 + B)
