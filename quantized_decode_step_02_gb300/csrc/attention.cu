@@ -48,6 +48,7 @@ constexpr uint32_t AFULL = 0xFFFFFFFFu;
 constexpr int ATT_MAX_STAGES = 8;
 constexpr int SEG_PART = 4 * (HD + 4);          // floats of one segment's partial per kv head
 constexpr long long ATT_WAIT_LIMIT = 1LL << 32;   // clock cycles (~2 s): a copy that never lands
+constexpr int ATT_PAGE_CACHE = 64;              // block-table entries a CTA stages in shared memory
 
 __host__ __device__ constexpr uint32_t att_stage_bytes(int kt, int vt) { return kv_region_bytes(kt) + kv_region_bytes(vt); }
 static int att_max_stages(int kt, int vt) {
@@ -231,14 +232,26 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     __shared__ __align__(8) uint64_t full[ATT_MAX_STAGES];
     __shared__ int s_map[4];                             // row, segment, segments of the row, chunks per segment
     __shared__ int s_bad, s_last;
+    __shared__ int s_pages[ATT_PAGE_CACHE];              // pages of this CTA's first chunks
 
     const int rank = blockIdx.x, g = blockIdx.y, z = blockIdx.z, CS = p.cs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     tl_min(p.tl, 0);
     // ---- which row and segment this cluster takes.  Positions, slots and
     // block tables are step inputs written before the step's first kernel,
-    // so this runs before the dependency wait.
-    if (warp == 0) {
+    // so this runs before the dependency wait.  One segment slot per row
+    // (gridDim.z == B) needs no search: row z, whole.
+    if (gridDim.z == (unsigned)p.B) {
+        if (threadIdx.x == 0) {
+            const int pos = p.positions[z];
+            const bool valid = pos >= 0 && pos < p.max_L;
+            s_map[0] = valid ? z : -1;
+            s_map[1] = 0;
+            s_map[2] = 1;
+            s_map[3] = valid ? (pos + PAGE_TOKENS) / PAGE_TOKENS : 1;
+            s_bad = 0;
+        }
+    } else if (warp == 0) {
         int nch = 0;
         if (lane < p.B) {
             const int pos = p.positions[lane];
@@ -312,11 +325,17 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     const int NS = p.stages;
     const size_t coff = kv_chunk_off(p.kv, p.layer, g);
     auto stage = [&](int i) { return smem + (size_t)(i % NS) * SB; };
-    // chunk c (of the row) into ring slot i; a chunk with no cached token
-    // (only the new one) or without a page completes its stage with no copy
-    auto issue = [&](int i, int c) {
+    // the block-table entries of this CTA's chunks, loaded in parallel
+    for (int t = threadIdx.x; t < nchunks && t < ATT_PAGE_CACHE; t += blockDim.x)
+        s_pages[t] = kv_page(p.kv, slot, (c_lo + t) * PAGE_TOKENS);
+    __syncthreads();
+    // chunk i of this CTA's range into ring slot i % NS; a chunk with no
+    // cached token (only the new one) or without a page completes its stage
+    // with no copy
+    auto issue = [&](int i) {
+        const int c = c_lo + i;
         uint64_t *bar = &full[i % NS];
-        const int page = kv_page(p.kv, slot, c * PAGE_TOKENS);
+        const int page = i < ATT_PAGE_CACHE ? s_pages[i] : kv_page(p.kv, slot, c * PAGE_TOKENS);
         if (c * PAGE_TOKENS < H && kv_page_ok(p.kv, page)) {
             const uint8_t *src = p.kv.base + (size_t)page * p.kv.page_bytes + coff;
             mbar_expect_tx(bar, SB);
@@ -328,11 +347,10 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         }
     };
     // the cached history does not depend on the previous kernel: the first
-    // NS - 1 chunks go out before the dependency wait
-    if (threadIdx.x == 0)
-        for (int i = 0; i < NS - 1 && i < nchunks; i++) issue(i, c_lo + i);
+    // NS - 1 chunks go out before the dependency wait, one issuing thread each
+    if ((int)threadIdx.x < NS - 1 && (int)threadIdx.x < nchunks) issue(threadIdx.x);
     int issued = min(NS - 1, nchunks);   // chunks due in the ring (the same count on every thread)
-    int sent = issued;                   // thread 0: chunks it actually put in flight
+    int sent = issued;                   // thread 0 (after the first refill): chunks in flight
 
     // the rotary row of the new token: a constant table, read before the wait
     float2 rope_new[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -432,7 +450,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         __syncthreads();   // every warp is done with chunk ci - 1: its slot may be refilled
         if (issued < nchunks) {   // chunk ci + NS - 1 into the slot chunk ci - 1 freed
             if (threadIdx.x == 0 && !s_bad) {
-                issue(issued, c_lo + issued);
+                issue(issued);
                 sent = issued + 1;
             }
             issued++;

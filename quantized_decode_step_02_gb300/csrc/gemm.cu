@@ -444,15 +444,6 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         s_gain[threadIdx.x] = grp * 128 + (int)threadIdx.x < p.N ? p.next_gain[grp * 128 + threadIdx.x] : 0.0f;
     if (EPI == EPI_STORE && p.q_frag && grp < p.q_heads && (int)threadIdx.x < B * 4)   // 4 lines of 128 B per row
         prefetch_l1(p.q_rope + (size_t)p.q_pos[threadIdx.x >> 2] * 64 + (threadIdx.x & 3) * 16);
-    // warm L2 with this CTA's slice of the next kernel's read-only bytes, so the
-    // HBM keeps streaming while this grid drains and the next one ramps up
-    if (p.pf_ptr && p.pf_bytes) {
-        const size_t per = ((p.pf_bytes + gridDim.x - 1) / gridDim.x + 4095) & ~(size_t)4095;
-        const size_t beg = (size_t)blockIdx.x * per;
-        const size_t end = min(p.pf_bytes, beg + per);
-        for (size_t off = beg + (size_t)threadIdx.x * 4096; off < end; off += (size_t)blockDim.x * 4096)
-            prefetch_l2(p.pf_ptr + off, (uint32_t)min((size_t)4096, end - off));
-    }
     pdl_launch_dependents();
     pdl_wait();
     tl_min(p.tl, 1);

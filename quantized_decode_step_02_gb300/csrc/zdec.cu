@@ -128,7 +128,6 @@ struct zdec_ctx {
     int slots_n = 0;
     int gemm_impl = 0, matvec_max_B = 0;
     int b1_impl = 3;                   // projection kernel at B = 1 (ZDEC_B1_IMPL)
-    size_t prefetch_cap = 0;   // bytes of the next matrix a GEMM warms in L2 (0: off; ZDEC_L2_PREFETCH_MB)
     long long wait_limit = 0;  // projection stage-wait bound in clock cycles (0: the kernels' ~2 s)
     std::map<std::tuple<int, const void *, int, int>, cudaGraphExec_t> graphs;   // (B, logits, impl, segments)
     std::string err;
@@ -286,7 +285,6 @@ extern "C" zdec_status zdec_create_cache(const zdec_model_desc *desc, const zdec
     ctx->len_host.assign(max_B, 0);
     if (const char *e = getenv("ZDEC_MATVEC_MAX_B")) ctx->matvec_max_B = std::max(0, std::min(4, atoi(e)));
     if (const char *e = getenv("ZDEC_B1_IMPL")) ctx->b1_impl = std::max(1, std::min(3, atoi(e)));
-    if (const char *e = getenv("ZDEC_L2_PREFETCH_MB")) ctx->prefetch_cap = (size_t)std::max(0, atoi(e)) << 20;
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -744,13 +742,6 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, int segs, float *logits_ou
     auto operand = [&](__half *hi, __half *lo, __half *sums) { gp.x16 = hi; gp.x16lo = lo; gp.sx = sums; };
     auto matrix = [&](const uint8_t *W, int N, int nrt, int nsb, int cs) {
         gp.W = W; gp.N = N; gp.nrt = nrt; gp.nsb = nsb; gp.cs = cs;
-        gp.pf_ptr = nullptr; gp.pf_bytes = 0;
-    };
-    // the next weight matrix to warm in L2 while a GEMM runs (capped so the
-    // prefetched bytes and the running kernel's stream fit in L2 together)
-    auto prefetch = [&](const uint8_t *W, int nrt, int nsb) {
-        gp.pf_ptr = W;
-        gp.pf_bytes = std::min(tile_bytes(nrt, nsb), ctx->prefetch_cap);
     };
     const AttnPlan plan = attn_plan(ctx, B, segs);
     AttnParams ap{};
@@ -794,7 +785,6 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, int segs, float *logits_ou
         const LayerW &lw = ctx->L[l];
         normed_input(l == 0 ? 1 : resid_groups);
         matrix(lw.qkv, ctx->qkv_ld, ctx->qkv_ld / 16, ctx->nsb_h, split(MAT_QKV));
-        prefetch(lw.o, H / 16, ctx->nsb_q);
         gp.out = ctx->qkv; gp.ldo = ctx->qkv_ld;
         gp.q_frag = ctx->qfrag; gp.q_pos = ctx->pos_dev; gp.q_rope = ctx->rope; gp.q_heads = d.n_q_heads;
         STEP(ZDEC_KERNEL_GEMM_QKV, (gp.tl = tlk, launch_gemm(gp, EPI_STORE, impl, pdl, s)));
@@ -803,21 +793,17 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, int segs, float *logits_ou
         STEP(ZDEC_KERNEL_ATTENTION, (ap.tl = tlk, launch_attention(ap, nz, pdl, s)));
         plain_input(ctx->o16, ctx->o16lo, ctx->osx);   // written by the attention merge
         matrix(lw.o, H, H / 16, ctx->nsb_q, split(MAT_O));
-        prefetch(lw.gu, F / 8, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
         gp.next_gain = lw.ffn_norm; gp.part_out = ctx->rms_part;
         gp.out16 = ctx->x16; gp.out16lo = ctx->x16lo; gp.out_sx = ctx->sx;
         STEP(ZDEC_KERNEL_GEMM_O, (gp.tl = tlk, launch_gemm(gp, EPI_RESID, impl, pdl, s)));
         normed_input(resid_groups);
         matrix(lw.gu, F, F / 8, ctx->nsb_h, split(MAT_GU));
-        prefetch(lw.down, H / 16, ctx->nsb_f);
         gp.out = nullptr; gp.ldo = F;
         gp.out16 = ctx->a16; gp.out16lo = ctx->a16lo; gp.out_sx = ctx->asx;
         STEP(ZDEC_KERNEL_GEMM_GATEUP, (gp.tl = tlk, launch_gemm(gp, EPI_SWIGLU, impl, pdl, s)));
         plain_input(ctx->a16, ctx->a16lo, ctx->asx);   // written by the gate/up epilogue
         matrix(lw.down, H, H / 16, ctx->nsb_f, split(MAT_DOWN));
-        if (l + 1 < d.n_layers) prefetch(ctx->L[l + 1].qkv, ctx->qkv_ld / 16, ctx->nsb_h);
-        else prefetch(ctx->embed, ctx->nrt_vocab, ctx->nsb_h);
         gp.out = ctx->x; gp.ldo = H;
         gp.next_gain = l + 1 < d.n_layers ? ctx->L[l + 1].attn_norm : ctx->final_norm;
         gp.part_out = ctx->rms_part;

@@ -82,10 +82,6 @@ __device__ __forceinline__ void pdl_wait() {
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-// Hint: bring [p, p+bytes) into L2.  p 16-byte aligned, bytes multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 // Hint: bring the 128-byte line holding p into this SM's L1.
 __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));

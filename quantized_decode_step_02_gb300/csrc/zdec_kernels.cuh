@@ -70,8 +70,6 @@ struct GemmParams {
     int pair;              // 1: stages consumed two at a time; 0: one at a time
     uint32_t red_off;      // cluster rank 0's area for the peers' partial tiles (set by the launcher)
     int red_alias;         // 1: that area is rank 0's stage ring, written once its K loop is done
-    const uint8_t *pf_ptr; // read-only bytes the next kernel streams (L2 prefetch), or null
-    size_t pf_bytes;       // multiple of 16, pf_ptr 16-byte aligned
     uint32_t *status;      // device status word (bounded-wait timeouts)
     long long wait_limit;  // clock cycles a stage wait may take before it gives up (0: ~2 s;
                            // < 0: the first stage wait gives up at once, for tests); the drain
