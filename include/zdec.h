@@ -220,8 +220,9 @@ zdec_status zdec_set_gemm_impl(zdec_ctx *ctx, int impl);
  * step: the first CTA's start, the first CTA past its dependency wait, the
  * last CTA's end, the launch's kind (ZDEC_KERNEL_*), then the latest CTA to
  * reach the kernel's milestones (for the projections: past the wait, first
- * stage landed, K loop done, cluster reduction done; zero where a kernel
- * records none).  on = 0 stops and frees it. */
+ * stage landed, K loop done, cluster reduction done; for the attention: past
+ * the wait, the cluster's partials landed in rank 0, chunk loop done, merge
+ * done; zero where a kernel records none).  on = 0 stops and frees it. */
 zdec_status zdec_set_trace(zdec_ctx *ctx, int on);
 /* Copy the trace of the last traced step (waits for the stream).  *n gets the
  * entry count (0 when tracing is off); out_host needs that many uint64

@@ -35,12 +35,10 @@
 // memory, fixed rank order), segments -> the last segment to finish (global
 // partials and a ticket per (row, kv head), merged in segment order), so the
 // result never depends on timing.
-#include <cooperative_groups.h>
 
 #include "kv_pool.cuh"
 #include "zdec_kernels.cuh"
 
-namespace cg = cooperative_groups;
 
 namespace zdec {
 
@@ -49,6 +47,7 @@ constexpr int ATT_MAX_STAGES = 8;
 constexpr int SEG_PART = 4 * (HD + 4);          // floats of one segment's partial per kv head
 constexpr long long ATT_WAIT_LIMIT = 1LL << 32;   // clock cycles (~2 s): a copy that never lands
 constexpr int ATT_PAGE_CACHE = 64;              // block-table entries a CTA stages in shared memory
+constexpr int ATT_MAX_CS = 16;                  // CTAs of a cluster (one segment of a row)
 
 __host__ __device__ constexpr uint32_t att_stage_bytes(int kt, int vt) { return kv_region_bytes(kt) + kv_region_bytes(vt); }
 static int att_max_stages(int kt, int vt) {
@@ -59,8 +58,9 @@ int attention_default_stages(int kt, int vt) { return (kt == KV_T_F16 && vt == K
 size_t attention_smem_bytes(int kt, int vt, int ns) {
     if (ns < 2 || ns > att_max_stages(kt, vt)) ns = attention_default_stages(kt, vt);
     const size_t stages = (size_t)ns * att_stage_bytes(kt, vt);
-    const size_t merge = (4 * 4 * 2 + 4 * 4 * HD) * sizeof(float);
-    return stages > merge ? stages : merge;
+    const size_t merge = (4 * 4 * 2 + 4 * 4 * (HD + 4)) * sizeof(float);   // the CTA's warp merge
+    const size_t recv = (size_t)(ATT_MAX_CS - 1) * GROUP * (HD + 4) * sizeof(float);   // rank 0: the peers' partials
+    return std::max(stages, std::max(merge, recv));
 }
 
 __device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
@@ -79,120 +79,140 @@ __device__ __forceinline__ void q8x4_to_h2(uint32_t w, uint32_t &lo, uint32_t &h
     lo = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, 0x64646464u, 0x4140)), bias));
     hi = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, 0x64646464u, 0x4342)), bias));
 }
-// fp16 hi + lo split of four values into an mma A fragment.
-__device__ __forceinline__ void split_p(const float (&v)[4], uint32_t (&pa)[4]) {
-    const __half2 h01 = __floats2half2_rn(v[0], v[1]), h23 = __floats2half2_rn(v[2], v[3]);
-    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-    pa[0] = h2_as_u32(h01);
-    pa[1] = h2_as_u32(__floats2half2_rn(v[0] - f01.x, v[1] - f01.y));
-    pa[2] = h2_as_u32(h23);
-    pa[3] = h2_as_u32(__floats2half2_rn(v[2] - f23.x, v[3] - f23.y));
-}
+// The chunk's tokens are the mma's M dimension and the group's 4 query heads
+// its N: column n of a B operand or an accumulator is head n >> 1, fp16 part
+// n & 1 (the query is carried as hi + lo parts, ~22 bits).  A warp takes 16
+// tokens of a chunk, 16 w .. 16 w + 15.  Along the mma's k index, the lane
+// positions 2 tig + {0, 1, 8, 9} stand for four adjacent dims (scores) or
+// tokens (output), 4 tig + {0, 1, 2, 3}, on both operands alike, so that
+// every lane reads four adjacent elements of a K row or a V^T row.
 
-// Scores of this warp's 16 tokens of a chunk against the 4 heads:
-// S[nt] = C fragment of the tokens 16 w + 4 (col >> 1) + 2 nt + (col & 1),
-// i.e. lane (gid, tig) ends with tokens 16 w + 4 tig + {0, 1} (nt = 0) and
-// {2, 3} (nt = 1), rows gid (q high part) and gid + 8 (q low part).
+// Scores S^T = K q^T of this warp's 16 tokens: returns the scores of head tig
+// for tokens ta = 16 w + gid and tb = ta + 8 (hi and lo parts summed).
 template <int KT>
-__device__ __forceinline__ void qk_tile(const uint8_t *sK, int warp, int gid, int tig, const uint32_t (&qa)[8][4],
-                                        float (&S)[2][4]) {
-    const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+__device__ __forceinline__ void qk_tile(const uint8_t *sK, int warp, int gid, int tig, const uint32_t (&qb)[8][2],
+                                        float &sa, float &sb) {
+    const int ta = 16 * warp + gid, tb = ta + 8;
+    float c[4];
+    if (KT == KV_T_Q8) {
+        const uint2 sca = *reinterpret_cast<const uint2 *>(sK + ks_off(ta, 0));   // 4 block scales
+        const uint2 scb = *reinterpret_cast<const uint2 *>(sK + ks_off(tb, 0));
+        const float2 a01 = __half22float2(u32_as_h2(sca.x)), a23 = __half22float2(u32_as_h2(sca.y));
+        const float2 b01 = __half22float2(u32_as_h2(scb.x)), b23 = __half22float2(u32_as_h2(scb.y));
+        const float ka[4] = {a01.x, a01.y, a23.x, a23.y}, kb[4] = {b01.x, b01.y, b23.x, b23.y};
+        const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int nt = 0; nt < 2; nt++) {
-        const int tr = 16 * warp + 4 * (gid >> 1) + 2 * nt + (gid & 1);   // token of B column gid
-        if (KT == KV_T_Q8) {
-            const int ta = 16 * warp + 4 * tig + 2 * nt;   // tokens of C columns 2 tig, 2 tig + 1
-            const uint2 sa = *reinterpret_cast<const uint2 *>(sK + ks_off(ta, 0));
-            const uint2 sb = *reinterpret_cast<const uint2 *>(sK + ks_off(ta + 1, 0));
-            const float2 a01 = __half22float2(u32_as_h2(sa.x)), a23 = __half22float2(u32_as_h2(sa.y));
-            const float2 b01 = __half22float2(u32_as_h2(sb.x)), b23 = __half22float2(u32_as_h2(sb.y));
-            const float ka[4] = {a01.x, a01.y, a23.x, a23.y}, kb[4] = {b01.x, b01.y, b23.x, b23.y};
+        for (int i = 0; i < 4; i++) c[i] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 4; i++) S[nt][i] = 0.0f;
+        for (int bl = 0; bl < 4; bl++) {   // one 32-dim block: two k steps, then its scales
+            float tmp[4];
 #pragma unroll
-            for (int bl = 0; bl < 4; bl++) {
-                float tmp[4];
-#pragma unroll
-                for (int hs = 0; hs < 2; hs++) {
-                    const int s8 = 2 * bl + hs;
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                        sK + tr * 128 + ((((uint32_t)s8 ^ (uint32_t)(tr & 7)) << 4) | ((uint32_t)tig << 2)));
-                    uint32_t b0, b1;
-                    q8x4_to_h2(w, b0, b1);
-                    if (hs) mma16816(tmp, qa[s8], b0, b1, tmp);
-                    else mma16816(tmp, qa[s8], b0, b1, zero4);
-                }
-                S[nt][0] += ka[bl] * tmp[0];
-                S[nt][1] += kb[bl] * tmp[1];
-                S[nt][2] += ka[bl] * tmp[2];
-                S[nt][3] += kb[bl] * tmp[3];
+            for (int hs = 0; hs < 2; hs++) {
+                const int s8 = 2 * bl + hs;
+                const uint32_t wa = *reinterpret_cast<const uint32_t *>(sK + k8_off(ta, 16 * s8 + 4 * tig));
+                const uint32_t wb = *reinterpret_cast<const uint32_t *>(sK + k8_off(tb, 16 * s8 + 4 * tig));
+                uint32_t a[4];
+                q8x4_to_h2(wa, a[0], a[2]);
+                q8x4_to_h2(wb, a[1], a[3]);
+                if (hs) mma16816(tmp, a, qb[s8][0], qb[s8][1], tmp);
+                else mma16816(tmp, a, qb[s8][0], qb[s8][1], zero4);
             }
-        } else {
-            // two independent accumulator chains (even / odd 16-dim steps)
-            float se[4] = {0.0f, 0.0f, 0.0f, 0.0f}, so[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int s8 = 0; s8 < 8; s8++) {
-                uint32_t b0, b1;
-                if (KT == KV_T_F16) {
-                    const uint2 kb = *reinterpret_cast<const uint2 *>(
-                        sK + tr * 256 + ((((uint32_t)(2 * s8 + (tig >> 1)) ^ (uint32_t)(tr & 7)) << 4) |
-                                         ((uint32_t)(tig & 1) << 3)));
-                    b0 = kb.x;
-                    b1 = kb.y;
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                        sK + tr * 128 + ((((uint32_t)s8 ^ (uint32_t)(tr & 7)) << 4) | ((uint32_t)tig << 2)));
-                    b0 = e4m3x2_to_h2((uint16_t)(w & 0xFFFFu));
-                    b1 = e4m3x2_to_h2((uint16_t)(w >> 16));
-                }
-                if (s8 & 1) mma16816(so, qa[s8], b0, b1, so);
-                else mma16816(se, qa[s8], b0, b1, se);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i++) S[nt][i] = se[i] + so[i];
+            c[0] += ka[bl] * tmp[0];
+            c[1] += ka[bl] * tmp[1];
+            c[2] += kb[bl] * tmp[2];
+            c[3] += kb[bl] * tmp[3];
         }
+    } else {
+        // two independent accumulator chains (even / odd k steps)
+        float ce[4] = {0.0f, 0.0f, 0.0f, 0.0f}, co[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int s8 = 0; s8 < 8; s8++) {
+            uint32_t a[4];
+            if (KT == KV_T_F16) {
+                const uint2 va = *reinterpret_cast<const uint2 *>(sK + k16_off(ta, 16 * s8 + 4 * tig));
+                const uint2 vb = *reinterpret_cast<const uint2 *>(sK + k16_off(tb, 16 * s8 + 4 * tig));
+                a[0] = va.x; a[2] = va.y;
+                a[1] = vb.x; a[3] = vb.y;
+            } else {
+                const uint32_t wa = *reinterpret_cast<const uint32_t *>(sK + k8_off(ta, 16 * s8 + 4 * tig));
+                const uint32_t wb = *reinterpret_cast<const uint32_t *>(sK + k8_off(tb, 16 * s8 + 4 * tig));
+                a[0] = e4m3x2_to_h2((uint16_t)(wa & 0xFFFFu)); a[2] = e4m3x2_to_h2((uint16_t)(wa >> 16));
+                a[1] = e4m3x2_to_h2((uint16_t)(wb & 0xFFFFu)); a[3] = e4m3x2_to_h2((uint16_t)(wb >> 16));
+            }
+            if (s8 & 1) mma16816(co, a, qb[s8][0], qb[s8][1], co);
+            else mma16816(ce, a, qb[s8][0], qb[s8][1], ce);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) c[i] = ce[i] + co[i];
     }
+    sa = c[0] + c[1];
+    sb = c[2] + c[3];
 }
 
-// out += P V for this warp's 16 tokens (lane tokens t0 .. t0 + 3, t0 = 16 w + 4 tig).
+// fp16 part `lo` (0: hi = fp16(x), 1: lo = fp16(x - hi)) of two values, packed.
+__device__ __forceinline__ uint32_t part2(float x0, float x1, bool lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - f.x, x1 - f.y);
+    return h2_as_u32(lo ? l : h);
+}
+
+// out^T += V^T P^T for this warp's 16 tokens.  pa, pb: this lane's
+// probabilities of head tig for tokens 16 w + gid and + 8.  Accumulator mt
+// holds dims 16 mt + gid (c0, c1) and + 8 (c2, c3), columns head tig hi, lo.
 template <int VT>
-__device__ __forceinline__ void pv_tile(const uint8_t *sV, int warp, int gid, int tig, const float (&pr)[4],
-                                        float (&oacc)[16][4]) {
-    const int t0 = 16 * warp + 4 * tig;
+__device__ __forceinline__ void pv_tile(const uint8_t *sV, int warp, int gid, int tig, float pa, float pb,
+                                        float (&oacc)[8][4]) {
+    // the P^T operand: lane (gid, tig) carries head gid >> 1, part gid & 1, of
+    // tokens 4 tig + e (e = 0..3) of the warp's 16; token j of head h is in
+    // lane (j & 7, h), as its first score for j < 8 and its second above
+    const int h = gid >> 1;
+    const bool lo = gid & 1;
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const int src = ((4 * (tig & 1) + e) << 2) | h;
+        const float x = __shfl_sync(AFULL, pa, src), y = __shfl_sync(AFULL, pb, src);
+        pv[e] = tig < 2 ? x : y;
+    }
+    const int t0 = 16 * warp + 4 * tig;   // the lane's four tokens along k
     if (VT == KV_T_Q8) {
+        // V's block scales (per token and 32 dims) go into the P^T operand
 #pragma unroll
         for (int bl = 0; bl < 4; bl++) {
-            const uint2 vsc = *reinterpret_cast<const uint2 *>(sV + vs_off(t0, bl));   // tokens t0..t0+3
-            const float2 v01 = __half22float2(u32_as_h2(vsc.x)), v23 = __half22float2(u32_as_h2(vsc.y));
-            const float q4[4] = {pr[0] * v01.x, pr[1] * v01.y, pr[2] * v23.x, pr[3] * v23.y};
-            uint32_t pa[4];
-            split_p(q4, pa);
+            const uint2 s4 = *reinterpret_cast<const uint2 *>(sV + vs_off(t0, bl));   // tokens t0..t0+3
+            const float2 s01 = __half22float2(u32_as_h2(s4.x)), s23 = __half22float2(u32_as_h2(s4.y));
+            const uint32_t b0 = part2(pv[0] * s01.x, pv[1] * s01.y, lo);
+            const uint32_t b1 = part2(pv[2] * s23.x, pv[3] * s23.y, lo);
 #pragma unroll
-            for (int dq = 0; dq < 4; dq++) {
-                const int dd = 32 * bl + 8 * dq + gid;
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, dd));
-                uint32_t b0, b1;
-                q8x4_to_h2(w, b0, b1);
-                mma16816(oacc[4 * bl + dq], pa, b0, b1, oacc[4 * bl + dq]);
+            for (int mh = 0; mh < 2; mh++) {
+                const int mt = 2 * bl + mh, da = 16 * mt + gid;
+                const uint32_t wa = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, da));
+                const uint32_t wb = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, da + 8));
+                uint32_t a[4];
+                q8x4_to_h2(wa, a[0], a[2]);
+                q8x4_to_h2(wb, a[1], a[3]);
+                mma16816(oacc[mt], a, b0, b1, oacc[mt]);
             }
         }
     } else {
-        uint32_t pa[4];
-        split_p(pr, pa);
+        const uint32_t b0 = part2(pv[0], pv[1], lo), b1 = part2(pv[2], pv[3], lo);
 #pragma unroll
-        for (int dn = 0; dn < 16; dn++) {
-            const int dd = 8 * dn + gid;
-            uint32_t b0, b1;
+        for (int mt = 0; mt < 8; mt++) {
+            const int da = 16 * mt + gid;
+            uint32_t a[4];
             if (VT == KV_T_F16) {
-                const uint2 vb = *reinterpret_cast<const uint2 *>(sV + v16_off(t0, dd));
-                b0 = vb.x;
-                b1 = vb.y;
+                const uint2 va = *reinterpret_cast<const uint2 *>(sV + v16_off(t0, da));
+                const uint2 vb = *reinterpret_cast<const uint2 *>(sV + v16_off(t0, da + 8));
+                a[0] = va.x; a[2] = va.y;
+                a[1] = vb.x; a[3] = vb.y;
             } else {
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, dd));
-                b0 = e4m3x2_to_h2((uint16_t)(w & 0xFFFFu));
-                b1 = e4m3x2_to_h2((uint16_t)(w >> 16));
+                const uint32_t wa = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, da));
+                const uint32_t wb = *reinterpret_cast<const uint32_t *>(sV + v8_off(t0, da + 8));
+                a[0] = e4m3x2_to_h2((uint16_t)(wa & 0xFFFFu)); a[2] = e4m3x2_to_h2((uint16_t)(wa >> 16));
+                a[1] = e4m3x2_to_h2((uint16_t)(wb & 0xFFFFu)); a[3] = e4m3x2_to_h2((uint16_t)(wb >> 16));
             }
-            mma16816(oacc[dn], pa, b0, b1, oacc[dn]);
+            mma16816(oacc[mt], a, b0, b1, oacc[mt]);
         }
     }
 }
@@ -221,15 +241,13 @@ __device__ __forceinline__ uint16_t encode_lane(__half h, uint16_t &scale_bits) 
 
 // ------------------------------------------------------------------ kernel ---
 template <int KT, int VT>
-__global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
+__global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
     constexpr uint32_t KB = kv_region_bytes(KT), VB = kv_region_bytes(VT), SB = KB + VB;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint16_t s_newk[HD], s_newv[HD];          // the new token in storage form
     __shared__ uint16_t s_newks[4], s_newvs[4];
-    // this CTA's (max, sum, output) per head; read as float4 (also through
-    // distributed shared memory), so 16-byte aligned
-    __shared__ __align__(16) float s_part[GROUP][HD + 4];
     __shared__ __align__(8) uint64_t full[ATT_MAX_STAGES];
+    __shared__ __align__(8) uint64_t merge_bar;           // rank 0: the peers' partials have landed
     __shared__ int s_map[4];                             // row, segment, segments of the row, chunks per segment
     __shared__ int s_bad, s_last;
     __shared__ int s_pages[ATT_PAGE_CACHE];              // pages of this CTA's first chunks
@@ -300,6 +318,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; i++) mbar_init(&full[i], 1);
+        mbar_init(&merge_bar, (uint32_t)max(1, CS - 1));
         mbar_fence_init();
     }
     __syncthreads();
@@ -347,10 +366,11 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         }
     };
     // the cached history does not depend on the previous kernel: the first
-    // NS - 1 chunks go out before the dependency wait, one issuing thread each
-    if ((int)threadIdx.x < NS - 1 && (int)threadIdx.x < nchunks) issue(threadIdx.x);
-    int issued = min(NS - 1, nchunks);   // chunks due in the ring (the same count on every thread)
-    int sent = issued;                   // thread 0 (after the first refill): chunks in flight
+    // NS chunks (the whole ring) go out before the dependency wait, one
+    // issuing thread each
+    if ((int)threadIdx.x < NS && (int)threadIdx.x < nchunks) issue(threadIdx.x);
+    int issued = min(NS, nchunks);   // chunks due in the ring (the same count on every thread)
+    int sent = issued;               // thread 0 (after the first refill): chunks in flight
 
     // the rotary row of the new token: a constant table, read before the wait
     float2 rope_new[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -365,21 +385,21 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     tl_min(p.tl, 1);
     tl_max(p.tl, 4);
 
-    // ---- query fragments: head 4g + gid (gid < 4), dims 16 s + 4 tig + {0..3}
-    uint32_t qa[8][4];
+    // ---- the query as the scores' B operand: lane (gid, tig) carries head
+    // 4 g + (gid >> 1), fp16 part gid & 1, of dims 16 s + 4 tig + {0..3}
+    uint32_t qb[8][2];
+    const bool qlo = gid & 1;
     if (p.q_frag) {   // prepared by the QKV projection's epilogue (rotated, scaled, hi/lo)
-        const uint4 *qf = p.q_frag + ((size_t)b * p.nq + GROUP * g + (gid < GROUP ? gid : 0)) * 32 + tig;
+        const uint4 *qf = p.q_frag + ((size_t)b * p.nq + GROUP * g + (gid >> 1)) * 32 + tig;
 #pragma unroll
         for (int st = 0; st < 8; st++) {
-            const uint4 f = gid < GROUP ? qf[st * 4] : make_uint4(0, 0, 0, 0);
-            qa[st][0] = f.x;
-            qa[st][1] = f.y;
-            qa[st][2] = f.z;
-            qa[st][3] = f.w;
+            const uint4 f = qf[st * 4];   // hi(d0, d1), lo(d0, d1), hi(d2, d3), lo(d2, d3)
+            qb[st][0] = qlo ? f.y : f.x;
+            qb[st][1] = qlo ? f.w : f.z;
         }
     } else {
         const float qscale = 0.12751743082459868f;   // log2(e)/sqrt(128): scores in log2 units
-        const int hq = GROUP * g + gid;
+        const int hq = GROUP * g + (gid >> 1);
         const float *qrow = p.qkv + (size_t)b * p.qkv_ld + (size_t)hq * HD;
         const float2 *cs = p.rope + (size_t)pos * (HD / 2);
 #pragma unroll
@@ -388,20 +408,17 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 const int d = 16 * st + 4 * tig + e;
-                float x = 0.0f;
-                if (gid < GROUP) {
-                    x = qrow[d];
-                    if (p.append) {
-                        const float2 c = cs[d & 63];
-                        x = d < 64 ? x * c.x - qrow[d + 64] * c.y : x * c.x + qrow[d - 64] * c.y;
-                    }
+                float x = qrow[d];
+                if (p.append) {
+                    const float2 c = cs[d & 63];
+                    x = d < 64 ? x * c.x - qrow[d + 64] * c.y : x * c.x + qrow[d - 64] * c.y;
                 }
                 v[e] = x * qscale;
             }
-            split_p(v, qa[st]);
+            qb[st][0] = part2(v[0], v[1], qlo);
+            qb[st][1] = part2(v[2], v[3], qlo);
         }
     }
-    tl_max(p.tl, 5);
 
     // ---- the new token (warp 0 of the CTA that holds it): its k and v rows
     // are loaded now, and rotated, rounded and encoded at the chunk that holds
@@ -434,13 +451,13 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         }
     };
 
-    // ---- online softmax state (meaningful on lanes gid < 4: head 4g + gid)
+    // ---- online softmax state of head 4 g + tig (l_run: this lane's tokens)
     float m_run = -INFINITY, l_run = 0.0f;
-    float oacc[16][4];
+    float oacc[8][4];
 #pragma unroll
-    for (int dn = 0; dn < 16; dn++)
+    for (int mt = 0; mt < 8; mt++)
 #pragma unroll
-        for (int i = 0; i < 4; i++) oacc[dn][i] = 0.0f;
+        for (int i = 0; i < 4; i++) oacc[mt][i] = 0.0f;
     bool ok = true;
 
     for (int ci = 0; ci < nchunks; ci++) {
@@ -448,7 +465,7 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         const int zfrom = max(H, c0) - c0;   // first local token not read from the cache
         if (zfrom < PAGE_TOKENS && has_new && warp == 0) encode_new();   // published by the barrier below
         __syncthreads();   // every warp is done with chunk ci - 1: its slot may be refilled
-        if (issued < nchunks) {   // chunk ci + NS - 1 into the slot chunk ci - 1 freed
+        if (ci > 0 && issued < nchunks) {   // chunk ci + NS - 1 into the slot chunk ci - 1 freed
             if (threadIdx.x == 0 && !s_bad) {
                 issue(issued);
                 sent = issued + 1;
@@ -478,38 +495,34 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             }
             __syncthreads();
         }
-        const int tb = c0 + 16 * warp;   // this warp's 16 tokens
-        if (ok && tb < T1) {
-            float S[2][4];
-            qk_tile<KT>(sK, warp, gid, tig, qa, S);
-            // ---- online softmax on this tile (head gid, tokens tb + 4 tig + {0..3})
-            float sc[4] = {S[0][0] + S[0][2], S[0][1] + S[0][3], S[1][0] + S[1][2], S[1][1] + S[1][3]};
-            if (gid >= GROUP) sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;   // zero A rows: no head
-            if (tb + 16 > T1)   // the range's last tile may end early
-#pragma unroll
-                for (int e = 0; e < 4; e++)
-                    if (tb + 4 * tig + e >= T1) sc[e] = -INFINITY;
-            float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 1));
-            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 2));
+        const int tw = c0 + 16 * warp;   // this warp's 16 tokens
+        if (ok && tw < T1) {
+            float sa, sb;   // head tig, tokens tw + gid and tw + gid + 8
+            qk_tile<KT>(sK, warp, gid, tig, qb, sa, sb);
+            if (tw + gid >= T1) sa = -INFINITY;   // the range's last tile may end early
+            if (tw + gid + 8 >= T1) sb = -INFINITY;
+            float mt = fmaxf(sa, sb);
+            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 4));
+            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 8));
+            mt = fmaxf(mt, __shfl_xor_sync(AFULL, mt, 16));
             // the output is rescaled only when some head's running max grew
             // (alpha = 1 exactly otherwise), which after the first tiles is rare
             const float m_new = fmaxf(m_run, mt);
             const bool grow = m_new > m_run;
             const float alpha = grow ? exp2f(m_run - m_new) : 1.0f;   // m_run = -inf -> 0
-            float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float pa = 0.0f, pb = 0.0f;
             if (m_new != -INFINITY) {
-#pragma unroll
-                for (int e = 0; e < 4; e++) pr[e] = exp2f(sc[e] - m_new);
+                pa = exp2f(sa - m_new);
+                pb = exp2f(sb - m_new);
             }
             m_run = m_new;
-            l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+            l_run = l_run * alpha + (pa + pb);
             if (__any_sync(AFULL, grow))
 #pragma unroll
-                for (int dn = 0; dn < 16; dn++)
+                for (int m = 0; m < 8; m++)
 #pragma unroll
-                    for (int i = 0; i < 4; i++) oacc[dn][i] *= alpha;
-            pv_tile<VT>(sV, warp, gid, tig, pr, oacc);
+                    for (int i = 0; i < 4; i++) oacc[m][i] *= alpha;
+            pv_tile<VT>(sV, warp, gid, tig, pa, pb, oacc);
         }
     }
     tl_max(p.tl, 6);
@@ -521,21 +534,21 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
     // ---- merge the 4 warps of this CTA (shared memory reused after the stages)
     float *wm = reinterpret_cast<float *>(smem);   // [4 warps][4 heads]
     float *wl = wm + 16;
-    float *wo = wl + 16;                            // [4][4][128]
-    float l_tot = l_run;
-    l_tot += __shfl_xor_sync(AFULL, l_tot, 1);
-    l_tot += __shfl_xor_sync(AFULL, l_tot, 2);
+    float *wo = wl + 16;                            // [4][4][HD + 4] (padded: no bank conflicts)
+    float l_tot = l_run;   // over the warp's tokens: the lanes of head tig
+    l_tot += __shfl_xor_sync(AFULL, l_tot, 4);
+    l_tot += __shfl_xor_sync(AFULL, l_tot, 8);
+    l_tot += __shfl_xor_sync(AFULL, l_tot, 16);
     __syncthreads();
-    if (gid < GROUP) {
-        if (tig == 0) { wm[warp * 4 + gid] = m_run; wl[warp * 4 + gid] = l_tot; }
+    if (gid == 0) { wm[warp * 4 + tig] = m_run; wl[warp * 4 + tig] = l_tot; }
 #pragma unroll
-        for (int dn = 0; dn < 16; dn++)
-#pragma unroll
-            for (int e = 0; e < 2; e++)
-                wo[(warp * 4 + gid) * HD + 8 * dn + 2 * tig + e] = oacc[dn][e] + oacc[dn][2 + e];
+    for (int m = 0; m < 8; m++) {
+        wo[(warp * 4 + tig) * (HD + 4) + 16 * m + gid] = oacc[m][0] + oacc[m][1];
+        wo[(warp * 4 + tig) * (HD + 4) + 16 * m + gid + 8] = oacc[m][2] + oacc[m][3];
     }
     __syncthreads();
     const int head = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
+    float cta_m, cta_l, cta_o[4];   // this CTA's (max, sum, output) of head `head`, dims d0..d0+3
     {
         float M = -INFINITY;
         for (int w = 0; w < 4; w++) M = fmaxf(M, wm[w * 4 + head]);
@@ -544,41 +557,55 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
             const float mw = wm[w * 4 + head];
             const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M);
             L += f * wl[w * 4 + head];
-            for (int e = 0; e < 4; e++) O[e] += f * wo[(w * 4 + head) * HD + d0 + e];
+            for (int e = 0; e < 4; e++) O[e] += f * wo[(w * 4 + head) * (HD + 4) + d0 + e];
         }
-        if ((threadIdx.x & 31) == 0) { s_part[head][0] = M; s_part[head][1] = L; }
-        for (int e = 0; e < 4; e++) s_part[head][4 + d0 + e] = O[e];
+        cta_m = M;
+        cta_l = L;
+#pragma unroll
+        for (int e = 0; e < 4; e++) cta_o[e] = O[e];
     }
-    // ---- rank 0 merges the cluster's partials through distributed shared memory
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster_arrive_release();   // the partials in s_part (shared memory only)
+    // ---- the cluster's partials meet in rank 0's shared memory: once every
+    // CTA is past its chunk loop (rank 0's ring is free), each peer stores its
+    // (max, sum, output) per head there and arrives on rank 0's merge barrier
+    cluster_arrive_release();
     cluster_wait_acquire();
-    if (rank == 0) {
-        // issue every peer's loads before using any (the distributed shared
-        // memory latency is paid once, not once per rank)
-        float mr[16], lr[16];
-        float4 orr[16];
-#pragma unroll
-        for (int r = 0; r < 16; r++) {
-            mr[r] = -INFINITY;
-            lr[r] = 0.0f;
-            orr[r] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (r < CS) {
-                const float *ps = cluster.map_shared_rank(&s_part[0][0], r) + head * (HD + 4);
-                mr[r] = ps[0];
-                lr[r] = ps[1];
-                orr[r] = *reinterpret_cast<const float4 *>(ps + 4 + d0);
-            }
+    float *recv = reinterpret_cast<float *>(smem);   // [peer rank - 1][head][HD + 4]
+    if (rank != 0) {
+        const uint32_t dst = map_to_rank(smem_u32(recv + ((rank - 1) * GROUP + head) * (HD + 4)), 0);
+        if ((threadIdx.x & 31) == 0) {
+            st_cluster_f32(dst, cta_m);
+            st_cluster_f32(dst + 4u, cta_l);
         }
-        float M = -INFINITY;
+        st_cluster_v4(dst + (uint32_t)(4 + d0) * 4u, make_float4(cta_o[0], cta_o[1], cta_o[2], cta_o[3]));
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            mbar_remote_arrive(map_to_rank(smem_u32(&merge_bar), 0));
+        }
+    } else {
+        bool landed = CS == 1 || mbar_try_wait_cluster(&merge_bar, 0);
+        if (!landed) {
+            const long long t0 = clock64();
+            while (!(landed = mbar_try_wait_cluster(&merge_bar, 0)))
+                if (clock64() - t0 > ATT_WAIT_LIMIT) break;
+            if (!landed && threadIdx.x == 0) atomicOr(p.status, STATUS_TIMEOUT);
+        }
+        tl_max(p.tl, 5);
+        // in rank order, two passes over the partials in shared memory
+        const int nrecv = landed ? CS - 1 : 0;
+        float M = cta_m;
+        for (int r = 0; r < nrecv; r++) M = fmaxf(M, recv[(r * GROUP + head) * (HD + 4)]);
+        const float f0 = cta_m == -INFINITY ? 0.0f : exp2f(cta_m - M);
+        float L = f0 * cta_l, O[4];
 #pragma unroll
-        for (int r = 0; r < 16; r++) M = fmaxf(M, mr[r]);
-        float L = 0.0f, O[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int r = 0; r < 16; r++) {
-            const float f = mr[r] == -INFINITY ? 0.0f : exp2f(mr[r] - M);
-            L += f * lr[r];
-            O[0] += f * orr[r].x; O[1] += f * orr[r].y; O[2] += f * orr[r].z; O[3] += f * orr[r].w;
+        for (int e = 0; e < 4; e++) O[e] = f0 * cta_o[e];
+        for (int r = 0; r < nrecv; r++) {
+            const float *ps = recv + (r * GROUP + head) * (HD + 4);
+            const float mr = ps[0];
+            const float f = mr == -INFINITY ? 0.0f : exp2f(mr - M);
+            L += f * ps[1];
+            const float4 o4 = *reinterpret_cast<const float4 *>(ps + 4 + d0);
+            O[0] += f * o4.x; O[1] += f * o4.y; O[2] += f * o4.z; O[3] += f * o4.w;
         }
         bool finish = nseg == 1;
         if (!finish) {
@@ -650,10 +677,6 @@ __global__ __launch_bounds__(128) void attention_kernel(const AttnParams p) {
         }
     }
     tl_max(p.tl, 7);
-    // peers keep their partials alive until rank 0 has read them (its reads
-    // have returned by the time it arrives; nothing needs ordering)
-    cluster_arrive_relaxed();
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     // the appended token into its page, unless a device check flagged the step
     // (the status word is final by now: every kernel that sets it completed
     // before this kernel's dependency wait)

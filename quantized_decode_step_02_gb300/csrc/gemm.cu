@@ -455,14 +455,20 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     // batch row (RMSNorm scale) and the residual rows it will update
     constexpr int NY = IMPL == 2 ? NT : 1;
     constexpr bool EARLY = NY == 1 || (NY == 2 && GemmOcc<NT, IMPL>::v < 3);   // registers hold the residual
-    // RMSNorm scale of every batch row, one warp per row, into shared memory
-    if (p.rms_part)
-        for (int b = warp; b < B && b < 4 * NY; b += 8) {
-            float ss = 0.0f;
-            for (int i = lane; i < p.rms_nparts; i += 32) ss += p.rms_part[i * MAX_B + b];
+    // RMSNorm sums of x^2 for the batch rows (warp w: rows w, w + 8, ...), only
+    // in the CTA that runs the epilogue (rank 0).  Loaded now and reduced after
+    // the K loop: the first partial of each lane is a plain load that nothing
+    // uses before then, so its latency hides behind the loop.
+    const bool rms_here = p.rms_part && rank == 0;
+    float rms_ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (rms_here)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-            if (lane == 0) s_rms[b] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
+        for (int j = 0; j < 4; j++) {
+            const int b = warp + 8 * j;
+            if (b < B && b < 4 * NY && lane < p.rms_nparts) {
+                rms_ss[j] = p.rms_part[lane * MAX_B + b];
+                for (int i = lane + 32; i < p.rms_nparts; i += 32) rms_ss[j] += p.rms_part[i * MAX_B + b];
+            }
         }
     float xin[NY][2];
     auto fetch_xin = [&]() {
@@ -640,10 +646,21 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         if (bad || s_bad) return;
         tl_max(p.tl, 7);
     }
-    if (p.rms_part) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
+    if (rms_here) {   // RMSNorm folded out of the operand: y = r_b * W (g * x_b)
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int b = warp + 8 * j;
+            if (b < B && b < 4 * NY) {   // warp-uniform
+                float ss = rms_ss[j];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+                if (lane == 0) s_rms[b] = 1.0f / sqrtf(ss / (float)p.rms_K + p.rms_eps);
+            }
+        }
+        __syncthreads();
 #pragma unroll
         for (int nt = 0; nt < NY; nt++) {
-            const int b = 4 * nt + tig;   // computed before the K loop
+            const int b = 4 * nt + tig;
             const float r_b = b < B ? s_rms[b] : 1.0f;
             y[nt][0] *= r_b;
             y[nt][1] *= r_b;

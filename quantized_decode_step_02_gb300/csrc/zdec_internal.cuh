@@ -179,6 +179,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t r) {
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {   // addr 16-byte aligned
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
