@@ -48,19 +48,29 @@ constexpr int SEG_PART = 4 * (HD + 4);          // floats of one segment's parti
 constexpr long long ATT_WAIT_LIMIT = 1LL << 32;   // clock cycles (~2 s): a copy that never lands
 constexpr int ATT_PAGE_CACHE = 64;              // block-table entries a CTA stages in shared memory
 constexpr int ATT_MAX_CS = 16;                  // CTAs of a cluster (one segment of a row)
+constexpr uint32_t ATT_PEER_BYTES = 128 * 16 + GROUP * 8;   // one peer's partial as pushed to rank 0
 
 __host__ __device__ constexpr uint32_t att_stage_bytes(int kt, int vt) { return kv_region_bytes(kt) + kv_region_bytes(vt); }
 static int att_max_stages(int kt, int vt) {
-    const int n = (int)((200u * 1024u) / att_stage_bytes(kt, vt));
+    // 227 KB of dynamic shared memory per CTA, less the static arrays (< 2 KB)
+    // and a 16-CTA cluster's receive area
+    const uint32_t budget = 227u * 1024u - 2048u - (uint32_t)(ATT_MAX_CS - 1) * GROUP * (HD + 4) * 4u;
+    const int n = (int)(budget / att_stage_bytes(kt, vt));
     return n < ATT_MAX_STAGES ? n : ATT_MAX_STAGES;
 }
 int attention_default_stages(int kt, int vt) { return (kt == KV_T_F16 && vt == KV_T_F16) ? 2 : 3; }
-size_t attention_smem_bytes(int kt, int vt, int ns) {
+// Shared memory of a CTA: the chunk ring (reused by the warp merge after the
+// loop), then rank 0's area for its cs - 1 peers' partials, which is never
+// aliased, so a peer may push as soon as its own loop is done.
+__host__ __device__ __forceinline__ uint32_t att_recv_off(int kt, int vt, int ns) {
+    const uint32_t stages = (uint32_t)ns * att_stage_bytes(kt, vt);
+    const uint32_t merge = (4 * 4 * 2 + 4 * 4 * (HD + 4)) * (uint32_t)sizeof(float);   // the CTA's warp merge
+    return ((stages > merge ? stages : merge) + 15u) & ~15u;
+}
+size_t attention_smem_bytes(int kt, int vt, int ns, int cs) {
     if (ns < 2 || ns > att_max_stages(kt, vt)) ns = attention_default_stages(kt, vt);
-    const size_t stages = (size_t)ns * att_stage_bytes(kt, vt);
-    const size_t merge = (4 * 4 * 2 + 4 * 4 * (HD + 4)) * sizeof(float);   // the CTA's warp merge
-    const size_t recv = (size_t)(ATT_MAX_CS - 1) * GROUP * (HD + 4) * sizeof(float);   // rank 0: the peers' partials
-    return std::max(stages, std::max(merge, recv));
+    cs = std::max(1, std::min(ATT_MAX_CS, cs));
+    return att_recv_off(kt, vt, ns) + (size_t)(cs - 1) * GROUP * (HD + 4) * sizeof(float);
 }
 
 __device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
@@ -318,10 +328,15 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; i++) mbar_init(&full[i], 1);
-        mbar_init(&merge_bar, (uint32_t)max(1, CS - 1));
+        mbar_init(&merge_bar, 1);
+        // rank 0 expects its peers' partials: per peer 128 threads x 16 B of
+        // output and 4 heads x 8 B of (max, sum), stored asynchronously
+        if (rank == 0 && CS > 1) mbar_expect_tx(&merge_bar, (uint32_t)(CS - 1) * ATT_PEER_BYTES);
         mbar_fence_init();
     }
     __syncthreads();
+    // publishes rank 0's merge barrier to the peers (waited on before they push)
+    if (CS > 1) cluster_arrive_release();
     const int b = s_map[0];
     if (b < 0) {   // an idle segment slot: every CTA of the cluster leaves here
         pdl_launch_dependents();
@@ -564,24 +579,16 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
 #pragma unroll
         for (int e = 0; e < 4; e++) cta_o[e] = O[e];
     }
-    // ---- the cluster's partials meet in rank 0's shared memory: once every
-    // CTA is past its chunk loop (rank 0's ring is free), each peer stores its
-    // (max, sum, output) per head there and arrives on rank 0's merge barrier
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    float *recv = reinterpret_cast<float *>(smem);   // [peer rank - 1][head][HD + 4]
+    // ---- the cluster's partials meet in rank 0's shared memory: each peer
+    // stores its (max, sum, output) per head into rank 0's receive area as
+    // soon as its own loop is done, and arrives on rank 0's merge barrier
+    if (CS > 1) cluster_wait_acquire();   // every CTA has initialised its barriers (long ago)
+    float *recv = reinterpret_cast<float *>(smem + att_recv_off(KT, VT, NS));   // [peer rank - 1][head][HD + 4]
     if (rank != 0) {
         const uint32_t dst = map_to_rank(smem_u32(recv + ((rank - 1) * GROUP + head) * (HD + 4)), 0);
-        if ((threadIdx.x & 31) == 0) {
-            st_cluster_f32(dst, cta_m);
-            st_cluster_f32(dst + 4u, cta_l);
-        }
-        st_cluster_v4(dst + (uint32_t)(4 + d0) * 4u, make_float4(cta_o[0], cta_o[1], cta_o[2], cta_o[3]));
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            asm volatile("fence.acq_rel.cluster;" ::: "memory");
-            mbar_remote_arrive(map_to_rank(smem_u32(&merge_bar), 0));
-        }
+        const uint32_t rbar = map_to_rank(smem_u32(&merge_bar), 0);
+        if ((threadIdx.x & 31) == 0) st_async_v2(dst, cta_m, cta_l, rbar);
+        st_async_v4(dst + (uint32_t)(4 + d0) * 4u, make_float4(cta_o[0], cta_o[1], cta_o[2], cta_o[3]), rbar);
     } else {
         bool landed = CS == 1 || mbar_try_wait_cluster(&merge_bar, 0);
         if (!landed) {
@@ -703,7 +710,7 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
 // ------------------------------------------------------------------ dispatch ---
 template <int KT, int VT>
 static cudaError_t set_attrs() {
-    const int smem = (int)attention_smem_bytes(KT, VT, att_max_stages(KT, VT));
+    const int smem = (int)attention_smem_bytes(KT, VT, att_max_stages(KT, VT), ATT_MAX_CS);
     cudaError_t e = cudaFuncSetAttribute(attention_kernel<KT, VT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attention_kernel<KT, VT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
@@ -713,7 +720,7 @@ static int max_clusters(int stages, int cs, int nkv) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, nkv, 8);
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = attention_smem_bytes(KT, VT, stages);
+    cfg.dynamicSmemBytes = attention_smem_bytes(KT, VT, stages, cs);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
@@ -731,7 +738,7 @@ static int max_clusters(int stages, int cs, int nkv) {
 template <int KT, int VT>
 static cudaError_t launch_kt(const AttnParams &p, bool pdl, cudaStream_t s, int nz) {
     return launch_k(attention_kernel<KT, VT>, dim3(p.cs, p.kv.n_kv, nz), dim3(128),
-                    attention_smem_bytes(KT, VT, p.stages), pdl, p.cs, s, p);
+                    attention_smem_bytes(KT, VT, p.stages, p.cs), pdl, p.cs, s, p);
 }
 
 // Evaluates CALL(KT, VT) for the runtime type pair (kt, vt) and returns it.

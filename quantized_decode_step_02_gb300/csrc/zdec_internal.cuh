@@ -184,6 +184,20 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {   // ad
                  "f"(v.w)
                  : "memory");
 }
+// Asynchronous store of registers into another CTA's shared memory (cluster
+// addresses), counted as bytes of a transaction on that CTA's mbarrier `bar`
+// (which expects them): no fence or separate arrive needed.  addr aligned to
+// the vector size.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 ::"r"(addr), "f"(a), "f"(b), "r"(bar)
+                 : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

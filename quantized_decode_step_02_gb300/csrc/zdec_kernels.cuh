@@ -137,8 +137,9 @@ cudaError_t launch_attention(const AttnParams &p, int nz, bool pdl, cudaStream_t
 // Raise the attention kernel's dynamic shared-memory limit for a (K, V) type
 // pair (once, before capture).
 cudaError_t attention_setup(int k_type, int v_type);
-// Dynamic shared memory of a launch with `stages` chunks in flight (0: default).
-size_t attention_smem_bytes(int k_type, int v_type, int stages);
+// Dynamic shared memory of a launch with `stages` chunks in flight (0: default)
+// and clusters of cs CTAs.
+size_t attention_smem_bytes(int k_type, int v_type, int stages, int cs);
 int attention_default_stages(int k_type, int v_type);
 int attention_stage_limit(int k_type, int v_type);
 // Clusters of cs attention CTAs (with `stages` chunks in flight) the GPU holds
