@@ -392,7 +392,11 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     if (threadIdx.x == 0) {
         s_bad = 0;
         for (int i = 0; i < D; i++) mbar_init(&full[i], 1);
-        if (cs > 1 && rank == 0) mbar_init(&red_bar, cs - 1);
+        if (cs > 1 && rank == 0) {
+            // the cs - 1 peers' partial tiles, stored asynchronously into the area
+            mbar_init(&red_bar, 1);
+            mbar_expect_tx(&red_bar, (uint32_t)(cs - 1) * GemmRed<NT, IMPL>::v);
+        }
         mbar_fence_init();
     }
     // rank 0 receives the peers' partial tiles after the barriers (see the end):
@@ -599,24 +603,15 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         cluster_wait_acquire();   // every CTA of the cluster has initialised its barriers
         constexpr int SLOT = GemmRed<NT, IMPL>::v / 4;   // floats of one peer's partial tile set
         const uint32_t red_local = smem_u32(smem + red_off);
-        if (rank != 0) {
+        if (rank != 0) {   // (y[nt][0], y[nt][1]) as one 8-byte store per lane
             const uint32_t dst = map_to_rank(red_local, 0) + (uint32_t)((rank - 1) * SLOT) * 4u;
+            const uint32_t rbar = map_to_rank(smem_u32(&red_bar), 0);
             if (IMPL == 3) {
-                if (tig == 0)
-#pragma unroll
-                    for (int r = 0; r < 2; r++)
-                        st_cluster_f32(dst + (uint32_t)((warp * 2 + r) * 8 + (lane >> 2)) * 4u, y[0][r]);
+                if (tig == 0) st_async_v2(dst + (uint32_t)(warp * 8 + (lane >> 2)) * 8u, y[0][0], y[0][1], rbar);
             } else
 #pragma unroll
             for (int nt = 0; nt < NY; nt++)
-#pragma unroll
-                for (int r = 0; r < 2; r++)
-                    st_cluster_f32(dst + (uint32_t)(((warp * NY + nt) * 2 + r) * 32 + lane) * 4u, y[nt][r]);
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                asm volatile("fence.acq_rel.cluster;" ::: "memory");
-                mbar_remote_arrive(map_to_rank(smem_u32(&red_bar), 0));
-            }
+                st_async_v2(dst + (uint32_t)((warp * NY + nt) * 32 + lane) * 8u, y[nt][0], y[nt][1], rbar);
             tl_end(p.tl);
             return;
         }
@@ -633,15 +628,19 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         const float *red = reinterpret_cast<const float *>(smem + red_off);
         if (IMPL == 3) {
             if (tig == 0)
-                for (int rr = 1; rr < cs; rr++)
-#pragma unroll
-                    for (int r = 0; r < 2; r++) y[0][r] += red[(rr - 1) * SLOT + (warp * 2 + r) * 8 + (lane >> 2)];
+                for (int rr = 1; rr < cs; rr++) {
+                    const float2 v = *reinterpret_cast<const float2 *>(red + (rr - 1) * SLOT + (warp * 8 + (lane >> 2)) * 2);
+                    y[0][0] += v.x;
+                    y[0][1] += v.y;
+                }
         } else
         for (int rr = 1; rr < cs; rr++)
 #pragma unroll
-            for (int nt = 0; nt < NY; nt++)
-#pragma unroll
-                for (int r = 0; r < 2; r++) y[nt][r] += red[(rr - 1) * SLOT + ((warp * NY + nt) * 2 + r) * 32 + lane];
+            for (int nt = 0; nt < NY; nt++) {
+                const float2 v = *reinterpret_cast<const float2 *>(red + (rr - 1) * SLOT + ((warp * NY + nt) * 32 + lane) * 2);
+                y[nt][0] += v.x;
+                y[nt][1] += v.y;
+            }
         __syncthreads();
         if (bad || s_bad) return;
         tl_max(p.tl, 7);

@@ -165,24 +165,11 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive without ordering this thread's earlier memory operations (a pure
-// execution barrier: nothing written before it needs to be seen after it).
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
 // Shared-memory address `a` of this CTA -> the same address in cluster rank r.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t r) {
     uint32_t out;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(r));
     return out;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {   // addr 16-byte aligned
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
 }
 // Asynchronous store of registers into another CTA's shared memory (cluster
 // addresses), counted as bytes of a transaction on that CTA's mbarrier `bar`
@@ -197,10 +184,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uin
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
                  ::"r"(addr), "f"(a), "f"(b), "r"(bar)
                  : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Wait on this CTA's mbarrier, acquiring what other CTAs of the cluster released.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
