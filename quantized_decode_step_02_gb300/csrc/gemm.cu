@@ -438,10 +438,8 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         mvo.sums = sum_off;
     }
     const int pre = min(D, n);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < pre; i++) issue_w(i, i);
-        s_issued = pre;
-    }
+    if ((int)threadIdx.x < pre) issue_w(threadIdx.x, threadIdx.x);   // one issuing thread per stage
+    if (threadIdx.x == 0) s_issued = pre;
     // epilogue inputs that no earlier kernel of the step writes (weights, the
     // rotary table, the step's positions), fetched before the dependency wait
     if (EPI == EPI_RESID && p.next_gain && threadIdx.x < 128)
@@ -452,8 +450,10 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     pdl_wait();
     tl_min(p.tl, 1);
     tl_max(p.tl, 4);
-    if (threadIdx.x == 0)
-        for (int i = 0; i < pre; i++) issue_act(i, i);
+    // the activation rows of the first stages, one issuing thread per stage (a
+    // copy that lands before thread 0's expect_tx only leaves the transaction
+    // count negative until then: the phase still needs that arrival)
+    if ((int)threadIdx.x < pre) issue_act(threadIdx.x, threadIdx.x);
     // the epilogue's inputs from earlier kernels, fetched now so that their
     // latency hides behind the K loop: this lane's partial sums of x^2 per
     // batch row (RMSNorm scale) and the residual rows it will update
