@@ -58,7 +58,7 @@ static int att_max_stages(int kt, int vt) {
     const int n = (int)(budget / att_stage_bytes(kt, vt));
     return n < ATT_MAX_STAGES ? n : ATT_MAX_STAGES;
 }
-int attention_default_stages(int kt, int vt) { return (kt == KV_T_F16 && vt == KV_T_F16) ? 2 : 3; }
+int attention_default_stages(int kt, int vt) { return att_max_stages(kt, vt) < 3 ? att_max_stages(kt, vt) : 3; }
 // Shared memory of a CTA: the chunk ring (reused by the warp merge after the
 // loop), then rank 0's area for its cs - 1 peers' partials, which is never
 // aliased, so a peer may push as soon as its own loop is done.
