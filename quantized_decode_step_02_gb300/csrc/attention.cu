@@ -336,7 +336,7 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
     }
     __syncthreads();
     // publishes rank 0's merge barrier to the peers (waited on before they push)
-    if (CS > 1) cluster_arrive_release();
+    if (CS > 1) cluster_arrive_relaxed();
     const int b = s_map[0];
     if (b < 0) {   // an idle segment slot: every CTA of the cluster leaves here
         pdl_launch_dependents();

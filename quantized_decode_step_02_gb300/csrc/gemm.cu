@@ -419,7 +419,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
     __syncthreads();
     // publishes red_bar's initialisation (waited on after the K loop); with an
     // aliased reduction area rank 0 arrives only when its stages are free
-    if (cs > 1 && !(p.red_alias && rank == 0)) cluster_arrive_release();
+    if (cs > 1 && !(p.red_alias && rank == 0)) cluster_arrive_relaxed();
     // this lane's fixed offsets into a stage: virtual column g of n-tile 0 is the
     // hi (g even) or lo (g odd) plane of batch row g/2
     const int g = lane >> 2;

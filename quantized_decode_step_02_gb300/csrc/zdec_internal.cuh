@@ -165,6 +165,12 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive without a release of this thread's memory operations: for a barrier
+// that only publishes mbarrier initialisations, which thread 0 has already
+// released with fence.mbarrier_init.release.cluster.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 // Shared-memory address `a` of this CTA -> the same address in cluster rank r.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t r) {
     uint32_t out;
