@@ -260,6 +260,8 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
     __shared__ __align__(8) uint64_t merge_bar;           // rank 0: the peers' partials have landed
     __shared__ int s_map[4];                             // row, segment, segments of the row, chunks per segment
     __shared__ int s_bad, s_last;
+    __shared__ int s_done[ATT_MAX_STAGES];               // warps done with the chunk in each ring slot
+    __shared__ int s_issued;                             // chunks whose copies have been issued
     __shared__ int s_pages[ATT_PAGE_CACHE];              // pages of this CTA's first chunks
 
     const int rank = blockIdx.x, g = blockIdx.y, z = blockIdx.z, CS = p.cs;
@@ -327,7 +329,10 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
         }
     }
     if (threadIdx.x == 0) {
-        for (int i = 0; i < p.stages; i++) mbar_init(&full[i], 1);
+        for (int i = 0; i < p.stages; i++) {
+            mbar_init(&full[i], 1);
+            s_done[i] = 0;
+        }
         mbar_init(&merge_bar, 1);
         // rank 0 expects its peers' partials: per peer 128 threads x 16 B of
         // output and 4 heads x 8 B of (max, sum), stored asynchronously
@@ -384,8 +389,9 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
     // NS chunks (the whole ring) go out before the dependency wait, one
     // issuing thread each
     if ((int)threadIdx.x < NS && (int)threadIdx.x < nchunks) issue(threadIdx.x);
-    int issued = min(NS, nchunks);   // chunks due in the ring (the same count on every thread)
-    int sent = issued;               // thread 0 (after the first refill): chunks in flight
+    // read only after the loop; the later writes come from the warp that
+    // releases a slot last, after every warp (thread 0's included) is past it
+    if (threadIdx.x == 0) s_issued = min(NS, nchunks);
 
     // the rotary row of the new token: a constant table, read before the wait
     float2 rope_new[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -475,17 +481,19 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
         for (int i = 0; i < 4; i++) oacc[mt][i] = 0.0f;
     bool ok = true;
 
+    // Each warp runs through the chunks on its own: no block barrier per
+    // chunk.  The last of the 4 warps done with a ring slot refills it with
+    // the chunk NS further on (a warp's loads of the slot are complete once
+    // their values have entered its MMAs; __syncwarp orders the lanes' loads
+    // before lane 0's release).  Only the chunks at the end of the history,
+    // which every thread edits first, take block barriers.
     for (int ci = 0; ci < nchunks; ci++) {
         const int c0 = (c_lo + ci) * PAGE_TOKENS;
         const int zfrom = max(H, c0) - c0;   // first local token not read from the cache
-        if (zfrom < PAGE_TOKENS && has_new && warp == 0) encode_new();   // published by the barrier below
-        __syncthreads();   // every warp is done with chunk ci - 1: its slot may be refilled
-        if (ci > 0 && issued < nchunks) {   // chunk ci + NS - 1 into the slot chunk ci - 1 freed
-            if (threadIdx.x == 0 && !s_bad) {
-                issue(issued);
-                sent = issued + 1;
-            }
-            issued++;
+        const bool fixup = zfrom < PAGE_TOKENS;   // the same on every warp
+        if (fixup) {
+            if (has_new && warp == 0) encode_new();
+            __syncthreads();   // the new token's codes, for every thread
         }
         if (ok && !att_wait(&full[ci % NS], (uint32_t)(ci / NS) & 1u, ATT_WAIT_LIMIT)) {
             ok = false;
@@ -493,7 +501,7 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
             atomicOr(p.status, STATUS_TIMEOUT);
         }
         uint8_t *sK = stage(ci), *sV = stage(ci) + KB;
-        if (zfrom < PAGE_TOKENS) {
+        if (fixup) {
             // the chunk holding the end of the history: clear what lies past
             // it (stale values of the page's earlier use may be Inf or NaN, and
             // 0 * NaN would reach the output) and insert the new token
@@ -539,11 +547,25 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
                     for (int i = 0; i < 4; i++) oacc[m][i] *= alpha;
             pv_tile<VT>(sV, warp, gid, tig, pa, pb, oacc);
         }
+        // this warp is done with slot ci % NS
+        __syncwarp();
+        if (lane == 0) {
+            const int slot = ci % NS;
+            __threadfence_block();
+            if (atomicAdd(&s_done[slot], 1) == 3) {   // the last of the 4 warps
+                s_done[slot] = 0;
+                if (ci + NS < nchunks && !s_bad) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the reads before the copy's writes
+                    issue(ci + NS);
+                    s_issued = ci + NS + 1;
+                }
+            }
+        }
     }
     tl_max(p.tl, 6);
     __syncthreads();
     if (s_bad && threadIdx.x == 0)   // copies still in flight land before the ring is reused
-        for (int i = max(0, sent - NS); i < sent; i++)
+        for (int i = max(0, s_issued - NS); i < s_issued; i++)
             att_wait(&full[i % NS], (uint32_t)(i / NS) & 1u, ATT_WAIT_LIMIT);
 
     // ---- merge the 4 warps of this CTA (shared memory reused after the stages)
