@@ -24,17 +24,20 @@
 //
 // Arithmetic (4 warps, 16 tokens each per chunk; the 4 query heads of the kv
 // head share every K/V tile): scores and P V run on mma.sync.m16n8k16 with
-// fp32 accumulation; q and p enter as fp16 high parts (rows 0-3) and low
-// parts (rows 8-11), ~22 bits.  Q8_0 codes become exact fp16 integers in
-// registers (byte_perm under exponent 1024, minus 1152) with K scales applied
-// to 32-dim partial scores and V scales folded into p per 32-dim block; FP8
-// codes convert exactly with the hardware's e4m3x2 -> f16x2 cvt.  Softmax in
-// log2 units (q carries log2(e)/sqrt(128)).
+// fp32 accumulation, the chunk's tokens as M and the 4 heads as N (column n:
+// head n >> 1, fp16 part n & 1 of q or p split into hi + lo, ~22 bits).  Q8_0
+// codes become exact fp16 integers in registers (byte_perm under exponent
+// 1024, minus 1152) with K scales applied to 32-dim partial scores and V
+// scales folded into p per 32-dim block; FP8 codes convert exactly with the
+// hardware's e4m3x2 -> f16x2 cvt.  Softmax in log2 units (q carries
+// log2(e)/sqrt(128)).  The warps run through the chunks without a block
+// barrier; the last warp done with a ring slot refills it.
 //
-// Merge: warps -> CTA (shared memory), ranks -> rank 0 (distributed shared
-// memory, fixed rank order), segments -> the last segment to finish (global
-// partials and a ticket per (row, kv head), merged in segment order), so the
-// result never depends on timing.
+// Merge: warps -> CTA (shared memory), ranks -> rank 0 (each peer stores its
+// partial into rank 0's shared memory with st.async, counted on rank 0's
+// mbarrier; merged in fixed rank order), segments -> the last segment to
+// finish (global partials and a ticket per (row, kv head), merged in segment
+// order), so the result never depends on timing.
 
 #include "kv_pool.cuh"
 #include "zdec_kernels.cuh"

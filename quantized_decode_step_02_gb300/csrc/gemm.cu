@@ -13,8 +13,9 @@
 // super-block's activation rows.  Weight copies are issued before the
 // programmatic-launch dependency wait (weights never depend on the previous
 // kernel), activation copies after it.  Small matrices split K across a
-// thread-block cluster and reduce the partial tiles through distributed
-// shared memory (fixed order, no atomics).
+// thread-block cluster: the peers store their partial tiles into rank 0's
+// shared memory with st.async (counted on rank 0's mbarrier) and rank 0 sums
+// them in rank order (no atomics).
 //
 // Arithmetic, per warp and super-block:
 //   * dequant: one lop3 puts two 4-bit codes under the fp16 exponent of 1024;
@@ -565,7 +566,7 @@ __global__ __launch_bounds__(256, (GemmOcc<NT, IMPL>::v)) void gemm_kernel(const
         if (threadIdx.x == 0)
             for (int i = max(0, s_issued - D); i < s_issued; i++) wait_stage(&full[i % D], (uint32_t)(i / D) & 1u, nullptr);
         __syncthreads();
-        if (cs == 1) return;   // cluster members still meet the two cluster barriers below
+        if (cs == 1) return;   // cluster members still take part in the reduction below
     }
     // per-lane outputs: y[nt][rho] for output row g + 8 rho, batch row 4nt + tig
     float y[NY][2];
