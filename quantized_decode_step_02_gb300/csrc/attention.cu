@@ -680,8 +680,10 @@ __global__ __launch_bounds__(128, 3) void attention_kernel(const AttnParams p) {
             const int kcol = (GROUP * g + head) * HD + d0;   // column of o, the O projection's input
             float y[4];
             for (int e = 0; e < 4; e++) y[e] = O[e] * inv;
-            float *o = p.o + (size_t)b * qd + kcol;
-            for (int e = 0; e < 4; e++) o[e] = y[e];
+            if (p.o) {   // the fp32 output (read-back paths; the step reads only the planes)
+                float *o = p.o + (size_t)b * qd + kcol;
+                for (int e = 0; e < 4; e++) o[e] = y[e];
+            }
             // the O projection's operand as fp16 hi + lo parts (elements 4..7 of
             // every 8 stored / 16) and the per-32 sub-block sums, as the GEMM
             // prep writes them

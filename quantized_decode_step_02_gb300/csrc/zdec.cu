@@ -756,7 +756,7 @@ static cudaError_t enqueue_step(zdec_ctx *ctx, int B, int segs, float *logits_ou
     ap.cs = plan.cs;
     ap.seg_min = 2;
     ap.stages = plan.stages;
-    ap.o = ctx->o;
+    ap.o = nullptr;   // the O projection reads the operand planes only
     ap.o16 = ctx->o16;
     ap.o16lo = ctx->o16lo;
     ap.osx = ctx->osx;

@@ -118,7 +118,7 @@ struct AttnParams {
     int append;            // 1: rotate q/k at pos and append k, v; 0: q already rotated, no append
     int cs;                // CTAs per (segment, kv head): one thread-block cluster (1..16)
     int seg_min;           // fewest 64-token chunks a segment takes (when rows are long enough)
-    float *o;              // [B][nq*128]
+    float *o;              // [B][nq*128] fp32 output, or null (then only the planes below)
     __half *o16;           // act planes (hi, lo) and sums of the O projection's input
     __half *o16lo;
     __half *osx;
