@@ -840,10 +840,21 @@ __global__ void argmax_final_kernel(const float *__restrict__ vals, const int *_
     __shared__ int si[32];
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
-    for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
-        float v = vals[i * MAX_B + b];
-        int ix = idxs[i * MAX_B + b];
-        if (v > bv || (v == bv && ix < bi)) { bv = v; bi = ix; }
+    // eight partials per thread per round, all loaded before any is compared
+    // (one latency per round instead of one per partial)
+    constexpr int U = 8;
+    for (int i0 = threadIdx.x; i0 < nparts; i0 += U * blockDim.x) {
+        float v[U];
+        int ix[U];
+#pragma unroll
+        for (int k = 0; k < U; k++) {
+            const int i = i0 + k * blockDim.x;
+            v[k] = i < nparts ? vals[i * MAX_B + b] : -INFINITY;
+            ix[k] = i < nparts ? idxs[i * MAX_B + b] : 0x7FFFFFFF;
+        }
+#pragma unroll
+        for (int k = 0; k < U; k++)
+            if (v[k] > bv || (v[k] == bv && ix[k] < bi)) { bv = v[k]; bi = ix[k]; }
     }
     for (int o = 16; o > 0; o >>= 1) {
         float ov = __shfl_xor_sync(FULL, bv, o);

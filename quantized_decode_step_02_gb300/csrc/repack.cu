@@ -167,7 +167,9 @@ cudaError_t launch_dequant_rows(const uint8_t *tiles, int row_map, int nsb, int 
 }
 
 // ---------------------------------------------------------------- embed ---
-// Block b gathers row tokens[b] of the tied embedding: thread = (sb, sub-block).
+// Block b gathers row tokens[b] of the tied embedding: one thread per 8
+// elements (super-block sb, sub-block j, quarter c), so the row's loads go out
+// at once.
 __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
                              const int32_t *tokens, const int32_t *positions, const int32_t *slots,
                              const int32_t *len_dev, uint32_t *status, int B,
@@ -179,38 +181,40 @@ __global__ void embed_kernel(const uint8_t *__restrict__ E, int nsb, int vocab,
     pdl_wait();
     tl_min(tl, 1);
     __shared__ float red[32];
-    int b = blockIdx.x;
-    if (b >= B) return;
+    const int b = blockIdx.x;   // the grid is B blocks
     int tok = tokens[b];
     if (threadIdx.x == 0 && positions[b] != len_dev[slots[b]]) atomicOr(status, STATUS_POSITION);
     if (tok < 0 || tok >= vocab) {               // flagged; row 0 keeps the step well defined
         if (threadIdx.x == 0) atomicOr(status, STATUS_TOKEN);
         tok = 0;
     }
-    int rt = tok >> 4, lr = tok & 15;
+    const int rt = tok >> 4, lr = tok & 15;
     float ss = 0.0f;
-    for (int t = threadIdx.x; t < nsb * 8; t += blockDim.x) {
-        int sb = t >> 3, j = t & 7;
+    // blockDim.x is a multiple of 32 and nsb * 32 items are whole warps, so the
+    // 4 quarters of a sub-block are 4 adjacent lanes of one warp
+    for (int t = threadIdx.x; t < nsb * 32; t += blockDim.x) {
+        const int sb = t >> 5, j = (t >> 2) & 7, c = t & 3;
         const uint8_t *tile = E + tile_offset(rt, sb, nsb);
         uint16_t dbits, mbits;
         int sc[8], m[8];
         tile_row_fields(tile, lr, dbits, mbits, sc, m);
-        float d = __half2float(__ushort_as_half(dbits)), dmin = __half2float(__ushort_as_half(mbits));
-        float *o = x + (size_t)b * ldx + sb * 256 + 32 * j;
-        float usum = 0.0f;
-        for (int c = 0; c < 4; c++) {
-            float y[8];
-            for (int i = 0; i < 8; i++) {
-                const int k = 32 * j + 8 * c + i;
-                float w = dq_value(d, sc[j], dmin, m[j], tile_q(tile, lr, k));
-                o[8 * c + i] = w;
-                ss = fmaf(w, w, ss);
-                y[i] = w * gain[sb * 256 + k];
-                usum += y[i];
-            }
-            store_act8(u, ulo, act_chunk(sb, b, 4 * j + c, Bp), y);
+        const float d = __half2float(__ushort_as_half(dbits)), dmin = __half2float(__ushort_as_half(mbits));
+        float *o = x + (size_t)b * ldx + sb * 256 + 32 * j + 8 * c;
+        float y[8], w[8], usum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int k = 32 * j + 8 * c + i;
+            w[i] = dq_value(d, sc[j], dmin, m[j], tile_q(tile, lr, k));
+            ss = fmaf(w[i], w[i], ss);
+            y[i] = w[i] * gain[sb * 256 + k];
+            usum += y[i];
         }
-        store_sum(usx, sb, b, j, Bp, usum);
+        reinterpret_cast<float4 *>(o)[0] = make_float4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<float4 *>(o)[1] = make_float4(w[4], w[5], w[6], w[7]);
+        store_act8(u, ulo, act_chunk(sb, b, 4 * j + c, Bp), y);
+        usum += __shfl_xor_sync(0xFFFFFFFFu, usum, 1);   // the sub-block's 4 quarters
+        usum += __shfl_xor_sync(0xFFFFFFFFu, usum, 2);
+        if (c == 0) store_sum(usx, sb, b, j, Bp, usum);
     }
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -228,7 +232,7 @@ cudaError_t launch_embed(const uint8_t *E, int nsb, int vocab, const int32_t *to
                          uint32_t *status, int B, float *x, int ldx, const float *gain, __half *u,
                          __half *ulo, __half *usx, int Bp, float *part, bool pdl, cudaStream_t stream,
                          unsigned long long *tl) {
-    return launch_k(embed_kernel, dim3(B), dim3(128), 0, pdl, 1, stream, E, nsb, vocab, tokens,
+    return launch_k(embed_kernel, dim3(B), dim3(512), 0, pdl, 1, stream, E, nsb, vocab, tokens,
                     positions, slots, len_dev, status, B, x, ldx, gain, u, ulo, usx, Bp, part, tl);
 }
 
