@@ -630,7 +630,9 @@ static int attn_stages(const zdec_ctx *ctx, int B) {
 // Segment slots per row for a step whose rows hold these many tokens: one
 // when the rows are about even (a cut row pays a cross-segment merge, ~3 us
 // at B = 1 measured), up to MAX_SEGS when the longest row is that many times
-// the mean, so that its clusters take about a mean row's work each.
+// the mean, so that its clusters take about a mean row's work each; the ratio
+// is rounded up from a quarter (B = 8, lengths 800..30,000, ratio 3.26:
+// 1 / 2 / 3 / 4 slots measured 6.49 / 4.07 / 4.11 / 3.82 ms per step).
 static int attn_segments(const zdec_ctx *ctx, int B) {
     static const int f_seg = getenv("ZDEC_ATT_SEGS") ? atoi(getenv("ZDEC_ATT_SEGS")) : 0;
     if (f_seg >= 1) return std::min(f_seg, MAX_SEGS);
@@ -641,7 +643,7 @@ static int attn_segments(const zdec_ctx *ctx, int B) {
         mx = std::max(mx, n);
     }
     const double ratio = sum > 0 ? (double)mx * B / (double)sum : 1.0;
-    return std::max(1, std::min(MAX_SEGS, (int)(ratio + 0.5)));
+    return std::max(1, std::min(MAX_SEGS, (int)(ratio + 0.75)));
 }
 // Attention launch shape for a batch of B rows cut into `segs` segment slots
 // per row: the cluster size cs (ranks per segment) of least modelled time,
