@@ -118,3 +118,32 @@ def test_bench_byte_accounting_matches_the_byte_model():
     # per layer, the attention launch moves 1/36 of the step's KV bytes
     att = bench.kernel_bytes(d, "attention", 8, 2400, "q8_0")
     assert att - 8 * (2 * 4096 + 2 * 1024) * 4 == pytest.approx(8 * 2402 * 78_336 / 36)
+
+
+def test_traffic_table_matches_its_captures():
+    """Every ncu traffic entry bench.py may report names a committed capture
+    summary under profiles/, and its DRAM bytes lie between what must come from
+    HBM (the weights, or the KV pages read) and the kernel's algorithmic bytes
+    plus 1 % (more would mean re-reads; less, an entry of another launch).
+    Activations and outputs may stay in L2, so they only bound from above."""
+    import bench
+    from synth.model import FULL as d
+    root = os.path.dirname(os.path.dirname(__file__))
+    tab = json.load(open(os.path.join(root, "profiles", "ncu_traffic.json")))["kernels"]
+    assert tab, "no traffic entries"
+    for key, ent in tab.items():
+        kind, bclass, tail = key.split("/")
+        assert os.path.exists(os.path.join(root, ent["source"])), ent["source"]
+        B = int(bclass[1:])
+        if kind == "attention":
+            # one layer's KV in whole 64-token pages: the captures ran at
+            # L = 2048 (B = 1) and L = 8192 (B = 8), in their second step
+            L = 2048 if B == 1 else 8192
+            pages = -(-(L + 2) // 64)
+            lo = B * pages * 64 * bench.kv_bytes_per_token(d, tail) / d.n_layers
+            hi = 1.01 * lo + B * 16 * 1024 * 4 + 4e6
+        else:
+            lo = bench.kernel_bytes(d, kind, 0, 0, "f16")   # the matrix alone
+            hi = 1.01 * bench.kernel_bytes(d, kind, B, 0, "f16")
+            assert bench.ncu_traffic(kind, B, "f16", int(tail[4:])) == ent["bytes"]
+        assert lo <= ent["bytes"] <= hi, (key, ent["bytes"], lo, hi)
