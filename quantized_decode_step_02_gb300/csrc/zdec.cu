@@ -631,8 +631,9 @@ static int attn_stages(const zdec_ctx *ctx, int B) {
 // when the rows are about even (a cut row pays a cross-segment merge, ~3 us
 // at B = 1 measured), up to MAX_SEGS when the longest row is that many times
 // the mean, so that its clusters take about a mean row's work each; the ratio
-// is rounded up from a quarter (B = 8, lengths 800..30,000, ratio 3.26:
-// 1 / 2 / 3 / 4 slots measured 6.49 / 4.07 / 4.11 / 3.82 ms per step).
+// is rounded to nearest (measured at B = 8: lengths 800..30,000, ratio 3.26,
+// 3 / 4 slots 4.11 / 3.82 ms with fp16 but 3.71 / 3.89 ms with Q8_0; lengths
+// 6,000 + 7 x 2,000, ratio 2.4, 2 / 3 slots 2.76 / 2.85 ms).
 static int attn_segments(const zdec_ctx *ctx, int B) {
     static const int f_seg = getenv("ZDEC_ATT_SEGS") ? atoi(getenv("ZDEC_ATT_SEGS")) : 0;
     if (f_seg >= 1) return std::min(f_seg, MAX_SEGS);
@@ -643,7 +644,7 @@ static int attn_segments(const zdec_ctx *ctx, int B) {
         mx = std::max(mx, n);
     }
     const double ratio = sum > 0 ? (double)mx * B / (double)sum : 1.0;
-    return std::max(1, std::min(MAX_SEGS, (int)(ratio + 0.75)));
+    return std::max(1, std::min(MAX_SEGS, (int)(ratio + 0.5)));
 }
 // Attention launch shape for a batch of B rows cut into `segs` segment slots
 // per row: the cluster size cs (ranks per segment) of least modelled time,
